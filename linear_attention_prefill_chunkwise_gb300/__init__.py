@@ -1,0 +1,157 @@
+"""GB300 (sm_103a) Lightning Attention chunkwise prefill.
+
+``la_prefill_fwd`` is a thin ctypes binding of the C entry point of the same
+name (include/la_prefill.h): it checks dtypes and shapes of torch tensors,
+passes their device pointers and the current CUDA stream, and raises on a
+non-OK status.  Every step of the computation runs in the library's CUDA
+kernel; there is no other implementation in this package and no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import build as _build
+
+__all__ = ["la_prefill_fwd", "LaError", "load_library", "SCHEDULES", "DEV_ERR_BAD_SEQLENS",
+           "DEV_ERR_BAD_INDEX", "DEV_ERR_TIMEOUT", "EXPORTED_SYMBOLS"]
+
+SCHEDULES = {"auto": 0, "persistent": 1, "non_persistent": 2}
+DEV_ERR_BAD_SEQLENS = 1
+DEV_ERR_BAD_INDEX = 2
+DEV_ERR_TIMEOUT = 4
+EXPORTED_SYMBOLS = ("la_prefill_fwd", "la_status_string", "la_last_error", "la_prefill_smem_bytes")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class LaError(RuntimeError):
+    """A non-OK la_status returned by the C library."""
+
+    def __init__(self, status: int, name: str, detail: str):
+        super().__init__(f"{name}: {detail}")
+        self.status = status
+        self.name = name
+
+
+def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libla_prefill.so (building it first when it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB_PATH
+            if build_if_missing:
+                path = _build.build()
+            if not os.path.exists(path):
+                raise RuntimeError(f"CUDA library not built: {path} (run linear_attention_prefill_chunkwise_gb300.build)")
+            lib = ctypes.CDLL(path)
+            vp, i32p, fp = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p
+            lib.la_prefill_fwd.argtypes = [vp, vp, vp, fp, ctypes.c_float, fp, i32p, i32p, vp, fp] + \
+                [ctypes.c_int] * 8 + [ctypes.c_int, vp, vp]
+            lib.la_prefill_fwd.restype = ctypes.c_int
+            lib.la_status_string.argtypes = [ctypes.c_int]
+            lib.la_status_string.restype = ctypes.c_char_p
+            lib.la_last_error.argtypes = []
+            lib.la_last_error.restype = ctypes.c_char_p
+            lib.la_prefill_smem_bytes.argtypes = []
+            lib.la_prefill_smem_bytes.restype = ctypes.c_int
+            _lib = lib
+        return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(t, name, dtype, ndim):
+    import torch
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def la_prefill_fwd(q, k, v, slopes, scale, h0=None, state_indices=None, cu_seqlens=None, o=None,
+                   h_final=None, seq_len=None, schedule="auto", dev_error=None, stream=None):
+    """Lightning Attention chunkwise prefill (forward) on the current CUDA device.
+
+    q, k: bf16 [tokens, H, 128]; v: bf16 [tokens, HV, 128]; slopes: fp32 [HV];
+    h0 / h_final: fp32 [P, HV, 128, 128] ([V, K] per state) or None;
+    state_indices: int32 [N] or None (negative = padded sequence);
+    cu_seqlens: int32 [N + 1] or None.  Without cu_seqlens the batch is fixed
+    length: ``seq_len`` tokens per sequence (tokens must be a multiple of it).
+    ``o`` (bf16 [tokens, HV, 128]) is allocated when not given.  h_final may be
+    the same tensor as h0 (in-place state pool).  Returns ``o``.
+    """
+    import torch
+    lib = load_library()
+    _check(q, "q", torch.bfloat16, 3)
+    _check(k, "k", torch.bfloat16, 3)
+    _check(v, "v", torch.bfloat16, 3)
+    _check(slopes, "slopes", torch.float32, 1)
+    _check(h0, "h0", torch.float32, 4)
+    _check(h_final, "h_final", torch.float32, 4)
+    _check(state_indices, "state_indices", torch.int32, 1)
+    _check(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    tokens, H, D = q.shape
+    _, HV, V = v.shape
+    if k.shape != q.shape or v.shape[0] != tokens:
+        raise ValueError("q, k, v token counts / shapes disagree")
+    if slopes.shape[0] != HV:
+        raise ValueError("slopes must have HV entries")
+    if o is None:
+        o = torch.empty((tokens, HV, V), dtype=torch.bfloat16, device=q.device)
+    _check(o, "o", torch.bfloat16, 3)
+    if cu_seqlens is not None:
+        N = cu_seqlens.shape[0] - 1
+        B, T = 1, tokens
+    else:
+        if seq_len is None:
+            raise ValueError("fixed-length mode needs seq_len")
+        T = int(seq_len)
+        if T == 0:
+            raise ValueError("seq_len must be positive in fixed-length mode")
+        if tokens % T:
+            raise ValueError("tokens must be a multiple of seq_len")
+        B = tokens // T
+        N = B
+    pool = 0
+    for t in (h0, h_final):
+        if t is not None:
+            if tuple(t.shape[1:]) != (HV, V, D):
+                raise ValueError("state tensors must be [P, HV, V, D]")
+            pool = t.shape[0] if pool == 0 else min(pool, t.shape[0])
+    if h0 is not None and h_final is not None and h0.shape[0] != h_final.shape[0]:
+        raise ValueError("h0 and h_final must have the same number of slots")
+    if state_indices is not None and state_indices.shape[0] != N:
+        raise ValueError("state_indices must have N entries")
+    if dev_error is not None:
+        _check(dev_error, "dev_error", torch.int32, 1)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif not isinstance(stream, int):
+        stream = stream.cuda_stream
+    if isinstance(schedule, str):
+        schedule = SCHEDULES[schedule]
+    st = lib.la_prefill_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes), ctypes.c_float(scale), _ptr(h0),
+                            _ptr(state_indices), _ptr(cu_seqlens), _ptr(o), _ptr(h_final),
+                            int(B), int(T), int(N), int(H), int(HV), int(D), int(V), int(pool),
+                            int(schedule), _ptr(dev_error), ctypes.c_void_p(stream))
+    if st != 0:
+        raise LaError(st, lib.la_status_string(st).decode(), lib.la_last_error().decode())
+    return o
+
+
+def la_prefill_fwd_raw(*args):
+    """Call the C entry point with raw integers / pointers (argument order of the header)."""
+    return load_library().la_prefill_fwd(*args)

@@ -1,0 +1,62 @@
+"""Compile the sm_103a C-ABI library ``libla_prefill.so`` in-tree.
+
+One translation unit, one ``-gencode`` (sm_103a), static CUDA runtime, no
+link-time dependency on the driver library (the tensor-map encoder is fetched
+through the runtime's driver entry-point query), so the library loads on a
+machine without a GPU.
+"""
+from __future__ import annotations
+
+import os
+import shutil
+import subprocess
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+CSRC = os.path.join(HERE, "csrc")
+BUILD_DIR = os.path.join(HERE, "_build")
+LIB_NAME = "libla_prefill.so"
+LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
+INCLUDE_DIR = os.path.join(os.path.dirname(HERE), "include")
+
+SOURCES = ["la_prefill_api.cu"]
+DEPENDS = ["la_prefill_api.cu", "la_prefill_kernel.cuh", "sm103_ptx.cuh"]
+ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def nvcc_path() -> str:
+    cand = shutil.which("nvcc")
+    if cand:
+        return cand
+    cuda_home = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    return os.path.join(cuda_home, "bin", "nvcc")
+
+
+def _stale() -> bool:
+    if not os.path.exists(LIB_PATH):
+        return True
+    t = os.path.getmtime(LIB_PATH)
+    deps = [os.path.join(CSRC, d) for d in DEPENDS] + [os.path.join(INCLUDE_DIR, "la_prefill.h")]
+    return any(os.path.getmtime(d) > t for d in deps)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Build the library if any source is newer than it; return its path."""
+    if not force and not _stale():
+        return LIB_PATH
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    cmd = [nvcc_path(), *ARCH_FLAGS, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
+           "-cudart", "static", "-I", INCLUDE_DIR, "-o", tmp] + [os.path.join(CSRC, s) for s in SOURCES]
+    if verbose:
+        cmd.insert(1, "-Xptxas=-v")
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + res.stdout + res.stderr)
+    if verbose:
+        print(res.stdout + res.stderr)
+    os.replace(tmp, LIB_PATH)
+    return LIB_PATH
+
+
+if __name__ == "__main__":
+    print(build(force=True, verbose=True))

@@ -1,0 +1,96 @@
+"""The C-ABI library on the CPU: it builds for sm_103a, loads without a GPU,
+exports every entry point the header declares, and rejects bad arguments on
+the host with the documented status before touching any device state."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import linear_attention_prefill_chunkwise_gb300 as lap
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
+
+LA_OK, LA_INVALID, LA_UNSUPPORTED, LA_CUDA = 0, 1, 2, 3
+
+
+def declared_functions():
+    names = []
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*([a-z_][a-z0-9_]*)\s*\(", text, re.M):
+            names.append(m.group(1))
+    return names
+
+
+def test_header_declares_entry_points():
+    names = declared_functions()
+    assert "la_prefill_fwd" in names
+    assert set(lap.EXPORTED_SYMBOLS) <= set(names)
+
+
+def test_library_loads_and_exports_every_declared_symbol():
+    lib = lap.load_library()
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} not exported"
+    assert lib.la_prefill_smem_bytes() <= 227 * 1024
+    assert lib.la_status_string(LA_UNSUPPORTED) == b"LA_ERR_UNSUPPORTED"
+
+
+FAKE = 0x10000  # never dereferenced: every call below is rejected on the host
+
+
+def call(**over):
+    args = dict(q=FAKE, k=FAKE, v=FAKE, slopes=FAKE, scale=1.0, h0=None, idx=None, cu=None, o=FAKE, hf=None,
+                B=2, T=128, N=2, H=2, HV=2, D=128, V=128, P=0, sched=0, err=None, stream=None)
+    args.update(over)
+    a = args
+    return lap.la_prefill_fwd_raw(a["q"], a["k"], a["v"], a["slopes"], ctypes.c_float(a["scale"]), a["h0"], a["idx"],
+                                  a["cu"], a["o"], a["hf"], a["B"], a["T"], a["N"], a["H"], a["HV"], a["D"], a["V"],
+                                  a["P"], a["sched"], a["err"], a["stream"])
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(D=64), LA_UNSUPPORTED),
+    (dict(V=256), LA_UNSUPPORTED),
+    (dict(H=3, HV=4), LA_UNSUPPORTED),
+    (dict(H=0), LA_INVALID),
+    (dict(N=-1), LA_INVALID),
+    (dict(N=3), LA_INVALID),                     # fixed mode needs N == B
+    (dict(cu=FAKE, B=2), LA_INVALID),            # packed mode needs B == 1
+    (dict(q=FAKE + 2), LA_INVALID),              # misaligned
+    (dict(h0=FAKE + 8), LA_INVALID),
+    (dict(slopes=None), LA_INVALID),
+    (dict(o=None), LA_INVALID),
+    (dict(sched=7), LA_INVALID),
+    (dict(h0=FAKE, P=1), LA_INVALID),            # pool smaller than N without indices
+    (dict(h0=FAKE, idx=FAKE, P=0), LA_INVALID),  # empty pool with indices
+])
+def test_host_validation(over, status):
+    assert call(**over) == status
+    assert lap.load_library().la_last_error() != b""
+
+
+def test_empty_batch_is_a_no_op():
+    assert call(N=0, B=0) == LA_OK
+    assert call(cu=FAKE, B=1, T=0, N=1) == LA_OK  # no tokens and no state requested
+
+
+def test_no_device_is_reported_not_hidden():
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert call() == LA_CUDA
+    assert b"cuda" in lap.load_library().la_last_error().lower() or b"device" in lap.load_library().la_last_error()
+
+
+def test_product_path_does_not_touch_the_oracle():
+    pkg = os.path.join(ROOT, "linear_attention_prefill_chunkwise_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "oracle" not in text.lower(), f"{f} mentions the oracle"
