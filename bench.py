@@ -1,0 +1,399 @@
+"""Benchmark: Lightning Attention chunkwise prefill, tokens/s and fraction of roofline.
+
+Workload: fixed-length MHA prefill, B=2, T=8192, H=HV=64, D=V=128, BF16 q/k/v/o,
+FP32 initial state N(0, 0.02^2) per (sequence, head) read and FP32 final state
+written (the seeded synthetic inputs of workloads.config(2)).  One step = one
+call of la_prefill_fwd over that batch.  The step's inputs (1.07 GB of Q/K/V/O)
+are larger than the 129 MB L2, so no flush is needed between steps.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the FP64 CPU oracle on
+the host cores instead (a bounded sample of the same workload per step).
+"""
+from __future__ import annotations
+
+import argparse
+import datetime
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "LA prefill tokens/s and % of roofline (B=2,T=8192,H=64,D=V=128) on 1 GB300"
+UNIT = "tokens/s"
+WORKLOAD = "fixed MHA prefill B=2 T=8192 H=HV=64 D=V=128, bf16 q/k/v/o, fp32 h0 in + final state out"
+B, T, H, HV, D, V = 2, 8192, 64, 64, 128, 128
+TOKENS = B * T
+# algorithmic bytes per step: Q + K read once per q/k head, V read, O written, h0 read, h_final written
+ALG_BYTES = 2 * TOKENS * H * D * 2 + 2 * TOKENS * HV * V * 2 + 2 * B * HV * V * D * 4
+# dense-tile FLOPs per step: 4*C*D*V + 4*C^2*D per 64-token chunk per value head
+ALG_FLOPS = (TOKENS // 64) * HV * (4 * 64 * D * V + 4 * 64 * 64 * D)
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+KERNEL_NAME = "la_prefill_fwd_kernel"
+KERNEL_SOURCES = ["linear_attention_prefill_chunkwise_gb300/csrc/la_prefill_kernel.cuh",
+                  "linear_attention_prefill_chunkwise_gb300/csrc/sm103_ptx.cuh",
+                  "linear_attention_prefill_chunkwise_gb300/csrc/la_prefill_api.cu"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "la_prefill_fwd_kernel_B2_T8192_H64.dram.txt")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as fh:
+                d = json.load(fh)
+            hbm = d.get("hbm_gbs")
+            if isinstance(hbm, dict):
+                hbm = hbm.get("value")
+            if hbm:
+                return float(hbm), "measured"
+        except (OSError, ValueError):
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def dram_traffic_per_launch():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernel source."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    vals = {}
+    with open(TRAFFIC_FILE) as fh:
+        for line in fh:
+            if "=" in line and not line.lstrip().startswith("#"):
+                k, v = line.split("=", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return int(float(vals["dram_bytes_per_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons; only samples taken inside
+    the marked timed window are summarised."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu = gpu_id
+        self.proc = None
+        self.out = None
+        self.t0 = self.t1 = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def mark_start(self):
+        self.t0 = datetime.datetime.now()
+
+    def mark_end(self):
+        self.t1 = datetime.datetime.now()
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        empty = {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        if not self.out:
+            return empty
+        sm, mx, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                if self.t0 and self.t1 and not (self.t0 <= ts <= self.t1):
+                    continue
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return empty
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "power_w_median": statistics.median(power), "samples": len(sm)}
+
+
+def gpu_id_for_smi(device) -> str:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(device).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except (AttributeError, RuntimeError):
+        return str(device.index)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def make_inputs(device):
+    import numpy as np
+    import torch
+
+    import workloads as W
+    p = W.config(2)
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+    host = {"q": bf(p.q_bits), "k": bf(p.k_bits), "v": bf(p.v_bits), "slopes": torch.from_numpy(p.slopes),
+            "h0": torch.from_numpy(p.h0)}
+    dev = {k_: t.to(device) for k_, t in host.items()}
+    dev["o"] = torch.empty((TOKENS, HV, V), dtype=torch.bfloat16, device=device)
+    dev["h_final"] = torch.empty((B, HV, V, D), dtype=torch.float32, device=device)
+    return p, host, dev
+
+
+def run_cuda(args):
+    import torch
+    import torch.distributed as dist
+
+    import linear_attention_prefill_chunkwise_gb300 as lap
+
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+    p, host, dev = make_inputs(device)
+    scale = p.scale
+
+    def step(d, s):
+        lap.la_prefill_fwd(d["q"], d["k"], d["v"], d["slopes"], scale, h0=d["h0"], o=d["o"],
+                           h_final=d["h_final"], seq_len=T, stream=s)
+
+    def barrier():
+        if world > 1:
+            dist.barrier(device_ids=[device.index])
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step(dev, stream)
+    torch.cuda.synchronize(device)
+
+    # ---- device-resident timing: K steps, one kernel launch each
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    barrier()
+    torch.cuda.synchronize(device)
+    with ClockSampler(gpu_id_for_smi(device)) as clk:
+        time.sleep(0.3)  # let the sampler start before the timed region
+        clk.mark_start()
+        with torch.cuda.stream(stream):
+            ev[0].record(stream)
+            for i in range(args.steps):
+                step(dev, stream)
+                ev[i + 1].record(stream)
+        torch.cuda.synchronize(device)
+        clk.mark_end()
+    barrier()
+    per_launch_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
+    total_ms = ev[0].elapsed_time(ev[-1])
+    if world > 1:
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * TOKENS * args.steps / (total_ms / 1e3)
+
+    # ---- end to end through the public API: pinned host inputs in, results out, every step
+    pinned = {k_: t.pin_memory() for k_, t in host.items()}
+    out_o = torch.empty((TOKENS, HV, V), dtype=torch.bfloat16).pin_memory()
+    out_h = torch.empty((B, HV, V, D), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values())
+    d2h = out_o.numel() * out_o.element_size() + out_h.numel() * out_h.element_size()
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+    scratch = {k_: torch.empty_like(t, device=device) for k_, t in pinned.items()}
+    scratch["o"] = dev["o"]
+    scratch["h_final"] = dev["h_final"]
+
+    def e2e_step():
+        for k_, t in pinned.items():
+            scratch[k_].copy_(t, non_blocking=True)
+        step(scratch, stream)
+        out_o.copy_(scratch["o"], non_blocking=True)
+        out_h.copy_(scratch["h_final"], non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            e2e_step()
+    torch.cuda.synchronize(device)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+    torch.cuda.synchronize(device)
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = world * TOKENS * e2e_steps / (e2e_ms / 1e3)
+
+    if rank == 0:
+        peak, peak_kind = measured_peaks()
+        launch_ms = statistics.fmean(per_launch_ms)
+        achieved = ALG_BYTES / (launch_ms / 1e3) / 1e9
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "global_batch": B * world, "seq_len": T, "heads": H, "value_heads": HV,
+                       "head_dim": D, "chunk": 64, "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (1.07 GB per step), no flush"},
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": dram_traffic_per_launch(),
+                         "peak_source": f"{peak_kind} hbm_gbs", "alg_bytes_per_launch": ALG_BYTES,
+                         "alg_flops_per_launch": ALG_FLOPS, "kernel": KERNEL_NAME,
+                         "launch_ms_mean": round(launch_ms, 5), "launch_ms_min": round(min(per_launch_ms), 5)},
+            "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "steps": e2e_steps},
+            "gpu_launches": args.steps,
+            "clocks": clk.summary(),
+        }
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(p, args.cpu_heads)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def cpu_baseline(p, heads):
+    """The FP64 oracle on the host cores over a bounded sample: both sequences, all T tokens,
+    the first `heads` of the 64 heads.  Reported in full-workload tokens/s (a token = all 64 heads)."""
+    import numpy as np
+
+    import oracle
+    q = p.q()[:, :heads]
+    k = p.k()[:, :heads]
+    v = p.v()[:, :heads]
+    h0 = p.h0[:, :heads].astype(np.float64)
+    threads = oracle.max_threads()
+    t0 = time.perf_counter()
+    oracle.tokenwise(q, k, v, p.slopes[:heads], p.scale, h0=h0, T=T, nthreads=threads)
+    dt = time.perf_counter() - t0
+    equiv_tokens = TOKENS * heads / HV
+    return {"value": round(equiv_tokens / dt, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"B=2 x T=8192 tokens x {heads} of {HV} heads (FP64 tokenwise recurrence, OpenMP over "
+                      f"(sequence, head)); wall {dt:.2f} s"}
+
+
+def oracle_step(p, ntok, nheads):
+    """One reference step: the oracle over sequence 0's first `ntok` tokens and `nheads` heads,
+    with its initial states.  Returns (seconds, full-workload-equivalent tokens, threads)."""
+    import numpy as np
+
+    import oracle
+    q = p.q()[:ntok, :nheads]
+    k = p.k()[:ntok, :nheads]
+    v = p.v()[:ntok, :nheads]
+    h0 = p.h0[:1, :nheads].astype(np.float64)
+    threads = oracle.max_threads()
+    t0 = time.perf_counter()
+    oracle.tokenwise(q, k, v, p.slopes[:nheads], p.scale, h0=h0, T=ntok, nthreads=threads)
+    return time.perf_counter() - t0, ntok * nheads / HV, threads
+
+
+def run_reference(args):
+    """The oracle, as it stands, on the host cores.  Each step is a bounded sample of the
+    workload (one sequence, one head per host thread, a token count sized so that all
+    warm-up and timed steps together take about --ref-budget seconds)."""
+    import workloads as W
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    p = W.config(2)
+    import oracle
+    nheads = max(1, min(HV, oracle.max_threads()))
+    dt, _, _ = oracle_step(p, 256, nheads)  # calibration
+    per_step = args.ref_budget / (args.steps + args.warmup)
+    ntok = int(max(64, min(T, 256 * per_step / max(dt, 1e-6))))
+    for _ in range(args.warmup):
+        oracle_step(p, ntok, nheads)
+    secs, toks = 0.0, 0.0
+    threads = 1
+    for _ in range(args.steps):
+        dt, eq, threads = oracle_step(p, ntok, nheads)
+        secs += dt
+        toks += eq
+    value = toks / secs
+    sample = (f"sequence 0, first {ntok} of {T} tokens, {nheads} of {HV} heads per step, with h0 "
+              f"(FP64 tokenwise recurrence, OpenMP over heads); value in full-workload tokens/s")
+    line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": WORKLOAD, "global_batch": B, "seq_len": T, "heads": H, "value_heads": HV,
+                       "head_dim": D, "chunk": 64, "parallelism": "host cores"},
+            "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["cuda", "reference"], default="cuda")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-heads", type=int, default=64, help="heads in the oracle CPU-baseline sample")
+    ap.add_argument("--ref-budget", type=float, default=60.0, help="seconds for the whole reference arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_cuda(args)
+
+
+if __name__ == "__main__":
+    main()
