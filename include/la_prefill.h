@@ -93,6 +93,17 @@ const char* la_last_error(void);
 /* Size in bytes of dynamic shared memory the kernel requests per CTA. */
 int la_prefill_smem_bytes(void);
 
+/*
+ * Timeline tracing (diagnostics).  A library built with -DLA_TRACE records, for CTA 0
+ * and its first 64 chunks, one %globaltimer stamp (ns) per pipeline event and chunk
+ * into a caller-owned device buffer of la_prefill_trace_events() uint64 values
+ * (event-major: [event][chunk]).  la_prefill_trace_events() returns 0 for a normal
+ * build, whose kernel contains no tracing code.  The buffer pointer is process-global
+ * and used by every later call until it is reset to NULL.
+ */
+int la_prefill_trace_events(void);
+void la_prefill_set_trace_buffer(void* device_buffer);
+
 #ifdef __cplusplus
 }
 #endif

@@ -21,7 +21,8 @@ SCHEDULES = {"auto": 0, "persistent": 1, "non_persistent": 2}
 DEV_ERR_BAD_SEQLENS = 1
 DEV_ERR_BAD_INDEX = 2
 DEV_ERR_TIMEOUT = 4
-EXPORTED_SYMBOLS = ("la_prefill_fwd", "la_status_string", "la_last_error", "la_prefill_smem_bytes")
+EXPORTED_SYMBOLS = ("la_prefill_fwd", "la_status_string", "la_last_error", "la_prefill_smem_bytes",
+                    "la_prefill_trace_events", "la_prefill_set_trace_buffer")
 
 _lock = threading.Lock()
 _lib = None

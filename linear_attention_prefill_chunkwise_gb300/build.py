@@ -16,6 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libla_prefill.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
+TRACE_LIB_PATH = os.path.join(BUILD_DIR, "libla_prefill_trace.so")
 INCLUDE_DIR = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["la_prefill_api.cu"]
@@ -31,31 +32,36 @@ def nvcc_path() -> str:
     return os.path.join(cuda_home, "bin", "nvcc")
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def _stale(path: str) -> bool:
+    if not os.path.exists(path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     deps = [os.path.join(CSRC, d) for d in DEPENDS] + [os.path.join(INCLUDE_DIR, "la_prefill.h")]
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Build the library if any source is newer than it; return its path."""
-    if not force and not _stale():
-        return LIB_PATH
+def build(force: bool = False, verbose: bool = False, trace: bool = False) -> str:
+    """Build the library if any source is newer than it; return its path.
+
+    trace=True builds the timeline-tracing variant (-DLA_TRACE) as a separate file."""
+    out = TRACE_LIB_PATH if trace else LIB_PATH
+    if not force and not _stale(out):
+        return out
     os.makedirs(BUILD_DIR, exist_ok=True)
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = out + f".tmp{os.getpid()}"
     cmd = [nvcc_path(), *ARCH_FLAGS, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
            "-cudart", "static", "-I", INCLUDE_DIR, "-o", tmp] + [os.path.join(CSRC, s) for s in SOURCES]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
+    if trace:
+        cmd.insert(1, "-DLA_TRACE")
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + res.stdout + res.stderr)
     if verbose:
         print(res.stdout + res.stderr)
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, out)
+    return out
 
 
 if __name__ == "__main__":

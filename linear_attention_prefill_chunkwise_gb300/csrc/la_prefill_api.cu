@@ -20,6 +20,7 @@
 namespace {
 
 thread_local char g_last_error[512] = "";
+unsigned long long* g_trace = nullptr;  // device buffer for timeline tracing builds
 
 la_status fail(la_status st, const char* fmt, ...) {
   va_list ap;
@@ -91,6 +92,16 @@ const char* la_status_string(la_status status) {
 const char* la_last_error(void) { return g_last_error; }
 
 int la_prefill_smem_bytes(void) { return smem_bytes(); }
+
+int la_prefill_trace_events(void) {
+#ifdef LA_TRACE
+  return lap::kTrEvents * lap::kTraceChunks;
+#else
+  return 0;
+#endif
+}
+
+void la_prefill_set_trace_buffer(void* device_buffer) { g_trace = static_cast<unsigned long long*>(device_buffer); }
 
 la_status la_prefill_fwd(const void* q, const void* k, const void* v, const float* slopes, float scale,
                          const float* h0, const int32_t* state_indices, const int32_t* cu_seqlens, void* o,
@@ -175,6 +186,7 @@ la_status la_prefill_fwd(const void* q, const void* k, const void* v, const floa
   p.o = static_cast<__nv_bfloat16*>(o);
   p.h_final = h_final;
   p.dev_error = dev_error;
+  p.trace = g_trace;
   p.scale = scale;
   p.num_tokens = static_cast<int>(tokens);
   p.T = cu_seqlens ? 0 : T;

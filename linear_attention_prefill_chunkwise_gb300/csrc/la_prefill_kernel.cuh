@@ -13,30 +13,38 @@
 //   o      = scale * O                               stored as BF16, rows s < L
 //   S     <- lambda^L S + V^T Kt,  Kt[j] = lambda^(L-1-j) k_j   state advance [128 v x 128 k]
 //
-// All four contractions run on the 5th-generation tensor cores (tcgen05.mma, BF16
-// operands, FP32 accumulation in tensor memory).  The outputs are computed
-// transposed (value dimension on the 128 TMEM lanes) so that every contraction except
-// the scores has M = 128.  The decayed operands P, Kt and the FP32 state S are fed to
-// the tensor cores as a BF16 pair hi + lo (hi = bf16(x), lo = bf16(x - hi)), so the
-// products keep ~16 significant bits; only the final output is rounded to BF16 once.
+// All four contractions run on the 5th-generation tensor cores (tcgen05.mma, FP32
+// accumulation in tensor memory).  The outputs are computed transposed (value
+// dimension on the 128 TMEM lanes) so that every contraction except the scores has
+// M = 128.  The inter-chunk decay lambda^(s+1) and the output scale are folded into a
+// converted copy of Q, Qt[s] = scale lambda^(s+1) q_s, and the scale into P, so that
+// O_inter and O_intra accumulate into one accumulator that already holds o.
+// Operand precision:
+//   scores   Q K^T           BF16 x BF16 (the inputs, exact)
+//   O_inter  S Qt^T          TF32 x TF32: the FP32 state as stored (the tensor core keeps
+//                            its top 10 mantissa bits) and Qt rounded to TF32
+//   O_intra  V^T P^T         BF16 x (P_hi + P_lo): P as a BF16 pair, ~16 significant bits
+//   dS       V^T Kt          BF16 x (Kt_hi + Kt_lo)
+// Only the final output is rounded to BF16; the state itself stays FP32 throughout.
 //
 // Warp-specialised pipeline, 512 threads per CTA, one CTA per SM:
-//   warp 0       TMA producer: Q/K/V chunk tiles into a kStages-deep shared-memory ring
+//   warp 0       TMA producer: Q/K chunk tiles into a 2-stage ring, V tiles into a 3-stage ring
 //   warp 1       TMEM allocator and the single MMA-issuing thread
-//   warps 2-3    idle
+//   warps 2-3    Q converter: BF16 Q tile -> Qt = scale lambda^(s+1) q in TF32 (B operand of
+//                O_inter), 2 buffers
 //   warps 4-11   state warpgroups: thread (quadrant qd, lane) of warpgroup wg owns state
 //                row v = 32 qd + lane, columns k in [64 wg, 64 wg + 64), in registers;
-//                they advance the state and write the output of their half of the chunk
+//                they advance the state, publish it to TMEM and write the output
 //   warps 12-15  operand warpgroup: builds the decayed BF16 hi/lo operands Kt and P
 //
-// Only the state advance and the inter-chunk MMA that reads it form a serial chain
-// from chunk to chunk; scores, P, Kt, O_intra and Delta S of later chunks are built
-// and multiplied ahead of it.  Per chunk i (a CTA-wide running chunk counter) the
-// MMA thread issues, in order:
-//   scores(i)    after stage i is loaded and the operand warpgroup read scores(i-1)
+// Per chunk i (a CTA-wide running chunk counter) the MMA thread issues, in order:
+//   scores(i+1)  one chunk ahead: after stage i+1 is loaded and scores(i) was read
 //   dS(i)        after Kt(i) is built and the state warpgroups read dS(i-1)
-//   O_intra(i)   after P(i) is built and the state warpgroups read O(i-1)
-//   O_inter(i)   after the state warpgroups wrote S(i) as hi/lo into TMEM
+//   O_inter(i)   into O[i%2], after S(i) is published, Qt(i) converted, O(i-2) read
+//                (the Q/K stage of chunk i is released as soon as Kt(i) and Qt(i) are built)
+//   O_intra(i)   accumulated into O[i%2], after P(i) is built
+// The serial chain from chunk to chunk is only: O_inter(i) done -> S(i+1) written to
+// TMEM -> O_inter(i+1); everything else is built ahead of it.
 #pragma once
 
 #include <cuda.h>
@@ -49,50 +57,55 @@ namespace lap {
 
 constexpr int kChunk = 64;        // tokens per chunk
 constexpr int kDim = 128;         // D = V = 128
-constexpr int kStages = 3;        // Q/K/V ring depth
+constexpr int kQKStages = 2;      // Q/K ring depth (released early: after scores, Kt, Qt)
+constexpr int kVStages = 3;       // V ring depth (held until O_intra)
 constexpr int kThreads = 512;
+constexpr int kConvThreads = 64;      // warps 2-3
 constexpr int kStateThreads = 256;    // warps 4-11
 constexpr int kOperandThreads = 128;  // warps 12-15
-constexpr uint32_t kTileBytes = 8192;             // one 64 x 64 BF16 box (128-byte rows)
-constexpr uint32_t kStageBytes = 6 * kTileBytes;  // Q, K, V: two boxes each
+constexpr uint32_t kTileBytes = 8192;  // one 64 x 64 BF16 box (128-byte rows)
 
 // TMEM column map (512 columns allocated, 128 lanes x 32 bit each)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColScores = 0;    // A = Q K^T, M = 64 accumulator, 64 columns
-constexpr uint32_t kColOIntra = 64;   // (V^T P^T), lanes = v, 64 columns = s
-constexpr uint32_t kColOInter = 128;  // (S Q^T),   lanes = v, 64 columns = s
-constexpr uint32_t kColDeltaS = 256;  // V^T Kt,    lanes = v, 128 columns = k
-constexpr uint32_t kColStateHi = 384; // S hi as MMA A operand: lanes = v, 64 columns = k pairs
-constexpr uint32_t kColStateLo = 448; // S lo
+constexpr uint32_t kColO = 64;        // O^T = S Qt^T + V^T P^T, 2 buffers of 64 columns (lanes = v, columns = s)
+constexpr uint32_t kColDeltaS = 256;  // V^T Kt, lanes = v, 128 columns = k
+constexpr uint32_t kColState = 384;   // S (TF32) as the A operand of O_inter: lanes = v, 128 columns = k
 
-constexpr int kLamStride = 68;  // floats per per-warp lambda^n table (65 used)
+constexpr int kTabStride = 68;  // per operand warp: lambda^n for n = 0..64
 
-struct __align__(1024) StageTiles {
+struct __align__(1024) QKTiles {
   uint8_t q[2][kTileBytes];  // [64 tokens][64 dims] x 2 halves of D, 128B-swizzled
   uint8_t k[2][kTileBytes];
-  uint8_t v[2][kTileBytes];
 };
 
 struct __align__(1024) SharedStorage {
-  StageTiles stage[kStages];
-  uint8_t p_hi[2][kTileBytes];   // P [64 s][64 j], K-major B operand of O_intra, 2 buffers
-  uint8_t p_lo[2][kTileBytes];
+  QKTiles qk[kQKStages];
+  uint8_t v[kVStages][2][kTileBytes];  // V [64 tokens][64 dims] x 2 halves, 128B-swizzled
+  uint8_t qt[2][4][kTileBytes];  // Qt, TF32 [64 s][128 d] (4 boxes of 32 d), K-major B of O_inter; 2 buffers
+  uint8_t p_hi[kTileBytes];      // P [64 s][64 j], K-major B operand of O_intra
+  uint8_t p_lo[kTileBytes];
   uint8_t kt_hi[2][kTileBytes];  // Kt [64 j][128 k] (2 boxes of 64 k), MN-major B operand of dS
   uint8_t kt_lo[2][kTileBytes];
-  float lam[12][kLamStride];     // per compute warp: lambda^n, n = 0..64, for that warp's current unit
-  uint64_t full_bar[kStages];    // stage loaded (TMA transaction bytes)
-  uint64_t empty_bar[kStages];   // stage consumed by every MMA that reads it
+  float tab[4][kTabStride];      // per operand warp: lambda^n for its current unit
+  uint64_t qk_full[kQKStages];   // Q/K stage loaded (TMA transaction bytes)
+  uint64_t qk_empty[kQKStages];  // Q/K stage consumed (scores MMA, Kt and Qt builders)
+  uint64_t v_full[kVStages];     // V stage loaded
+  uint64_t v_empty[kVStages];    // V stage consumed (dS and O_intra MMAs)
   uint64_t scores_full;          // MMA -> operand wg
   uint64_t scores_free;          // operand wg -> MMA
   uint64_t kt_ready;             // operand wg -> MMA
   uint64_t kt_free;              // MMA -> operand wg
-  uint64_t p_ready[2];           // operand wg -> MMA
-  uint64_t p_free[2];            // MMA -> operand wg
+  uint64_t p_ready;              // operand wg -> MMA
+  uint64_t p_free;               // MMA -> operand wg
+  uint64_t qt_ready[2];          // converter -> MMA
+  uint64_t qt_free[2];           // MMA -> converter (O_inter done reading Qt)
   uint64_t ds_full;              // MMA -> state wgs
   uint64_t ds_free;              // state wgs -> MMA
-  uint64_t s_ready;              // state wgs -> MMA (S hi/lo written)
-  uint64_t o_full;               // MMA -> state wgs (O_intra, O_inter done; S hi/lo free)
-  uint64_t o_free;               // state wgs -> MMA
+  uint64_t s_ready;              // state wgs -> MMA (S written to TMEM)
+  uint64_t s_free;               // MMA -> state wgs (O_inter done reading S)
+  uint64_t o_full[2];            // MMA -> state wgs (O(i) complete)
+  uint64_t o_free[2];            // state wgs -> MMA
   uint64_t final_bar;            // every MMA retired (teardown)
   uint32_t tmem_base;
   int abort;
@@ -106,6 +119,7 @@ struct KernelParams {
   __nv_bfloat16* o;
   float* h_final;
   int* dev_error;
+  unsigned long long* trace;  // per-chunk timestamps of CTA 0 (builds with LA_TRACE only)
   float scale;
   int num_tokens;
   int T;          // fixed-length mode sequence length
@@ -162,6 +176,40 @@ __device__ __forceinline__ Unit decode_unit(const KernelParams& p, int u) {
   return w;
 }
 
+// ---- optional timeline tracing (compiled in with -DLA_TRACE): one %globaltimer stamp
+// per (event, chunk) for the first kTraceChunks chunks of CTA 0, written by one thread of
+// the role that reaches the event.
+enum TraceEvent {
+  kTrProducerIssue = 0,  // producer: stage free, TMA loads issued
+  kTrMmaScores,          // MMA: scores of chunk i issued (one chunk ahead)
+  kTrMmaDeltaS,          // MMA: Kt ready, dS issued
+  kTrMmaOInter,          // MMA: S and Q ready, O_inter issued
+  kTrMmaOIntra,          // MMA: P ready, O_intra issued
+  kTrOperKtStart,        // operand wg: stage loaded, Kt build starts
+  kTrOperKtDone,         // operand wg: Kt published
+  kTrOperScores,         // operand wg: scores available
+  kTrOperPDone,          // operand wg: P published
+  kTrConvDone,           // converter: Qt(i) published
+  kTrStateDeltaS,        // state wgs: dS available
+  kTrStateUpdated,       // state wgs: S advanced in registers, dS released
+  kTrStateOInter,        // state wgs: O_inter(i) complete (S free)
+  kTrStateSReady,        // state wgs: S(i+1) published
+  kTrStateEpilogue,      // state wgs: O(i) stored, accumulators released
+  kTrEvents
+};
+constexpr int kTraceChunks = 64;
+#ifdef LA_TRACE
+#define LA_TRACE_AT(p, ev, it, who)                                                          \
+  do {                                                                                       \
+    if ((who) && (p).trace && blockIdx.x == 0 && (it) < static_cast<uint32_t>(kTraceChunks)) \
+      (p).trace[(ev) * kTraceChunks + (it)] = globaltimer_ns();                              \
+  } while (0)
+#else
+#define LA_TRACE_AT(p, ev, it, who) \
+  do {                              \
+  } while (0)
+#endif
+
 // Byte offset of 16-byte chunk c (0..7) of row r inside a 128-byte-swizzled tile.
 __device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t c) { return r * 128u + ((c ^ (r & 7u)) << 4); }
 
@@ -172,12 +220,24 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, ok);
 }
 
-// lambda^n for n = 0..64 into the calling warp's own table; lambda^0 is exactly 1.
+// The calling warp's lambda^n table (n = 0..64, lambda^0 exactly 1) for a new unit.
 // Warp-local (two __syncwarp), so no role ever waits on another warp outside an mbarrier.
-__device__ __forceinline__ void fill_lambda_table(float* tab, float slope, int lane) {
+__device__ __forceinline__ float* fill_lambda_table(SharedStorage& sm, int warp, int lane, float slope) {
+  float* tab = sm.tab[warp];
   __syncwarp();  // every lane is done with the previous unit's table
   for (int t = lane; t <= kChunk; t += 32) tab[t] = t == 0 ? 1.f : expf(-slope * static_cast<float>(t));
   __syncwarp();
+  return tab;
+}
+
+// Number of chunks this CTA processes (all roles walk the same units in the same order).
+__device__ __forceinline__ uint32_t cta_chunk_count(const KernelParams& p) {
+  uint32_t n = 0;
+  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+    const Unit w = decode_unit(p, u);
+    if (w.run) n += w.nchunks;
+  }
+  return n;
 }
 
 // ------------------------------------------------------------------------------ roles
@@ -185,221 +245,295 @@ __device__ __forceinline__ void fill_lambda_table(float* tab, float slope, int l
 __device__ __forceinline__ void producer_loop(SharedStorage& sm, const KernelParams& p, const CUtensorMap* tm_q,
                                               const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                               volatile int* abort) {
-  uint32_t it = 0;
+  uint32_t nqk = 0, nv = 0;  // chunks whose Q/K (V) loads have been issued
   bool ok = true;
   for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
     const Unit w = decode_unit(p, u);
     if (!w.run) continue;
-    for (int c = 0; c < w.nchunks; ++c, ++it) {
-      const uint32_t st = it % kStages;
-      if (!mbar_wait(&sm.empty_bar[st], ((it / kStages) & 1u) ^ 1u, abort)) {
+    for (int c = 0; c < w.nchunks; ++c) {
+      const int row = w.bos + c * kChunk;
+      const uint32_t it = nqk;
+      const uint32_t sq = it % kQKStages, sv = it % kVStages;
+      if (!mbar_wait(&sm.qk_empty[sq], ((it / kQKStages) & 1u) ^ 1u, abort)) {
         ok = false;
         break;
       }
-      mbar_arrive_expect_tx(&sm.full_bar[st], kStageBytes);
-      const int row = w.bos + c * kChunk;
-      StageTiles& t = sm.stage[st];
+      LA_TRACE_AT(p, kTrProducerIssue, it, true);
+      mbar_arrive_expect_tx(&sm.qk_full[sq], 4 * kTileBytes);
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        tma_load_2d(t.q[h], tm_q, &sm.full_bar[st], w.hq * kDim + 64 * h, row);
-        tma_load_2d(t.k[h], tm_k, &sm.full_bar[st], w.hq * kDim + 64 * h, row);
-        tma_load_2d(t.v[h], tm_v, &sm.full_bar[st], w.hv * kDim + 64 * h, row);
+        tma_load_2d(sm.qk[sq].q[h], tm_q, &sm.qk_full[sq], w.hq * kDim + 64 * h, row);
+        tma_load_2d(sm.qk[sq].k[h], tm_k, &sm.qk_full[sq], w.hq * kDim + 64 * h, row);
       }
+      ++nqk;
+      if (!mbar_wait(&sm.v_empty[sv], ((it / kVStages) & 1u) ^ 1u, abort)) {
+        ok = false;
+        break;
+      }
+      mbar_arrive_expect_tx(&sm.v_full[sv], 2 * kTileBytes);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) tma_load_2d(sm.v[sv][h], tm_v, &sm.v_full[sv], w.hv * kDim + 64 * h, row);
+      ++nv;
     }
   }
-  // Before leaving, make sure no load this thread issued is still writing shared memory.
-  const uint32_t outstanding = it < kStages ? it : kStages;
-  for (uint32_t i = 0; i < outstanding; ++i) {
-    const uint32_t j = it - 1 - i;
-    mbar_wait(&sm.full_bar[j % kStages], (j / kStages) & 1u, abort);
+  // Before leaving, make sure no load this thread issued is still writing shared memory:
+  // wait for the most recent phase of every ring slot that was armed.
+  for (uint32_t i = 0; i < kQKStages && i < nqk; ++i) {
+    const uint32_t j = nqk - 1 - i;
+    mbar_wait(&sm.qk_full[j % kQKStages], (j / kQKStages) & 1u, abort);
+  }
+  for (uint32_t i = 0; i < kVStages && i < nv; ++i) {
+    const uint32_t j = nv - 1 - i;
+    mbar_wait(&sm.v_full[j % kVStages], (j / kVStages) & 1u, abort);
   }
 }
 
+// Shared-memory descriptors are built once; per K step only the 14-bit start-address
+// field changes, by a compile-time byte offset (>> 4) added to the low word.  This keeps
+// the single issuing thread to a few instructions per MMA, so issue never limits the
+// tensor pipe (rebuilding both 64-bit descriptors per MMA costs more than an N = 128 MMA).
+__device__ __forceinline__ uint64_t desc_at(uint64_t base, uint32_t byte_off) { return base + (byte_off >> 4); }
+
 __device__ __forceinline__ void mma_loop(SharedStorage& sm, const KernelParams& p, uint32_t tmem,
                                          volatile int* abort) {
-  const uint32_t id_scores = idesc_bf16_f32(64, 64, false, false);   // Q (K-major) x K (K-major)
-  const uint32_t id_ointra = idesc_bf16_f32(128, 64, true, false);   // V^T (MN-major) x P (K-major)
-  const uint32_t id_ointer = idesc_bf16_f32(128, 64, false, false);  // S (TMEM) x Q (K-major)
-  const uint32_t id_dstate = idesc_bf16_f32(128, 128, true, true);   // V^T (MN-major) x Kt (MN-major)
-  const uint32_t kt_hi = smem_u32(sm.kt_hi), kt_lo = smem_u32(sm.kt_lo);
-  uint32_t it = 0;
-  bool ok = true;
-  for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-    const Unit w = decode_unit(p, u);
-    if (!w.run) continue;
-    for (int c = 0; c < w.nchunks; ++c, ++it) {
-      const uint32_t st = it % kStages;
-      const uint32_t ph = it & 1u;
-      const uint32_t pb = it & 1u;          // P buffer
-      const uint32_t pph = (it >> 1) & 1u;  // its phase
-      const uint32_t q0 = smem_u32(sm.stage[st].q), k0 = smem_u32(sm.stage[st].k);
-      const uint32_t v0 = smem_u32(sm.stage[st].v);
+  constexpr uint32_t id_scores = idesc_bf16_f32(64, 64, false, false);   // Q (K-major) x K (K-major)
+  constexpr uint32_t id_dstate = idesc_bf16_f32(128, 128, true, true);   // V^T (MN-major) x Kt (MN-major)
+  constexpr uint32_t id_ointer = idesc_tf32_f32(128, 64, false, false);  // S (TMEM) x Qt (K-major)
+  constexpr uint32_t id_ointra = idesc_bf16_f32(128, 64, true, false);   // V^T (MN-major) x P (K-major)
+  // K-major operands: sbo = 1024 (8 rows of 128 B); MN-major: lbo = 8192 (next 64-wide box), sbo = 1024
+  const uint64_t dq0 = sdesc_sw128(smem_u32(sm.qk[0].q), 16, 1024);
+  const uint64_t dk0 = sdesc_sw128(smem_u32(sm.qk[0].k), 16, 1024);
+  const uint64_t qk_step = sizeof(QKTiles) >> 4;  // descriptor distance between Q/K stages
+  const uint64_t dv0 = sdesc_sw128(smem_u32(sm.v[0]), kTileBytes, 1024);
+  const uint64_t v_step = (2 * kTileBytes) >> 4;
+  const uint64_t dqt0 = sdesc_sw128(smem_u32(sm.qt[0]), 16, 1024);
+  const uint64_t qt_step = (4 * kTileBytes) >> 4;
+  const uint64_t dkt_hi = sdesc_sw128(smem_u32(sm.kt_hi), kTileBytes, 1024);
+  const uint64_t dkt_lo = sdesc_sw128(smem_u32(sm.kt_lo), kTileBytes, 1024);
+  const uint64_t dp_hi = sdesc_sw128(smem_u32(sm.p_hi), 16, 1024);
+  const uint64_t dp_lo = sdesc_sw128(smem_u32(sm.p_lo), 16, 1024);
+  const uint32_t t_scores = tmem + kColScores, t_ds = tmem + kColDeltaS, t_state = tmem + kColState;
 
-      // scores A = Q K^T : M=64, N=64, K=128 (8 steps of 16)
-      if (!mbar_wait(&sm.full_bar[st], (it / kStages) & 1u, abort) || !mbar_wait(&sm.scores_free, ph ^ 1u, abort)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
+  const uint32_t total = cta_chunk_count(p);
+  // scores(j) = Q K^T of chunk j : M=64, N=64, K=128 (8 steps of 16)
+  auto issue_scores = [&](uint32_t j) -> bool {
+    const uint32_t sq = j % kQKStages;
+    if (!mbar_wait(&sm.qk_full[sq], (j / kQKStages) & 1u, abort)) return false;
+    if (j > 0 && !mbar_wait(&sm.scores_free, (j - 1) & 1u, abort)) return false;
+    tc_fence_after();
+    LA_TRACE_AT(p, kTrMmaScores, j, true);
+    const uint64_t q0 = dq0 + sq * qk_step, k0 = dk0 + sq * qk_step;
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) {
-        const uint32_t off = (kk >> 2) * kTileBytes + (kk & 3) * 32;
-        mma_ss(tmem + kColScores, sdesc_sw128(q0 + off, 16, 1024), sdesc_sw128(k0 + off, 16, 1024), id_scores,
-               kk > 0);
-      }
-      mma_commit(&sm.scores_full);
-
-      // Delta S = V^T (Kt_hi + Kt_lo) : M=128, N=128, K=64
-      if (!mbar_wait(&sm.kt_ready, ph, abort) || !mbar_wait(&sm.ds_free, ph ^ 1u, abort)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        const uint32_t kb = part ? kt_lo : kt_hi;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ss(tmem + kColDeltaS, sdesc_sw128(v0 + kk * 2048, kTileBytes, 1024),
-                 sdesc_sw128(kb + kk * 2048, kTileBytes, 1024), id_dstate, (part | kk) != 0);
-      }
-      mma_commit(&sm.ds_full);
-      mma_commit(&sm.kt_free);
-
-      // O_intra^T = V^T (P_hi + P_lo)^T : M=128, N=64, K=64
-      if (!mbar_wait(&sm.p_ready[pb], pph, abort) || !mbar_wait(&sm.o_free, ph ^ 1u, abort)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t p_hi = smem_u32(sm.p_hi[pb]), p_lo = smem_u32(sm.p_lo[pb]);
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        const uint32_t pbase = part ? p_lo : p_hi;
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ss(tmem + kColOIntra, sdesc_sw128(v0 + kk * 2048, kTileBytes, 1024),
-                 sdesc_sw128(pbase + kk * 32, 16, 1024), id_ointra, (part | kk) != 0);
-      }
-
-      // O_inter^T = (S_hi + S_lo) Q^T : M=128, N=64, K=128, A from TMEM
-      if (!mbar_wait(&sm.s_ready, ph, abort)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-#pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        const uint32_t a0 = tmem + (part ? kColStateLo : kColStateHi);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint32_t off = (kk >> 2) * kTileBytes + (kk & 3) * 32;
-          mma_ts(tmem + kColOInter, a0 + kk * 8, sdesc_sw128(q0 + off, 16, 1024), id_ointer, (part | kk) != 0);
-        }
-      }
-      mma_commit(&sm.o_full);
-      mma_commit(&sm.p_free[pb]);
-      mma_commit(&sm.empty_bar[st]);
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint32_t off = (kk >> 2) * kTileBytes + (kk & 3) * 32;
+      mma_ss(t_scores, desc_at(q0, off), desc_at(k0, off), id_scores, kk > 0);
     }
+    mma_commit(&sm.scores_full);
+    return true;
+  };
+
+  bool ok = total == 0 || issue_scores(0);
+  for (uint32_t it = 0; it < total && ok; ++it) {
+    const uint32_t sq = it % kQKStages, sv = it % kVStages;
+    const uint32_t ph = it & 1u;
+    const uint32_t b = it & 1u, bph = (it >> 1) & 1u;  // double-buffered Qt and O
+    const uint64_t v0 = dv0 + sv * v_step;
+
+    if (it + 1 < total && !issue_scores(it + 1)) break;
+
+    // Delta S = V^T (Kt_hi + Kt_lo) : M=128, N=128, K=64
+    if (!mbar_wait(&sm.v_full[sv], (it / kVStages) & 1u, abort) || !mbar_wait(&sm.kt_ready, ph, abort) ||
+        !mbar_wait(&sm.ds_free, ph ^ 1u, abort))
+      break;
+    tc_fence_after();
+    LA_TRACE_AT(p, kTrMmaDeltaS, it, true);
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_ss(t_ds, desc_at(v0, kk * 2048), desc_at(part ? dkt_lo : dkt_hi, kk * 2048), id_dstate,
+               (part | kk) != 0);
+    }
+    mma_commit(&sm.ds_full);
+    mma_commit(&sm.kt_free);
+
+    // Qt(i) is built too: every reader of the Q/K stage of chunk i is done once scores(i) retires.
+    if (!mbar_wait(&sm.qt_ready[b], bph, abort)) break;
+    mma_commit(&sm.qk_empty[sq]);
+
+    // O^T = S Qt^T : M=128, N=64, K=128 in TF32 (16 steps of 8), A = S from TMEM; starts O[b]
+    if (!mbar_wait(&sm.s_ready, ph, abort) || !mbar_wait(&sm.o_free[b], bph ^ 1u, abort)) break;
+    tc_fence_after();
+    LA_TRACE_AT(p, kTrMmaOInter, it, true);
+    const uint32_t t_o = tmem + kColO + 64 * b;
+    const uint64_t qt0 = dqt0 + b * qt_step;
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      const uint32_t off = (kk >> 2) * kTileBytes + (kk & 3) * 32;
+      mma_tf32_ts(t_o, t_state + kk * 8, desc_at(qt0, off), id_ointer, kk > 0);
+    }
+    mma_commit(&sm.s_free);
+    mma_commit(&sm.qt_free[b]);
+
+    // O^T += V^T (P_hi + P_lo)^T : M=128, N=64, K=64
+    if (!mbar_wait(&sm.p_ready, ph, abort)) break;
+    tc_fence_after();
+    LA_TRACE_AT(p, kTrMmaOIntra, it, true);
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_ss(t_o, desc_at(v0, kk * 2048), desc_at(part ? dp_lo : dp_hi, kk * 32), id_ointra, 1);
+    }
+    mma_commit(&sm.o_full[b]);
+    mma_commit(&sm.p_free);
+    mma_commit(&sm.v_empty[sv]);
   }
   // Retire every MMA before the accumulators are released.
   mma_commit(&sm.final_bar);
   mbar_wait(&sm.final_bar, 0, abort);
 }
 
-// Operand warpgroup: Kt = lambda^(L-1-j) k_j and P = A * lambda^(s-j) (causal, tail masked), as BF16 hi/lo.
-__device__ __forceinline__ void operand_loop(SharedStorage& sm, const KernelParams& p, uint32_t tmem, int otid,
+// Q converter (warps 2-3): the BF16 Q tile (K-major, 128B-swizzled, 2 boxes of 64 d) into
+// Qt = scale lambda^(s+1) q rounded to TF32 (K-major, 128B-swizzled, 4 boxes of 32 d).
+// Thread t owns token row s = t of the chunk.
+__device__ __forceinline__ void convert_loop(SharedStorage& sm, const KernelParams& p, int ctid,
                                              volatile int* abort) {
-  const int warp = otid >> 5, lane = otid & 31;
-  const int qd = warp & 3;  // TMEM lane quadrant (warps 12..15 -> 0..3)
-  const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
+  const int s = ctid;
   uint32_t it = 0;
   bool ok = true;
   for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
     const Unit w = decode_unit(p, u);
     if (!w.run) continue;
-    float* lam = sm.lam[8 + warp];
-    fill_lambda_table(lam, __ldg(p.slopes + w.hv), lane);
+    const float f = p.scale * expf(-__ldg(p.slopes + w.hv) * static_cast<float>(s + 1));  // scale lambda^(s+1)
+    const uint64_t ff = f2_pack(f, f);
     for (int c = 0; c < w.nchunks; ++c, ++it) {
-      const uint32_t st = it % kStages;
-      const uint32_t ph = it & 1u;
-      const uint32_t pb = it & 1u, pph = (it >> 1) & 1u;
-      const int L = min(kChunk, w.len - c * kChunk);
-
-      // ---- Kt: same swizzled layout as the K tile; thread -> row j, one of the two 64-column boxes
-      if (!warp_wait(&sm.full_bar[st], (it / kStages) & 1u, abort) || !warp_wait(&sm.kt_free, ph ^ 1u, abort)) {
+      const uint32_t sq = it % kQKStages, qph = (it / kQKStages) & 1u;
+      const uint32_t b = it & 1u, bph = (it >> 1) & 1u;
+      if (!warp_wait(&sm.qk_full[sq], qph, abort) || !warp_wait(&sm.qt_free[b], bph ^ 1u, abort)) {
         ok = false;
         break;
       }
-      {
-        const int j = otid >> 1, box = otid & 1;
-        const float wj = (j < L) ? lam[L - 1 - j] : 0.f;
-        const uint8_t* ksrc = sm.stage[st].k[box];
+#pragma unroll 1
+      for (int h = 0; h < 2; ++h) {
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
-          const uint32_t off = swz(j, cc);
+          const uint4 x = *reinterpret_cast<const uint4*>(sm.qk[sq].q[h] + swz(s, cc));
+          uint8_t* dst = sm.qt[b][2 * h + (cc >> 2)];
+          const uint32_t fc = 2 * (cc & 3);
+          const float2 q0 = f2_unpack(f2_mul(ff, bf16x2_to_f2(x.x))), q1 = f2_unpack(f2_mul(ff, bf16x2_to_f2(x.y)));
+          const float2 q2 = f2_unpack(f2_mul(ff, bf16x2_to_f2(x.z))), q3 = f2_unpack(f2_mul(ff, bf16x2_to_f2(x.w)));
+          *reinterpret_cast<uint4*>(dst + swz(s, fc)) =
+              make_uint4(round_tf32(q0.x), round_tf32(q0.y), round_tf32(q1.x), round_tf32(q1.y));
+          *reinterpret_cast<uint4*>(dst + swz(s, fc + 1)) =
+              make_uint4(round_tf32(q2.x), round_tf32(q2.y), round_tf32(q3.x), round_tf32(q3.y));
+        }
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&sm.qt_ready[b]);
+      LA_TRACE_AT(p, kTrConvDone, it, ctid == 0);
+    }
+  }
+}
+
+// Operand warpgroup: Kt = lambda^(L-1-j) k_j and P = A * lambda^(s-j) (causal, tail masked), as BF16 hi/lo.
+__device__ __forceinline__ void operand_loop(SharedStorage& sm, const KernelParams& p, uint32_t tmem, int otid,
+                                             volatile int* abort) {
+  const int warp = otid >> 5, lane = otid & 31;
+  const int qd = warp;                     // TMEM lane quadrant (warps 12..15 -> 0..3)
+  const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
+  const int prow = 16 * qd + (lane & 15);  // P: score row s of this thread
+  const int pcol = 32 * (lane >> 4);       //    and its first column j
+  const int krow = otid & 63;              // Kt: token row j of this thread
+  const int kbox = otid >> 6;              //     and its 64-column box of k
+  uint32_t it = 0;
+  bool ok = true;
+  for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+    const Unit w = decode_unit(p, u);
+    if (!w.run) continue;
+    const float* lam = fill_lambda_table(sm, warp, lane, __ldg(p.slopes + w.hv));
+    // decay row of P for this thread: scale lambda^(s-j) for j <= s, 0 above the diagonal
+    float drow[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) drow[i] = (pcol + i <= prow) ? p.scale * lam[max(prow - pcol - i, 0)] : 0.f;
+    for (int c = 0; c < w.nchunks; ++c, ++it) {
+      const uint32_t sq = it % kQKStages, qph = (it / kQKStages) & 1u;
+      const uint32_t ph = it & 1u;
+      const int L = min(kChunk, w.len - c * kChunk);
+
+      // ---- Kt: same swizzled layout as the K tile
+      if (!warp_wait(&sm.qk_full[sq], qph, abort) || !warp_wait(&sm.kt_free, ph ^ 1u, abort)) {
+        ok = false;
+        break;
+      }
+      LA_TRACE_AT(p, kTrOperKtStart, it, otid == 0);
+      {
+        const float wjf = (krow < L) ? lam[L - 1 - krow] : 0.f;
+        const uint64_t wj = f2_pack(wjf, wjf);
+        const uint8_t* ksrc = sm.qk[sq].k[kbox];
+#pragma unroll 4
+        for (int cc = 0; cc < 8; ++cc) {
+          const uint32_t off = swz(krow, cc);
           const uint4 kx = *reinterpret_cast<const uint4*>(ksrc + off);
           const uint32_t kw[4] = {kx.x, kx.y, kx.z, kx.w};
           uint32_t hi[4], lo[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) split_bf16x2(wj * bf16lo_to_f32(kw[e]), wj * bf16hi_to_f32(kw[e]), hi[e], lo[e]);
-          *reinterpret_cast<uint4*>(sm.kt_hi[box] + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(sm.kt_lo[box] + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          for (int e = 0; e < 4; ++e) split_bf16x2(f2_mul(wj, bf16x2_to_f2(kw[e])), hi[e], lo[e]);
+          *reinterpret_cast<uint4*>(sm.kt_hi[kbox] + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(sm.kt_lo[kbox] + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
       }
       fence_proxy_async_smem();
       mbar_arrive(&sm.kt_ready);
+      LA_TRACE_AT(p, kTrOperKtDone, it, otid == 0);
 
-      // ---- P from the scores (M = 64 layout: row s in lane 32*(s/16) + s%16, lanes 16..31 unused)
+      // ---- P from the scores: row prow, columns pcol .. pcol + 31 (16x32bx2 loads use all 32 lanes)
       if (!warp_wait(&sm.scores_full, ph, abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      if (!warp_wait(&sm.p_free[pb], pph ^ 1u, abort)) {
+      LA_TRACE_AT(p, kTrOperScores, it, otid == 0);
+      float a[2][16];
+      tmem_ld16_x2split32(tmem + lane_base + kColScores, a[0]);
+      tmem_ld16_x2split32(tmem + lane_base + kColScores + 16, a[1]);
+      tc_fence_before();
+      mbar_arrive(&sm.scores_free);
+      if (!warp_wait(&sm.p_free, ph ^ 1u, abort)) {
         ok = false;
         break;
       }
+      {
+        const bool full = (L == kChunk);
 #pragma unroll
-      for (int gh = 0; gh < 2; ++gh) {  // columns j = 32 gh .. 32 gh + 31
-        float a[2][16];
-        tmem_ld16(tmem + lane_base + kColScores + 32 * gh, a[0]);
-        tmem_ld16(tmem + lane_base + kColScores + 32 * gh + 16, a[1]);
-        if (gh == 1) {
-          tc_fence_before();
-          mbar_arrive(&sm.scores_free);
-        }
-        if (lane < 16) {
-          const int s = 16 * qd + lane;
+        for (int g = 0; g < 2; ++g) {  // 16 columns -> 16-byte chunks (pcol/8) + 2g, +1
+          uint32_t hi[8], lo[8];
 #pragma unroll
-          for (int g2 = 0; g2 < 2; ++g2) {  // 16 columns -> 16-byte chunks 2g, 2g+1
-            const int g = 2 * gh + g2;
-            uint32_t hi[8], lo[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int j0 = 16 * g + 2 * i, j1 = j0 + 1;
-              const float p0 = (j0 <= s && j0 < L) ? a[g2][2 * i] * lam[max(s - j0, 0)] : 0.f;
-              const float p1 = (j1 <= s && j1 < L) ? a[g2][2 * i + 1] * lam[max(s - j1, 0)] : 0.f;
-              split_bf16x2(p0, p1, hi[i], lo[i]);
+          for (int i = 0; i < 8; ++i) {
+            const int i0 = 16 * g + 2 * i;
+            uint64_t pp = f2_mul(f2_pack(a[g][2 * i], a[g][2 * i + 1]), f2_pack(drow[i0], drow[i0 + 1]));
+            if (!full) {
+              const float2 v = f2_unpack(pp);
+              pp = f2_pack((pcol + i0 < L) ? v.x : 0.f, (pcol + i0 + 1 < L) ? v.y : 0.f);
             }
+            split_bf16x2(pp, hi[i], lo[i]);
+          }
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const uint32_t off = swz(s, 2 * g + h);
-              *reinterpret_cast<uint4*>(sm.p_hi[pb] + off) =
-                  make_uint4(hi[4 * h], hi[4 * h + 1], hi[4 * h + 2], hi[4 * h + 3]);
-              *reinterpret_cast<uint4*>(sm.p_lo[pb] + off) =
-                  make_uint4(lo[4 * h], lo[4 * h + 1], lo[4 * h + 2], lo[4 * h + 3]);
-            }
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t off = swz(prow, (pcol >> 3) + 2 * g + h);
+            *reinterpret_cast<uint4*>(sm.p_hi + off) = make_uint4(hi[4 * h], hi[4 * h + 1], hi[4 * h + 2], hi[4 * h + 3]);
+            *reinterpret_cast<uint4*>(sm.p_lo + off) = make_uint4(lo[4 * h], lo[4 * h + 1], lo[4 * h + 2], lo[4 * h + 3]);
           }
         }
       }
       fence_proxy_async_smem();
-      mbar_arrive(&sm.p_ready[pb]);
+      mbar_arrive(&sm.p_ready);
+      LA_TRACE_AT(p, kTrOperPDone, it, otid == 0);
     }
   }
 }
 
-// State warpgroups: own S in registers, advance it, feed it to the MMA as hi/lo, write the output.
+// State warpgroups: own S in registers, advance it, publish it to TMEM, write the output.
 __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams& p, uint32_t tmem, int ctid,
                                           volatile int* abort) {
   const int warp = ctid >> 5, lane = ctid & 31;
@@ -413,23 +547,25 @@ __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams&
   bool ok = true;
   int err = 0;
 
-  auto write_state_operand = [&]() {
+  // S into its TMEM columns (the TF32 MMA reads its top 10 mantissa bits), then tell the MMA thread.
+  auto publish_state = [&]() {
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      uint32_t hi[16], lo[16];
+    for (int q4 = 0; q4 < 4; ++q4) {
+      uint32_t u[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) split_bf16x2(S[32 * half + 2 * i], S[32 * half + 2 * i + 1], hi[i], lo[i]);
-      tmem_st16(tmem + lane_base + kColStateHi + 32 * wg + 16 * half, hi);
-      tmem_st16(tmem + lane_base + kColStateLo + 32 * wg + 16 * half, lo);
+      for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(S[16 * q4 + i]);
+      tmem_st16(tmem + lane_base + kColState + kbase + 16 * q4, u);
     }
+    tc_fence_before();
+    mbar_arrive(&sm.s_ready);
   };
 
   for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
     const Unit w = decode_unit(p, u);
     err |= w.error;
     if (!w.run) continue;
-    float* lam = sm.lam[warp];
-    fill_lambda_table(lam, __ldg(p.slopes + w.hv), lane);
+    const float slope = __ldg(p.slopes + w.hv);
+    const float lam_chunk = expf(-slope * static_cast<float>(kChunk));  // lambda^64
 
     // state gather
     const size_t state_off = ((static_cast<size_t>(w.slot) * p.HV + w.hv) * kDim + vrow) * kDim + kbase;
@@ -447,69 +583,82 @@ __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams&
 #pragma unroll
       for (int i = 0; i < 64; ++i) S[i] = 0.f;
     }
-    if (w.nchunks > 0) {
-      // S hi/lo is free: the previous unit's last O_inter was waited on (o_full) below
-      write_state_operand();
-      tc_fence_before();
-      mbar_arrive(&sm.s_ready);
-    }
+    // The state's TMEM columns are free: the previous chunk's s_free was waited on below.
+    if (w.nchunks > 0) publish_state();
 
-    __nv_bfloat16* obase =
-        p.o + static_cast<size_t>(w.bos) * p.HV * kDim + static_cast<size_t>(w.hv) * kDim + vrow;
     const size_t ostride = static_cast<size_t>(p.HV) * kDim;
+    __nv_bfloat16* obase = p.o + (static_cast<size_t>(w.bos) + 32 * wg) * ostride +
+                           static_cast<size_t>(w.hv) * kDim + vrow;
     for (int c = 0; c < w.nchunks; ++c, ++it) {
       const uint32_t ph = it & 1u;
+      const uint32_t b = it & 1u, bph = (it >> 1) & 1u;
       const int L = min(kChunk, w.len - c * kChunk);
 
-      // ---- S <- lambda^L S + Delta S
+      // ---- S(i+1) = lambda^L S(i) + Delta S(i), in registers
       if (!warp_wait(&sm.ds_full, ph, abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      LA_TRACE_AT(p, kTrStateDeltaS, it, ctid == 0);
       {
-        const float lamL = lam[L];
+        const float lamLf = (L == kChunk) ? lam_chunk : expf(-slope * static_cast<float>(L));
+        const uint64_t lamL = f2_pack(lamLf, lamLf);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {
           float d[16];
           tmem_ld16(tmem + lane_base + kColDeltaS + kbase + 16 * q4, d);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) S[16 * q4 + i] = fmaf(lamL, S[16 * q4 + i], d[i]);
+          for (int i = 0; i < 16; i += 2) {
+            const float2 r = f2_unpack(f2_fma(lamL, f2_pack(S[16 * q4 + i], S[16 * q4 + i + 1]), f2_pack(d[i], d[i + 1])));
+            S[16 * q4 + i] = r.x;
+            S[16 * q4 + i + 1] = r.y;
+          }
         }
       }
       tc_fence_before();
       mbar_arrive(&sm.ds_free);
+      LA_TRACE_AT(p, kTrStateUpdated, it, ctid == 0);
 
-      // ---- O(c) is complete and S(c) hi/lo has been read: publish S(c+1)
-      if (!warp_wait(&sm.o_full, ph, abort)) {
+      // ---- O_inter(i) has read S(i): publish S(i+1)
+      if (!warp_wait(&sm.s_free, ph, abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      if (c + 1 < w.nchunks) {
-        write_state_operand();
-        tc_fence_before();
-        mbar_arrive(&sm.s_ready);
-      }
+      LA_TRACE_AT(p, kTrStateOInter, it, ctid == 0);
+      if (c + 1 < w.nchunks) publish_state();
+      LA_TRACE_AT(p, kTrStateSReady, it, ctid == 0);
 
-      // ---- o = scale (O_intra + lambda^(s+1) O_inter), this warpgroup's 32 rows s
-      {
-        const float sc = p.scale;
-        __nv_bfloat16* orow = obase + static_cast<size_t>(c) * kChunk * ostride;
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          float oi[16], oe[16];
-          tmem_ld16(tmem + lane_base + kColOIntra + 32 * wg + 16 * half, oi);
-          tmem_ld16(tmem + lane_base + kColOInter + 32 * wg + 16 * half, oe);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int s = 32 * wg + 16 * half + i;
-            if (s < L) orow[s * ostride] = __float2bfloat16_rn(sc * fmaf(lam[s + 1], oe[i], oi[i]));
-          }
-        }
-        tc_fence_before();
-        mbar_arrive(&sm.o_free);
+      // ---- o = O (the scale is folded into Qt and P), this warpgroup's 32 rows s of the chunk
+      if (!warp_wait(&sm.o_full[b], bph, abort)) {
+        ok = false;
+        break;
       }
+      tc_fence_after();
+      {
+        float o0[16], o1[16];
+        tmem_ld16(tmem + lane_base + kColO + 64 * b + 32 * wg, o0);
+        tmem_ld16(tmem + lane_base + kColO + 64 * b + 32 * wg + 16, o1);
+        tc_fence_before();
+        mbar_arrive(&sm.o_free[b]);
+        __nv_bfloat16* orow = obase + static_cast<size_t>(c) * kChunk * ostride;
+        const int rows = L - 32 * wg;  // valid rows of this warpgroup's half (may be <= 0 or > 32)
+        if (rows >= 32) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) orow[i * ostride] = __float2bfloat16_rn(o0[i]);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) orow[(16 + i) * ostride] = __float2bfloat16_rn(o1[i]);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (i < rows) orow[i * ostride] = __float2bfloat16_rn(o0[i]);
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (16 + i < rows) orow[(16 + i) * ostride] = __float2bfloat16_rn(o1[i]);
+        }
+      }
+      LA_TRACE_AT(p, kTrStateEpilogue, it, ctid == 0);
     }
     if (!ok) break;
     // state scatter
@@ -538,23 +687,30 @@ la_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     tmem_relinquish();
   }
   if (tid == 0) {
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&sm.full_bar[i], 1);
-      mbar_init(&sm.empty_bar[i], 1);
+    for (int i = 0; i < kQKStages; ++i) {
+      mbar_init(&sm.qk_full[i], 1);
+      mbar_init(&sm.qk_empty[i], 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
+      mbar_init(&sm.v_full[i], 1);
+      mbar_init(&sm.v_empty[i], 1);
     }
     mbar_init(&sm.scores_full, 1);
     mbar_init(&sm.scores_free, kOperandThreads);
     mbar_init(&sm.kt_ready, kOperandThreads);
     mbar_init(&sm.kt_free, 1);
+    mbar_init(&sm.p_ready, kOperandThreads);
+    mbar_init(&sm.p_free, 1);
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&sm.p_ready[b], kOperandThreads);
-      mbar_init(&sm.p_free[b], 1);
+      mbar_init(&sm.qt_ready[b], kConvThreads);
+      mbar_init(&sm.qt_free[b], 1);
+      mbar_init(&sm.o_full[b], 1);
+      mbar_init(&sm.o_free[b], kStateThreads);
     }
     mbar_init(&sm.ds_full, 1);
     mbar_init(&sm.ds_free, kStateThreads);
     mbar_init(&sm.s_ready, kStateThreads);
-    mbar_init(&sm.o_full, 1);
-    mbar_init(&sm.o_free, kStateThreads);
+    mbar_init(&sm.s_free, 1);
     mbar_init(&sm.final_bar, 1);
     sm.abort = 0;
     fence_mbar_init();
@@ -571,10 +727,12 @@ la_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     if (lane == 0) producer_loop(sm, p, &tm_q, &tm_k, &tm_v, abort);
   } else if (warp == 1) {
     if (lane == 0) mma_loop(sm, p, tmem, abort);
-  } else if (warp >= 4 && warp < 12) {
+  } else if (warp < 4) {
+    convert_loop(sm, p, tid - 64, abort);
+  } else if (warp < 12) {
     const int err = state_loop(sm, p, tmem, tid - 128, abort);
     if (err && tid == 128 && p.dev_error) atomicOr(p.dev_error, err);
-  } else if (warp >= 12) {
+  } else {
     operand_loop(sm, p, tmem, tid - 384, abort);
   }
 

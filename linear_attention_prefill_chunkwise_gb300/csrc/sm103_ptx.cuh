@@ -58,11 +58,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // microseconds; a second means something upstream has stopped.
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
-// Wait until the barrier's phase with the given parity has completed.
-// Returns false (without waiting further) once *abort is set by any thread of
-// the CTA, or after kWaitLimitNs, in which case it sets *abort itself.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
+// Slow path of mbar_wait, kept out of line so that every call site inlines only the
+// first test: the spin loop, the abort check and the watchdog are emitted once.
+__device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, volatile int* abort) {
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -74,6 +72,14 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       }
     }
   }
+}
+
+// Wait until the barrier's phase with the given parity has completed.
+// Returns false (without waiting further) once *abort is set by any thread of
+// the CTA, or after kWaitLimitNs, in which case it sets *abort itself.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort);
 }
 
 // Named barrier over a subset of the CTA's warps (ids 1..15; 0 is __syncthreads).
@@ -151,6 +157,24 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&r)[16]) {
   for (int i = 0; i < 16; ++i) r[i] = __uint_as_float(u[i]);
 }
 
+// 16x32bx2 shape: thread t (0..31) of the warp reads lane base + t%16 of its quadrant,
+// columns [c, c+16) for t < 16 and [c+32, c+48) for t >= 16, waiting for completion in
+// the same statement.  Used on an M = 64 accumulator, whose rows occupy lanes 0..15
+// of each quadrant, so that all 32 threads of a warp receive data.
+__device__ __forceinline__ void tmem_ld16_x2split32(uint32_t taddr, float (&r)[16]) {
+  uint32_t u[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16], 32;\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]), "=r"(u[7]),
+        "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]), "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) r[i] = __uint_as_float(u[i]);
+}
+
 // Store 16 consecutive 32-bit columns of the warp's 32 lanes and wait for completion.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&u)[16]) {
   asm volatile(
@@ -214,6 +238,28 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
+// Instruction descriptor for kind::tf32 (FP32 storage, TF32 multiply) with FP32 accumulation.
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(uint32_t M, uint32_t N, bool a_mn, bool b_mn) {
+  return (1u << 4)                      // D format: f32
+         | (2u << 7)                    // A format: tf32
+         | (2u << 10)                   // B format: tf32
+         | ((a_mn ? 1u : 0u) << 15)
+         | ((b_mn ? 1u : 0u) << 16)
+         | ((N >> 3) << 17)
+         | ((M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[tmem] * B[smem], TF32 operands (K = 8 per instruction)
+__device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread has completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -222,6 +268,14 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
 }
 
 // ---------------------------------------------------------------- BF16 helpers
+
+// Round an FP32 value to TF32 (10 explicit mantissa bits, nearest with ties away from
+// zero); the result is an FP32 bit pattern whose low 13 bits are zero.
+__device__ __forceinline__ uint32_t round_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
 
 // Round two floats to BF16 (nearest-even) and pack: lo -> bits 15..0, hi -> bits 31..16.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -233,11 +287,50 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t p) { return __uint_as_float(p << 16); }
 __device__ __forceinline__ float bf16hi_to_f32(uint32_t p) { return __uint_as_float(p & 0xFFFF0000u); }
 
-// Split a pair of floats into a BF16 "high" pair and a BF16 pair holding the
-// rounding residual, so that hi + lo reproduces each float to ~2^-16 relative.
-__device__ __forceinline__ void split_bf16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
-  hi = pack_bf16x2(a, b);
-  lo = pack_bf16x2(a - bf16lo_to_f32(hi), b - bf16hi_to_f32(hi));
+// ---------------------------------------------------------------- packed FP32 pairs
+
+// Two FP32 values in one 64-bit register pair (x in the low half), for the f32x2 ALU ops.
+__device__ __forceinline__ uint64_t f2_pack(float x, float y) {
+  uint64_t d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(x), "f"(y));
+  return d;
+}
+__device__ __forceinline__ float2 f2_unpack(uint64_t v) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(v));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// The two BF16 values of a packed pair (element 0 in bits 15..0) as a packed FP32 pair.
+__device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t p) {
+  return f2_pack(bf16lo_to_f32(p), bf16hi_to_f32(p));
+}
+
+// Split a pair of FP32 values (packed, x low) into a BF16 "high" pair and a BF16 pair
+// holding the residual, so that hi + lo reproduces each value to ~2^-15 relative:
+// hi is x truncated to BF16 (its top 16 bits, no rounding needed), lo = x - hi is
+// exact in FP32 and then rounded to BF16.
+__device__ __forceinline__ void split_bf16x2(uint64_t xy, uint32_t& hi, uint32_t& lo) {
+  const float2 v = f2_unpack(xy);
+  const uint32_t bx = __float_as_uint(v.x), by = __float_as_uint(v.y);
+  hi = __byte_perm(bx, by, 0x7632);  // upper halves: x -> bits 15..0, y -> bits 31..16
+  const float2 r = f2_unpack(f2_sub(xy, f2_pack(__uint_as_float(bx & 0xFFFF0000u), __uint_as_float(by & 0xFFFF0000u))));
+  lo = pack_bf16x2(r.x, r.y);
 }
 
 }  // namespace lap
