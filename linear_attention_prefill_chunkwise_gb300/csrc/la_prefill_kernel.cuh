@@ -28,8 +28,13 @@
 // Only the final output is rounded to BF16; the state itself stays FP32 throughout.
 //
 // Warp-specialised pipeline, 512 threads per CTA, one CTA per SM:
-//   warp 0       TMA producer: Q/K chunk tiles into a 2-stage ring, V tiles into a 3-stage ring
-//   warp 1       TMEM allocator and the single MMA-issuing thread
+//   warp 0       TMA and MMA thread B, one polling loop: Q/K chunk tiles into a 2-stage ring,
+//                V tiles into a 3-stage ring (the two rings refill independently), and the
+//                scores and dS MMAs, each issued as soon as its operands are ready
+//   warp 1       TMEM allocator and MMA thread A: O_inter(i) then O_intra(i), chunk by chunk
+//                (tcgen05.mma issue stalls its thread while the tensor pipe is busy; with two
+//                issuing threads one keeps the pipe fed while the other waits, tests a
+//                barrier or commits, and the small MMAs of the two streams overlap)
 //   warps 2-3    Q converter: BF16 Q tile -> Qt = scale lambda^(s+1) q in TF32 (B operand of
 //                O_inter), 2 buffers
 //   warps 4-11   state warpgroups: thread (quadrant qd, lane) of warpgroup wg owns state
@@ -37,12 +42,13 @@
 //                they advance the state, publish it to TMEM and write the output
 //   warps 12-15  operand warpgroup: builds the decayed BF16 hi/lo operands Kt and P
 //
-// Per chunk i (a CTA-wide running chunk counter) the MMA thread issues, in order:
-//   scores(i+1)  one chunk ahead: after stage i+1 is loaded and scores(i) was read
-//   dS(i)        after Kt(i) is built and the state warpgroups read dS(i-1)
-//   O_inter(i)   into O[i%2], after S(i) is published, Qt(i) converted, O(i-2) read
-//                (the Q/K stage of chunk i is released as soon as Kt(i) and Qt(i) are built)
-//   O_intra(i)   accumulated into O[i%2], after P(i) is built
+// Per chunk i (a CTA-wide running chunk counter) the MMA groups and their operands:
+//   scores(i)    thread B, after stage i is loaded and scores(i-1) was read
+//   dS(i)        thread B, after Kt(i) is built and the state warpgroups read dS(i-1)
+//   O_inter(i)   thread A, into O[i%2], after S(i) is published, Qt(i) converted, O(i-2) read
+//   O_intra(i)   thread A, accumulated into O[i%2], after P(i) is built
+// The Q/K stage of chunk i is released as soon as its three readers (the scores MMAs, the
+// Kt builders and the Qt converter) are done; a V stage after dS and O_intra.
 // The serial chain from chunk to chunk is only: O_inter(i) done -> S(i+1) written to
 // TMEM -> O_inter(i+1); everything else is built ahead of it.
 #pragma once
@@ -89,9 +95,9 @@ struct __align__(1024) SharedStorage {
   uint8_t kt_lo[2][kTileBytes];
   float tab[4][kTabStride];      // per operand warp: lambda^n for its current unit
   uint64_t qk_full[kQKStages];   // Q/K stage loaded (TMA transaction bytes)
-  uint64_t qk_empty[kQKStages];  // Q/K stage consumed (scores MMA, Kt and Qt builders)
+  uint64_t qk_empty[kQKStages];  // Q/K stage consumed: scores MMA commit + every Kt and Qt builder thread
   uint64_t v_full[kVStages];     // V stage loaded
-  uint64_t v_empty[kVStages];    // V stage consumed (dS and O_intra MMAs)
+  uint64_t v_empty[kVStages];    // V stage consumed: one commit from each MMA thread (dS, O_intra)
   uint64_t scores_full;          // MMA -> operand wg
   uint64_t scores_free;          // operand wg -> MMA
   uint64_t kt_ready;             // operand wg -> MMA
@@ -106,7 +112,7 @@ struct __align__(1024) SharedStorage {
   uint64_t s_free;               // MMA -> state wgs (O_inter done reading S)
   uint64_t o_full[2];            // MMA -> state wgs (O(i) complete)
   uint64_t o_free[2];            // state wgs -> MMA
-  uint64_t final_bar;            // every MMA retired (teardown)
+  uint64_t final_bar[2];         // every MMA of thread A / B retired (teardown)            // every MMA retired (teardown)
   uint32_t tmem_base;
   int abort;
 };
@@ -242,42 +248,136 @@ __device__ __forceinline__ uint32_t cta_chunk_count(const KernelParams& p) {
 
 // ------------------------------------------------------------------------------ roles
 
-__device__ __forceinline__ void producer_loop(SharedStorage& sm, const KernelParams& p, const CUtensorMap* tm_q,
-                                              const CUtensorMap* tm_k, const CUtensorMap* tm_v,
-                                              volatile int* abort) {
-  uint32_t nqk = 0, nv = 0;  // chunks whose Q/K (V) loads have been issued
-  bool ok = true;
-  for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
+__device__ __forceinline__ uint64_t desc_at(uint64_t base, uint32_t byte_off) { return base + (byte_off >> 4); }
+
+// The walk of this CTA's chunks by a role that runs ahead of the others.
+struct ChunkCursor {
+  int u, c, row, hq, hv, nchunks;
+  bool valid;
+};
+__device__ __forceinline__ void cursor_seek(const KernelParams& p, ChunkCursor& k, int u) {
+  for (; u < p.num_units; u += gridDim.x) {
     const Unit w = decode_unit(p, u);
-    if (!w.run) continue;
-    for (int c = 0; c < w.nchunks; ++c) {
-      const int row = w.bos + c * kChunk;
-      const uint32_t it = nqk;
-      const uint32_t sq = it % kQKStages, sv = it % kVStages;
-      if (!mbar_wait(&sm.qk_empty[sq], ((it / kQKStages) & 1u) ^ 1u, abort)) {
-        ok = false;
-        break;
-      }
-      LA_TRACE_AT(p, kTrProducerIssue, it, true);
-      mbar_arrive_expect_tx(&sm.qk_full[sq], 4 * kTileBytes);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        tma_load_2d(sm.qk[sq].q[h], tm_q, &sm.qk_full[sq], w.hq * kDim + 64 * h, row);
-        tma_load_2d(sm.qk[sq].k[h], tm_k, &sm.qk_full[sq], w.hq * kDim + 64 * h, row);
-      }
-      ++nqk;
-      if (!mbar_wait(&sm.v_empty[sv], ((it / kVStages) & 1u) ^ 1u, abort)) {
-        ok = false;
-        break;
-      }
-      mbar_arrive_expect_tx(&sm.v_full[sv], 2 * kTileBytes);
-#pragma unroll
-      for (int h = 0; h < 2; ++h) tma_load_2d(sm.v[sv][h], tm_v, &sm.v_full[sv], w.hv * kDim + 64 * h, row);
-      ++nv;
+    if (w.run && w.nchunks > 0) {
+      k.u = u;
+      k.c = 0;
+      k.row = w.bos;
+      k.hq = w.hq;
+      k.hv = w.hv;
+      k.nchunks = w.nchunks;
+      k.valid = true;
+      return;
     }
   }
-  // Before leaving, make sure no load this thread issued is still writing shared memory:
-  // wait for the most recent phase of every ring slot that was armed.
+  k.valid = false;
+}
+__device__ __forceinline__ void cursor_next(const KernelParams& p, ChunkCursor& k) {
+  if (++k.c < k.nchunks) {
+    k.row += kChunk;
+  } else {
+    cursor_seek(p, k, k.u + gridDim.x);
+  }
+}
+
+// TMA and MMA thread B, one polling loop: each pass issues, in this order, every job whose
+// inputs are ready (mbarrier.test_wait, no blocking): dS(i) = V(i)^T Kt(i), scores(i) =
+// Q(i) K(i)^T, and the next Q/K and V loads once their ring slots have been released.
+__device__ __forceinline__ void tma_mma_loop(SharedStorage& sm, const KernelParams& p, const CUtensorMap* tm_q,
+                                             const CUtensorMap* tm_k, const CUtensorMap* tm_v, uint32_t tmem,
+                                             volatile int* abort) {
+  constexpr uint32_t id_scores = idesc_bf16_f32(64, 64, false, false);
+  constexpr uint32_t id_dstate = idesc_bf16_f32(128, 128, true, true);
+  const uint64_t dq0 = sdesc_sw128(smem_u32(sm.qk[0].q), 16, 1024);
+  const uint64_t dk0 = sdesc_sw128(smem_u32(sm.qk[0].k), 16, 1024);
+  const uint64_t qk_step = sizeof(QKTiles) >> 4;
+  const uint64_t dv0 = sdesc_sw128(smem_u32(sm.v[0]), kTileBytes, 1024);
+  const uint64_t v_step = (2 * kTileBytes) >> 4;
+  const uint64_t dkt_hi = sdesc_sw128(smem_u32(sm.kt_hi), kTileBytes, 1024);
+  const uint64_t dkt_lo = sdesc_sw128(smem_u32(sm.kt_lo), kTileBytes, 1024);
+  const uint32_t t_scores = tmem + kColScores, t_ds = tmem + kColDeltaS;
+  const uint32_t total = cta_chunk_count(p);
+  uint32_t n_ds = 0, n_sc = 0, nqk = 0, nv = 0;
+  ChunkCursor cq, cv;
+  cursor_seek(p, cq, blockIdx.x);
+  cv = cq;
+  uint64_t last = globaltimer_ns();
+  while (n_ds < total || n_sc < total || cq.valid || cv.valid) {
+    bool progressed = false;
+    if (n_ds < total) {
+      const uint32_t j = n_ds, sv = j % kVStages;
+      if (mbar_test(&sm.kt_ready, j & 1u) && mbar_test(&sm.v_full[sv], (j / kVStages) & 1u) &&
+          mbar_test(&sm.ds_free, (j & 1u) ^ 1u)) {
+        tc_fence_after();
+        LA_TRACE_AT(p, kTrMmaDeltaS, j, true);
+        const uint64_t v0 = dv0 + sv * v_step;
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ss(t_ds, desc_at(v0, kk * 2048), desc_at(part ? dkt_lo : dkt_hi, kk * 2048), id_dstate,
+                   (part | kk) != 0);
+        }
+        mma_commit(&sm.ds_full);
+        mma_commit(&sm.kt_free);
+        mma_commit(&sm.v_empty[sv]);
+        ++n_ds;
+        progressed = true;
+      }
+    }
+    if (n_sc < total) {
+      const uint32_t j = n_sc, sq = j % kQKStages;
+      if (mbar_test(&sm.qk_full[sq], (j / kQKStages) & 1u) && (j == 0 || mbar_test(&sm.scores_free, (j - 1) & 1u))) {
+        tc_fence_after();
+        LA_TRACE_AT(p, kTrMmaScores, j, true);
+        const uint64_t q0 = dq0 + sq * qk_step, k0 = dk0 + sq * qk_step;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint32_t off = (kk >> 2) * kTileBytes + (kk & 3) * 32;
+          mma_ss(t_scores, desc_at(q0, off), desc_at(k0, off), id_scores, kk > 0);
+        }
+        mma_commit(&sm.scores_full);
+        mma_commit(&sm.qk_empty[sq]);
+        ++n_sc;
+        progressed = true;
+      }
+    }
+    if (cq.valid) {
+      const uint32_t sq = nqk % kQKStages;
+      if (mbar_test(&sm.qk_empty[sq], ((nqk / kQKStages) & 1u) ^ 1u)) {
+        LA_TRACE_AT(p, kTrProducerIssue, nqk, true);
+        mbar_arrive_expect_tx(&sm.qk_full[sq], 4 * kTileBytes);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          tma_load_2d(sm.qk[sq].q[h], tm_q, &sm.qk_full[sq], cq.hq * kDim + 64 * h, cq.row);
+          tma_load_2d(sm.qk[sq].k[h], tm_k, &sm.qk_full[sq], cq.hq * kDim + 64 * h, cq.row);
+        }
+        ++nqk;
+        cursor_next(p, cq);
+        progressed = true;
+      }
+    }
+    if (cv.valid) {
+      const uint32_t sv = nv % kVStages;
+      if (mbar_test(&sm.v_empty[sv], ((nv / kVStages) & 1u) ^ 1u)) {
+        mbar_arrive_expect_tx(&sm.v_full[sv], 2 * kTileBytes);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) tma_load_2d(sm.v[sv][h], tm_v, &sm.v_full[sv], cv.hv * kDim + 64 * h, cv.row);
+        ++nv;
+        cursor_next(p, cv);
+        progressed = true;
+      }
+    }
+    if (progressed) {
+      last = globaltimer_ns();
+    } else {
+      if (*abort) break;
+      if (globaltimer_ns() - last > kWaitLimitNs) {
+        *abort = 1;
+        break;
+      }
+      __nanosleep(32);
+    }
+  }
   for (uint32_t i = 0; i < kQKStages && i < nqk; ++i) {
     const uint32_t j = nqk - 1 - i;
     mbar_wait(&sm.qk_full[j % kQKStages], (j / kQKStages) & 1u, abort);
@@ -286,83 +386,31 @@ __device__ __forceinline__ void producer_loop(SharedStorage& sm, const KernelPar
     const uint32_t j = nv - 1 - i;
     mbar_wait(&sm.v_full[j % kVStages], (j / kVStages) & 1u, abort);
   }
+  mma_commit(&sm.final_bar[1]);
+  mbar_wait(&sm.final_bar[1], 0, abort);
 }
 
-// Shared-memory descriptors are built once; per K step only the 14-bit start-address
-// field changes, by a compile-time byte offset (>> 4) added to the low word.  This keeps
-// the single issuing thread to a few instructions per MMA, so issue never limits the
-// tensor pipe (rebuilding both 64-bit descriptors per MMA costs more than an N = 128 MMA).
-__device__ __forceinline__ uint64_t desc_at(uint64_t base, uint32_t byte_off) { return base + (byte_off >> 4); }
-
-__device__ __forceinline__ void mma_loop(SharedStorage& sm, const KernelParams& p, uint32_t tmem,
-                                         volatile int* abort) {
-  constexpr uint32_t id_scores = idesc_bf16_f32(64, 64, false, false);   // Q (K-major) x K (K-major)
-  constexpr uint32_t id_dstate = idesc_bf16_f32(128, 128, true, true);   // V^T (MN-major) x Kt (MN-major)
-  constexpr uint32_t id_ointer = idesc_tf32_f32(128, 64, false, false);  // S (TMEM) x Qt (K-major)
-  constexpr uint32_t id_ointra = idesc_bf16_f32(128, 64, true, false);   // V^T (MN-major) x P (K-major)
-  // K-major operands: sbo = 1024 (8 rows of 128 B); MN-major: lbo = 8192 (next 64-wide box), sbo = 1024
-  const uint64_t dq0 = sdesc_sw128(smem_u32(sm.qk[0].q), 16, 1024);
-  const uint64_t dk0 = sdesc_sw128(smem_u32(sm.qk[0].k), 16, 1024);
-  const uint64_t qk_step = sizeof(QKTiles) >> 4;  // descriptor distance between Q/K stages
+// MMA thread A: the output accumulator, in chunk order, with blocking waits (this is the
+// serial chain of the pipeline):
+//   O_inter(i) = S(i) Qt(i)^T     into O[i%2]: needs Qt(i), O(i-2) read out, S(i) published
+//   O_intra(i) += V(i)^T P(i)^T   needs V(i) and P(i); after O_inter(i) (same thread, in order)
+__device__ __forceinline__ void mma_o_loop(SharedStorage& sm, const KernelParams& p, uint32_t tmem,
+                                           volatile int* abort) {
+  constexpr uint32_t id_ointer = idesc_tf32_f32(128, 64, false, false);
+  constexpr uint32_t id_ointra = idesc_bf16_f32(128, 64, true, false);
   const uint64_t dv0 = sdesc_sw128(smem_u32(sm.v[0]), kTileBytes, 1024);
   const uint64_t v_step = (2 * kTileBytes) >> 4;
   const uint64_t dqt0 = sdesc_sw128(smem_u32(sm.qt[0]), 16, 1024);
   const uint64_t qt_step = (4 * kTileBytes) >> 4;
-  const uint64_t dkt_hi = sdesc_sw128(smem_u32(sm.kt_hi), kTileBytes, 1024);
-  const uint64_t dkt_lo = sdesc_sw128(smem_u32(sm.kt_lo), kTileBytes, 1024);
   const uint64_t dp_hi = sdesc_sw128(smem_u32(sm.p_hi), 16, 1024);
   const uint64_t dp_lo = sdesc_sw128(smem_u32(sm.p_lo), 16, 1024);
-  const uint32_t t_scores = tmem + kColScores, t_ds = tmem + kColDeltaS, t_state = tmem + kColState;
-
+  const uint32_t t_state = tmem + kColState;
   const uint32_t total = cta_chunk_count(p);
-  // scores(j) = Q K^T of chunk j : M=64, N=64, K=128 (8 steps of 16)
-  auto issue_scores = [&](uint32_t j) -> bool {
-    const uint32_t sq = j % kQKStages;
-    if (!mbar_wait(&sm.qk_full[sq], (j / kQKStages) & 1u, abort)) return false;
-    if (j > 0 && !mbar_wait(&sm.scores_free, (j - 1) & 1u, abort)) return false;
-    tc_fence_after();
-    LA_TRACE_AT(p, kTrMmaScores, j, true);
-    const uint64_t q0 = dq0 + sq * qk_step, k0 = dk0 + sq * qk_step;
-#pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
-      const uint32_t off = (kk >> 2) * kTileBytes + (kk & 3) * 32;
-      mma_ss(t_scores, desc_at(q0, off), desc_at(k0, off), id_scores, kk > 0);
-    }
-    mma_commit(&sm.scores_full);
-    return true;
-  };
-
-  bool ok = total == 0 || issue_scores(0);
-  for (uint32_t it = 0; it < total && ok; ++it) {
-    const uint32_t sq = it % kQKStages, sv = it % kVStages;
-    const uint32_t ph = it & 1u;
-    const uint32_t b = it & 1u, bph = (it >> 1) & 1u;  // double-buffered Qt and O
-    const uint64_t v0 = dv0 + sv * v_step;
-
-    if (it + 1 < total && !issue_scores(it + 1)) break;
-
-    // Delta S = V^T (Kt_hi + Kt_lo) : M=128, N=128, K=64
-    if (!mbar_wait(&sm.v_full[sv], (it / kVStages) & 1u, abort) || !mbar_wait(&sm.kt_ready, ph, abort) ||
-        !mbar_wait(&sm.ds_free, ph ^ 1u, abort))
+  for (uint32_t it = 0; it < total; ++it) {
+    const uint32_t sv = it % kVStages, ph = it & 1u, b = it & 1u, bph = (it >> 1) & 1u;
+    if (!mbar_wait(&sm.qt_ready[b], bph, abort) || !mbar_wait(&sm.o_free[b], bph ^ 1u, abort) ||
+        !mbar_wait(&sm.s_ready, ph, abort))
       break;
-    tc_fence_after();
-    LA_TRACE_AT(p, kTrMmaDeltaS, it, true);
-#pragma unroll
-    for (int part = 0; part < 2; ++part) {
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk)
-        mma_ss(t_ds, desc_at(v0, kk * 2048), desc_at(part ? dkt_lo : dkt_hi, kk * 2048), id_dstate,
-               (part | kk) != 0);
-    }
-    mma_commit(&sm.ds_full);
-    mma_commit(&sm.kt_free);
-
-    // Qt(i) is built too: every reader of the Q/K stage of chunk i is done once scores(i) retires.
-    if (!mbar_wait(&sm.qt_ready[b], bph, abort)) break;
-    mma_commit(&sm.qk_empty[sq]);
-
-    // O^T = S Qt^T : M=128, N=64, K=128 in TF32 (16 steps of 8), A = S from TMEM; starts O[b]
-    if (!mbar_wait(&sm.s_ready, ph, abort) || !mbar_wait(&sm.o_free[b], bph ^ 1u, abort)) break;
     tc_fence_after();
     LA_TRACE_AT(p, kTrMmaOInter, it, true);
     const uint32_t t_o = tmem + kColO + 64 * b;
@@ -374,11 +422,10 @@ __device__ __forceinline__ void mma_loop(SharedStorage& sm, const KernelParams& 
     }
     mma_commit(&sm.s_free);
     mma_commit(&sm.qt_free[b]);
-
-    // O^T += V^T (P_hi + P_lo)^T : M=128, N=64, K=64
-    if (!mbar_wait(&sm.p_ready, ph, abort)) break;
+    if (!mbar_wait(&sm.v_full[sv], (it / kVStages) & 1u, abort) || !mbar_wait(&sm.p_ready, ph, abort)) break;
     tc_fence_after();
     LA_TRACE_AT(p, kTrMmaOIntra, it, true);
+    const uint64_t v0 = dv0 + sv * v_step;
 #pragma unroll
     for (int part = 0; part < 2; ++part) {
 #pragma unroll
@@ -389,9 +436,8 @@ __device__ __forceinline__ void mma_loop(SharedStorage& sm, const KernelParams& 
     mma_commit(&sm.p_free);
     mma_commit(&sm.v_empty[sv]);
   }
-  // Retire every MMA before the accumulators are released.
-  mma_commit(&sm.final_bar);
-  mbar_wait(&sm.final_bar, 0, abort);
+  mma_commit(&sm.final_bar[0]);
+  mbar_wait(&sm.final_bar[0], 0, abort);
 }
 
 // Q converter (warps 2-3): the BF16 Q tile (K-major, 128B-swizzled, 2 boxes of 64 d) into
@@ -431,6 +477,7 @@ __device__ __forceinline__ void convert_loop(SharedStorage& sm, const KernelPara
       }
       fence_proxy_async_smem();
       mbar_arrive(&sm.qt_ready[b]);
+      mbar_arrive(&sm.qk_empty[sq]);
       LA_TRACE_AT(p, kTrConvDone, it, ctid == 0);
     }
   }
@@ -485,6 +532,7 @@ __device__ __forceinline__ void operand_loop(SharedStorage& sm, const KernelPara
       }
       fence_proxy_async_smem();
       mbar_arrive(&sm.kt_ready);
+      mbar_arrive(&sm.qk_empty[sq]);
       LA_TRACE_AT(p, kTrOperKtDone, it, otid == 0);
 
       // ---- P from the scores: row prow, columns pcol .. pcol + 31 (16x32bx2 loads use all 32 lanes)
@@ -689,11 +737,11 @@ la_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   if (tid == 0) {
     for (int i = 0; i < kQKStages; ++i) {
       mbar_init(&sm.qk_full[i], 1);
-      mbar_init(&sm.qk_empty[i], 1);
+      mbar_init(&sm.qk_empty[i], 1 + kOperandThreads + kConvThreads);
     }
     for (int i = 0; i < kVStages; ++i) {
       mbar_init(&sm.v_full[i], 1);
-      mbar_init(&sm.v_empty[i], 1);
+      mbar_init(&sm.v_empty[i], 2);
     }
     mbar_init(&sm.scores_full, 1);
     mbar_init(&sm.scores_free, kOperandThreads);
@@ -711,7 +759,8 @@ la_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     mbar_init(&sm.ds_free, kStateThreads);
     mbar_init(&sm.s_ready, kStateThreads);
     mbar_init(&sm.s_free, 1);
-    mbar_init(&sm.final_bar, 1);
+    mbar_init(&sm.final_bar[0], 1);
+    mbar_init(&sm.final_bar[1], 1);
     sm.abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tm_q);
@@ -724,9 +773,9 @@ la_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   const uint32_t tmem = sm.tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) producer_loop(sm, p, &tm_q, &tm_k, &tm_v, abort);
+    if (lane == 0) tma_mma_loop(sm, p, &tm_q, &tm_k, &tm_v, tmem, abort);
   } else if (warp == 1) {
-    if (lane == 0) mma_loop(sm, p, tmem, abort);
+    if (lane == 0) mma_o_loop(sm, p, tmem, abort);
   } else if (warp < 4) {
     convert_loop(sm, p, tid - 64, abort);
   } else if (warp < 12) {

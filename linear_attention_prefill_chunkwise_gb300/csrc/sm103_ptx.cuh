@@ -140,6 +140,9 @@ __device__ __forceinline__ void bulk_copy_s2g(void* gdst, const void* ssrc, uint
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until every committed bulk copy of this thread has finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// Wait until at most the most recently committed bulk group of this thread is still
+// reading shared memory (every older group has finished reading).
+__device__ __forceinline__ void bulk_wait_read_1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 // Wait until every committed bulk copy of this thread has completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
@@ -209,6 +212,17 @@ __device__ __forceinline__ void tmem_ld16_x2split32(uint32_t taddr, float (&r)[1
   for (int i = 0; i < 16; ++i) r[i] = __uint_as_float(u[i]);
 }
 
+// 16x256b shape, one repetition: thread t of the warp receives lane base + t/4 in r0, r1
+// (columns c + 2 (t%4), c + 2 (t%4) + 1) and lane base + 8 + t/4 in r2, r3 (same columns):
+// the fragment layout of an m16n8 accumulator.  No wait: call tmem_wait_ld() before use.
+__device__ __forceinline__ void tmem_ld_16x256b(uint32_t taddr, uint32_t (&r)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x1.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
 // Store 16 consecutive 32-bit columns of the warp's 32 lanes and wait for completion.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&u)[16]) {
   asm volatile(
@@ -218,6 +232,16 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&u)[16
       "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]), "r"(u[7]), "r"(u[8]),
       "r"(u[9]), "r"(u[10]), "r"(u[11]), "r"(u[12]), "r"(u[13]), "r"(u[14]), "r"(u[15])
       : "memory");
+}
+
+// Four 8x8 b16 matrices, transposed on the way to shared memory: lane 8m + r gives the
+// address of row r of matrix m; register m holds this thread's fragment of matrix m
+// (row t/4, columns 2 (t%4), 2 (t%4) + 1, lower column in the low half).
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t saddr, uint32_t m0, uint32_t m1, uint32_t m2,
+                                                  uint32_t m3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(m0),
+               "r"(m1), "r"(m2), "r"(m3)
+               : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05.mma
