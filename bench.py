@@ -67,6 +67,23 @@ def measured_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_bf16_tflops():
+    """Dense BF16 tensor peak (burst) from MEASURED_PEAKS.json, else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            with open(path) as fh:
+                d = json.load(fh)
+            tf = d.get("bf16_tflops")
+            if isinstance(tf, dict):
+                tf = tf.get("value")
+            if tf:
+                return float(tf), "measured"
+        except (OSError, ValueError):
+            pass
+    return FALLBACK_BF16_TFLOPS, "fallback"
+
+
 def dram_traffic_per_launch():
     """DRAM bytes per launch from the committed ncu summary, if it was taken on the current kernel source."""
     if not os.path.exists(TRAFFIC_FILE):
@@ -303,6 +320,92 @@ def run_cuda(args):
         dist.destroy_process_group()
 
 
+def workload_roofline(p):
+    """Algorithmic bytes and dense-tile FLOPs of one call on workload ``p``: per non-padded
+    sequence, Q and K once per q/k head, V read and O written per value head, h0 read and the
+    final state written per value head when present; 4*C*D*V + 4*C^2*D FLOPs per 64-token
+    chunk (C = 64) per value head.  Returns (tokens, bytes, flops)."""
+    import numpy as np
+    lengths = p.lengths()
+    live = np.ones(len(lengths), dtype=bool) if p.state_indices is None else p.state_indices >= 0
+    toks = int(lengths[live].sum())
+    nseq = int(live.sum())
+    state_bytes = p.HV * V * D * 4
+    nbytes = 2 * toks * p.H * D * 2 + 2 * toks * p.HV * V * 2
+    if p.h0 is not None:
+        nbytes += nseq * state_bytes
+    if p.want_final:
+        nbytes += nseq * state_bytes
+    chunks = int(((lengths[live] + 63) // 64).sum())
+    flops = chunks * p.HV * (4 * 64 * D * V + 4 * 64 * 64 * D)
+    return toks, nbytes, flops
+
+
+def run_sweep(args):
+    """Every workload of workloads.config(1..5): mean kernel time over ``--sweep-steps``
+    launches (CUDA events around each launch, L2 flushed between launches by writing a
+    256 MB buffer), tokens/s over non-padded tokens, and the fraction of the roofline
+    max(bytes / HBM peak, FLOPs / BF16 tensor peak).  One JSON line per workload."""
+    import numpy as np
+    import torch
+
+    import linear_attention_prefill_chunkwise_gb300 as lap
+    import workloads as W
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.Stream(device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    hbm, hbm_kind = measured_peaks()
+    tflops, tf_kind = measured_bf16_tflops()
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+    for i in range(1, 6):
+        p = W.config(i)
+        q, k, v = bf(p.q_bits), bf(p.k_bits), bf(p.v_bits)
+        sl = torch.from_numpy(p.slopes).to(device)
+        h0 = None if p.h0 is None else torch.from_numpy(p.h0).to(device)
+        idx = None if p.state_indices is None else torch.from_numpy(p.state_indices).to(device)
+        cu = None if p.cu_seqlens is None else torch.from_numpy(p.cu_seqlens).to(device)
+        o = torch.empty((p.tokens, p.HV, V), dtype=torch.bfloat16, device=device)
+        if p.in_place:
+            hf = h0
+        elif p.want_final:
+            hf = torch.empty((p.pool_size, p.HV, V, D), dtype=torch.float32, device=device)
+        else:
+            hf = None
+
+        def call():
+            lap.la_prefill_fwd(q, k, v, sl, p.scale, h0=h0, state_indices=idx, cu_seqlens=cu, o=o, h_final=hf,
+                               seq_len=None if cu is not None else p.T, stream=stream)
+
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                call()
+            times = []
+            for _ in range(args.sweep_steps):
+                flush.fill_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                call()
+                e1.record(stream)
+                times.append((e0, e1))
+        torch.cuda.synchronize(device)
+        ms = statistics.fmean(a.elapsed_time(b) for a, b in times)
+        toks, nbytes, flops = workload_roofline(p)
+        t_roof = max(nbytes / (hbm * 1e9), flops / (tflops * 1e12))
+        line = {"sweep": True, "workload": i, "name": p.name, "ms": round(ms, 5),
+                "tokens_per_s": round(toks / (ms / 1e3), 1), "tokens": toks, "alg_bytes": nbytes,
+                "alg_flops": flops, "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
+                "roofline_ms": round(t_roof * 1e3, 5), "frac": round(t_roof * 1e3 / ms, 4),
+                "bound": "hbm" if nbytes / (hbm * 1e9) >= flops / (tflops * 1e12) else "tensor",
+                "peaks": {"hbm_gbs": hbm, "hbm_source": hbm_kind, "bf16_tflops": tflops, "tflops_source": tf_kind},
+                "steps": args.sweep_steps, "l2": "flushed between launches (256 MB write)"}
+        print(json.dumps(line), flush=True)
+
+
 def cpu_baseline(p, heads):
     """The FP64 oracle on the host cores over a bounded sample: both sequences, all T tokens,
     the first `heads` of the 64 heads.  Reported in full-workload tokens/s (a token = all 64 heads)."""
@@ -386,10 +489,15 @@ def main():
     ap.add_argument("--cpu-heads", type=int, default=64, help="heads in the oracle CPU-baseline sample")
     ap.add_argument("--ref-budget", type=float, default=60.0, help="seconds for the whole reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every workload (1..5) instead, one JSON line each (not the headline line)")
+    ap.add_argument("--sweep-steps", type=int, default=50)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    if args.impl == "reference":
+    if args.sweep:
+        run_sweep(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_cuda(args)
