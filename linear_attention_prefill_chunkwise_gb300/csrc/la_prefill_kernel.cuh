@@ -21,8 +21,8 @@
 // O_inter and O_intra accumulate into one accumulator that already holds o.
 // Operand precision:
 //   scores   Q K^T           BF16 x BF16 (the inputs, exact)
-//   O_inter  S Qt^T          TF32 x TF32: the FP32 state as stored (the tensor core keeps
-//                            its top 10 mantissa bits) and Qt rounded to TF32
+//   O_inter  S Qt^T          TF32 x TF32: the FP32 state and Qt as stored (the tensor core
+//                            reads the top 10 mantissa bits of each FP32 operand)
 //   O_intra  V^T P^T         BF16 x (P_hi + P_lo): P as a BF16 pair, ~16 significant bits
 //   dS       V^T Kt          BF16 x (Kt_hi + Kt_lo)
 // Only the final output is rounded to BF16; the state itself stays FP32 throughout.
@@ -441,8 +441,10 @@ __device__ __forceinline__ void mma_o_loop(SharedStorage& sm, const KernelParams
 }
 
 // Q converter (warps 2-3): the BF16 Q tile (K-major, 128B-swizzled, 2 boxes of 64 d) into
-// Qt = scale lambda^(s+1) q rounded to TF32 (K-major, 128B-swizzled, 4 boxes of 32 d).
-// Thread t owns token row s = t of the chunk.
+// Qt = scale lambda^(s+1) q in FP32 (K-major, 128B-swizzled, 4 boxes of 32 d), which the
+// tensor core reads as TF32, i.e. truncated to 10 mantissa bits; rounding it here instead
+// would cost two more instructions per element on the critical conversion and changes the
+// output by far less than its BF16 step.  Thread t owns token row s = t of the chunk.
 __device__ __forceinline__ void convert_loop(SharedStorage& sm, const KernelParams& p, int ctid,
                                              volatile int* abort) {
   const int s = ctid;
@@ -469,10 +471,8 @@ __device__ __forceinline__ void convert_loop(SharedStorage& sm, const KernelPara
           const uint32_t fc = 2 * (cc & 3);
           const float2 q0 = f2_unpack(f2_mul(ff, bf16x2_to_f2(x.x))), q1 = f2_unpack(f2_mul(ff, bf16x2_to_f2(x.y)));
           const float2 q2 = f2_unpack(f2_mul(ff, bf16x2_to_f2(x.z))), q3 = f2_unpack(f2_mul(ff, bf16x2_to_f2(x.w)));
-          *reinterpret_cast<uint4*>(dst + swz(s, fc)) =
-              make_uint4(round_tf32(q0.x), round_tf32(q0.y), round_tf32(q1.x), round_tf32(q1.y));
-          *reinterpret_cast<uint4*>(dst + swz(s, fc + 1)) =
-              make_uint4(round_tf32(q2.x), round_tf32(q2.y), round_tf32(q3.x), round_tf32(q3.y));
+          *reinterpret_cast<float4*>(dst + swz(s, fc)) = make_float4(q0.x, q0.y, q1.x, q1.y);
+          *reinterpret_cast<float4*>(dst + swz(s, fc + 1)) = make_float4(q2.x, q2.y, q3.x, q3.y);
         }
       }
       fence_proxy_async_smem();
