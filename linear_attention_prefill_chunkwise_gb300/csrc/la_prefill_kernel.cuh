@@ -464,7 +464,7 @@ __device__ __forceinline__ void convert_loop(SharedStorage& sm, const KernelPara
       }
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
-#pragma unroll
+#pragma unroll 2
         for (int cc = 0; cc < 8; ++cc) {
           const uint4 x = *reinterpret_cast<const uint4*>(sm.qk[sq].q[h] + swz(s, cc));
           uint8_t* dst = sm.qt[b][2 * h + (cc >> 2)];
