@@ -404,6 +404,69 @@ def run_sweep(args):
                 "peaks": {"hbm_gbs": hbm, "hbm_source": hbm_kind, "bf16_tflops": tflops, "tflops_source": tf_kind},
                 "steps": args.sweep_steps, "l2": "flushed between launches (256 MB write)"}
         print(json.dumps(line), flush=True)
+    run_decode_sweep(args, device, stream, flush, hbm, hbm_kind)
+
+
+def run_decode_sweep(args, device, stream, flush, hbm, hbm_kind):
+    """The speculative-decoding ops on the short-continuation workload (workloads.config(5):
+    128 requests of 8 draft tokens, H=HV=64, 256-slot pool, 16 padded): MTP decode, verify
+    with the KV-buffer copy, and commit of every accepted token.  Bytes: per live (request,
+    value head) the 64 KB state read (and written, decode and commit), the tokens' q, k
+    (once per q/k head), v and o, and the KV buffer written (verify) or read (commit)."""
+    import numpy as np
+    import torch
+
+    import linear_attention_prefill_chunkwise_gb300 as lap
+    import workloads as W
+
+    p = W.config(5)
+    Bq, Tq = p.N, 8
+    live = int((p.state_indices >= 0).sum())
+    toks = live * Tq
+    state_b = live * p.HV * V * D * 4
+    tok_b = toks * (2 * p.H * D * 2 + 2 * p.HV * V * 2)
+    kv_b = toks * (p.H * D * 2 + p.HV * V * 2)
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+    q, k, v = bf(p.q_bits), bf(p.k_bits), bf(p.v_bits)
+    sl = torch.from_numpy(p.slopes).to(device)
+    pool = torch.from_numpy(p.h0).to(device)
+    idx = torch.from_numpy(p.state_indices).to(device)
+    o = torch.empty((p.tokens, p.HV, V), dtype=torch.bfloat16, device=device)
+    kbuf = torch.zeros((p.pool_size, Tq, p.H, D), dtype=torch.bfloat16, device=device)
+    vbuf = torch.zeros((p.pool_size, Tq, p.HV, V), dtype=torch.bfloat16, device=device)
+    acc = torch.full((Bq,), Tq, dtype=torch.int32, device=device)
+    ops = {
+        "la_decode_mtp": (lambda: lap.la_decode_mtp(q, k, v, sl, p.scale, pool, Tq, state_indices=idx, o=o,
+                                                    stream=stream), 2 * state_b + tok_b),
+        "la_verify": (lambda: lap.la_verify(q, k, v, sl, p.scale, pool, Tq, state_indices=idx, o=o, kbuf=kbuf,
+                                            vbuf=vbuf, stream=stream), state_b + tok_b + kv_b),
+        "la_commit": (lambda: lap.la_commit(pool, kbuf, vbuf, acc, sl, state_indices=idx, stream=stream),
+                      2 * state_b + kv_b),
+    }
+    for name, (fn, nbytes) in ops.items():
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            times = []
+            for _ in range(args.sweep_steps):
+                flush.fill_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                times.append((e0, e1))
+        torch.cuda.synchronize(device)
+        ms = statistics.fmean(a.elapsed_time(b) for a, b in times)
+        t_roof = nbytes / (hbm * 1e9)
+        print(json.dumps({"sweep": True, "op": name, "workload": "B=128 requests x T=8 draft tokens, H=HV=64, "
+                          "256-slot pool, 16 padded", "ms": round(ms, 5), "tokens_per_s": round(toks / (ms / 1e3), 1),
+                          "alg_bytes": nbytes, "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
+                          "roofline_ms": round(t_roof * 1e3, 5), "frac": round(t_roof * 1e3 / ms, 4), "bound": "hbm",
+                          "peaks": {"hbm_gbs": hbm, "hbm_source": hbm_kind}, "steps": args.sweep_steps,
+                          "l2": "flushed between launches (256 MB write)"}), flush=True)
 
 
 def cpu_baseline(p, heads):

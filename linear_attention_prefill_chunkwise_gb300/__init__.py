@@ -1,10 +1,11 @@
-"""GB300 (sm_103a) Lightning Attention chunkwise prefill.
+"""GB300 (sm_103a) Lightning Attention chunkwise prefill and speculative-decoding ops.
 
-``la_prefill_fwd`` is a thin ctypes binding of the C entry point of the same
-name (include/la_prefill.h): it checks dtypes and shapes of torch tensors,
-passes their device pointers and the current CUDA stream, and raises on a
-non-OK status.  Every step of the computation runs in the library's CUDA
-kernel; there is no other implementation in this package and no fallback.
+``la_prefill_fwd`` (include/la_prefill.h) and ``la_decode_mtp``, ``la_verify``,
+``la_commit`` (include/la_decode.h) are thin ctypes bindings of the C entry points of
+the same names: they check dtypes and shapes of torch tensors, pass their device
+pointers and the current CUDA stream, and raise on a non-OK status.  Every step of the
+computation runs in the library's CUDA kernels; there is no other implementation in
+this package and no fallback.
 """
 from __future__ import annotations
 
@@ -14,7 +15,7 @@ import threading
 
 from . import build as _build
 
-__all__ = ["la_prefill_fwd", "LaError", "load_library", "SCHEDULES", "DEV_ERR_BAD_SEQLENS",
+__all__ = ["la_prefill_fwd", "la_decode_mtp", "la_verify", "la_commit", "LaError", "load_library", "SCHEDULES", "DEV_ERR_BAD_SEQLENS",
            "DEV_ERR_BAD_INDEX", "DEV_ERR_TIMEOUT", "EXPORTED_SYMBOLS"]
 
 SCHEDULES = {"auto": 0, "persistent": 1, "non_persistent": 2}
@@ -22,7 +23,8 @@ DEV_ERR_BAD_SEQLENS = 1
 DEV_ERR_BAD_INDEX = 2
 DEV_ERR_TIMEOUT = 4
 EXPORTED_SYMBOLS = ("la_prefill_fwd", "la_status_string", "la_last_error", "la_prefill_smem_bytes",
-                    "la_prefill_trace_events", "la_prefill_set_trace_buffer")
+                    "la_prefill_trace_events", "la_prefill_set_trace_buffer", "la_decode_mtp", "la_verify",
+                    "la_commit")
 
 _lock = threading.Lock()
 _lib = None
@@ -58,6 +60,13 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.la_last_error.restype = ctypes.c_char_p
             lib.la_prefill_smem_bytes.argtypes = []
             lib.la_prefill_smem_bytes.restype = ctypes.c_int
+            ints = [ctypes.c_int] * 7  # B, T, H, HV, D, V, pool_size
+            lib.la_decode_mtp.argtypes = [vp, vp, vp, fp, ctypes.c_float, fp, i32p, vp] + ints + [vp, vp]
+            lib.la_decode_mtp.restype = ctypes.c_int
+            lib.la_verify.argtypes = [vp, vp, vp, fp, ctypes.c_float, fp, i32p, vp, vp, vp] + ints + [vp, vp]
+            lib.la_verify.restype = ctypes.c_int
+            lib.la_commit.argtypes = [fp, i32p, vp, vp, i32p, fp] + ints + [vp, vp]
+            lib.la_commit.restype = ctypes.c_int
             _lib = lib
         return _lib
 
@@ -151,6 +160,96 @@ def la_prefill_fwd(q, k, v, slopes, scale, h0=None, state_indices=None, cu_seqle
     if st != 0:
         raise LaError(st, lib.la_status_string(st).decode(), lib.la_last_error().decode())
     return o
+
+
+def _decode_common(q, k, v, slopes, state, state_indices, T, dev_error, stream):
+    """Shape checks shared by the speculative-decoding ops; returns (lib, B, H, HV, pool, stream)."""
+    import torch
+    lib = load_library()
+    for t, name, dt, nd in ((q, "q", torch.bfloat16, 3), (k, "k", torch.bfloat16, 3), (v, "v", torch.bfloat16, 3),
+                            (slopes, "slopes", torch.float32, 1), (state, "state", torch.float32, 4),
+                            (state_indices, "state_indices", torch.int32, 1), (dev_error, "dev_error", torch.int32, 1)):
+        _check(t, name, dt, nd)
+    T = int(T)
+    if T < 1:
+        raise ValueError("T must be >= 1")
+    tokens, H, D = q.shape
+    _, HV, V = v.shape
+    if k.shape != q.shape or v.shape[0] != tokens or tokens % T:
+        raise ValueError("q, k: [B*T, H, 128]; v: [B*T, HV, 128] with the same B*T")
+    B = tokens // T
+    if tuple(state.shape[1:]) != (HV, V, D):
+        raise ValueError("state must be [P, HV, V, D]")
+    if state_indices is not None and state_indices.shape[0] != B:
+        raise ValueError("state_indices must have B entries")
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif not isinstance(stream, int):
+        stream = stream.cuda_stream
+    return lib, B, H, HV, state.shape[0], stream
+
+
+def _raise(lib, st):
+    if st != 0:
+        raise LaError(st, lib.la_status_string(st).decode(), lib.la_last_error().decode())
+
+
+def la_decode_mtp(q, k, v, slopes, scale, state, T, state_indices=None, o=None, dev_error=None, stream=None):
+    """Multi-token decode: advance each request's pooled state over its T draft tokens (in
+    place) and return the outputs o (bf16 [B*T, HV, 128])."""
+    import torch
+    lib, B, H, HV, pool, stream = _decode_common(q, k, v, slopes, state, state_indices, T, dev_error, stream)
+    if o is None:
+        o = torch.empty(v.shape, dtype=torch.bfloat16, device=q.device)
+    _check(o, "o", torch.bfloat16, 3)
+    _raise(lib, lib.la_decode_mtp(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes), ctypes.c_float(scale), _ptr(state),
+                                  _ptr(state_indices), _ptr(o), B, int(T), H, HV, q.shape[2], v.shape[2], pool,
+                                  _ptr(dev_error), ctypes.c_void_p(stream)))
+    return o
+
+
+def la_verify(q, k, v, slopes, scale, state, T, state_indices=None, o=None, kbuf=None, vbuf=None, dev_error=None,
+              stream=None):
+    """Parallel verify: the outputs of all T draft tokens from the pooled states, which are
+    left untouched; with kbuf/vbuf (bf16 [P, T, H, 128] / [P, T, HV, 128]) the draft k, v
+    are copied to the request's slot for la_commit.  Returns o."""
+    import torch
+    lib, B, H, HV, pool, stream = _decode_common(q, k, v, slopes, state, state_indices, T, dev_error, stream)
+    if o is None:
+        o = torch.empty(v.shape, dtype=torch.bfloat16, device=q.device)
+    _check(o, "o", torch.bfloat16, 3)
+    _check(kbuf, "kbuf", torch.bfloat16, 4)
+    _check(vbuf, "vbuf", torch.bfloat16, 4)
+    _raise(lib, lib.la_verify(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes), ctypes.c_float(scale), _ptr(state),
+                              _ptr(state_indices), _ptr(o), _ptr(kbuf), _ptr(vbuf), B, int(T), H, HV, q.shape[2],
+                              v.shape[2], pool, _ptr(dev_error), ctypes.c_void_p(stream)))
+    return o
+
+
+def la_commit(state, kbuf, vbuf, accepted_len, slopes, state_indices=None, dev_error=None, stream=None):
+    """Commit: advance each request's pooled state (in place) by its accepted prefix of the
+    draft tokens held in kbuf/vbuf; accepted_len is int32 [B] (0 = no-op)."""
+    import torch
+    lib = load_library()
+    _check(state, "state", torch.float32, 4)
+    _check(kbuf, "kbuf", torch.bfloat16, 4)
+    _check(vbuf, "vbuf", torch.bfloat16, 4)
+    _check(accepted_len, "accepted_len", torch.int32, 1)
+    _check(slopes, "slopes", torch.float32, 1)
+    _check(state_indices, "state_indices", torch.int32, 1)
+    _check(dev_error, "dev_error", torch.int32, 1)
+    P, T, H, D = kbuf.shape
+    HV, V = state.shape[1], state.shape[2]
+    if tuple(vbuf.shape) != (P, T, HV, V) or state.shape[0] != P:
+        raise ValueError("kbuf [P, T, H, D], vbuf [P, T, HV, V] and state [P, HV, V, D] must agree")
+    B = accepted_len.shape[0]
+    if stream is None:
+        stream = torch.cuda.current_stream(state.device).cuda_stream
+    elif not isinstance(stream, int):
+        stream = stream.cuda_stream
+    _raise(lib, lib.la_commit(_ptr(state), _ptr(state_indices), _ptr(kbuf), _ptr(vbuf), _ptr(accepted_len),
+                              _ptr(slopes), B, T, H, HV, D, V, P, _ptr(dev_error), ctypes.c_void_p(stream)))
+    return state
 
 
 def la_prefill_fwd_raw(*args):

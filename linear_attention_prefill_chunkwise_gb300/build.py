@@ -1,6 +1,7 @@
 """Compile the sm_103a C-ABI library ``libla_prefill.so`` in-tree.
 
-One translation unit, one ``-gencode`` (sm_103a), static CUDA runtime, no
+Two translation units (prefill; speculative-decoding ops), one ``-gencode`` (sm_103a),
+static CUDA runtime, no
 link-time dependency on the driver library (the tensor-map encoder is fetched
 through the runtime's driver entry-point query), so the library loads on a
 machine without a GPU.
@@ -19,8 +20,10 @@ LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 TRACE_LIB_PATH = os.path.join(BUILD_DIR, "libla_prefill_trace.so")
 INCLUDE_DIR = os.path.join(os.path.dirname(HERE), "include")
 
-SOURCES = ["la_prefill_api.cu"]
-DEPENDS = ["la_prefill_api.cu", "la_prefill_kernel.cuh", "sm103_ptx.cuh"]
+SOURCES = ["la_prefill_api.cu", "la_decode_api.cu"]
+DEPENDS = ["la_prefill_api.cu", "la_prefill_kernel.cuh", "sm103_ptx.cuh", "la_decode_api.cu", "la_decode_kernels.cuh",
+           "la_host_common.h"]
+HEADERS = ["la_prefill.h", "la_decode.h"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -36,7 +39,7 @@ def _stale(path: str) -> bool:
     if not os.path.exists(path):
         return True
     t = os.path.getmtime(path)
-    deps = [os.path.join(CSRC, d) for d in DEPENDS] + [os.path.join(INCLUDE_DIR, "la_prefill.h")]
+    deps = [os.path.join(CSRC, d) for d in DEPENDS] + [os.path.join(INCLUDE_DIR, h) for h in HEADERS]
     return any(os.path.getmtime(d) > t for d in deps)
 
 

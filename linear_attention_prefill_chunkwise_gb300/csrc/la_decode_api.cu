@@ -1,0 +1,136 @@
+// la_decode_api.cu -- host side of the C ABI declared in include/la_decode.h: argument
+// validation and one launch per call (one CTA per (request, value head)).  Nothing here
+// allocates device memory, reads device memory or synchronises with the host.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/la_decode.h"
+#include "la_decode_kernels.cuh"
+#include "la_host_common.h"
+
+namespace {
+
+using la_host::aligned16;
+using la_host::aligned4;
+using la_host::fail;
+
+la_host::DeviceState g_dev[la_host::kMaxDevices];
+
+// Shape checks shared by the three entry points.
+la_status check_shapes(int B, int T, int H, int HV, int D, int V, int pool_size, const int32_t* state_indices) {
+  if (D != lad::kDim || V != lad::kDim)
+    return fail(LA_ERR_UNSUPPORTED, "only D == V == 128 is implemented (got D=%d, V=%d)", D, V);
+  if (H <= 0 || HV <= 0) return fail(LA_ERR_INVALID_ARGUMENT, "H and HV must be positive (got %d, %d)", H, HV);
+  if (HV % H != 0) return fail(LA_ERR_UNSUPPORTED, "HV (%d) must be a multiple of H (%d)", HV, H);
+  if (B < 0) return fail(LA_ERR_INVALID_ARGUMENT, "B must be >= 0 (got %d)", B);
+  if (T < 1) return fail(LA_ERR_INVALID_ARGUMENT, "T must be >= 1 (got %d)", T);
+  if (static_cast<int64_t>(B) * HV > INT32_MAX || static_cast<int64_t>(B) * T > INT32_MAX)
+    return fail(LA_ERR_UNSUPPORTED, "B*HV or B*T too large");
+  if (state_indices ? pool_size <= 0 : pool_size < B)
+    return fail(LA_ERR_INVALID_ARGUMENT, "pool_size (%d) must be positive, and >= B (%d) without state_indices",
+                pool_size, B);
+  if (!aligned4(state_indices)) return fail(LA_ERR_INVALID_ARGUMENT, "state_indices must be 4-byte aligned");
+  return LA_OK;
+}
+
+template <int kMode>
+la_status launch(const lad::Params& p, void* stream) {
+  la_host::DeviceState* ds = nullptr;
+  la_status st = la_host::current_device(g_dev, &ds, [] { return cudaSuccess; });
+  if (st != LA_OK) return st;
+  const int grid = p.B * p.HV;
+  lad::la_tokenwise_kernel<kMode><<<grid, lad::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(p);
+  const cudaError_t ce = cudaGetLastError();
+  if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(ce));
+  return LA_OK;
+}
+
+lad::Params base_params(const float* slopes, float scale, float* state, const int32_t* state_indices, int* dev_error,
+                        int B, int T, int H, int HV, int pool_size) {
+  lad::Params p{};
+  p.slopes = slopes;
+  p.state = state;
+  p.state_indices = state_indices;
+  p.dev_error = dev_error;
+  p.scale = scale;
+  p.B = B;
+  p.T = T;
+  p.H = H;
+  p.HV = HV;
+  p.G = HV / H;
+  p.pool_size = pool_size;
+  return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+la_status la_decode_mtp(const void* q, const void* k, const void* v, const float* slopes, float scale,
+                        float* state, const int32_t* state_indices, void* o, int B, int T, int H, int HV, int D,
+                        int V, int pool_size, int* dev_error, void* stream) {
+  la_host::g_last_error[0] = '\0';
+  la_status st = check_shapes(B, T, H, HV, D, V, pool_size, state_indices);
+  if (st != LA_OK) return st;
+  if (B == 0) return LA_OK;
+  if (!q || !k || !v || !o || !state || !slopes)
+    return fail(LA_ERR_INVALID_ARGUMENT, "q, k, v, o, state and slopes must be non-null");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(state) || !aligned4(slopes) ||
+      !aligned4(dev_error))
+    return fail(LA_ERR_INVALID_ARGUMENT, "q, k, v, o, state must be 16-byte and slopes, dev_error 4-byte aligned");
+  lad::Params p = base_params(slopes, scale, state, state_indices, dev_error, B, T, H, HV, pool_size);
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.o = static_cast<__nv_bfloat16*>(o);
+  return launch<lad::kDecode>(p, stream);
+}
+
+la_status la_verify(const void* q, const void* k, const void* v, const float* slopes, float scale,
+                    const float* state, const int32_t* state_indices, void* o, void* kbuf, void* vbuf, int B, int T,
+                    int H, int HV, int D, int V, int pool_size, int* dev_error, void* stream) {
+  la_host::g_last_error[0] = '\0';
+  la_status st = check_shapes(B, T, H, HV, D, V, pool_size, state_indices);
+  if (st != LA_OK) return st;
+  if (B == 0) return LA_OK;
+  if (!q || !k || !v || !o || !state || !slopes)
+    return fail(LA_ERR_INVALID_ARGUMENT, "q, k, v, o, state and slopes must be non-null");
+  if ((kbuf == nullptr) != (vbuf == nullptr))
+    return fail(LA_ERR_INVALID_ARGUMENT, "kbuf and vbuf must be both given or both null");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(state) || !aligned16(kbuf) ||
+      !aligned16(vbuf) || !aligned4(slopes) || !aligned4(dev_error))
+    return fail(LA_ERR_INVALID_ARGUMENT,
+                "q, k, v, o, state, kbuf, vbuf must be 16-byte and slopes, dev_error 4-byte aligned");
+  lad::Params p = base_params(slopes, scale, const_cast<float*>(state), state_indices, dev_error, B, T, H, HV,
+                              pool_size);
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.k = static_cast<const __nv_bfloat16*>(k);
+  p.v = static_cast<const __nv_bfloat16*>(v);
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.kbuf = static_cast<__nv_bfloat16*>(kbuf);
+  p.vbuf = static_cast<__nv_bfloat16*>(vbuf);
+  return launch<lad::kVerify>(p, stream);
+}
+
+la_status la_commit(float* state, const int32_t* state_indices, const void* kbuf, const void* vbuf,
+                    const int32_t* accepted_len, const float* slopes, int B, int T, int H, int HV, int D, int V,
+                    int pool_size, int* dev_error, void* stream) {
+  la_host::g_last_error[0] = '\0';
+  la_status st = check_shapes(B, T, H, HV, D, V, pool_size, state_indices);
+  if (st != LA_OK) return st;
+  if (B == 0) return LA_OK;
+  if (!state || !kbuf || !vbuf || !accepted_len || !slopes)
+    return fail(LA_ERR_INVALID_ARGUMENT, "state, kbuf, vbuf, accepted_len and slopes must be non-null");
+  if (!aligned16(state) || !aligned16(kbuf) || !aligned16(vbuf) || !aligned4(accepted_len) || !aligned4(slopes) ||
+      !aligned4(dev_error))
+    return fail(LA_ERR_INVALID_ARGUMENT,
+                "state, kbuf, vbuf must be 16-byte and accepted_len, slopes, dev_error 4-byte aligned");
+  lad::Params p = base_params(slopes, 0.f, state, state_indices, dev_error, B, T, H, HV, pool_size);
+  p.kbuf = const_cast<__nv_bfloat16*>(static_cast<const __nv_bfloat16*>(kbuf));
+  p.vbuf = const_cast<__nv_bfloat16*>(static_cast<const __nv_bfloat16*>(vbuf));
+  p.accepted_len = accepted_len;
+  return launch<lad::kCommit>(p, stream);
+}
+
+}  // extern "C"

@@ -8,29 +8,21 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
-#include <cstdarg>
 #include <cstdint>
-#include <cstdio>
 #include <cstring>
 #include <mutex>
 
 #include "../../include/la_prefill.h"
+#include "la_host_common.h"
 #include "la_prefill_kernel.cuh"
 
 namespace {
 
-thread_local char g_last_error[512] = "";
+using la_host::aligned16;
+using la_host::fail;
+using la_host::g_last_error;
+
 unsigned long long* g_trace = nullptr;  // device buffer for timeline tracing builds
-
-la_status fail(la_status st, const char* fmt, ...) {
-  va_list ap;
-  va_start(ap, fmt);
-  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
-  va_end(ap);
-  return st;
-}
-
-bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static std::once_flag once;
@@ -46,16 +38,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// Per-device facts looked up once: SM count and whether the kernel's shared-memory
-// attribute has been set.
-constexpr int kMaxDevices = 64;
-struct DeviceState {
-  std::once_flag once;
-  cudaError_t status = cudaSuccess;
-  int sms = 0;
-  int cc_major = 0, cc_minor = 0;
-};
-DeviceState g_dev[kMaxDevices];
+// Per-device facts looked up once: SM count, and the kernel's shared-memory attribute set.
+la_host::DeviceState g_dev[la_host::kMaxDevices];
 
 int smem_bytes() { return static_cast<int>(sizeof(lap::SharedStorage)) + 1024; }
 
@@ -146,25 +130,14 @@ la_status la_prefill_fwd(const void* q, const void* k, const void* v, const floa
   if (tokens == 0 && !h_final) return LA_OK;  // no output rows and no state to write
 
   // ---- device
-  int dev = 0;
-  cudaError_t ce = cudaGetDevice(&dev);
-  if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(ce));
-  if (dev < 0 || dev >= kMaxDevices) return fail(LA_ERR_CUDA, "device ordinal %d out of range", dev);
-  DeviceState& ds = g_dev[dev];
-  std::call_once(ds.once, [&ds, dev] {
-    cudaError_t e = cudaDeviceGetAttribute(&ds.sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&ds.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
-    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&ds.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(lap::la_prefill_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               smem_bytes());
-    ds.status = e;
+  la_host::DeviceState* dsp = nullptr;
+  la_status dst = la_host::current_device(g_dev, &dsp, [] {
+    return cudaFuncSetAttribute(lap::la_prefill_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                smem_bytes());
   });
-  if (ds.status != cudaSuccess)
-    return fail(LA_ERR_CUDA, "device %d setup failed: %s", dev, cudaGetErrorString(ds.status));
-  if (ds.cc_major != 10 || ds.cc_minor != 3)
-    return fail(LA_ERR_CUDA, "device %d is sm_%d%d; this library is built for sm_103a only", dev, ds.cc_major,
-                ds.cc_minor);
+  if (dst != LA_OK) return dst;
+  la_host::DeviceState& ds = *dsp;
+  cudaError_t ce;
 
   // ---- tensor maps (unused when there are no tokens)
   CUtensorMap tm_q, tm_k, tm_v;

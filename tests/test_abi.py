@@ -94,3 +94,51 @@ def test_product_path_does_not_touch_the_oracle():
             if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
                 text = open(os.path.join(dirpath, f)).read()
                 assert "oracle" not in text.lower(), f"{f} mentions the oracle"
+
+
+def call_decode(fn="la_decode_mtp", **over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, slopes=FAKE, scale=1.0, state=FAKE, idx=None, o=FAKE, kbuf=None, vbuf=None,
+             acc=FAKE, B=2, T=8, H=2, HV=2, D=128, V=128, P=2, err=None, stream=None)
+    a.update(over)
+    lib = lap.load_library()
+    ints = (a["B"], a["T"], a["H"], a["HV"], a["D"], a["V"], a["P"])
+    if fn == "la_decode_mtp":
+        return lib.la_decode_mtp(a["q"], a["k"], a["v"], a["slopes"], ctypes.c_float(a["scale"]), a["state"], a["idx"],
+                                 a["o"], *ints, a["err"], a["stream"])
+    if fn == "la_verify":
+        return lib.la_verify(a["q"], a["k"], a["v"], a["slopes"], ctypes.c_float(a["scale"]), a["state"], a["idx"],
+                             a["o"], a["kbuf"], a["vbuf"], *ints, a["err"], a["stream"])
+    return lib.la_commit(a["state"], a["idx"], a["kbuf"], a["vbuf"], a["acc"], a["slopes"], *ints, a["err"],
+                         a["stream"])
+
+
+@pytest.mark.parametrize("fn,over,status", [
+    ("la_decode_mtp", dict(D=64), LA_UNSUPPORTED),
+    ("la_decode_mtp", dict(H=3, HV=4), LA_UNSUPPORTED),
+    ("la_decode_mtp", dict(T=0), LA_INVALID),
+    ("la_decode_mtp", dict(B=-1), LA_INVALID),
+    ("la_decode_mtp", dict(P=1), LA_INVALID),             # pool smaller than B without indices
+    ("la_decode_mtp", dict(idx=FAKE, P=0), LA_INVALID),   # empty pool with indices
+    ("la_decode_mtp", dict(state=None), LA_INVALID),
+    ("la_decode_mtp", dict(o=FAKE + 4), LA_INVALID),      # misaligned
+    ("la_verify", dict(kbuf=FAKE), LA_INVALID),           # kbuf without vbuf
+    ("la_verify", dict(V=64), LA_UNSUPPORTED),
+    ("la_commit", dict(kbuf=FAKE, vbuf=FAKE, acc=None), LA_INVALID),
+    ("la_commit", dict(kbuf=None, vbuf=FAKE), LA_INVALID),
+    ("la_commit", dict(kbuf=FAKE, vbuf=FAKE, acc=FAKE + 2), LA_INVALID),
+])
+def test_decode_host_validation(fn, over, status):
+    assert call_decode(fn, **over) == status
+    assert lap.load_library().la_last_error() != b""
+
+
+def test_decode_empty_batch_is_a_no_op():
+    for fn in ("la_decode_mtp", "la_verify", "la_commit"):
+        assert call_decode(fn, B=0, kbuf=FAKE, vbuf=FAKE) == LA_OK
+
+
+def test_decode_no_device_is_reported():
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert call_decode("la_decode_mtp") == LA_CUDA
