@@ -7,18 +7,29 @@
 // (request, value head) unit costs one read of its 64 KB FP32 state, T token updates and,
 // for decode and commit, one write of the state: the work is bound by the state traffic,
 // and the state fits the registers of one CTA.  One CTA of 256 threads per unit: thread t
-// owns state row v = t / 2, columns k in [64 (t % 2), 64 (t % 2) + 64), and for every token
+// owns the 4 x 16 block of state rows v = 4 (t / 8) .. +3 and columns k = 16 (t % 8) .. +15,
+// and for every token
 //     S[v][k] = lambda S[v][k] + v_t[v] k_t[k]              (FP32, fused multiply-add)
-//     o_t[v]  = scale sum_k S[v][k] q_t[k]                    (two half-row partial sums)
-// with the tokens' q, k, v staged in shared memory as FP32, 16 tokens at a time.  The three
-// operations run this same per-token code, so a commit of all T tokens leaves bitwise the
-// state a decode leaves, and verify's outputs are bitwise decode's.
+//     o_t[v]  = scale sum_k S[v][k] q_t[k]                    (8 column-group partial sums,
+//                                                             added across lanes t^1, t^2, t^4)
+// with the tokens' q, k, v staged in shared memory as FP32, 16 tokens at a time.  Each staged
+// k or q value feeds four rows, which keeps the shared-memory traffic per FMA low; the column
+// groups are padded to 20 floats so that the 8 groups a warp reads sit in distinct banks.
+// The three operations run this same per-token code, so a commit of all T tokens leaves
+// bitwise the state a decode leaves, and verify's outputs are bitwise decode's.
 #pragma once
 
 #include <cuda_bf16.h>
 #include <cstdint>
 
+#include "sm103_ptx.cuh"
+
 namespace lad {
+
+using lap::f2_fma;
+using lap::f2_mul;
+using lap::f2_pack;
+using lap::f2_unpack;
 
 constexpr int kDim = 128;   // D = V = 128
 constexpr int kThreads = 256;
@@ -52,10 +63,12 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& x, float (&f)[8]) {
   }
 }
 
+constexpr int kGroupStride = 20;  // floats per staged 16-column group (16 + 4 padding)
+
 template <int kMode>
 __global__ void __launch_bounds__(kThreads, 2) la_tokenwise_kernel(const Params p) {
-  __shared__ __align__(16) float ks[kTileT][kDim];
-  __shared__ __align__(16) float qs[kTileT][kDim];
+  __shared__ __align__(16) float ks[kTileT][8 * kGroupStride];
+  __shared__ __align__(16) float qs[kTileT][8 * kGroupStride];
   __shared__ __align__(16) float vs[kTileT][kDim];
 
   const int unit = blockIdx.x;  // b * HV + hv
@@ -78,20 +91,21 @@ __global__ void __launch_bounds__(kThreads, 2) la_tokenwise_kernel(const Params 
   }
 
   const int t = threadIdx.x;
-  const int vrow = t >> 1, kh = t & 1;
+  const int cg = t & 7, rg = t >> 3;  // columns 16 cg .. +15, rows 4 rg .. +3
   const float lam = expf(-__ldg(p.slopes + hv));
+  const uint64_t lam2 = f2_pack(lam, lam);
 
-  // ---- state row v, columns 64 kh .. 64 kh + 63
-  float S[64];
-  float* srow = p.state + ((static_cast<size_t>(slot) * p.HV + hv) * kDim + vrow) * kDim + 64 * kh;
+  // ---- state block: S[r][j] pairs = (S[4 rg + r][16 cg + 2 j], S[4 rg + r][16 cg + 2 j + 1])
+  uint64_t S[4][8];
+  float* sblk = p.state + ((static_cast<size_t>(slot) * p.HV + hv) * kDim + 4 * rg) * kDim + 16 * cg;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const float4 x = __ldg(reinterpret_cast<const float4*>(srow) + i);
-    S[4 * i] = x.x;
-    S[4 * i + 1] = x.y;
-    S[4 * i + 2] = x.z;
-    S[4 * i + 3] = x.w;
-  }
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 x = __ldg(reinterpret_cast<const float4*>(sblk + r * kDim) + i);
+      S[r][2 * i] = f2_pack(x.x, x.y);
+      S[r][2 * i + 1] = f2_pack(x.z, x.w);
+    }
 
   const size_t qk_tok = static_cast<size_t>(p.H) * kDim;   // elements between tokens of q / k
   const size_t v_tok = static_cast<size_t>(p.HV) * kDim;   // ... of v / o
@@ -100,7 +114,8 @@ __global__ void __launch_bounds__(kThreads, 2) la_tokenwise_kernel(const Params 
     __syncthreads();  // the previous tile has been consumed
     // Stage tokens t0 .. t0 + nt - 1: 16 bytes (8 values) per thread and array per step.
     for (int e = t; e < nt * (kDim / 8); e += kThreads) {
-      const int i = e >> 4, c = e & 15;
+      const int i = e >> 4, c = e & 15;              // token, 8-value chunk (column group c / 2)
+      const int kpos = (c >> 1) * kGroupStride + 8 * (c & 1);
       uint4 kx, vx;
       if (kMode == kCommit) {
         kx = __ldg(reinterpret_cast<const uint4*>(p.kbuf + ((static_cast<size_t>(slot) * p.T + t0 + i) * p.H + hq) *
@@ -114,8 +129,8 @@ __global__ void __launch_bounds__(kThreads, 2) la_tokenwise_kernel(const Params 
         const uint4 qx = __ldg(reinterpret_cast<const uint4*>(p.q + row * qk_tok + static_cast<size_t>(hq) * kDim) + c);
         float f[8];
         bf16x8_to_f32(qx, f);
-        reinterpret_cast<float4*>(&qs[i][8 * c])[0] = make_float4(f[0], f[1], f[2], f[3]);
-        reinterpret_cast<float4*>(&qs[i][8 * c])[1] = make_float4(f[4], f[5], f[6], f[7]);
+        reinterpret_cast<float4*>(&qs[i][kpos])[0] = make_float4(f[0], f[1], f[2], f[3]);
+        reinterpret_cast<float4*>(&qs[i][kpos])[1] = make_float4(f[4], f[5], f[6], f[7]);
         if (kMode == kVerify && p.kbuf) {  // the KV buffer copy (k once per q/k head)
           const size_t brow = static_cast<size_t>(slot) * p.T + t0 + i;
           if (hv % p.G == 0)
@@ -125,8 +140,8 @@ __global__ void __launch_bounds__(kThreads, 2) la_tokenwise_kernel(const Params 
       }
       float f[8];
       bf16x8_to_f32(kx, f);
-      reinterpret_cast<float4*>(&ks[i][8 * c])[0] = make_float4(f[0], f[1], f[2], f[3]);
-      reinterpret_cast<float4*>(&ks[i][8 * c])[1] = make_float4(f[4], f[5], f[6], f[7]);
+      reinterpret_cast<float4*>(&ks[i][kpos])[0] = make_float4(f[0], f[1], f[2], f[3]);
+      reinterpret_cast<float4*>(&ks[i][kpos])[1] = make_float4(f[4], f[5], f[6], f[7]);
       bf16x8_to_f32(vx, f);
       reinterpret_cast<float4*>(&vs[i][8 * c])[0] = make_float4(f[0], f[1], f[2], f[3]);
       reinterpret_cast<float4*>(&vs[i][8 * c])[1] = make_float4(f[4], f[5], f[6], f[7]);
@@ -134,42 +149,63 @@ __global__ void __launch_bounds__(kThreads, 2) la_tokenwise_kernel(const Params 
     __syncthreads();
 
     for (int i = 0; i < nt; ++i) {
-      const float vv = vs[i][vrow];
-      const float4* kr = reinterpret_cast<const float4*>(&ks[i][64 * kh]);
+      const float4 vv = *reinterpret_cast<const float4*>(&vs[i][4 * rg]);
+      const float vr[4] = {vv.x, vv.y, vv.z, vv.w};
+      uint64_t kk[8];
+      {
+        const float4* kr = reinterpret_cast<const float4*>(&ks[i][cg * kGroupStride]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float4 x = kr[j];
+          kk[2 * j] = f2_pack(x.x, x.y);
+          kk[2 * j + 1] = f2_pack(x.z, x.w);
+        }
+      }
       // S = lambda S + v_t[v] k_t
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float4 kk = kr[j];
-        S[4 * j] = fmaf(vv, kk.x, lam * S[4 * j]);
-        S[4 * j + 1] = fmaf(vv, kk.y, lam * S[4 * j + 1]);
-        S[4 * j + 2] = fmaf(vv, kk.z, lam * S[4 * j + 2]);
-        S[4 * j + 3] = fmaf(vv, kk.w, lam * S[4 * j + 3]);
+      for (int r = 0; r < 4; ++r) {
+        const uint64_t v2 = f2_pack(vr[r], vr[r]);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) S[r][j] = f2_fma(v2, kk[j], f2_mul(lam2, S[r][j]));
       }
       if (kMode != kCommit) {
-        // o_t[v] = scale S[v] . q_t: four partial sums per half row, then the two halves
-        const float4* qr = reinterpret_cast<const float4*>(&qs[i][64 * kh]);
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        // o_t[v] = scale S[v] . q_t over this thread's 16 columns, then across the 8 groups
+        uint64_t qq[8];
+        const float4* qr = reinterpret_cast<const float4*>(&qs[i][cg * kGroupStride]);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const float4 qq = qr[j];
-          a0 = fmaf(S[4 * j], qq.x, a0);
-          a1 = fmaf(S[4 * j + 1], qq.y, a1);
-          a2 = fmaf(S[4 * j + 2], qq.z, a2);
-          a3 = fmaf(S[4 * j + 3], qq.w, a3);
+        for (int j = 0; j < 4; ++j) {
+          const float4 x = qr[j];
+          qq[2 * j] = f2_pack(x.x, x.y);
+          qq[2 * j + 1] = f2_pack(x.z, x.w);
         }
-        float dot = (a0 + a1) + (a2 + a3);
-        dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-        if (kh == 0)
-          p.o[(static_cast<size_t>(b) * p.T + t0 + i) * v_tok + static_cast<size_t>(hv) * kDim + vrow] =
-              __float2bfloat16_rn(p.scale * dot);
+        float dot[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          uint64_t acc = f2_pack(0.f, 0.f);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc = f2_fma(S[r][j], qq[j], acc);
+          const float2 a2 = f2_unpack(acc);
+          dot[r] = a2.x + a2.y;
+        }
+#pragma unroll
+        for (int m = 1; m < 8; m <<= 1)
+#pragma unroll
+          for (int r = 0; r < 4; ++r) dot[r] += __shfl_xor_sync(0xffffffffu, dot[r], m);
+        if (cg < 4)  // lane group cg writes row 4 rg + cg
+          p.o[(static_cast<size_t>(b) * p.T + t0 + i) * v_tok + static_cast<size_t>(hv) * kDim + 4 * rg + cg] =
+              __float2bfloat16_rn(p.scale * (cg == 0 ? dot[0] : cg == 1 ? dot[1] : cg == 2 ? dot[2] : dot[3]));
       }
     }
   }
 
   if (kMode != kVerify) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-      reinterpret_cast<float4*>(srow)[i] = make_float4(S[4 * i], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 a = f2_unpack(S[r][2 * i]), c = f2_unpack(S[r][2 * i + 1]);
+        reinterpret_cast<float4*>(sblk + r * kDim)[i] = make_float4(a.x, a.y, c.x, c.y);
+      }
   }
 }
 
