@@ -184,6 +184,24 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x, world, device=None):
+    """The largest of every rank's ``x`` (the slowest rank's time); ``x`` itself on one rank.
+    Uses the default process group (NCCL with CUDA tensors, gloo with CPU tensors)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, steps, world, slowest_ms):
+    """Whole-job throughput of ``world`` replicas, each processing ``units_per_rank`` per step,
+    over ``steps`` steps that took ``slowest_ms`` on the slowest rank."""
+    return world * units_per_rank * steps / (slowest_ms / 1e3)
+
+
 def make_inputs(device):
     import numpy as np
     import torch
@@ -247,13 +265,9 @@ def run_cuda(args):
         clk.mark_end()
     barrier()
     per_launch_ms = [ev[i].elapsed_time(ev[i + 1]) for i in range(args.steps)]
-    total_ms = ev[0].elapsed_time(ev[-1])
-    if world > 1:
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(ev[0].elapsed_time(ev[-1]), world, device)
     ms_per_step = total_ms / args.steps
-    value = world * TOKENS * args.steps / (total_ms / 1e3)
+    value = job_throughput(TOKENS, args.steps, world, total_ms)
 
     # ---- end to end through the public API: pinned host inputs in, results out, every step
     pinned = {k_: t.pin_memory() for k_, t in host.items()}
@@ -285,12 +299,8 @@ def run_cuda(args):
             e2e_step()
         e1.record(stream)
     torch.cuda.synchronize(device)
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = world * TOKENS * e2e_steps / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
+    e2e_value = job_throughput(TOKENS, e2e_steps, world, e2e_ms)
 
     if rank == 0:
         peak, peak_kind = measured_peaks()

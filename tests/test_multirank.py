@@ -1,0 +1,68 @@
+"""The multi-rank host logic of bench.py on the CPU: two gloo ranks on 127.0.0.1.
+
+The path shards with no exchange (independent (sequence, head) units), so N GPUs run N
+replicas; the bench takes the slowest rank's time (a max all-reduce) and reports the
+whole-job throughput, and only rank 0 runs the reference arm and prints."""
+import os
+import socket
+
+import pytest
+
+torch = pytest.importorskip("torch")
+import torch.distributed as dist  # noqa: E402
+import torch.multiprocessing as mp  # noqa: E402
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def worker(rank, world, port, out):
+    import sys
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    import bench
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    r, w, local = bench.dist_env()
+    slowest = bench.max_over_ranks(10.0 + 5.0 * rank, w)  # rank 1 is the slow one
+    value = bench.job_throughput(1000, 4, w, slowest)
+    out[rank] = (r, w, local, slowest, value)
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_the_slowest_rank_and_sum_the_work():
+    world = 2
+    with mp.Manager() as m:
+        out = m.dict()
+        mp.spawn(worker, args=(world, free_port(), out), nprocs=world, join=True)
+        res = dict(out)
+    for rank in range(world):
+        r, w, local, slowest, value = res[rank]
+        assert (r, w, local) == (rank, world, rank)
+        assert slowest == 15.0                      # the max over ranks, on every rank
+        assert value == pytest.approx(2 * 1000 * 4 / 0.015)
+
+
+def test_single_rank_needs_no_process_group():
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(3.5, 1) == 3.5
+    assert bench.job_throughput(16384, 10, 1, 2.0) == pytest.approx(16384 * 10 / 0.002)
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
+    import sys
+    import types
+    sys.path.insert(0, ROOT)
+    import bench
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    bench.run_reference(types.SimpleNamespace(steps=1, warmup=3, ref_budget=1.0))
+    assert capsys.readouterr().out == ""  # no work, no line: rank 0 alone prints
