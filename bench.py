@@ -372,7 +372,7 @@ def run_sweep(args):
     def bf(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
 
-    for i in range(1, 6):
+    for i in (range(1, 6) if args.sweep_what != "decode" else ()):
         p = W.config(i)
         q, k, v = bf(p.q_bits), bf(p.k_bits), bf(p.v_bits)
         sl = torch.from_numpy(p.slopes).to(device)
@@ -414,7 +414,8 @@ def run_sweep(args):
                 "peaks": {"hbm_gbs": hbm, "hbm_source": hbm_kind, "bf16_tflops": tflops, "tflops_source": tf_kind},
                 "steps": args.sweep_steps, "l2": "flushed between launches (256 MB write)"}
         print(json.dumps(line), flush=True)
-    run_decode_sweep(args, device, stream, flush, hbm, hbm_kind)
+    if args.sweep_what != "prefill":
+        run_decode_sweep(args, device, stream, flush, hbm, hbm_kind)
 
 
 def run_decode_sweep(args, device, stream, flush, hbm, hbm_kind):
@@ -565,6 +566,8 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="time every workload (1..5) instead, one JSON line each (not the headline line)")
     ap.add_argument("--sweep-steps", type=int, default=50)
+    ap.add_argument("--sweep-what", choices=["all", "prefill", "decode"], default="all",
+                    help="with --sweep: the five prefill workloads, the speculative-decoding ops, or both")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
