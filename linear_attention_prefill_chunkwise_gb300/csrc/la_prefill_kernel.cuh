@@ -415,7 +415,7 @@ __device__ __forceinline__ void mma_o_loop(SharedStorage& sm, const KernelParams
     LA_TRACE_AT(p, kTrMmaOInter, it, true);
     const uint32_t t_o = tmem + kColO + 64 * b;
     const uint64_t qt0 = dqt0 + b * qt_step;
-#pragma unroll
+#pragma unroll 4
     for (int kk = 0; kk < 16; ++kk) {
       const uint32_t off = (kk >> 2) * kTileBytes + (kk & 3) * 32;
       mma_tf32_ts(t_o, t_state + kk * 8, desc_at(qt0, off), id_ointer, kk > 0);
@@ -518,7 +518,7 @@ __device__ __forceinline__ void operand_loop(SharedStorage& sm, const KernelPara
         const float wjf = (krow < L) ? lam[L - 1 - krow] : 0.f;
         const uint64_t wj = f2_pack(wjf, wjf);
         const uint8_t* ksrc = sm.qk[sq].k[kbox];
-#pragma unroll 4
+#pragma unroll 2
         for (int cc = 0; cc < 8; ++cc) {
           const uint32_t off = swz(krow, cc);
           const uint4 kx = *reinterpret_cast<const uint4*>(ksrc + off);
