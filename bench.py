@@ -372,7 +372,7 @@ def run_sweep(args):
     def bf(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
 
-    for i in (range(1, 6) if args.sweep_what != "decode" else ()):
+    for i in (range(1, 6) if args.sweep_what in ("all", "prefill") else ()):
         p = W.config(i)
         q, k, v = bf(p.q_bits), bf(p.k_bits), bf(p.v_bits)
         sl = torch.from_numpy(p.slopes).to(device)
@@ -414,8 +414,10 @@ def run_sweep(args):
                 "peaks": {"hbm_gbs": hbm, "hbm_source": hbm_kind, "bf16_tflops": tflops, "tflops_source": tf_kind},
                 "steps": args.sweep_steps, "l2": "flushed between launches (256 MB write)"}
         print(json.dumps(line), flush=True)
-    if args.sweep_what != "prefill":
+    if args.sweep_what in ("all", "decode"):
         run_decode_sweep(args, device, stream, flush, hbm, hbm_kind)
+    if args.sweep_what in ("all", "segmented"):
+        run_segment_sweep(args, device, stream, flush, hbm, hbm_kind, tflops, tf_kind)
 
 
 def run_decode_sweep(args, device, stream, flush, hbm, hbm_kind):
@@ -478,6 +480,71 @@ def run_decode_sweep(args, device, stream, flush, hbm, hbm_kind):
                           "roofline_ms": round(t_roof * 1e3, 5), "frac": round(t_roof * 1e3 / ms, 4), "bound": "hbm",
                           "peaks": {"hbm_gbs": hbm, "hbm_source": hbm_kind}, "steps": args.sweep_steps,
                           "l2": "flushed between launches (256 MB write)"}), flush=True)
+
+
+SEGMENT_WORKLOADS = (
+    # (seed, B, T, H, HV, name)
+    (2001, 1, 8192, 64, 64, "one 8K prompt, H=HV=64"),
+    (2002, 1, 32768, 16, 16, "B=1 T=32768 H=HV=16 (a 4-way head shard)"),
+    (2003, 1, 65536, 8, 8, "B=1 T=65536 H=HV=8 (an 8-way head shard)"),
+    (2004, 2, 8192, 64, 64, "fixed MHA B=2 T=8192 H=64"),
+)
+
+
+def run_segment_sweep(args, device, stream, flush, hbm, hbm_kind, tflops, tf_kind):
+    """Segmented-sequence prefill against the plain chunkwise prefill on batches with few
+    (sequence, value head) chains: fixed length, random h0, final state returned.  Same
+    timing as the other sweeps; the roofline is the plain prefill's (the segmented path's
+    extra pass over K and V is overhead, not work)."""
+    import numpy as np
+    import torch
+
+    import linear_attention_prefill_chunkwise_gb300 as lap
+    import workloads as W
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                fn()
+            times = []
+            for _ in range(args.sweep_steps):
+                flush.fill_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                times.append((e0, e1))
+        torch.cuda.synchronize(device)
+        return statistics.fmean(a.elapsed_time(b) for a, b in times)
+
+    for seed, B, T, H, HV, name in SEGMENT_WORKLOADS:
+        p = W.custom(seed=seed, B=B, T=T, H=H, HV=HV, name=name)
+        q, k, v = bf(p.q_bits), bf(p.k_bits), bf(p.v_bits)
+        sl = torch.from_numpy(p.slopes).to(device)
+        h0 = torch.from_numpy(p.h0).to(device)
+        o = torch.empty((p.tokens, HV, V), dtype=torch.bfloat16, device=device)
+        hf = torch.empty_like(h0)
+        nbytes_ws, seg = lap.la_prefill_segmented_workspace(B, T, B, HV, False, 0)
+        ws = torch.empty(max(nbytes_ws, 1), dtype=torch.uint8, device=device)
+        ms_plain = timed(lambda: lap.la_prefill_fwd(q, k, v, sl, p.scale, h0=h0, o=o, h_final=hf, seq_len=T,
+                                                    stream=stream))
+        ms_seg = timed(lambda: lap.la_prefill_fwd_segmented(q, k, v, sl, p.scale, h0=h0, o=o, h_final=hf,
+                                                            seq_len=T, segment_len=0, workspace=ws, stream=stream))
+        toks, nbytes, flops = workload_roofline(p)
+        t_roof = max(nbytes / (hbm * 1e9), flops / (tflops * 1e12))
+        print(json.dumps({"sweep": True, "op": "la_prefill_fwd_segmented", "workload": name, "segment_len": seg,
+                          "chains": B * HV, "workspace_bytes": nbytes_ws, "ms": round(ms_seg, 5),
+                          "ms_plain": round(ms_plain, 5), "speedup_vs_plain": round(ms_plain / ms_seg, 3),
+                          "tokens_per_s": round(toks / (ms_seg / 1e3), 1), "alg_bytes": nbytes,
+                          "achieved_gbs": round(nbytes / (ms_seg / 1e3) / 1e9, 1),
+                          "roofline_ms": round(t_roof * 1e3, 5), "frac": round(t_roof * 1e3 / ms_seg, 4),
+                          "frac_plain": round(t_roof * 1e3 / ms_plain, 4),
+                          "peaks": {"hbm_gbs": hbm, "hbm_source": hbm_kind, "bf16_tflops": tflops,
+                                    "tflops_source": tf_kind},
+                          "steps": args.sweep_steps, "l2": "flushed between launches (256 MB write)"}), flush=True)
 
 
 def cpu_baseline(p, heads):
@@ -566,8 +633,9 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="time every workload (1..5) instead, one JSON line each (not the headline line)")
     ap.add_argument("--sweep-steps", type=int, default=50)
-    ap.add_argument("--sweep-what", choices=["all", "prefill", "decode"], default="all",
-                    help="with --sweep: the five prefill workloads, the speculative-decoding ops, or both")
+    ap.add_argument("--sweep-what", choices=["all", "prefill", "decode", "segmented"], default="all",
+                    help="with --sweep: the five prefill workloads, the speculative-decoding ops, the "
+                         "segmented prefill on few-chain batches, or all of them")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -1,0 +1,86 @@
+/*
+ * la_segment.h -- C ABI of the segmented-sequence Lightning Attention prefill (GB300, sm_103a).
+ *
+ * The same operation as la_prefill_fwd (include/la_prefill.h, whose contract every argument
+ * below shares), for batches with few (sequence, value head) chains: a long prefill on a
+ * tensor-parallel shard of a few heads, say, where one chain per SM would leave most of the
+ * GPU idle while each chain walks its chunks in order.  Each sequence is cut into segments
+ * of S tokens.  Since a chain's state is affine in its initial state (a segment of L tokens
+ * maps H to lambda^L H + Sloc, Sloc being the segment run from a zero state), the segments
+ * run in parallel in three passes:
+ *   1. Sloc of every segment but the last of each sequence (tensor cores, reads K and V);
+ *   2. a scan over each sequence's segments: H_0 = h0, H_{i+1} = lambda^{L_i} H_i + Sloc_i;
+ *   3. the chunkwise prefill of every segment from its initial state H_i (la_prefill_fwd's
+ *      kernel), whose last segment leaves the sequence's final state.
+ * The segment-parallel scan is the one page "feat(kda): add bitwise-aligned SM100 CuTeDSL
+ * forward" (Description) describes for a decayed recurrence of the same shape.  The
+ * outputs equal la_prefill_fwd's up to FP32 rounding order (the initial states are exact
+ * sums computed in another order); they are not bitwise equal.
+ *
+ * Cost: pass 1 reads K and V of every segment but the last once more, so it pays off only
+ * when the batch has far fewer chains than SMs.  With segment_len == 0 the library decides:
+ * it runs la_prefill_fwd unchanged (no workspace used) unless N * HV is at most half the SM
+ * count, and otherwise picks S so that the segments fill the SMs about once.
+ *
+ * Every pointer is a DEVICE pointer owned by the caller.  The call allocates nothing, never
+ * synchronises with the host and enqueues its kernels (5 at most) on `stream`.
+ */
+#ifndef LA_SEGMENT_H
+#define LA_SEGMENT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "la_prefill.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * la_prefill_segmented_workspace -- device workspace bytes la_prefill_fwd_segmented needs.
+ *
+ * Same B, T, N, HV and mode (packed = 1 when cu_seqlens will be given) as the call, and the
+ * same segment_len (0 = automatic, resolved with the CURRENT device's SM count; else a
+ * positive multiple of 64).  Writes the byte count to *bytes (0 when the call would run
+ * la_prefill_fwd unchanged) and the resolved segment length to *resolved_segment_len
+ * (nullable; 0 when no segmentation is done).  Errors: LA_ERR_INVALID_ARGUMENT for bad sizes
+ * or a segment_len that is not a positive multiple of 64, LA_ERR_CUDA when the device
+ * query fails.
+ *
+ * The workspace holds one FP32 [128 x 128] state per (segment, value head) -- 64 KiB each --
+ * plus five int32 tables; the segment count is at most N + floor(B*T / S) (packed) or
+ * B * ceil(T / S) (fixed length).
+ */
+la_status la_prefill_segmented_workspace(int B, int T, int N, int HV, int packed, int segment_len, size_t* bytes,
+                                         int* resolved_segment_len);
+
+/*
+ * la_prefill_fwd_segmented -- la_prefill_fwd over segments of segment_len tokens.
+ *
+ * Arguments as la_prefill_fwd (no schedule), plus:
+ *   segment_len      0 = automatic, else a positive multiple of 64 (the same value given to
+ *                    la_prefill_segmented_workspace)
+ *   workspace        device buffer of at least the queried size, 256-byte aligned; may be
+ *                    null when the queried size is 0.  Its contents on entry do not matter,
+ *                    and it may be reused as soon as the stream has run the call; two calls
+ *                    that share one workspace must not overlap on the GPU.
+ *   workspace_bytes  its size
+ *
+ * Device-side errors go to *dev_error as for la_prefill_fwd; bounds whose segments would not
+ * fit the workspace (overlapping cu_seqlens ranges) also set LA_DEV_ERR_BAD_SEQLENS and
+ * skip the sequences concerned.  Returns LA_OK after enqueueing; LA_ERR_INVALID_ARGUMENT /
+ * LA_ERR_UNSUPPORTED with nothing enqueued; LA_ERR_CUDA if a launch failed (earlier passes
+ * may then have been enqueued).
+ */
+la_status la_prefill_fwd_segmented(const void* q, const void* k, const void* v, const float* slopes, float scale,
+                                   const float* h0, const int32_t* state_indices, const int32_t* cu_seqlens,
+                                   void* o, float* h_final, int B, int T, int N, int H, int HV, int D, int V,
+                                   int pool_size, int segment_len, void* workspace, size_t workspace_bytes,
+                                   int* dev_error, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LA_SEGMENT_H */

@@ -1,8 +1,9 @@
 """GB300 (sm_103a) Lightning Attention chunkwise prefill and speculative-decoding ops.
 
-``la_prefill_fwd`` (include/la_prefill.h) and ``la_decode_mtp``, ``la_verify``,
-``la_commit`` (include/la_decode.h) are thin ctypes bindings of the C entry points of
-the same names: they check dtypes and shapes of torch tensors, pass their device
+``la_prefill_fwd`` (include/la_prefill.h), ``la_prefill_fwd_segmented`` and
+``la_prefill_segmented_workspace`` (include/la_segment.h) and ``la_decode_mtp``,
+``la_verify``, ``la_commit`` (include/la_decode.h) are thin ctypes bindings of the C
+entry points of the same names: they check dtypes and shapes of torch tensors, pass their device
 pointers and the current CUDA stream, and raise on a non-OK status.  Every step of the
 computation runs in the library's CUDA kernels; there is no other implementation in
 this package and no fallback.
@@ -15,7 +16,7 @@ import threading
 
 from . import build as _build
 
-__all__ = ["la_prefill_fwd", "la_decode_mtp", "la_verify", "la_commit", "LaError", "load_library", "SCHEDULES", "DEV_ERR_BAD_SEQLENS",
+__all__ = ["la_prefill_fwd", "la_prefill_fwd_segmented", "la_prefill_segmented_workspace", "la_decode_mtp", "la_verify", "la_commit", "LaError", "load_library", "SCHEDULES", "DEV_ERR_BAD_SEQLENS",
            "DEV_ERR_BAD_INDEX", "DEV_ERR_TIMEOUT", "EXPORTED_SYMBOLS"]
 
 SCHEDULES = {"auto": 0, "persistent": 1, "non_persistent": 2}
@@ -24,7 +25,7 @@ DEV_ERR_BAD_INDEX = 2
 DEV_ERR_TIMEOUT = 4
 EXPORTED_SYMBOLS = ("la_prefill_fwd", "la_status_string", "la_last_error", "la_prefill_smem_bytes",
                     "la_prefill_trace_events", "la_prefill_set_trace_buffer", "la_decode_mtp", "la_verify",
-                    "la_commit")
+                    "la_commit", "la_prefill_segmented_workspace", "la_prefill_fwd_segmented")
 
 _lock = threading.Lock()
 _lib = None
@@ -67,6 +68,11 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.la_verify.restype = ctypes.c_int
             lib.la_commit.argtypes = [fp, i32p, vp, vp, i32p, fp] + ints + [vp, vp]
             lib.la_commit.restype = ctypes.c_int
+            lib.la_prefill_segmented_workspace.argtypes = [ctypes.c_int] * 6 + [vp, vp]
+            lib.la_prefill_segmented_workspace.restype = ctypes.c_int
+            lib.la_prefill_fwd_segmented.argtypes = [vp, vp, vp, fp, ctypes.c_float, fp, i32p, i32p, vp, fp] + \
+                [ctypes.c_int] * 9 + [vp, ctypes.c_size_t, vp, vp]
+            lib.la_prefill_fwd_segmented.restype = ctypes.c_int
             _lib = lib
         return _lib
 
@@ -91,20 +97,9 @@ def _check(t, name, dtype, ndim):
         raise ValueError(f"{name} must be contiguous")
 
 
-def la_prefill_fwd(q, k, v, slopes, scale, h0=None, state_indices=None, cu_seqlens=None, o=None,
-                   h_final=None, seq_len=None, schedule="auto", dev_error=None, stream=None):
-    """Lightning Attention chunkwise prefill (forward) on the current CUDA device.
-
-    q, k: bf16 [tokens, H, 128]; v: bf16 [tokens, HV, 128]; slopes: fp32 [HV];
-    h0 / h_final: fp32 [P, HV, 128, 128] ([V, K] per state) or None;
-    state_indices: int32 [N] or None (negative = padded sequence);
-    cu_seqlens: int32 [N + 1] or None.  Without cu_seqlens the batch is fixed
-    length: ``seq_len`` tokens per sequence (tokens must be a multiple of it).
-    ``o`` (bf16 [tokens, HV, 128]) is allocated when not given.  h_final may be
-    the same tensor as h0 (in-place state pool).  Returns ``o``.
-    """
+def _prefill_args(q, k, v, slopes, h0, state_indices, cu_seqlens, o, h_final, seq_len, dev_error, stream):
+    """Checks shared by the prefill entry points; returns (o, B, T, N, H, HV, D, V, pool, stream)."""
     import torch
-    lib = load_library()
     _check(q, "q", torch.bfloat16, 3)
     _check(k, "k", torch.bfloat16, 3)
     _check(v, "v", torch.bfloat16, 3)
@@ -151,6 +146,24 @@ def la_prefill_fwd(q, k, v, slopes, scale, h0=None, state_indices=None, cu_seqle
         stream = torch.cuda.current_stream(q.device).cuda_stream
     elif not isinstance(stream, int):
         stream = stream.cuda_stream
+    return o, B, T, N, H, HV, D, V, pool, stream
+
+
+def la_prefill_fwd(q, k, v, slopes, scale, h0=None, state_indices=None, cu_seqlens=None, o=None,
+                   h_final=None, seq_len=None, schedule="auto", dev_error=None, stream=None):
+    """Lightning Attention chunkwise prefill (forward) on the current CUDA device.
+
+    q, k: bf16 [tokens, H, 128]; v: bf16 [tokens, HV, 128]; slopes: fp32 [HV];
+    h0 / h_final: fp32 [P, HV, 128, 128] ([V, K] per state) or None;
+    state_indices: int32 [N] or None (negative = padded sequence);
+    cu_seqlens: int32 [N + 1] or None.  Without cu_seqlens the batch is fixed
+    length: ``seq_len`` tokens per sequence (tokens must be a multiple of it).
+    ``o`` (bf16 [tokens, HV, 128]) is allocated when not given.  h_final may be
+    the same tensor as h0 (in-place state pool).  Returns ``o``.
+    """
+    lib = load_library()
+    o, B, T, N, H, HV, D, V, pool, stream = _prefill_args(q, k, v, slopes, h0, state_indices, cu_seqlens, o,
+                                                          h_final, seq_len, dev_error, stream)
     if isinstance(schedule, str):
         schedule = SCHEDULES[schedule]
     st = lib.la_prefill_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes), ctypes.c_float(scale), _ptr(h0),
@@ -158,7 +171,50 @@ def la_prefill_fwd(q, k, v, slopes, scale, h0=None, state_indices=None, cu_seqle
                             int(B), int(T), int(N), int(H), int(HV), int(D), int(V), int(pool),
                             int(schedule), _ptr(dev_error), ctypes.c_void_p(stream))
     if st != 0:
-        raise LaError(st, lib.la_status_string(st).decode(), lib.la_last_error().decode())
+        _raise(lib, st)
+    return o
+
+
+def la_prefill_segmented_workspace(B, T, N, HV, packed, segment_len=0):
+    """(workspace bytes, resolved segment length) of la_prefill_fwd_segmented for these sizes.
+
+    segment_len 0 = automatic (uses the current device's SM count); both values are 0 when
+    the call would run la_prefill_fwd unchanged."""
+    lib = load_library()
+    nbytes = ctypes.c_size_t(0)
+    seg = ctypes.c_int(0)
+    st = lib.la_prefill_segmented_workspace(int(B), int(T), int(N), int(HV), int(bool(packed)), int(segment_len),
+                                            ctypes.byref(nbytes), ctypes.byref(seg))
+    if st != 0:
+        _raise(lib, st)
+    return nbytes.value, seg.value
+
+
+def la_prefill_fwd_segmented(q, k, v, slopes, scale, h0=None, state_indices=None, cu_seqlens=None, o=None,
+                             h_final=None, seq_len=None, segment_len=0, workspace=None, dev_error=None,
+                             stream=None):
+    """la_prefill_fwd with every sequence cut into segments of ``segment_len`` tokens (0 =
+    automatic) that run in parallel from their exact initial states.
+
+    Arguments as la_prefill_fwd; ``workspace`` is a CUDA uint8 tensor of at least
+    la_prefill_segmented_workspace(...)[0] bytes, allocated here when None.  Returns ``o``."""
+    import torch
+    lib = load_library()
+    o, B, T, N, H, HV, D, V, pool, stream = _prefill_args(q, k, v, slopes, h0, state_indices, cu_seqlens, o,
+                                                          h_final, seq_len, dev_error, stream)
+    if workspace is None:
+        nbytes, _ = la_prefill_segmented_workspace(B, T, N, HV, cu_seqlens is not None, segment_len)
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device) if nbytes else None
+    if workspace is not None:
+        _check(workspace, "workspace", torch.uint8, 1)
+    st = lib.la_prefill_fwd_segmented(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes), ctypes.c_float(scale), _ptr(h0),
+                                      _ptr(state_indices), _ptr(cu_seqlens), _ptr(o), _ptr(h_final),
+                                      int(B), int(T), int(N), int(H), int(HV), int(D), int(V), int(pool),
+                                      int(segment_len), _ptr(workspace),
+                                      ctypes.c_size_t(0 if workspace is None else workspace.numel()),
+                                      _ptr(dev_error), ctypes.c_void_p(stream))
+    if st != 0:
+        _raise(lib, st)
     return o
 
 

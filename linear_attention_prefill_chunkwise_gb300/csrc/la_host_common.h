@@ -1,7 +1,10 @@
 // la_host_common.h -- host-side helpers shared by the C-ABI translation units: the
-// per-thread last-error text, argument checks and the one-time per-device lookup.
+// per-thread last-error text, argument checks, the one-time per-device lookup and the
+// TMA tensor maps over the token-major BF16 inputs.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <cstdarg>
@@ -60,6 +63,91 @@ la_status current_device(DeviceState (&table)[kMaxDevices], DeviceState** out, S
                 ds.cc_minor);
   *out = &ds;
   return LA_OK;
+}
+
+// cuTensorMapEncodeTiled, fetched once through the runtime's driver entry-point query (so the
+// library has no link-time dependency on the driver library).
+inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// Map over a token-major [rows, heads * 128] BF16 matrix: 64 x 64 boxes (64 tokens x 64
+// dims, 128-byte rows), 128-byte swizzle, the layout the kernels' MMA descriptors expect.
+inline la_status encode_bf16_rows_map(CUtensorMap* map, const void* base, int64_t rows, int64_t heads,
+                                      const char* name) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return fail(LA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the CUDA driver");
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(heads * 128), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(heads * 128 * 2)};
+  const cuuint32_t box[2] = {64, 64};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  const CUresult r =
+      enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, elem_strides,
+          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(LA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", name, (int)r);
+  return LA_OK;
+}
+
+// Argument checks of a prefill call (la_prefill_fwd's contract): shapes, modes, pointers,
+// alignment and the state pool.  Sets *nothing_to_do when the call has no work.
+inline la_status check_prefill_args(const void* q, const void* k, const void* v, const float* slopes,
+                                    const float* h0, const int32_t* state_indices, const int32_t* cu_seqlens,
+                                    const void* o, const float* h_final, int B, int T, int N, int H, int HV, int D,
+                                    int V, int pool_size, const int* dev_error, bool* nothing_to_do) {
+  *nothing_to_do = false;
+  if (D != 128 || V != 128)
+    return fail(LA_ERR_UNSUPPORTED, "only D == V == 128 is implemented (got D=%d, V=%d)", D, V);
+  if (H <= 0 || HV <= 0) return fail(LA_ERR_INVALID_ARGUMENT, "H and HV must be positive (got %d, %d)", H, HV);
+  if (HV % H != 0) return fail(LA_ERR_UNSUPPORTED, "HV (%d) must be a multiple of H (%d)", HV, H);
+  if (B < 0 || T < 0 || N < 0) return fail(LA_ERR_INVALID_ARGUMENT, "B, T, N must be >= 0");
+  if (cu_seqlens) {
+    if (B != 1) return fail(LA_ERR_INVALID_ARGUMENT, "packed mode (cu_seqlens given) needs B == 1 (got %d)", B);
+  } else if (N != B) {
+    return fail(LA_ERR_INVALID_ARGUMENT, "fixed-length mode needs N == B (got N=%d, B=%d)", N, B);
+  }
+  const int64_t tokens = static_cast<int64_t>(B) * T;
+  if (tokens + 64 > INT32_MAX) return fail(LA_ERR_UNSUPPORTED, "B*T too large (%lld)", (long long)tokens);
+  const int64_t units = static_cast<int64_t>(N) * HV;
+  if (units > INT32_MAX) return fail(LA_ERR_UNSUPPORTED, "N*HV too large (%lld)", (long long)units);
+  if (static_cast<int64_t>(HV) * 128 * 2 > (int64_t(1) << 39))
+    return fail(LA_ERR_UNSUPPORTED, "HV too large for a tensor map stride");
+  if (N == 0) {
+    *nothing_to_do = true;
+    return LA_OK;
+  }
+  if (!slopes) return fail(LA_ERR_INVALID_ARGUMENT, "slopes is null");
+  if (tokens > 0 && (!q || !k || !v || !o)) return fail(LA_ERR_INVALID_ARGUMENT, "q, k, v and o must be non-null");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(h0) || !aligned16(h_final))
+    return fail(LA_ERR_INVALID_ARGUMENT, "q, k, v, o, h0 and h_final must be 16-byte aligned");
+  if (!aligned4(slopes) || !aligned4(dev_error) || !aligned4(state_indices) || !aligned4(cu_seqlens))
+    return fail(LA_ERR_INVALID_ARGUMENT, "slopes, dev_error, state_indices, cu_seqlens must be 4-byte aligned");
+  if (h0 || h_final) {
+    if (state_indices) {
+      if (pool_size <= 0) return fail(LA_ERR_INVALID_ARGUMENT, "pool_size must be positive with state_indices");
+    } else if (pool_size < N) {
+      return fail(LA_ERR_INVALID_ARGUMENT, "pool_size (%d) must be >= N (%d) without state_indices", pool_size, N);
+    }
+  }
+  if (tokens == 0 && !h_final) *nothing_to_do = true;  // no output rows and no state to write
+  return LA_OK;
+}
+
+// The pool size the kernels check state indices against: the caller's when a state buffer
+// is given, otherwise no bound (indices then only select which sequences run).
+inline int effective_pool_size(const float* h0, const float* h_final, const int32_t* state_indices, int pool_size,
+                               int N) {
+  return (h0 || h_final) ? pool_size : (state_indices ? INT32_MAX : N);
 }
 
 }  // namespace la_host

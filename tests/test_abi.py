@@ -142,3 +142,71 @@ def test_decode_no_device_is_reported():
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     assert call_decode("la_decode_mtp") == LA_CUDA
+
+
+# ---- segmented prefill (include/la_segment.h)
+
+def _ws_bytes(nseg, HV, N):
+    a = lambda x: (x + 255) // 256 * 256
+    return a(nseg * HV * 128 * 128 * 4) + a((nseg + 1) * 4) + 2 * a(nseg * 4) + a((N + 1) * 4) + a(N * 4)
+
+
+@pytest.mark.parametrize("B,T,N,HV,packed,S,nseg", [
+    (2, 1000, 2, 4, 0, 192, 12),      # fixed: B * ceil(T / S)
+    (1, 5000, 7, 2, 1, 128, 46),      # packed: N + floor(tokens / S)
+    (3, 64 * 9, 3, 1, 0, 64, 27),
+])
+def test_segmented_workspace_size(B, T, N, HV, packed, S, nseg):
+    nbytes, seg = lap.la_prefill_segmented_workspace(B, T, N, HV, packed, S)
+    assert seg == S
+    assert nbytes == _ws_bytes(nseg, HV, N)
+
+
+def test_segmented_workspace_none_when_every_sequence_fits_one_segment():
+    assert lap.la_prefill_segmented_workspace(2, 1000, 2, 4, 0, 1024) == (0, 0)
+    assert lap.la_prefill_segmented_workspace(1, 1000, 3, 4, 1, 1024) == (0, 0)
+    assert lap.la_prefill_segmented_workspace(0, 0, 0, 4, 0, 64) == (0, 0)
+
+
+@pytest.mark.parametrize("seg", [100, -64, 32])
+def test_segmented_workspace_rejects_bad_segment_len(seg):
+    with pytest.raises(lap.LaError) as e:
+        lap.la_prefill_segmented_workspace(2, 1000, 2, 4, 0, seg)
+    assert e.value.status == LA_INVALID
+
+
+def call_segmented(**over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, slopes=FAKE, scale=1.0, h0=None, idx=None, cu=None, o=FAKE, hf=None,
+             B=2, T=1000, N=2, H=2, HV=2, D=128, V=128, P=0, seg=128, ws=FAKE, wsb=1 << 30, err=None, stream=None)
+    a.update(over)
+    lib = lap.load_library()
+    return lib.la_prefill_fwd_segmented(a["q"], a["k"], a["v"], a["slopes"], ctypes.c_float(a["scale"]), a["h0"],
+                                        a["idx"], a["cu"], a["o"], a["hf"], a["B"], a["T"], a["N"], a["H"], a["HV"],
+                                        a["D"], a["V"], a["P"], a["seg"], a["ws"], a["wsb"], a["err"], a["stream"])
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(D=64), LA_UNSUPPORTED),
+    (dict(H=3, HV=4), LA_UNSUPPORTED),
+    (dict(N=3), LA_INVALID),
+    (dict(seg=100), LA_INVALID),        # not a multiple of 64
+    (dict(ws=None), LA_INVALID),        # workspace needed
+    (dict(wsb=1024), LA_INVALID),       # workspace too small
+    (dict(ws=FAKE + 16), LA_INVALID),   # workspace not 256-byte aligned
+    (dict(q=FAKE + 2), LA_INVALID),
+])
+def test_segmented_host_validation(over, status):
+    assert call_segmented(**over) == status
+    assert lap.load_library().la_last_error() != b""
+
+
+def test_segmented_empty_batch_is_a_no_op():
+    assert call_segmented(N=0, B=0, T=0) == LA_OK
+
+
+def test_segmented_no_device_is_reported():
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert call_segmented() == LA_CUDA          # workspace fine: the first device query fails
+    assert call_segmented(seg=0) == LA_CUDA     # automatic length needs the device

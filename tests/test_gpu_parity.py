@@ -12,43 +12,18 @@ import numpy as np
 import pytest
 
 import workloads as W
-from harness import (bf16_tensor_to_f32, check_output, check_state, oracle_full, oracle_unit, run_gpu,
-                     unit_bounds, upload)
+from harness import compare_full, compare_sampled, run_gpu, upload
 
 pytestmark = pytest.mark.gpu
 
 torch = pytest.importorskip("torch")
 
 
-def _compare_full(p, d, label):
-    torch.cuda.synchronize()
-    o_ref, h_ref = oracle_full(p)
-    o_gpu = bf16_tensor_to_f32(d["o"])
-    written = ~np.isnan(o_ref[:, 0, 0])
-    # rows the oracle leaves unwritten (padded sequences) must stay poisoned
-    assert np.all(np.isnan(o_gpu[~written])), f"{label}: padded rows were written"
-    if written.any():
-        check_output(o_gpu[written], o_ref[written], label)
-    if d["h_final"] is not None:
-        h_gpu = d["h_final"].cpu().numpy()
-        sel = ~np.isnan(h_ref[:, 0, 0, 0])
-        if p.in_place and p.h0 is not None:
-            # unselected slots keep their initial value bit for bit
-            unsel = np.ones(p.pool_size, bool)
-            unsel[[s for s in (p.state_indices if p.state_indices is not None else range(p.N)) if s >= 0]] = False
-            assert np.array_equal(h_gpu[unsel], p.h0[unsel]), f"{label}: unselected pool slots changed"
-            sel = ~unsel
-        else:
-            assert np.all(np.isnan(h_gpu[~sel])), f"{label}: unselected h_final slots were written"
-        if sel.any():
-            check_state(h_gpu[sel], h_ref[sel], label)
-
-
 def test_tiny_workload_full():
     p = W.config(1)
     d = upload(p)
     run_gpu(p, d)
-    _compare_full(p, d, "tiny B=1 T=256 H=4")
+    compare_full(p, d, "tiny B=1 T=256 H=4")
 
 
 EDGE_CASES = {
@@ -76,31 +51,14 @@ def test_edge_cases_full(name):
     p = W.custom(seed=zlib.crc32(name.encode()) % 10000, name=name, **kw)
     d = upload(p)
     run_gpu(p, d)
-    _compare_full(p, d, name)
-
-
-def _sampled(p, d, units, label):
-    torch.cuda.synchronize()
-    o_gpu_t = d["o"]
-    hf = d["h_final"]
-    for (n, hv) in units:
-        res = oracle_unit(p, n, hv)
-        if res is None:
-            continue
-        o_ref, h_ref = res
-        a, b = unit_bounds(p, n)
-        o_gpu = o_gpu_t[a:b, hv].float().cpu().numpy()
-        check_output(o_gpu, o_ref, f"{label} unit (n={n}, hv={hv})")
-        if hf is not None:
-            slot = n if p.state_indices is None else int(p.state_indices[n])
-            check_state(hf[slot, hv].cpu().numpy(), h_ref, f"{label} state (n={n}, hv={hv})")
+    compare_full(p, d, name)
 
 
 def test_fixed_mha_b2_t8192_sampled():
     p = W.config(2)
     d = upload(p)
     run_gpu(p, d)
-    _sampled(p, d, [(0, 0), (1, 63), (0, 31), (1, 1), (1, 40)], "B=2 T=8192 H=64")
+    compare_sampled(p, d, [(0, 0), (1, 63), (0, 31), (1, 1), (1, 40)], "B=2 T=8192 H=64")
     assert not torch.isnan(d["o"]).any().item()
 
 
@@ -113,7 +71,7 @@ def test_packed_varlen_pool_sampled():
     order = np.argsort(lengths)
     picks = [(int(order[-1]), 0), (int(order[-1]), 31), (int(order[0]), 5), (int(order[1]), 16),
              (int(order[len(order) // 2]), 7)]
-    _sampled(p, d, picks, "packed N=32 H=32")
+    compare_sampled(p, d, picks, "packed N=32 H=32")
     assert not torch.isnan(d["o"]).any().item()
     h_gpu = d["h_final"].cpu().numpy()
     unsel = np.setdiff1d(np.arange(p.pool_size), p.state_indices)
@@ -124,14 +82,14 @@ def test_gva_long_sampled():
     p = W.config(4)
     d = upload(p)
     run_gpu(p, d)
-    _sampled(p, d, [(0, 0), (3, 63), (2, 17)], "GVA B=4 T=16384 H=16 HV=64")
+    compare_sampled(p, d, [(0, 0), (3, 63), (2, 17)], "GVA B=4 T=16384 H=16 HV=64")
 
 
 def test_short_sequences_pool_full():
     p = W.config(5)
     d = upload(p)
     run_gpu(p, d)
-    _compare_full(p, d, "short packed N=128 T=8")
+    compare_full(p, d, "short packed N=128 T=8")
 
 
 @pytest.mark.parametrize("which", ["small", "packed_full"])

@@ -234,6 +234,42 @@ def test_continuation():
     assert rel(hb, hf) < 1e-12
 
 
+def test_segmented_scan_decomposition():
+    """The segment-parallel form of the recurrence (page "feat(kda): add bitwise-aligned SM100
+    CuTeDSL forward", Description, segmented chunk scan, applied to the scalar decay): each
+    segment's local state from a zero start equals the closed form
+    sum_j lambda^(L-1-j) v_j k_j^T; chaining H_{i+1} = lambda^{L_i} H_i + Sloc_i gives every
+    segment's exact initial state; running each segment from it reproduces the whole
+    sequence's outputs and final state."""
+    seg = [64 * 3, 64 * 3, 64 + 17]
+    total = sum(seg)
+    # small slopes keep lambda^L away from 0, so the initial state still matters at every boundary
+    q, k, v, slopes, scale, h0, _ = rand_problem(81, [total], 1, 2, slopes=[0.003, 0.02])
+    o, hf = oracle.tokenwise(q, k, v, slopes, scale, h0=h0, T=total)
+    H = h0[0].copy()  # [HV, V, D]
+    outs = []
+    a = 0
+    for L in seg:
+        b = a + L
+        _, sloc = oracle.tokenwise(q[a:b], k[a:b], v[a:b], slopes, scale, h0=None, T=L)
+        for hv in range(2):
+            _, hT = oracle.closed_form(q[a:b, 0], k[a:b, 0], v[a:b, hv], slopes[hv], scale)
+            assert rel(sloc[0, hv], hT) < 1e-12
+        oi, hi = oracle.tokenwise(q[a:b], k[a:b], v[a:b], slopes, scale, h0=H[None], T=L)
+        outs.append(oi)
+        lamL = np.exp(-slopes.astype(np.float64) * L)[:, None, None]
+        H = lamL * H + sloc[0]
+        assert rel(H, hi[0]) < 1e-12
+        a = b
+    assert rel(np.concatenate(outs), o) < 1e-12
+    assert rel(H, hf[0]) < 1e-12
+    # the plausible slip of decaying the local state by lambda^(L-1) instead of lambda^L
+    lam_wrong = np.exp(-slopes.astype(np.float64) * (seg[0] - 1))[:, None, None]
+    _, s0 = oracle.tokenwise(q[:seg[0]], k[:seg[0]], v[:seg[0]], slopes, scale, h0=None, T=seg[0])
+    _, h_true = oracle.tokenwise(q[:seg[0]], k[:seg[0]], v[:seg[0]], slopes, scale, h0=h0, T=seg[0])
+    assert rel(lam_wrong * h0[0] + s0[0], h_true[0]) > 1e-6
+
+
 def test_scale_is_linear():
     q, k, v, slopes, _, h0, cu = rand_problem(71, [20], 1, 1)
     o1, h1 = oracle.tokenwise(q, k, v, slopes, 1.0, h0=h0, cu_seqlens=cu)
