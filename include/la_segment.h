@@ -79,6 +79,35 @@ la_status la_prefill_fwd_segmented(const void* q, const void* k, const void* v, 
                                    int pool_size, int segment_len, void* workspace, size_t workspace_bytes,
                                    int* dev_error, void* stream);
 
+/*
+ * la_prefill_fwd_segmented_static -- la_prefill_fwd_segmented without a caller workspace.
+ *
+ * No counterpart in the pages: an addition of this library for callers that cannot allocate
+ * device memory -- a plugin inside an inference server or framework that owns every byte of
+ * device memory and offers its extensions no allocation call, or a latency-critical path that
+ * must not call cudaMalloc (which may synchronise the device).  The scratch the segmented
+ * prefill needs comes from a 16 MiB buffer built into the library: a file-scope device array
+ * that every GPU holds, once the library's code is loaded on it, until the process exits.  The
+ * call itself allocates no device memory.
+ *
+ * Arguments as la_prefill_fwd_segmented, without workspace / workspace_bytes.
+ *   - Calls whose plan needs more than 16 MiB (la_prefill_segmented_workspace) return
+ *     LA_ERR_UNSUPPORTED and launch nothing; every automatic segment length (segment_len = 0) on
+ *     a GB300 (152 SMs) needs at most about 14.3 MiB.
+ *   - The first call on a device that segments looks the buffer's address up (one
+ *     cudaGetSymbolAddress, with that device current, which may load the library's code on it);
+ *     make that first call before any stream capture.
+ *   - Every call on a device shares the one buffer and leaves its contents behind; nothing in it
+ *     has to start at zero (each call rewrites every table entry and state before reading it).
+ *     Two calls that overlap on the GPU (different streams, or threads without ordering) race on
+ *     the buffer and corrupt each other's results: order them on one stream.
+ */
+la_status la_prefill_fwd_segmented_static(const void* q, const void* k, const void* v, const float* slopes,
+                                          float scale, const float* h0, const int32_t* state_indices,
+                                          const int32_t* cu_seqlens, void* o, float* h_final, int B, int T, int N,
+                                          int H, int HV, int D, int V, int pool_size, int segment_len,
+                                          int* dev_error, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

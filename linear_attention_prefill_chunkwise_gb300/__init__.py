@@ -1,7 +1,8 @@
 """GB300 (sm_103a) Lightning Attention chunkwise prefill and speculative-decoding ops.
 
-``la_prefill_fwd`` (include/la_prefill.h), ``la_prefill_fwd_segmented`` and
-``la_prefill_segmented_workspace`` (include/la_segment.h) and ``la_decode_mtp``,
+``la_prefill_fwd`` (include/la_prefill.h), ``la_prefill_fwd_segmented``,
+``la_prefill_fwd_segmented_static`` and ``la_prefill_segmented_workspace``
+(include/la_segment.h) and ``la_decode_mtp``,
 ``la_verify``, ``la_commit`` (include/la_decode.h) are thin ctypes bindings of the C
 entry points of the same names: they check dtypes and shapes of torch tensors, pass their device
 pointers and the current CUDA stream, and raise on a non-OK status.  Every step of the
@@ -16,7 +17,8 @@ import threading
 
 from . import build as _build
 
-__all__ = ["la_prefill_fwd", "la_prefill_fwd_segmented", "la_prefill_segmented_workspace", "la_decode_mtp", "la_verify", "la_commit", "LaError", "load_library", "SCHEDULES", "DEV_ERR_BAD_SEQLENS",
+__all__ = ["la_prefill_fwd", "la_prefill_fwd_segmented", "la_prefill_fwd_segmented_static",
+           "la_prefill_segmented_workspace", "la_decode_mtp", "la_verify", "la_commit", "LaError", "load_library", "SCHEDULES", "DEV_ERR_BAD_SEQLENS",
            "DEV_ERR_BAD_INDEX", "DEV_ERR_TIMEOUT", "EXPORTED_SYMBOLS"]
 
 SCHEDULES = {"auto": 0, "persistent": 1, "non_persistent": 2}
@@ -25,7 +27,8 @@ DEV_ERR_BAD_INDEX = 2
 DEV_ERR_TIMEOUT = 4
 EXPORTED_SYMBOLS = ("la_prefill_fwd", "la_status_string", "la_last_error", "la_prefill_smem_bytes",
                     "la_prefill_trace_events", "la_prefill_set_trace_buffer", "la_decode_mtp", "la_verify",
-                    "la_commit", "la_prefill_segmented_workspace", "la_prefill_fwd_segmented")
+                    "la_commit", "la_prefill_segmented_workspace", "la_prefill_fwd_segmented",
+                    "la_prefill_fwd_segmented_static")
 
 _lock = threading.Lock()
 _lib = None
@@ -73,6 +76,9 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.la_prefill_fwd_segmented.argtypes = [vp, vp, vp, fp, ctypes.c_float, fp, i32p, i32p, vp, fp] + \
                 [ctypes.c_int] * 9 + [vp, ctypes.c_size_t, vp, vp]
             lib.la_prefill_fwd_segmented.restype = ctypes.c_int
+            lib.la_prefill_fwd_segmented_static.argtypes = [vp, vp, vp, fp, ctypes.c_float, fp, i32p, i32p, vp,
+                                                            fp] + [ctypes.c_int] * 9 + [vp, vp]
+            lib.la_prefill_fwd_segmented_static.restype = ctypes.c_int
             _lib = lib
         return _lib
 
@@ -213,6 +219,25 @@ def la_prefill_fwd_segmented(q, k, v, slopes, scale, h0=None, state_indices=None
                                       int(segment_len), _ptr(workspace),
                                       ctypes.c_size_t(0 if workspace is None else workspace.numel()),
                                       _ptr(dev_error), ctypes.c_void_p(stream))
+    if st != 0:
+        _raise(lib, st)
+    return o
+
+
+def la_prefill_fwd_segmented_static(q, k, v, slopes, scale, h0=None, state_indices=None, cu_seqlens=None,
+                                    o=None, h_final=None, seq_len=None, segment_len=0, dev_error=None,
+                                    stream=None):
+    """la_prefill_fwd_segmented with the scratch taken from the library's built-in 16 MiB
+    device buffer instead of a workspace, for callers that cannot allocate device memory.
+    Calls share that buffer: calls that overlap on the GPU race.  Returns ``o``."""
+    lib = load_library()
+    o, B, T, N, H, HV, D, V, pool, stream = _prefill_args(q, k, v, slopes, h0, state_indices, cu_seqlens, o,
+                                                          h_final, seq_len, dev_error, stream)
+    st = lib.la_prefill_fwd_segmented_static(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes), ctypes.c_float(scale),
+                                             _ptr(h0), _ptr(state_indices), _ptr(cu_seqlens), _ptr(o),
+                                             _ptr(h_final), int(B), int(T), int(N), int(H), int(HV), int(D),
+                                             int(V), int(pool), int(segment_len), _ptr(dev_error),
+                                             ctypes.c_void_p(stream))
     if st != 0:
         _raise(lib, st)
     return o
