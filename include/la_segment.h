@@ -12,8 +12,8 @@
  *   2. a scan over each sequence's segments: H_0 = h0, H_{i+1} = lambda^{L_i} H_i + Sloc_i;
  *   3. the chunkwise prefill of every segment from its initial state H_i (la_prefill_fwd's
  *      kernel), whose last segment leaves the sequence's final state.
- * The segment-parallel scan is the one page "feat(kda): add bitwise-aligned SM100 CuTeDSL
- * forward" (Description) describes for a decayed recurrence of the same shape.  The
+ * The segmented affine scan is the one page "linear_attention: add a Hopper (sm90) KDA
+ * prefill path - #1017" (How) uses for a decayed recurrence of the same shape.  The
  * outputs equal la_prefill_fwd's up to FP32 rounding order (the initial states are exact
  * sums computed in another order); they are not bitwise equal.
  *

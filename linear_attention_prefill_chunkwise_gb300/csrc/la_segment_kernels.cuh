@@ -5,10 +5,10 @@
 // The recurrence of one chain is affine in its state: a segment of length L that starts
 // from state H ends in lambda^L H + Sloc, where
 //     Sloc = sum_{j<L} lambda^(L-1-j) v_j^T k_j          (the segment run from a zero state)
-// depends only on the segment's own tokens.  This is the segment-parallel scan that page
-// "feat(kda): add bitwise-aligned SM100 CuTeDSL forward" (Description, the segmented
-// chunk scan) describes for another decayed recurrence, applied to Lightning Attention's
-// scalar decay.  The pipeline:
+// depends only on the segment's own tokens.  This is the segmented affine scan that page
+// "linear_attention: add a Hopper (sm90) KDA prefill path - #1017" (How) pairs with short
+// chunks for another decayed recurrence, applied to Lightning Attention's scalar decay.
+// The pipeline:
 //   plan      one CTA: sequence bounds -> segment table (bounds, state slots, which segments
 //             need a local state), device-side, so the host never reads cu_seqlens
 //   state     la_segment_state_kernel: Sloc of every segment that is not the last of its

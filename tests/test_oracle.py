@@ -235,8 +235,8 @@ def test_continuation():
 
 
 def test_segmented_scan_decomposition():
-    """The segment-parallel form of the recurrence (page "feat(kda): add bitwise-aligned SM100
-    CuTeDSL forward", Description, segmented chunk scan, applied to the scalar decay): each
+    """The segment-parallel form of the recurrence (page "linear_attention: add a Hopper (sm90) KDA
+    prefill path - #1017", How: the segmented affine scan, applied to the scalar decay): each
     segment's local state from a zero start equals the closed form
     sum_j lambda^(L-1-j) v_j k_j^T; chaining H_{i+1} = lambda^{L_i} H_i + Sloc_i gives every
     segment's exact initial state; running each segment from it reproduces the whole
