@@ -39,7 +39,8 @@ FALLBACK_BF16_TFLOPS = 1900.0
 KERNEL_NAME = "la_prefill_fwd_kernel"
 KERNEL_SOURCES = ["linear_attention_prefill_chunkwise_gb300/csrc/la_prefill_kernel.cuh",
                   "linear_attention_prefill_chunkwise_gb300/csrc/sm103_ptx.cuh",
-                  "linear_attention_prefill_chunkwise_gb300/csrc/la_prefill_api.cu"]
+                  "linear_attention_prefill_chunkwise_gb300/csrc/la_prefill_api.cu",
+                  "linear_attention_prefill_chunkwise_gb300/csrc/la_host_common.h"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "la_prefill_fwd_kernel_B2_T8192_H64.dram.txt")
 
 
@@ -202,6 +203,32 @@ def job_throughput(units_per_rank, steps, world, slowest_ms):
     return world * units_per_rank * steps / (slowest_ms / 1e3)
 
 
+def pin_to_gpu_numa_node(device):
+    """Run this process on the CPUs next to ``device`` (the PCI device's local_cpulist) so that
+    the pinned host buffers allocated next are first touched on the GPU's own NUMA node.
+    Returns (CPU list used or None, the previous affinity to restore afterwards)."""
+    import subprocess
+    before = os.sched_getaffinity(0)
+    try:
+        out = subprocess.run(["nvidia-smi", "--query-gpu=pci.bus_id", "--format=csv,noheader",
+                              "-i", gpu_id_for_smi(device)], capture_output=True, text=True, timeout=20).stdout
+        dom, rest = out.strip().split(":", 1)
+        path = f"/sys/bus/pci/devices/{int(dom, 16):04x}:{rest.lower()}/local_cpulist"
+        with open(path) as fh:
+            spec = fh.read().strip()
+        cpus = set()
+        for part in spec.split(","):
+            lo, _, hi = part.partition("-")
+            cpus.update(range(int(lo), int(hi or lo) + 1))
+        cpus &= before
+        if not cpus:
+            return None, before
+        os.sched_setaffinity(0, cpus)
+        return spec, before
+    except (OSError, ValueError, subprocess.SubprocessError):
+        return None, before
+
+
 def make_inputs(device):
     import numpy as np
     import torch
@@ -269,35 +296,61 @@ def run_cuda(args):
     ms_per_step = total_ms / args.steps
     value = job_throughput(TOKENS, args.steps, world, total_ms)
 
-    # ---- end to end through the public API: pinned host inputs in, results out, every step
+    # ---- end to end through the public API: every step copies its inputs from pinned host
+    #      memory and reads its outputs (o and the final states) back.  Steps are pipelined
+    #      over two device buffer sets, as a serving loop runs them: the inputs of step i+1
+    #      travel (copy stream) while step i computes (launch stream) and the outputs of step
+    #      i-1 return (return stream).
+    numa, affinity = pin_to_gpu_numa_node(device)
     pinned = {k_: t.pin_memory() for k_, t in host.items()}
-    out_o = torch.empty((TOKENS, HV, V), dtype=torch.bfloat16).pin_memory()
-    out_h = torch.empty((B, HV, V, D), dtype=torch.float32).pin_memory()
+    nset = 2
+    out_o = [torch.empty((TOKENS, HV, V), dtype=torch.bfloat16).pin_memory() for _ in range(nset)]
+    out_h = [torch.empty((B, HV, V, D), dtype=torch.float32).pin_memory() for _ in range(nset)]
+    os.sched_setaffinity(0, affinity)  # the buffers are placed; the CPU baseline gets every core back
     h2d = sum(t.numel() * t.element_size() for t in pinned.values())
-    d2h = out_o.numel() * out_o.element_size() + out_h.numel() * out_h.element_size()
+    d2h = out_o[0].numel() * out_o[0].element_size() + out_h[0].numel() * out_h[0].element_size()
     e2e_steps = max(3, min(args.steps, args.e2e_steps))
-    scratch = {k_: torch.empty_like(t, device=device) for k_, t in pinned.items()}
-    scratch["o"] = dev["o"]
-    scratch["h_final"] = dev["h_final"]
+    sets = []
+    for _ in range(nset):
+        sb = {k_: torch.empty_like(t, device=device) for k_, t in pinned.items()}
+        sb["o"] = torch.empty((TOKENS, HV, V), dtype=torch.bfloat16, device=device)
+        sb["h_final"] = torch.empty((B, HV, V, D), dtype=torch.float32, device=device)
+        sets.append(sb)
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    ev_loaded = [torch.cuda.Event() for _ in range(nset)]
+    ev_done = [torch.cuda.Event() for _ in range(nset)]
+    ev_back = [torch.cuda.Event() for _ in range(nset)]
+    used = [False] * nset
 
-    def e2e_step():
-        for k_, t in pinned.items():
-            scratch[k_].copy_(t, non_blocking=True)
-        step(scratch, stream)
-        out_o.copy_(scratch["o"], non_blocking=True)
-        out_h.copy_(scratch["h_final"], non_blocking=True)
+    def e2e_step(i):
+        b = i % nset
+        sb = sets[b]
+        if used[b]:
+            s_in.wait_event(ev_done[b])      # the set's previous kernel has read its inputs
+            stream.wait_event(ev_back[b])    # and its previous outputs have been copied back
+        with torch.cuda.stream(s_in):
+            for k_, t in pinned.items():
+                sb[k_].copy_(t, non_blocking=True)
+            ev_loaded[b].record(s_in)
+        stream.wait_event(ev_loaded[b])
+        step(sb, stream)
+        ev_done[b].record(stream)
+        s_out.wait_event(ev_done[b])
+        with torch.cuda.stream(s_out):
+            out_o[b].copy_(sb["o"], non_blocking=True)
+            out_h[b].copy_(sb["h_final"], non_blocking=True)
+            ev_back[b].record(s_out)
+        used[b] = True
 
-    with torch.cuda.stream(stream):
-        for _ in range(2):
-            e2e_step()
+    for i in range(2 * nset):
+        e2e_step(i)
     torch.cuda.synchronize(device)
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        e1.record(stream)
+    e0.record(s_in)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e1.record(s_out)  # after the last step's outputs are back, which follow every earlier copy and launch
     torch.cuda.synchronize(device)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
     e2e_value = job_throughput(TOKENS, e2e_steps, world, e2e_ms)
@@ -319,7 +372,8 @@ def run_cuda(args):
                          "alg_flops_per_launch": ALG_FLOPS, "kernel": KERNEL_NAME,
                          "launch_ms_mean": round(launch_ms, 5), "launch_ms_min": round(min(per_launch_ms), 5)},
             "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "steps": e2e_steps},
+                    "steps": e2e_steps, "pipelined": "2 buffer sets: copy-in, launch and copy-out streams",
+                    "host_numa": numa},
             "gpu_launches": args.steps,
             "clocks": clk.summary(),
         }

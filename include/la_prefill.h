@@ -17,6 +17,12 @@
  * causal decay lambda^(s-j)) V, an inter-chunk term lambda^(s+1) Q S^T, and one state
  * advance S <- lambda^L S + sum_j lambda^(L-1-j) v_j^T k_j per chunk of L tokens.
  *
+ * Short sequences are evaluated token by token instead (one read and write of the state
+ * and a few FP32 updates cost less than a chunkwise pipeline for one partial chunk), with
+ * results within the same bounds: every sequence of a fixed-length batch with T <= 32, and
+ * the sequences of at most 32 tokens of a packed batch whose average length is at most 64
+ * (both kernels are then enqueued and each skips the other's sequences).
+ *
  * Every pointer argument is a DEVICE pointer owned by the caller; the library keeps no
  * reference after the call returns and allocates no device memory.  The call is
  * asynchronous on `stream` and never synchronises with the host, so it may be
@@ -76,8 +82,10 @@ typedef enum {
  * (including 0 and lengths that are not multiples of 64).  q, k, v, o, h0, h_final
  * must be 16-byte aligned.
  *
- * Returns LA_OK after enqueueing the kernel (or with nothing to do when N == 0 or
- * B*T == 0 and no state is requested); any other status means nothing was launched.
+ * Returns LA_OK after enqueueing the kernels (or with nothing to do when N == 0 or
+ * B*T == 0 and no state is requested).  LA_ERR_INVALID_ARGUMENT and LA_ERR_UNSUPPORTED
+ * mean nothing was launched; LA_ERR_CUDA from a failed launch may follow an enqueued
+ * tokenwise kernel of the same call.
  */
 la_status la_prefill_fwd(const void* q, const void* k, const void* v, const float* slopes, float scale,
                          const float* h0, const int32_t* state_indices, const int32_t* cu_seqlens, void* o,

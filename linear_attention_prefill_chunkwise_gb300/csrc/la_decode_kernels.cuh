@@ -17,6 +17,12 @@
 // groups are padded to 20 floats so that the 8 groups a warp reads sit in distinct banks.
 // The three operations run this same per-token code, so a commit of all T tokens leaves
 // bitwise the state a decode leaves, and verify's outputs are bitwise decode's.
+//
+// A fourth mode serves the prefill of short sequences (at most short_max tokens; the
+// chunkwise prefill kernel takes the others): bounds from cu_seqlens or n T, the initial
+// state from h0 (or zero), the final state to h_final.  For a few tokens the tokenwise
+// recurrence costs one state read and write plus a little arithmetic, while a chunkwise
+// unit pays its whole pipeline for one partial chunk.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -35,7 +41,7 @@ constexpr int kDim = 128;   // D = V = 128
 constexpr int kThreads = 256;
 constexpr int kTileT = 16;  // tokens staged in shared memory per pass
 
-enum Mode : int { kDecode = 0, kVerify = 1, kCommit = 2 };
+enum Mode : int { kDecode = 0, kVerify = 1, kCommit = 2, kPrefill = 3 };
 
 struct Params {
   const __nv_bfloat16* q;  // [B*T, H, 128]   (decode, verify)
@@ -48,9 +54,14 @@ struct Params {
   __nv_bfloat16* kbuf;     // [P, T, H, 128]  (written by verify when given, read by commit)
   __nv_bfloat16* vbuf;     // [P, T, HV, 128]
   const int32_t* accepted_len;  // [B] (commit)
+  const float* h0;              // [P, HV, 128, 128] or null (prefill: initial states)
+  float* h_final;               // [P, HV, 128, 128] or null (prefill: final states)
+  const int32_t* cu_seqlens;    // [B + 1] or null (prefill: packed sequence bounds)
   int* dev_error;
   float scale;
   int B, T, H, HV, G, pool_size;
+  int num_tokens;  // prefill: rows of q, k, v, o
+  int short_max;   // prefill: longer sequences are left to the chunkwise kernel
 };
 
 // Eight BF16 values (one 16-byte word) as FP32.
@@ -85,6 +96,16 @@ __global__ void __launch_bounds__(kThreads, 2) la_tokenwise_kernel(const Params 
     }
   }
   int ntok = p.T;
+  size_t row0 = static_cast<size_t>(b) * p.T;  // first token row of this unit
+  if (kMode == kPrefill) {
+    if (p.cu_seqlens) {
+      const int bb = __ldg(p.cu_seqlens + b), ee = __ldg(p.cu_seqlens + b + 1);
+      if (bb < 0 || ee < bb || ee > p.num_tokens) return;  // flagged by the chunkwise kernel
+      row0 = bb;
+      ntok = ee - bb;
+    }
+    if (ntok > p.short_max) return;  // the chunkwise kernel's unit
+  }
   if (kMode == kCommit) {
     ntok = min(max(__ldg(p.accepted_len + b), 0), p.T);
     if (ntok == 0) return;  // nothing accepted: the state stays as it is
@@ -97,15 +118,24 @@ __global__ void __launch_bounds__(kThreads, 2) la_tokenwise_kernel(const Params 
 
   // ---- state block: S[r][j] pairs = (S[4 rg + r][16 cg + 2 j], S[4 rg + r][16 cg + 2 j + 1])
   uint64_t S[4][8];
-  float* sblk = p.state + ((static_cast<size_t>(slot) * p.HV + hv) * kDim + 4 * rg) * kDim + 16 * cg;
+  const size_t soff = ((static_cast<size_t>(slot) * p.HV + hv) * kDim + 4 * rg) * kDim + 16 * cg;
+  const float* s_in = (kMode == kPrefill) ? p.h0 : p.state;
+  float* s_out = (kMode == kPrefill) ? p.h_final : p.state;
+  if (kMode != kPrefill || s_in) {
 #pragma unroll
-  for (int r = 0; r < 4; ++r)
+    for (int r = 0; r < 4; ++r)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 x = __ldg(reinterpret_cast<const float4*>(sblk + r * kDim) + i);
-      S[r][2 * i] = f2_pack(x.x, x.y);
-      S[r][2 * i + 1] = f2_pack(x.z, x.w);
-    }
+      for (int i = 0; i < 4; ++i) {
+        const float4 x = __ldg(reinterpret_cast<const float4*>(s_in + soff + r * kDim) + i);
+        S[r][2 * i] = f2_pack(x.x, x.y);
+        S[r][2 * i + 1] = f2_pack(x.z, x.w);
+      }
+  } else {
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) S[r][j] = f2_pack(0.f, 0.f);
+  }
 
   const size_t qk_tok = static_cast<size_t>(p.H) * kDim;   // elements between tokens of q / k
   const size_t v_tok = static_cast<size_t>(p.HV) * kDim;   // ... of v / o
@@ -123,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 2) la_tokenwise_kernel(const Params 
         vx = __ldg(reinterpret_cast<const uint4*>(p.vbuf + ((static_cast<size_t>(slot) * p.T + t0 + i) * p.HV + hv) *
                                                                kDim) + c);
       } else {
-        const size_t row = static_cast<size_t>(b) * p.T + t0 + i;
+        const size_t row = row0 + t0 + i;
         kx = __ldg(reinterpret_cast<const uint4*>(p.k + row * qk_tok + static_cast<size_t>(hq) * kDim) + c);
         vx = __ldg(reinterpret_cast<const uint4*>(p.v + row * v_tok + static_cast<size_t>(hv) * kDim) + c);
         const uint4 qx = __ldg(reinterpret_cast<const uint4*>(p.q + row * qk_tok + static_cast<size_t>(hq) * kDim) + c);
@@ -192,19 +222,19 @@ __global__ void __launch_bounds__(kThreads, 2) la_tokenwise_kernel(const Params 
 #pragma unroll
           for (int r = 0; r < 4; ++r) dot[r] += __shfl_xor_sync(0xffffffffu, dot[r], m);
         if (cg < 4)  // lane group cg writes row 4 rg + cg
-          p.o[(static_cast<size_t>(b) * p.T + t0 + i) * v_tok + static_cast<size_t>(hv) * kDim + 4 * rg + cg] =
+          p.o[(row0 + t0 + i) * v_tok + static_cast<size_t>(hv) * kDim + 4 * rg + cg] =
               __float2bfloat16_rn(p.scale * (cg == 0 ? dot[0] : cg == 1 ? dot[1] : cg == 2 ? dot[2] : dot[3]));
       }
     }
   }
 
-  if (kMode != kVerify) {
+  if (kMode != kVerify && (kMode != kPrefill || s_out)) {
 #pragma unroll
     for (int r = 0; r < 4; ++r)
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float2 a = f2_unpack(S[r][2 * i]), c = f2_unpack(S[r][2 * i + 1]);
-        reinterpret_cast<float4*>(sblk + r * kDim)[i] = make_float4(a.x, a.y, c.x, c.y);
+        reinterpret_cast<float4*>(s_out + soff + r * kDim)[i] = make_float4(a.x, a.y, c.x, c.y);
       }
   }
 }

@@ -1,9 +1,15 @@
 // la_prefill_api.cu -- host side of the C ABI declared in include/la_prefill.h:
-// argument validation, TMA tensor-map construction and the kernel launch.
+// argument validation, TMA tensor-map construction and the kernel launches.
 //
-// Nothing here allocates device memory, reads device memory or synchronises with
-// the host: a call only encodes three tensor maps on the host stack and enqueues
-// one kernel on the caller's stream.
+// Sequences of at most kShortMax tokens go to the tokenwise kernel (one state read and
+// write and a few token updates), the others to the chunkwise kernel.  A fixed-length batch
+// goes to one of the two; a packed batch, whose lengths only the device knows, launches both
+// (each skips the other's units) when its average length is at most kSplitAvg tokens, and
+// otherwise leaves every sequence to the chunkwise kernel rather than pay a second launch
+// for the few short ones it may hold.
+// Nothing here allocates device memory, reads device memory or synchronises with the
+// host: a call only encodes three tensor maps on the host stack and enqueues one or two
+// kernels on the caller's stream.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -11,6 +17,7 @@
 #include <cstring>
 
 #include "../../include/la_prefill.h"
+#include "la_decode_kernels.cuh"
 #include "la_host_common.h"
 #include "la_prefill_kernel.cuh"
 
@@ -25,6 +32,11 @@ unsigned long long* g_trace = nullptr;  // device buffer for timeline tracing bu
 la_host::DeviceState g_dev[la_host::kMaxDevices];
 
 int smem_bytes() { return static_cast<int>(sizeof(lap::SharedStorage)) + 1024; }
+
+// Longest sequence the tokenwise kernel takes: up to two of its 16-token staging tiles.
+constexpr int kShortMax = 32;
+// Packed batches with at most this many tokens per sequence on average are split.
+constexpr int kSplitAvg = 64;
 
 }  // namespace
 
@@ -90,6 +102,39 @@ la_status la_prefill_fwd(const void* q, const void* k, const void* v, const floa
     if ((st = la_host::encode_bf16_rows_map(&tm_v, v, tokens, HV, "v")) != LA_OK) return st;
   }
 
+  const bool packed = cu_seqlens != nullptr;
+  const bool split = packed && tokens <= static_cast<int64_t>(kSplitAvg) * N;
+  const bool run_tokenwise = split || (!packed && T <= kShortMax);
+  const bool run_chunkwise = packed || T > kShortMax;
+  const int pool = la_host::effective_pool_size(h0, h_final, state_indices, pool_size, N);
+  if (run_tokenwise) {
+    lad::Params tp{};
+    tp.q = static_cast<const __nv_bfloat16*>(q);
+    tp.k = static_cast<const __nv_bfloat16*>(k);
+    tp.v = static_cast<const __nv_bfloat16*>(v);
+    tp.slopes = slopes;
+    tp.state_indices = state_indices;
+    tp.o = static_cast<__nv_bfloat16*>(o);
+    tp.h0 = h0;
+    tp.h_final = h_final;
+    tp.cu_seqlens = cu_seqlens;
+    tp.dev_error = dev_error;
+    tp.scale = scale;
+    tp.B = N;
+    tp.T = packed ? 0 : T;
+    tp.H = H;
+    tp.HV = HV;
+    tp.G = HV / H;
+    tp.pool_size = pool;
+    tp.num_tokens = static_cast<int>(tokens);
+    tp.short_max = kShortMax;
+    lad::la_tokenwise_kernel<lad::kPrefill>
+        <<<static_cast<int>(units), lad::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(tp);
+    ce = cudaGetLastError();
+    if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "tokenwise kernel launch failed: %s", cudaGetErrorString(ce));
+  }
+  if (!run_chunkwise) return LA_OK;
+
   lap::KernelParams p;
   p.slopes = slopes;
   p.h0 = h0;
@@ -106,8 +151,9 @@ la_status la_prefill_fwd(const void* q, const void* k, const void* v, const floa
   p.H = H;
   p.HV = HV;
   p.G = HV / H;
-  p.pool_size = la_host::effective_pool_size(h0, h_final, state_indices, pool_size, N);
+  p.pool_size = pool;
   p.num_units = static_cast<int>(units);
+  p.short_max = split ? kShortMax : -1;
 
   int grid = static_cast<int>(units);
   if (schedule != LA_SCHED_NON_PERSISTENT && grid > ds.sms) grid = ds.sms;

@@ -135,6 +135,7 @@ struct KernelParams {
   int G;          // HV / H
   int pool_size;
   int num_units;  // N * HV
+  int short_max;  // sequences of at most this many tokens belong to the tokenwise kernel (-1: none)
 };
 
 // One unit's sequence bounds, state slot and chunk count, decoded identically by every role.
@@ -163,6 +164,7 @@ __device__ __forceinline__ Unit decode_unit(const KernelParams& p, int u) {
     } else {
       w.bos = b;
       w.len = e - b;
+      if (w.len <= p.short_max) w.run = false;  // run by the tokenwise kernel
     }
   } else {
     w.bos = w.n * p.T;

@@ -42,6 +42,11 @@ EDGE_CASES = {
     "lambda_one": dict(lengths=[150, 20], H=1, HV=2, slopes=[0.0, 0.0]),
     "lambda_zero": dict(lengths=[150, 20], H=1, HV=2, slopes=[100.0, 100.0]),
     "long_two_chunks_plus": dict(lengths=[64 * 9 + 17], H=1, HV=1),
+    # sequences of at most 32 tokens run in the tokenwise kernel, longer ones in the chunkwise one
+    "short_long_boundary": dict(lengths=[32, 33, 31, 16, 17, 0, 100, 1, 64], H=2, HV=4, pool=11,
+                                indices=[3, 10, -1, 0, 7, 5, 1, 9, 2], in_place=True),
+    "fixed_T32_tokenwise": dict(B=3, T=32, H=2, HV=2),
+    "fixed_T33_chunkwise": dict(B=3, T=33, H=2, HV=2),
 }
 
 
