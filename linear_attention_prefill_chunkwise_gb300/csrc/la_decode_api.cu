@@ -1,5 +1,5 @@
 // la_decode_api.cu -- host side of the C ABI declared in include/la_decode.h: argument
-// validation and one launch per call (one CTA per (request, value head)).  Nothing here
+// validation and one launch per call (lad::kSplit CTAs per (request, value head)).  Nothing here
 // allocates device memory, reads device memory or synchronises with the host.
 #include <cuda_runtime.h>
 
@@ -25,7 +25,7 @@ la_status check_shapes(int B, int T, int H, int HV, int D, int V, int pool_size,
   if (HV % H != 0) return fail(LA_ERR_UNSUPPORTED, "HV (%d) must be a multiple of H (%d)", HV, H);
   if (B < 0) return fail(LA_ERR_INVALID_ARGUMENT, "B must be >= 0 (got %d)", B);
   if (T < 1) return fail(LA_ERR_INVALID_ARGUMENT, "T must be >= 1 (got %d)", T);
-  if (static_cast<int64_t>(B) * HV > INT32_MAX || static_cast<int64_t>(B) * T > INT32_MAX)
+  if (static_cast<int64_t>(B) * HV * lad::kSplit > INT32_MAX || static_cast<int64_t>(B) * T > INT32_MAX)
     return fail(LA_ERR_UNSUPPORTED, "B*HV or B*T too large");
   if (state_indices ? pool_size <= 0 : pool_size < B)
     return fail(LA_ERR_INVALID_ARGUMENT, "pool_size (%d) must be positive, and >= B (%d) without state_indices",
@@ -39,7 +39,7 @@ la_status launch(const lad::Params& p, void* stream) {
   la_host::DeviceState* ds = nullptr;
   la_status st = la_host::current_device(g_dev, &ds, [] { return cudaSuccess; });
   if (st != LA_OK) return st;
-  const int grid = p.B * p.HV;
+  const int grid = p.B * p.HV * lad::kSplit;
   lad::la_tokenwise_kernel<kMode><<<grid, lad::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(p);
   const cudaError_t ce = cudaGetLastError();
   if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(ce));

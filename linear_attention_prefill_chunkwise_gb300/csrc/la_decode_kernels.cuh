@@ -5,10 +5,12 @@
 //
 // A request carries a handful of draft tokens (T <= 8 in the pages' workloads), so each
 // (request, value head) unit costs one read of its 64 KB FP32 state, T token updates and,
-// for decode and commit, one write of the state: the work is bound by the state traffic,
-// and the state fits the registers of one CTA.  One CTA of 256 threads per unit: thread t
-// owns the 4 x 16 block of state rows v = 4 (t / 8) .. +3 and columns k = 16 (t % 8) .. +15,
-// and for every token
+// for decode and commit, one write of the state: the work is bound by the state traffic.
+// Each row of the state evolves, and gives its output, independently of the others, so a
+// unit is split over kSplit CTAs of 128 threads that each keep 64 state rows in registers
+// (more, smaller CTAs per SM overlap one CTA's state load with another's arithmetic).
+// Thread t of part h owns the 4 x 16 block of state rows v = 64 h + 4 (t / 8) .. +3 and
+// columns k = 16 (t % 8) .. +15, and for every token
 //     S[v][k] = lambda S[v][k] + v_t[v] k_t[k]              (FP32, fused multiply-add)
 //     o_t[v]  = scale sum_k S[v][k] q_t[k]                    (8 column-group partial sums,
 //                                                             added across lanes t^1, t^2, t^4)
@@ -38,7 +40,9 @@ using lap::f2_pack;
 using lap::f2_unpack;
 
 constexpr int kDim = 128;   // D = V = 128
-constexpr int kThreads = 256;
+constexpr int kSplit = 2;                 // CTAs per (request, value head)
+constexpr int kRows = kDim / kSplit;      // state rows per CTA
+constexpr int kThreads = kRows / 4 * 8;   // 4 rows x 16 columns per thread
 constexpr int kTileT = 16;  // tokens staged in shared memory per pass
 
 enum Mode : int { kDecode = 0, kVerify = 1, kCommit = 2, kPrefill = 3 };
@@ -77,12 +81,14 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& x, float (&f)[8]) {
 constexpr int kGroupStride = 20;  // floats per staged 16-column group (16 + 4 padding)
 
 template <int kMode>
-__global__ void __launch_bounds__(kThreads, 2) la_tokenwise_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, 2 * kSplit) la_tokenwise_kernel(const Params p) {
   __shared__ __align__(16) float ks[kTileT][8 * kGroupStride];
   __shared__ __align__(16) float qs[kTileT][8 * kGroupStride];
-  __shared__ __align__(16) float vs[kTileT][kDim];
+  __shared__ __align__(16) float vs[kTileT][kRows];
 
-  const int unit = blockIdx.x;  // b * HV + hv
+  const int unit = blockIdx.x / kSplit;  // b * HV + hv
+  const int part = blockIdx.x - unit * kSplit;
+  const int vbase = part * kRows;        // first state row (value index) of this CTA
   const int b = unit / p.HV;
   const int hv = unit - b * p.HV;
   const int hq = hv / p.G;
@@ -112,13 +118,13 @@ __global__ void __launch_bounds__(kThreads, 2) la_tokenwise_kernel(const Params 
   }
 
   const int t = threadIdx.x;
-  const int cg = t & 7, rg = t >> 3;  // columns 16 cg .. +15, rows 4 rg .. +3
+  const int cg = t & 7, rg = t >> 3;  // columns 16 cg .. +15, rows vbase + 4 rg .. +3
   const float lam = expf(-__ldg(p.slopes + hv));
   const uint64_t lam2 = f2_pack(lam, lam);
 
-  // ---- state block: S[r][j] pairs = (S[4 rg + r][16 cg + 2 j], S[4 rg + r][16 cg + 2 j + 1])
+  // ---- state block: S[r][j] pairs = (S[v + r][16 cg + 2 j], S[v + r][16 cg + 2 j + 1]), v = vbase + 4 rg
   uint64_t S[4][8];
-  const size_t soff = ((static_cast<size_t>(slot) * p.HV + hv) * kDim + 4 * rg) * kDim + 16 * cg;
+  const size_t soff = ((static_cast<size_t>(slot) * p.HV + hv) * kDim + vbase + 4 * rg) * kDim + 16 * cg;
   const float* s_in = (kMode == kPrefill) ? p.h0 : p.state;
   float* s_out = (kMode == kPrefill) ? p.h_final : p.state;
   if (kMode != kPrefill || s_in) {
@@ -146,35 +152,37 @@ __global__ void __launch_bounds__(kThreads, 2) la_tokenwise_kernel(const Params 
     for (int e = t; e < nt * (kDim / 8); e += kThreads) {
       const int i = e >> 4, c = e & 15;              // token, 8-value chunk (column group c / 2)
       const int kpos = (c >> 1) * kGroupStride + 8 * (c & 1);
-      uint4 kx, vx;
+      const bool vmine = c / (kRows / 8) == part;    // values 8c .. 8c + 7 are rows of this CTA
+      uint4 kx, vx = make_uint4(0u, 0u, 0u, 0u);
       if (kMode == kCommit) {
-        kx = __ldg(reinterpret_cast<const uint4*>(p.kbuf + ((static_cast<size_t>(slot) * p.T + t0 + i) * p.H + hq) *
-                                                               kDim) + c);
-        vx = __ldg(reinterpret_cast<const uint4*>(p.vbuf + ((static_cast<size_t>(slot) * p.T + t0 + i) * p.HV + hv) *
-                                                               kDim) + c);
+        const size_t brow = static_cast<size_t>(slot) * p.T + t0 + i;
+        kx = __ldg(reinterpret_cast<const uint4*>(p.kbuf + (brow * p.H + hq) * kDim) + c);
+        if (vmine) vx = __ldg(reinterpret_cast<const uint4*>(p.vbuf + (brow * p.HV + hv) * kDim) + c);
       } else {
         const size_t row = row0 + t0 + i;
         kx = __ldg(reinterpret_cast<const uint4*>(p.k + row * qk_tok + static_cast<size_t>(hq) * kDim) + c);
-        vx = __ldg(reinterpret_cast<const uint4*>(p.v + row * v_tok + static_cast<size_t>(hv) * kDim) + c);
+        if (vmine) vx = __ldg(reinterpret_cast<const uint4*>(p.v + row * v_tok + static_cast<size_t>(hv) * kDim) + c);
         const uint4 qx = __ldg(reinterpret_cast<const uint4*>(p.q + row * qk_tok + static_cast<size_t>(hq) * kDim) + c);
         float f[8];
         bf16x8_to_f32(qx, f);
         reinterpret_cast<float4*>(&qs[i][kpos])[0] = make_float4(f[0], f[1], f[2], f[3]);
         reinterpret_cast<float4*>(&qs[i][kpos])[1] = make_float4(f[4], f[5], f[6], f[7]);
-        if (kMode == kVerify && p.kbuf) {  // the KV buffer copy (k once per q/k head)
+        if (kMode == kVerify && p.kbuf) {  // the KV buffer copy (k once per q/k head, by part 0)
           const size_t brow = static_cast<size_t>(slot) * p.T + t0 + i;
-          if (hv % p.G == 0)
+          if (hv % p.G == 0 && part == 0)
             reinterpret_cast<uint4*>(p.kbuf + (brow * p.H + hq) * kDim)[c] = kx;
-          reinterpret_cast<uint4*>(p.vbuf + (brow * p.HV + hv) * kDim)[c] = vx;
+          if (vmine) reinterpret_cast<uint4*>(p.vbuf + (brow * p.HV + hv) * kDim)[c] = vx;
         }
       }
       float f[8];
       bf16x8_to_f32(kx, f);
       reinterpret_cast<float4*>(&ks[i][kpos])[0] = make_float4(f[0], f[1], f[2], f[3]);
       reinterpret_cast<float4*>(&ks[i][kpos])[1] = make_float4(f[4], f[5], f[6], f[7]);
-      bf16x8_to_f32(vx, f);
-      reinterpret_cast<float4*>(&vs[i][8 * c])[0] = make_float4(f[0], f[1], f[2], f[3]);
-      reinterpret_cast<float4*>(&vs[i][8 * c])[1] = make_float4(f[4], f[5], f[6], f[7]);
+      if (vmine) {
+        bf16x8_to_f32(vx, f);
+        reinterpret_cast<float4*>(&vs[i][8 * c - vbase])[0] = make_float4(f[0], f[1], f[2], f[3]);
+        reinterpret_cast<float4*>(&vs[i][8 * c - vbase])[1] = make_float4(f[4], f[5], f[6], f[7]);
+      }
     }
     __syncthreads();
 
@@ -221,8 +229,8 @@ __global__ void __launch_bounds__(kThreads, 2) la_tokenwise_kernel(const Params 
         for (int m = 1; m < 8; m <<= 1)
 #pragma unroll
           for (int r = 0; r < 4; ++r) dot[r] += __shfl_xor_sync(0xffffffffu, dot[r], m);
-        if (cg < 4)  // lane group cg writes row 4 rg + cg
-          p.o[(row0 + t0 + i) * v_tok + static_cast<size_t>(hv) * kDim + 4 * rg + cg] =
+        if (cg < 4)  // lane group cg writes row vbase + 4 rg + cg
+          p.o[(row0 + t0 + i) * v_tok + static_cast<size_t>(hv) * kDim + vbase + 4 * rg + cg] =
               __float2bfloat16_rn(p.scale * (cg == 0 ? dot[0] : cg == 1 ? dot[1] : cg == 2 ? dot[2] : dot[3]));
       }
     }

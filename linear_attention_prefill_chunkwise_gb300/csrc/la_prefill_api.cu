@@ -128,8 +128,9 @@ la_status la_prefill_fwd(const void* q, const void* k, const void* v, const floa
     tp.pool_size = pool;
     tp.num_tokens = static_cast<int>(tokens);
     tp.short_max = kShortMax;
+    if (units * lad::kSplit > INT32_MAX) return fail(LA_ERR_UNSUPPORTED, "N*HV too large (%lld)", (long long)units);
     lad::la_tokenwise_kernel<lad::kPrefill>
-        <<<static_cast<int>(units), lad::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(tp);
+        <<<static_cast<int>(units * lad::kSplit), lad::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(tp);
     ce = cudaGetLastError();
     if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "tokenwise kernel launch failed: %s", cudaGetErrorString(ce));
   }
