@@ -66,3 +66,17 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     monkeypatch.setenv("WORLD_SIZE", "2")
     bench.run_reference(types.SimpleNamespace(steps=1, warmup=3, ref_budget=1.0))
     assert capsys.readouterr().out == ""  # no work, no line: rank 0 alone prints
+
+
+def test_numa_pinning_degrades_gracefully_and_restores_affinity():
+    """Without a readable GPU node (no GPU here) the e2e leg's NUMA placement is skipped and the
+    process keeps its CPU affinity."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    before = os.sched_getaffinity(0)
+    spec, prev = bench.pin_to_gpu_numa_node(torch.device("cpu"))
+    assert prev == before
+    if spec is None:
+        assert os.sched_getaffinity(0) == before
+    os.sched_setaffinity(0, prev)
