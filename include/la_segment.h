@@ -23,7 +23,7 @@
  * count, and otherwise picks S so that the segments fill the SMs about once.
  *
  * Every pointer is a DEVICE pointer owned by the caller.  The call allocates nothing, never
- * synchronises with the host and enqueues its kernels (5 at most) on `stream`.
+ * synchronises with the host and enqueues its kernels (6 at most) on `stream`.
  */
 #ifndef LA_SEGMENT_H
 #define LA_SEGMENT_H
