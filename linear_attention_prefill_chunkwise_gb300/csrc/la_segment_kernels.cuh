@@ -32,10 +32,8 @@
 namespace las {
 
 using lap::bf16x2_to_f2;
-using lap::f2_fma;
 using lap::f2_mul;
 using lap::f2_pack;
-using lap::f2_unpack;
 using lap::split_bf16x2;
 
 constexpr int kChunk = 64;

@@ -47,6 +47,9 @@ EDGE_CASES = {
                                 indices=[3, 10, -1, 0, 7, 5, 1, 9, 2], in_place=True),
     "fixed_T32_tokenwise": dict(B=3, T=32, H=2, HV=2),
     "fixed_T33_chunkwise": dict(B=3, T=33, H=2, HV=2),
+    "short_no_h0": dict(lengths=[5, 20, 0, 3, 32], H=1, HV=2, with_h0=False),
+    "short_no_final": dict(lengths=[5, 20, 3, 31], H=2, HV=2, want_final=False),
+    "fixed_T8_gva_pool": dict(B=4, T=8, H=1, HV=4, pool=6, indices=[5, -1, 0, 3], in_place=True),
 }
 
 
