@@ -357,6 +357,7 @@ def run_cuda(args):
 
     if rank == 0:
         peak, peak_kind = measured_peaks()
+        tflops, tf_kind = measured_bf16_tflops()
         launch_ms = statistics.fmean(per_launch_ms)
         achieved = ALG_BYTES / (launch_ms / 1e3) / 1e9
         line = {
@@ -370,7 +371,11 @@ def run_cuda(args):
                          "frac": round(achieved / peak, 4), "traffic": dram_traffic_per_launch(),
                          "peak_source": f"{peak_kind} hbm_gbs", "alg_bytes_per_launch": ALG_BYTES,
                          "alg_flops_per_launch": ALG_FLOPS, "kernel": KERNEL_NAME,
-                         "launch_ms_mean": round(launch_ms, 5), "launch_ms_min": round(min(per_launch_ms), 5)},
+                         "launch_ms_mean": round(launch_ms, 5), "launch_ms_min": round(min(per_launch_ms), 5),
+                         "tensor": {"achieved": round(ALG_FLOPS / (launch_ms / 1e3) / 1e12, 1), "peak": tflops,
+                                    "unit": "TFLOP/s",
+                                    "frac": round(ALG_FLOPS / (launch_ms / 1e3) / 1e12 / tflops, 4),
+                                    "peak_source": f"{tf_kind} bf16_tflops (dense)"}},
             "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "steps": e2e_steps, "pipelined": "2 buffer sets: copy-in, launch and copy-out streams",
                     "host_numa": numa},
