@@ -12,7 +12,6 @@ the host cores instead (a bounded sample of the same workload per step).
 from __future__ import annotations
 
 import argparse
-import datetime
 import hashlib
 import json
 import math
@@ -104,69 +103,120 @@ def dram_traffic_per_launch():
 
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons; only samples taken inside
-    the marked timed window are summarised."""
+    """SM clock, power and clock-event (throttle) reasons sampled during the timed region.
 
-    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    A thread polls NVML (read-only queries through ctypes on the driver's libnvidia-ml) about
+    once a millisecond, so that even a timed region of a few milliseconds holds samples; only
+    samples taken between mark_start() and mark_end() are summarised.  Without NVML it falls
+    back to `nvidia-smi -lms`, started before the timed region and given time to print its
+    first line."""
 
-    def __init__(self, gpu_id: str):
-        self.gpu = gpu_id
-        self.proc = None
-        self.out = None
+    REASON_BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                   0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    SMI_FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                  "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_uuid: str, period_s: float = 0.001):
+        self.uuid = gpu_uuid
+        self.period = period_s
+        self.samples = []  # (perf_counter, sm_mhz, max_mhz, power_w, reason names)
+        self.source = None
         self.t0 = self.t1 = None
+        self._stop = None
+        self._thread = None
+        self._smi = None
 
-    def __enter__(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", self.gpu, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
-        return self
+    # ---- NVML through ctypes
+    def _nvml_open(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByUUID(self.uuid.encode(), ctypes.byref(h)) != 0:
+            raise OSError(f"no NVML device {self.uuid}")
+        reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        return lib, h, reasons_fn
 
-    def mark_start(self):
-        self.t0 = datetime.datetime.now()
+    def _nvml_loop(self, lib, h, reasons_fn):
+        import ctypes
+        sm, mx, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self._stop.is_set():
+            ok = (lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0 and
+                  lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0)
+            if ok:
+                power = pw.value / 1000.0 if lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw)) == 0 else None
+                names = [n for bit, n in self.REASON_BITS.items() if reasons_fn(h, ctypes.byref(rs)) == 0
+                         and rs.value & bit]
+                self.samples.append((time.perf_counter(), float(sm.value), float(mx.value), power, names))
+            self._stop.wait(self.period)
 
-    def mark_end(self):
-        self.t1 = datetime.datetime.now()
-
-    def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.out, _ = self.proc.communicate(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-                self.out, _ = self.proc.communicate()
-
-    def summary(self):
-        empty = {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
-        if not self.out:
-            return empty
-        sm, mx, power, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.out.strip().splitlines():
+    # ---- nvidia-smi fallback
+    def _smi_reader(self):
+        for line in self._smi.stdout:
             parts = [x.strip() for x in line.split(",")]
             if len(parts) < 9:
                 continue
             try:
-                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
-                if self.t0 and self.t1 and not (self.t0 <= ts <= self.t1):
-                    continue
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
-                power.append(float(parts[3]))
+                names = [n for n, val in zip(["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                              "sw_power_cap"], parts[5:9]) if val.lower().startswith("active")]
+                self.samples.append((time.perf_counter(), float(parts[1]), float(parts[2]), float(parts[3]),
+                                     names))
             except ValueError:
                 continue
-            for name, val in zip(names, parts[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
-        if not sm:
-            return empty
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "power_w_median": statistics.median(power), "samples": len(sm)}
+
+    def __enter__(self):
+        import threading
+        self._stop = threading.Event()
+        try:
+            lib, h, reasons_fn = self._nvml_open()
+            self._thread = threading.Thread(target=self._nvml_loop, args=(lib, h, reasons_fn), daemon=True)
+            self.source = "nvml"
+        except (OSError, AttributeError):
+            try:
+                self._smi = subprocess.Popen(
+                    ["nvidia-smi", "-i", self.uuid, f"--query-gpu={self.SMI_FIELDS}", "--format=csv,noheader,nounits",
+                     "-lms", "20"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self._thread = threading.Thread(target=self._smi_reader, daemon=True)
+                self.source = "nvidia-smi"
+            except OSError:
+                return self
+        self._thread.start()
+        deadline = time.perf_counter() + 5.0
+        while not self.samples and time.perf_counter() < deadline:  # sampling is live before timing starts
+            time.sleep(0.005)
+        return self
+
+    def mark_start(self):
+        self.t0 = time.perf_counter()
+
+    def mark_end(self):
+        self.t1 = time.perf_counter()
+
+    def __exit__(self, *exc):
+        if self._stop is not None:
+            self._stop.set()
+        if self._smi is not None:
+            self._smi.terminate()
+            try:
+                self._smi.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self._smi.kill()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
+
+    def summary(self):
+        inside = [s for s in self.samples if self.t0 is not None and self.t1 is not None and self.t0 <= s[0] <= self.t1]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0,
+                    "source": self.source}
+        reasons = sorted({n for s in inside for n in s[4]})
+        power = [s[3] for s in inside if s[3] is not None]
+        return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": max(s[2] for s in inside),
+                "reasons": reasons, "power_w_median": statistics.median(power) if power else None,
+                "samples": len(inside), "source": self.source}
 
 
 def gpu_id_for_smi(device) -> str:
@@ -281,7 +331,6 @@ def run_cuda(args):
     barrier()
     torch.cuda.synchronize(device)
     with ClockSampler(gpu_id_for_smi(device)) as clk:
-        time.sleep(0.3)  # let the sampler start before the timed region
         clk.mark_start()
         with torch.cuda.stream(stream):
             ev[0].record(stream)

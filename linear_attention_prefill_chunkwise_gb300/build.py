@@ -44,21 +44,31 @@ def _stale(path: str) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, trace: bool = False) -> str:
+def build(force: bool = False, verbose: bool = False, trace: bool = False, wait_limit_ns: int = 0) -> str:
     """Build the library if any source is newer than it; return its path.
 
-    trace=True builds the timeline-tracing variant (-DLA_TRACE) as a separate file."""
-    out = TRACE_LIB_PATH if trace else LIB_PATH
+    trace=True builds the timeline-tracing variant (-DLA_TRACE) as a separate file.
+    wait_limit_ns > 0 builds the prefill entry point alone, as a separate file, with that
+    limit on every pipeline wait instead of one second: ordinary waits then exceed it, so the
+    kernels' timeout exit can be exercised on a healthy input."""
+    if wait_limit_ns:
+        out = os.path.join(BUILD_DIR, f"libla_prefill_wait{int(wait_limit_ns)}ns.so")
+        sources = ["la_prefill_api.cu"]
+    else:
+        out = TRACE_LIB_PATH if trace else LIB_PATH
+        sources = SOURCES
     if not force and not _stale(out):
         return out
     os.makedirs(BUILD_DIR, exist_ok=True)
     tmp = out + f".tmp{os.getpid()}"
     cmd = [nvcc_path(), *ARCH_FLAGS, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
-           "-cudart", "static", "-I", INCLUDE_DIR, "-o", tmp] + [os.path.join(CSRC, s) for s in SOURCES]
+           "-cudart", "static", "-I", INCLUDE_DIR, "-o", tmp] + [os.path.join(CSRC, s) for s in sources]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     if trace:
         cmd.insert(1, "-DLA_TRACE")
+    if wait_limit_ns:
+        cmd.insert(1, f"-DLA_WAIT_LIMIT_NS={int(wait_limit_ns)}ull")
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError("nvcc failed:\n" + " ".join(cmd) + "\n" + res.stdout + res.stderr)

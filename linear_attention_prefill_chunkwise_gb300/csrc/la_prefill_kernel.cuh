@@ -380,16 +380,20 @@ __device__ __forceinline__ void tma_mma_loop(SharedStorage& sm, const KernelPara
       __nanosleep(32);
     }
   }
+  // Teardown, also after an abort: every load issued has landed and every MMA issued has
+  // retired before the CTA releases its shared and tensor memory.  A load is issued only
+  // after the previous one into its slot was consumed, so the last loads of each ring are the
+  // only ones that can still be in flight.
   for (uint32_t i = 0; i < kQKStages && i < nqk; ++i) {
     const uint32_t j = nqk - 1 - i;
-    mbar_wait(&sm.qk_full[j % kQKStages], (j / kQKStages) & 1u, abort);
+    mbar_wait_drain(&sm.qk_full[j % kQKStages], (j / kQKStages) & 1u);
   }
   for (uint32_t i = 0; i < kVStages && i < nv; ++i) {
     const uint32_t j = nv - 1 - i;
-    mbar_wait(&sm.v_full[j % kVStages], (j / kVStages) & 1u, abort);
+    mbar_wait_drain(&sm.v_full[j % kVStages], (j / kVStages) & 1u);
   }
   mma_commit(&sm.final_bar[1]);
-  mbar_wait(&sm.final_bar[1], 0, abort);
+  mbar_wait_drain(&sm.final_bar[1], 0);
 }
 
 // MMA thread A: the output accumulator, in chunk order, with blocking waits (this is the
@@ -439,7 +443,7 @@ __device__ __forceinline__ void mma_o_loop(SharedStorage& sm, const KernelParams
     mma_commit(&sm.v_empty[sv]);
   }
   mma_commit(&sm.final_bar[0]);
-  mbar_wait(&sm.final_bar[0], 0, abort);
+  mbar_wait_drain(&sm.final_bar[0], 0);  // every MMA of this thread retired, also after an abort
 }
 
 // Q converter (warps 2-3): the BF16 Q tile (K-major, 128B-swizzled, 2 boxes of 64 d) into
@@ -516,8 +520,25 @@ __device__ __forceinline__ void operand_loop(SharedStorage& sm, const KernelPara
         break;
       }
       LA_TRACE_AT(p, kTrOperKtStart, it, otid == 0);
-      {
-        const float wjf = (krow < L) ? lam[L - 1 - krow] : 0.f;
+      if (L < kChunk) {
+        // Rows j >= L of a ragged chunk's tiles belong to the next packed sequence (or are the
+        // TMA's zero fill).  They are zeroed, not multiplied by zero: a non-finite value there
+        // must not reach this sequence (0 * inf is NaN).  Kt rows are zeroed below; the V rows
+        // feed the dS and O_intra MMAs directly, so this thread clears its row of the V stage,
+        // which both MMAs read only after kt_ready (arrived below).
+        const uint32_t sv = it % kVStages;
+        if (!warp_wait(&sm.v_full[sv], (it / kVStages) & 1u, abort)) {
+          ok = false;
+          break;
+        }
+        if (krow >= L) {
+          uint8_t* vrow_s = sm.v[sv][kbox] + krow * 128;
+#pragma unroll
+          for (int cc = 0; cc < 8; ++cc) *reinterpret_cast<uint4*>(vrow_s + 16 * cc) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      if (krow < L) {
+        const float wjf = lam[L - 1 - krow];
         const uint64_t wj = f2_pack(wjf, wjf);
         const uint8_t* ksrc = sm.qk[sq].k[kbox];
 #pragma unroll 2
@@ -530,6 +551,13 @@ __device__ __forceinline__ void operand_loop(SharedStorage& sm, const KernelPara
           for (int e = 0; e < 4; ++e) split_bf16x2(f2_mul(wj, bf16x2_to_f2(kw[e])), hi[e], lo[e]);
           *reinterpret_cast<uint4*>(sm.kt_hi[kbox] + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
           *reinterpret_cast<uint4*>(sm.kt_lo[kbox] + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+      } else {
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          const uint32_t off = swz(krow, cc);
+          *reinterpret_cast<uint4*>(sm.kt_hi[kbox] + off) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(sm.kt_lo[kbox] + off) = make_uint4(0, 0, 0, 0);
         }
       }
       fence_proxy_async_smem();

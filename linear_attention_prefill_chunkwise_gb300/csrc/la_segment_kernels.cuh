@@ -238,7 +238,7 @@ drain:
   // no copy may still be landing in shared memory when the CTA exits
   for (uint32_t i = 0; i < kStStages && i < it; ++i) {
     const uint32_t j = it - 1 - i;
-    lap::mbar_wait(&sm.full[j % kStStages], (j / kStStages) & 1u, abort);
+    lap::mbar_wait_drain(&sm.full[j % kStStages], (j / kStStages) & 1u);
   }
 }
 
@@ -282,7 +282,7 @@ __device__ __forceinline__ void st_mma(StateSmem& sm, const StateParams& p, uint
     lap::mma_commit(&sm.acc_full[a]);
   }
   lap::mma_commit(&sm.final_bar);
-  lap::mbar_wait(&sm.final_bar, 0, abort);
+  lap::mbar_wait_drain(&sm.final_bar, 0);  // every MMA retired before TMEM is released, also after an abort
 }
 
 // Warps 4..11: Kt_j = lambda^(L-1-j) k_j as a BF16 hi/lo pair, in the K tile's own swizzled
@@ -300,21 +300,35 @@ __device__ __forceinline__ void st_builder(StateSmem& sm, const StateParams& p, 
           !st_warp_wait(&sm.kt_free[b], ((it >> 1) & 1u) ^ 1u, abort))
         return;
       const int j = c * kChunk + row;  // token index inside the segment
-      const float wj = (j < w.len) ? expf(-slope * static_cast<float>(w.len - 1 - j)) : 0.f;
-      const uint64_t w2 = f2_pack(wj, wj);
       const uint8_t* src = sm.k[s][box];
       uint8_t* dhi = sm.kt_hi[b][box];
       uint8_t* dlo = sm.kt_lo[b][box];
+      if (j < w.len) {
+        const float wj = expf(-slope * static_cast<float>(w.len - 1 - j));
+        const uint64_t w2 = f2_pack(wj, wj);
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        const uint32_t off = st_swz(row, c0 + cc);
-        const uint4 kx = *reinterpret_cast<const uint4*>(src + off);
-        const uint32_t kw[4] = {kx.x, kx.y, kx.z, kx.w};
-        uint32_t hi[4], lo[4];
+        for (int cc = 0; cc < 4; ++cc) {
+          const uint32_t off = st_swz(row, c0 + cc);
+          const uint4 kx = *reinterpret_cast<const uint4*>(src + off);
+          const uint32_t kw[4] = {kx.x, kx.y, kx.z, kx.w};
+          uint32_t hi[4], lo[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) split_bf16x2(f2_mul(w2, bf16x2_to_f2(kw[e])), hi[e], lo[e]);
-        *reinterpret_cast<uint4*>(dhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-        *reinterpret_cast<uint4*>(dlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          for (int e = 0; e < 4; ++e) split_bf16x2(f2_mul(w2, bf16x2_to_f2(kw[e])), hi[e], lo[e]);
+          *reinterpret_cast<uint4*>(dhi + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(dlo + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+      } else {
+        // Past the segment's end (segments that need a local state are whole chunks, so this
+        // is defensive): Kt and V rows are zeroed rather than multiplied by zero, so that a
+        // non-finite value of a neighbouring sequence cannot reach this state (0 * inf = NaN).
+        uint8_t* vrow = sm.v[s][box] + row * 128;
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          const uint32_t off = st_swz(row, c0 + cc);
+          *reinterpret_cast<uint4*>(dhi + off) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(dlo + off) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vrow + 16 * (c0 + cc)) = make_uint4(0, 0, 0, 0);
+        }
       }
       lap::fence_proxy_async_smem();
       lap::mbar_arrive(&sm.kt_ready[b]);

@@ -59,8 +59,13 @@ la_status la_prefill_fwd_segmented_static(const void* q, const void* k, const vo
                                           int H, int HV, int D, int V, int pool_size, int segment_len,
                                           int* dev_error, void* stream) {
   la_host::g_last_error[0] = '\0';
+  // The arguments first, so that an invalid call is reported as such whatever its size.
+  bool nothing = false;
+  la_status st = la_host::check_prefill_args(q, k, v, slopes, h0, state_indices, cu_seqlens, o, h_final, B, T, N, H,
+                                             HV, D, V, pool_size, dev_error, &nothing);
+  if (st != LA_OK || nothing) return st;
   size_t need = 0;
-  la_status st = la_prefill_segmented_workspace(B, T, N, HV, cu_seqlens != nullptr, segment_len, &need, nullptr);
+  st = la_prefill_segmented_workspace(B, T, N, HV, cu_seqlens != nullptr, segment_len, &need, nullptr);
   if (st != LA_OK) return st;
   if (need > kScratchBytes)
     return fail(LA_ERR_UNSUPPORTED,

@@ -55,8 +55,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait limit for one phase of one barrier.  A healthy pipeline step takes
-// microseconds; a second means something upstream has stopped.
+// microseconds; a second means something upstream has stopped.  A build may set a
+// shorter limit (-DLA_WAIT_LIMIT_NS=...) so that ordinary waits exceed it and the
+// timeout exit runs on a healthy input.
+#ifdef LA_WAIT_LIMIT_NS
+constexpr uint64_t kWaitLimitNs = LA_WAIT_LIMIT_NS;
+#else
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
+#endif
+// Limit of a drain wait: the wait at teardown for this CTA's own copies and MMAs in
+// flight, which finish by themselves whatever the rest of the pipeline did.
+constexpr uint64_t kDrainLimitNs = 1000000000ull;
 
 // Non-blocking test of a phase's completion.
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
@@ -93,6 +102,19 @@ static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parit
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, abort);
+}
+
+// Teardown wait for an asynchronous operation this CTA issued itself (a TMA load landing,
+// an MMA group retiring): it ignores the abort flag, since shared memory and tensor memory
+// must not be released while such an operation may still write them, and gives up only
+// after kDrainLimitNs.  Returns whether the phase completed.
+static __device__ __noinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kDrainLimitNs) return false;
+  }
 }
 
 // Named barrier over a subset of the CTA's warps (ids 1..15; 0 is __syncthreads).

@@ -166,3 +166,65 @@ def compare_sampled(p, d, units, label):
         if hf is not None:
             slot = n if p.state_indices is None else int(p.state_indices[n])
             check_state(hf[slot, hv].cpu().numpy(), h_ref, f"{label} state (n={n}, hv={hv})")
+
+
+def unit_metrics(o_gpu, o_ref):
+    """(rel RMS, max abs error, max |o_ref|) of one unit's output rows."""
+    o_gpu = np.asarray(o_gpu, dtype=np.float64)
+    o_ref = np.asarray(o_ref, dtype=np.float64)
+    diff = o_gpu - o_ref
+    den = np.sqrt(np.sum(o_ref ** 2))
+    return (float(np.sqrt(np.sum(diff ** 2)) / max(den, 1e-300)), float(np.max(np.abs(diff))),
+            float(np.max(np.abs(o_ref))))
+
+
+def compare_every_unit(p, d, label, nthreads=0):
+    """The whole problem against the oracle, unit by unit: every (sequence, value head) unit's
+    output rows and final state must meet the output and state bounds on their own, rows of
+    padded sequences must stay poisoned and state slots no sequence selects must keep their
+    initial value bit for bit (or stay poisoned).  A failure lists every failing (n, hv) unit
+    with its figures.  Returns the worst unit's (output rel RMS, state rel RMS)."""
+    import torch
+    torch.cuda.synchronize()
+    o_ref, h_ref = oracle_full(p, nthreads=nthreads)
+    o_gpu = d["o"].float().cpu().numpy()
+    hf = None if d["h_final"] is None else d["h_final"].cpu().numpy()
+    slots = list(p.state_indices) if p.state_indices is not None else list(range(p.N))
+    bad, worst_o, worst_s = [], 0.0, 0.0
+    for n in range(p.N):
+        a, b = unit_bounds(p, n)
+        slot = int(slots[n])
+        if slot < 0:
+            if b > a and not np.all(np.isnan(o_gpu[a:b])):
+                bad.append(f"(n={n}) padded sequence has written rows")
+            continue
+        for hv in range(p.HV):
+            if b > a:
+                og = o_gpu[a:b, hv]
+                if not np.all(np.isfinite(og)):
+                    bad.append(f"(n={n}, hv={hv}) non-finite output")
+                    continue
+                r, ma, mref = unit_metrics(og, o_ref[a:b, hv])
+                worst_o = max(worst_o, r)
+                if r > O_REL_RMS or ma > O_MAX_ABS_FRAC * mref + 1e-30:
+                    bad.append(f"(n={n}, hv={hv}) output rel RMS {r:.3e}, max abs {ma:.3e} vs max |o| {mref:.3e}")
+            if hf is not None:
+                hs = hf[slot, hv]
+                if not np.all(np.isfinite(hs)):
+                    bad.append(f"(n={n}, hv={hv}) non-finite state")
+                    continue
+                rs = rel_rms(hs, h_ref[slot, hv])
+                worst_s = max(worst_s, rs)
+                if rs > STATE_REL_RMS:
+                    bad.append(f"(n={n}, hv={hv}) state rel RMS {rs:.3e}")
+    if hf is not None:
+        live = [int(s) for s in slots if s >= 0]
+        unsel = np.ones(hf.shape[0], bool)
+        unsel[live] = False
+        if p.in_place and p.h0 is not None:
+            if not np.array_equal(hf[unsel].view(np.uint32), p.h0[unsel].view(np.uint32)):
+                bad.append("state slots no sequence selects were changed")
+        elif not np.all(np.isnan(hf[unsel])):
+            bad.append("state slots no sequence selects were written")
+    assert not bad, f"{label}: {len(bad)} failing units:\n  " + "\n  ".join(bad[:40])
+    return worst_o, worst_s

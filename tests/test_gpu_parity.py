@@ -1,10 +1,10 @@
 """CUDA path vs the FP64 oracle, element by element, on seeded inputs.
 
 Small problems are compared in full (several chunks, ragged tails, empty and
-padded sequences, GVA, state pools); the five benchmark workloads at full size
-are compared on sampled (sequence, value head) units the oracle computes one by
-one, plus properties that hold at any size (untouched pool slots and padded
-rows, finite outputs everywhere they are written).
+padded sequences, GVA, state pools), and so are the five benchmark workloads at
+full size: every (sequence, value head) unit's output rows and final state must
+meet the bounds on its own, padded rows stay unwritten and unselected pool slots
+keep their initial value bit for bit.
 """
 import zlib
 
@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 import workloads as W
-from harness import compare_full, compare_sampled, run_gpu, upload
+from harness import compare_every_unit, compare_full, run_gpu, upload
 
 pytestmark = pytest.mark.gpu
 
@@ -24,6 +24,7 @@ def test_tiny_workload_full():
     d = upload(p)
     run_gpu(p, d)
     compare_full(p, d, "tiny B=1 T=256 H=4")
+    compare_every_unit(p, d, "tiny B=1 T=256 H=4")
 
 
 EDGE_CASES = {
@@ -62,42 +63,38 @@ def test_edge_cases_full(name):
     compare_full(p, d, name)
 
 
-def test_fixed_mha_b2_t8192_sampled():
+# The four large workloads, every (sequence, value head) unit against the oracle run over the
+# whole problem (0.5 to 2 s of host time each on 16 cores).
+
+
+def test_fixed_mha_b2_t8192_every_unit():
     p = W.config(2)
     d = upload(p)
     run_gpu(p, d)
-    compare_sampled(p, d, [(0, 0), (1, 63), (0, 31), (1, 1), (1, 40)], "B=2 T=8192 H=64")
-    assert not torch.isnan(d["o"]).any().item()
+    compare_every_unit(p, d, "B=2 T=8192 H=64")
 
 
-def test_packed_varlen_pool_sampled():
+def test_packed_varlen_pool_every_unit():
     p = W.config(3)
-    h0_before = p.h0.copy()
     d = upload(p)
     run_gpu(p, d)
-    lengths = p.lengths()
-    order = np.argsort(lengths)
-    picks = [(int(order[-1]), 0), (int(order[-1]), 31), (int(order[0]), 5), (int(order[1]), 16),
-             (int(order[len(order) // 2]), 7)]
-    compare_sampled(p, d, picks, "packed N=32 H=32")
-    assert not torch.isnan(d["o"]).any().item()
-    h_gpu = d["h_final"].cpu().numpy()
-    unsel = np.setdiff1d(np.arange(p.pool_size), p.state_indices)
-    assert np.array_equal(h_gpu[unsel], h0_before[unsel])
+    # all 32 sequences x 32 heads, the 32 slots not selected bit-identical to their initial value
+    compare_every_unit(p, d, "packed N=32 H=32")
 
 
-def test_gva_long_sampled():
+def test_gva_long_every_unit():
     p = W.config(4)
     d = upload(p)
     run_gpu(p, d)
-    compare_sampled(p, d, [(0, 0), (3, 63), (2, 17)], "GVA B=4 T=16384 H=16 HV=64")
+    compare_every_unit(p, d, "GVA B=4 T=16384 H=16 HV=64")
 
 
-def test_short_sequences_pool_full():
+def test_short_sequences_pool_every_unit():
     p = W.config(5)
     d = upload(p)
     run_gpu(p, d)
     compare_full(p, d, "short packed N=128 T=8")
+    compare_every_unit(p, d, "short packed N=128 T=8")
 
 
 @pytest.mark.parametrize("which", ["small", "packed_full"])
@@ -200,3 +197,57 @@ def test_rejected_shapes_return_status_without_launch():
     with pytest.raises(lap.LaError) as e:
         lap.la_prefill_fwd(qq, qq, v, sl, 1.0, seq_len=64)
     assert e.value.name == "LA_ERR_INVALID_ARGUMENT"
+
+
+# Packed sequences are unrelated requests: a non-finite value in one must not reach another.
+# Sequence 2 holds +inf keys, NaN values and -inf queries; sequence 1 (77 tokens) ends inside a
+# chunk whose tile rows past its end are sequence 2's, and sequence 4 (40 tokens) likewise reads
+# sequence 5's clean rows.  Every other sequence must be bit-identical to running it alone.
+ISOLATION_LENGTHS = [100, 77, 150, 64, 40, 200, 33, 65]
+POISONED = 2
+
+
+def _poisoned_problem():
+    p = W.custom(seed=4242, lengths=ISOLATION_LENGTHS, H=2, HV=4)
+    a, b = int(p.cu_seqlens[POISONED]), int(p.cu_seqlens[POISONED + 1])
+    p.k_bits[a:b] = 0x7F80  # +inf
+    p.v_bits[a:b] = 0x7FC0  # NaN
+    p.q_bits[a:b] = 0xFF80  # -inf
+    return p
+
+
+def _alone(p, n):
+    a, b = int(p.cu_seqlens[n]), int(p.cu_seqlens[n + 1])
+    return W.Problem(f"sequence {n} alone", p.q_bits[a:b].copy(), p.k_bits[a:b].copy(), p.v_bits[a:b].copy(),
+                     p.slopes, p.scale, p.H, p.HV, 1, b - a, np.array([0, b - a], dtype=np.int32), None,
+                     p.h0[n:n + 1].copy())
+
+
+def _run_path(path, p, d):
+    import linear_attention_prefill_chunkwise_gb300 as lap
+    if path == "prefill":
+        run_gpu(p, d)
+    else:
+        lap.la_prefill_fwd_segmented(d["q"], d["k"], d["v"], d["slopes"], p.scale, h0=d["h0"], cu_seqlens=d["cu"],
+                                     o=d["o"], h_final=d["h_final"], segment_len=64)
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("path", ["prefill", "segmented"])
+def test_nonfinite_sequence_does_not_reach_its_neighbours(path):
+    p = _poisoned_problem()
+    d = upload(p)
+    _run_path(path, p, d)
+    o_all = d["o"].view(torch.int16).cpu().numpy()
+    h_all = d["h_final"].view(torch.int32).cpu().numpy()
+    for n in range(len(ISOLATION_LENGTHS)):
+        if n == POISONED:
+            continue
+        a, b = int(p.cu_seqlens[n]), int(p.cu_seqlens[n + 1])
+        pa = _alone(p, n)
+        da = upload(pa)
+        _run_path(path, pa, da)
+        o_one = da["o"].view(torch.int16).cpu().numpy()
+        h_one = da["h_final"].view(torch.int32).cpu().numpy()
+        assert np.array_equal(o_all[a:b], o_one), f"{path}: sequence {n} output differs from running it alone"
+        assert np.array_equal(h_all[n], h_one[0]), f"{path}: sequence {n} final state differs from running it alone"

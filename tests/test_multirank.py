@@ -80,3 +80,21 @@ def test_numa_pinning_degrades_gracefully_and_restores_affinity():
     if spec is None:
         assert os.sched_getaffinity(0) == before
     os.sched_setaffinity(0, prev)
+
+
+def test_clock_summary_keeps_only_the_timed_window_and_reports_reasons():
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    c = bench.ClockSampler("GPU-none")
+    c.samples = [(0.2, 1500.0, 2070.0, 500.0, []),                 # before the timed region
+                 (1.0, 2070.0, 2070.0, 900.0, []),
+                 (1.5, 1980.0, 2070.0, 1300.0, ["sw_power_cap"]),
+                 (2.0, 2010.0, 2070.0, 1200.0, []),
+                 (4.0, 300.0, 2070.0, 100.0, ["hw_slowdown"])]     # after it
+    c.t0, c.t1 = 0.9, 2.5
+    s = c.summary()
+    assert s["samples"] == 3 and s["sm_mhz"] == 2010.0 and s["sm_max_mhz"] == 2070.0
+    assert s["reasons"] == ["sw_power_cap"]
+    c.t0, c.t1 = 2.1, 3.0  # a window with no sample is reported as such, not guessed
+    assert c.summary()["reasons"] == ["unavailable"]
