@@ -99,6 +99,22 @@ inline la_status encode_bf16_rows_map(CUtensorMap* map, const void* base, int64_
   return LA_OK;
 }
 
+// Map over the token-major [rows, heads * 128] BF16 output for the epilogue's stores: 32 x 32
+// boxes (32 tokens x 32 values, 64-byte rows), 64-byte swizzle.
+inline la_status encode_bf16_out_map(CUtensorMap* map, void* base, int64_t rows, int64_t heads) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return fail(LA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the CUDA driver");
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(heads * 128), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(heads * 128 * 2)};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, elem_strides,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(LA_ERR_CUDA, "cuTensorMapEncodeTiled(o) failed with CUresult %d", (int)r);
+  return LA_OK;
+}
+
 // Argument checks of a prefill call (la_prefill_fwd's contract): shapes, modes, pointers,
 // alignment and the state pool.  Sets *nothing_to_do when the call has no work.
 inline la_status check_prefill_args(const void* q, const void* k, const void* v, const float* slopes,

@@ -91,15 +91,17 @@ la_status la_prefill_fwd(const void* q, const void* k, const void* v, const floa
   cudaError_t ce;
 
   // ---- tensor maps (unused when there are no tokens)
-  CUtensorMap tm_q, tm_k, tm_v;
+  CUtensorMap tm_q, tm_k, tm_v, tm_o;
   memset(&tm_q, 0, sizeof(tm_q));
   memset(&tm_k, 0, sizeof(tm_k));
   memset(&tm_v, 0, sizeof(tm_v));
+  memset(&tm_o, 0, sizeof(tm_o));
   if (tokens > 0) {
     la_status st;
     if ((st = la_host::encode_bf16_rows_map(&tm_q, q, tokens, H, "q")) != LA_OK) return st;
     if ((st = la_host::encode_bf16_rows_map(&tm_k, k, tokens, H, "k")) != LA_OK) return st;
     if ((st = la_host::encode_bf16_rows_map(&tm_v, v, tokens, HV, "v")) != LA_OK) return st;
+    if ((st = la_host::encode_bf16_out_map(&tm_o, o, tokens, HV)) != LA_OK) return st;
   }
 
   const bool packed = cu_seqlens != nullptr;
@@ -159,7 +161,7 @@ la_status la_prefill_fwd(const void* q, const void* k, const void* v, const floa
   int grid = static_cast<int>(units);
   if (schedule != LA_SCHED_NON_PERSISTENT && grid > ds.sms) grid = ds.sms;
   lap::la_prefill_fwd_kernel<<<grid, lap::kThreads, smem_bytes(), static_cast<cudaStream_t>(stream)>>>(
-      tm_q, tm_k, tm_v, p);
+      tm_q, tm_k, tm_v, tm_o, p);
   ce = cudaGetLastError();
   if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(ce));
   return LA_OK;

@@ -39,7 +39,9 @@
 //                O_inter), 2 buffers
 //   warps 4-11   state warpgroups: thread (quadrant qd, lane) of warpgroup wg owns state
 //                row v = 32 qd + lane, columns k in [64 wg, 64 wg + 64), in registers;
-//                they advance the state, publish it to TMEM and write the output
+//                they advance the state, publish it to TMEM and write the output: each warp
+//                stages its 32 x 32 block of o as BF16 in the chunk's V stage (stmatrix) and
+//                stores it with one TMA store (16-byte rows of the tile, not 2-byte scalars)
 //   warps 12-15  operand warpgroup: builds the decayed BF16 hi/lo operands Kt and P
 //
 // Per chunk i (a CTA-wide running chunk counter) the MMA groups and their operands:
@@ -48,7 +50,11 @@
 //   O_inter(i)   thread A, into O[i%2], after S(i) is published, Qt(i) converted, O(i-2) read
 //   O_intra(i)   thread A, accumulated into O[i%2], after P(i) is built
 // The Q/K stage of chunk i is released as soon as its three readers (the scores MMAs, the
-// Kt builders and the Qt converter) are done; a V stage after dS and O_intra.
+// Kt builders and the Qt converter) are done; a V stage after dS, O_intra and the output
+// stores staged in it.
+// Sequence isolation: the rows of a ragged chunk's tiles past the sequence's end belong to the
+// next packed sequence; the operand warpgroup zeroes those K and V rows before any MMA that
+// could mix them into this sequence reads them, and P is masked by a select.
 // The serial chain from chunk to chunk is only: O_inter(i) done -> S(i+1) written to
 // TMEM -> O_inter(i+1); everything else is built ahead of it.
 #pragma once
@@ -255,7 +261,10 @@ __device__ __forceinline__ uint64_t desc_at(uint64_t base, uint32_t byte_off) { 
 // The walk of this CTA's chunks by a role that runs ahead of the others.
 struct ChunkCursor {
   int u, c, row, hq, hv, nchunks;
+  int tail;  // valid rows of the unit's last chunk (1..64)
   bool valid;
+  // The current chunk ends inside its 64-row tiles: rows past the sequence's end are there.
+  __device__ __forceinline__ bool ragged() const { return c == nchunks - 1 && tail < kChunk; }
 };
 __device__ __forceinline__ void cursor_seek(const KernelParams& p, ChunkCursor& k, int u) {
   for (; u < p.num_units; u += gridDim.x) {
@@ -267,6 +276,7 @@ __device__ __forceinline__ void cursor_seek(const KernelParams& p, ChunkCursor& 
       k.hq = w.hq;
       k.hv = w.hv;
       k.nchunks = w.nchunks;
+      k.tail = w.len - kChunk * (w.nchunks - 1);
       k.valid = true;
       return;
     }
@@ -347,7 +357,8 @@ __device__ __forceinline__ void tma_mma_loop(SharedStorage& sm, const KernelPara
       const uint32_t sq = nqk % kQKStages;
       if (mbar_test(&sm.qk_empty[sq], ((nqk / kQKStages) & 1u) ^ 1u)) {
         LA_TRACE_AT(p, kTrProducerIssue, nqk, true);
-        mbar_arrive_expect_tx(&sm.qk_full[sq], 4 * kTileBytes);
+        // a ragged chunk's V tile lands on this stage's barrier as well (see the V load)
+        mbar_arrive_expect_tx(&sm.qk_full[sq], (cq.ragged() ? 6 : 4) * kTileBytes);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           tma_load_2d(sm.qk[sq].q[h], tm_q, &sm.qk_full[sq], cq.hq * kDim + 64 * h, cq.row);
@@ -360,10 +371,23 @@ __device__ __forceinline__ void tma_mma_loop(SharedStorage& sm, const KernelPara
     }
     if (cv.valid) {
       const uint32_t sv = nv % kVStages;
-      if (mbar_test(&sm.v_empty[sv], ((nv / kVStages) & 1u) ^ 1u)) {
-        mbar_arrive_expect_tx(&sm.v_full[sv], 2 * kTileBytes);
+      // The V tile of a ragged chunk holds rows of the next packed sequence past the end.  The
+      // operand warpgroup zeroes them before any MMA reads the tile: the tile lands on the Q/K
+      // stage's barrier, which the operand warpgroup waits on anyway (so its Q/K load must have
+      // been issued, with these bytes in its expected count), and v_full's phase is completed
+      // by a plain arrival; dS and O_intra read the tile only after kt_ready / p_ready, which
+      // the operand warpgroup gives after the zeroing.
+      const bool ragged = cv.ragged();
+      if (mbar_test(&sm.v_empty[sv], ((nv / kVStages) & 1u) ^ 1u) && (!ragged || nqk > nv)) {
+        uint64_t* bar = &sm.v_full[sv];
+        if (ragged) {
+          mbar_arrive(bar);
+          bar = &sm.qk_full[nv % kQKStages];
+        } else {
+          mbar_arrive_expect_tx(bar, 2 * kTileBytes);
+        }
 #pragma unroll
-        for (int h = 0; h < 2; ++h) tma_load_2d(sm.v[sv][h], tm_v, &sm.v_full[sv], cv.hv * kDim + 64 * h, cv.row);
+        for (int h = 0; h < 2; ++h) tma_load_2d(sm.v[sv][h], tm_v, bar, cv.hv * kDim + 64 * h, cv.row);
         ++nv;
         cursor_next(p, cv);
         progressed = true;
@@ -520,25 +544,21 @@ __device__ __forceinline__ void operand_loop(SharedStorage& sm, const KernelPara
         break;
       }
       LA_TRACE_AT(p, kTrOperKtStart, it, otid == 0);
-      if (L < kChunk) {
-        // Rows j >= L of a ragged chunk's tiles belong to the next packed sequence (or are the
-        // TMA's zero fill).  They are zeroed, not multiplied by zero: a non-finite value there
-        // must not reach this sequence (0 * inf is NaN).  Kt rows are zeroed below; the V rows
-        // feed the dS and O_intra MMAs directly, so this thread clears its row of the V stage,
-        // which both MMAs read only after kt_ready (arrived below).
-        const uint32_t sv = it % kVStages;
-        if (!warp_wait(&sm.v_full[sv], (it / kVStages) & 1u, abort)) {
-          ok = false;
-          break;
-        }
-        if (krow >= L) {
-          uint8_t* vrow_s = sm.v[sv][kbox] + krow * 128;
+      if (krow >= L) {
+        // Rows j >= L of a ragged chunk belong to the next packed sequence (or are the TMA's zero
+        // fill): this thread's K row and V row are zeroed, so that a non-finite value there cannot
+        // reach this sequence (0 * inf is NaN); the V tile of a ragged chunk has landed with the
+        // Q/K stage.
+        uint8_t* kr = sm.qk[sq].k[kbox] + krow * 128;
+        uint8_t* vr = sm.v[it % kVStages][kbox] + krow * 128;
 #pragma unroll
-          for (int cc = 0; cc < 8; ++cc) *reinterpret_cast<uint4*>(vrow_s + 16 * cc) = make_uint4(0, 0, 0, 0);
+        for (int cc = 0; cc < 8; ++cc) {
+          *reinterpret_cast<uint4*>(kr + 16 * cc) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vr + 16 * cc) = make_uint4(0, 0, 0, 0);
         }
       }
-      if (krow < L) {
-        const float wjf = lam[L - 1 - krow];
+      {
+        const float wjf = (krow < L) ? lam[L - 1 - krow] : 0.f;
         const uint64_t wj = f2_pack(wjf, wjf);
         const uint8_t* ksrc = sm.qk[sq].k[kbox];
 #pragma unroll 2
@@ -551,13 +571,6 @@ __device__ __forceinline__ void operand_loop(SharedStorage& sm, const KernelPara
           for (int e = 0; e < 4; ++e) split_bf16x2(f2_mul(wj, bf16x2_to_f2(kw[e])), hi[e], lo[e]);
           *reinterpret_cast<uint4*>(sm.kt_hi[kbox] + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
           *reinterpret_cast<uint4*>(sm.kt_lo[kbox] + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
-      } else {
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          const uint32_t off = swz(krow, cc);
-          *reinterpret_cast<uint4*>(sm.kt_hi[kbox] + off) = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(sm.kt_lo[kbox] + off) = make_uint4(0, 0, 0, 0);
         }
       }
       fence_proxy_async_smem();
@@ -612,8 +625,8 @@ __device__ __forceinline__ void operand_loop(SharedStorage& sm, const KernelPara
 }
 
 // State warpgroups: own S in registers, advance it, publish it to TMEM, write the output.
-__device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams& p, uint32_t tmem, int ctid,
-                                          volatile int* abort) {
+__device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams& p, const CUtensorMap* tm_o,
+                                          uint32_t tmem, int ctid, volatile int* abort) {
   const int warp = ctid >> 5, lane = ctid & 31;
   const int wg = warp >> 2;         // which half of k (state) and of s (output)
   const int qd = warp & 3;          // TMEM lane quadrant
@@ -665,8 +678,6 @@ __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams&
     if (w.nchunks > 0) publish_state();
 
     const size_t ostride = static_cast<size_t>(p.HV) * kDim;
-    __nv_bfloat16* obase = p.o + (static_cast<size_t>(w.bos) + 32 * wg) * ostride +
-                           static_cast<size_t>(w.hv) * kDim + vrow;
     for (int c = 0; c < w.nchunks; ++c, ++it) {
       const uint32_t ph = it & 1u;
       const uint32_t b = it & 1u, bph = (it >> 1) & 1u;
@@ -708,33 +719,70 @@ __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams&
       if (c + 1 < w.nchunks) publish_state();
       LA_TRACE_AT(p, kTrStateSReady, it, ctid == 0);
 
-      // ---- o = O (the scale is folded into Qt and P), this warpgroup's 32 rows s of the chunk
+      // ---- o = O (the scale is folded into Qt and P): this warp's 32 rows s x 32 values v of the
+      //      chunk, staged as BF16 in the chunk's V stage (dS and O_intra, its readers, are done:
+      //      ds_full and o_full were waited on) and stored by one TMA store of a 32 x 32 box.
       if (!warp_wait(&sm.o_full[b], bph, abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
       {
-        float o0[16], o1[16];
-        tmem_ld16(tmem + lane_base + kColO + 64 * b + 32 * wg, o0);
-        tmem_ld16(tmem + lane_base + kColO + 64 * b + 32 * wg + 16, o1);
-        tc_fence_before();
-        mbar_arrive(&sm.o_free[b]);
-        __nv_bfloat16* orow = obase + static_cast<size_t>(c) * kChunk * ostride;
-        const int rows = L - 32 * wg;  // valid rows of this warpgroup's half (may be <= 0 or > 32)
-        if (rows >= 32) {
+        const uint32_t sv = it % kVStages;
+        uint8_t* stage = sm.v[sv][0] + (wg * 4 + qd) * 2048;  // 32 rows of 64 bytes, 64-byte swizzle
+        const int rows = L - 32 * wg;  // valid rows of this warp's box (may be <= 0 or > 32)
+        // stmatrix.trans: lane l gives row j = l % 8 of matrix m = l / 8; the matrices of one call
+        // are (repetition rr, value half h) = (2 k2 + m / 2, m % 2): row sl = 8 rr + j of the box,
+        // 16-byte chunk 2 g + h (lanes 16 g .. 16 g + 15 of this warp's quadrant)
+        const int m = lane >> 3, j = lane & 7;
+#pragma unroll 1
+        for (int g = 0; g < 2; ++g) {
+          uint32_t rg[16];
+          tmem_ld_16x256b_x4(tmem + lane_base + (static_cast<uint32_t>(16 * g) << 16) + kColO + 64 * b + 32 * wg, rg);
+          if (g == 1) {
+            tc_fence_before();
+            mbar_arrive(&sm.o_free[b]);
+          }
+          if (rows > 0) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) orow[i * ostride] = __float2bfloat16_rn(o0[i]);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) orow[(16 + i) * ostride] = __float2bfloat16_rn(o1[i]);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (i < rows) orow[i * ostride] = __float2bfloat16_rn(o0[i]);
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (16 + i < rows) orow[(16 + i) * ostride] = __float2bfloat16_rn(o1[i]);
+            for (int k2 = 0; k2 < 2; ++k2) {
+              const uint32_t sl = 8 * (2 * k2 + (m >> 1)) + j, ch = 2 * g + (m & 1);
+              const uint32_t addr = smem_u32(stage) + sl * 64 + ((ch ^ ((sl >> 1) & 3u)) << 4);
+              const int ra = 8 * k2, rb = 8 * k2 + 4;
+              stmatrix_x4_trans(addr, pack_bf16x2(__uint_as_float(rg[ra]), __uint_as_float(rg[ra + 1])),
+                                pack_bf16x2(__uint_as_float(rg[ra + 2]), __uint_as_float(rg[ra + 3])),
+                                pack_bf16x2(__uint_as_float(rg[rb]), __uint_as_float(rg[rb + 1])),
+                                pack_bf16x2(__uint_as_float(rg[rb + 2]), __uint_as_float(rg[rb + 3])));
+            }
+          }
         }
+        if (rows > 0) {
+          const int y0 = w.bos + c * kChunk + 32 * wg;
+          if (rows >= 32) {
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(tm_o, stage, w.hv * kDim + 32 * qd, y0);
+              bulk_commit();
+              bulk_wait_read_all();  // the stage is handed back to the V loads below
+            }
+          } else {
+            // a ragged chunk's last rows: copy the valid ones, 16 bytes per lane
+            __syncwarp();
+            __nv_bfloat16* orow0 = p.o + static_cast<size_t>(y0) * ostride + static_cast<size_t>(w.hv) * kDim + 32 * qd;
+#pragma unroll
+            for (int pass = 0; pass < 4; ++pass) {
+              const int sl = pass * 8 + (lane >> 2), ch = lane & 3;
+              if (sl < rows) {
+                const uint4 x = *reinterpret_cast<const uint4*>(stage + sl * 64 + ((ch ^ ((sl >> 1) & 3)) << 4));
+                *reinterpret_cast<uint4*>(orow0 + static_cast<size_t>(sl) * ostride + 8 * ch) = x;
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+        }
+        if (lane == 0) mbar_arrive(&sm.v_empty[sv]);
       }
       LA_TRACE_AT(p, kTrStateEpilogue, it, ctid == 0);
     }
@@ -751,7 +799,8 @@ __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams&
 
 __global__ void __launch_bounds__(kThreads, 1)
 la_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const KernelParams p) {
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                      const KernelParams p) {
   extern __shared__ uint8_t smem_raw[];
   SharedStorage& sm =
       *reinterpret_cast<SharedStorage*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -771,7 +820,7 @@ la_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     }
     for (int i = 0; i < kVStages; ++i) {
       mbar_init(&sm.v_full[i], 1);
-      mbar_init(&sm.v_empty[i], 2);
+      mbar_init(&sm.v_empty[i], 2 + kStateThreads / 32);
     }
     mbar_init(&sm.scores_full, 1);
     mbar_init(&sm.scores_free, kOperandThreads);
@@ -796,6 +845,7 @@ la_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_o);
   }
   tc_fence_before();
   __syncthreads();
@@ -809,8 +859,9 @@ la_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   } else if (warp < 4) {
     convert_loop(sm, p, tid - 64, abort);
   } else if (warp < 12) {
-    const int err = state_loop(sm, p, tmem, tid - 128, abort);
+    const int err = state_loop(sm, p, &tm_o, tmem, tid - 128, abort);
     if (err && tid == 128 && p.dev_error) atomicOr(p.dev_error, err);
+    if ((tid & 31) == 0) bulk_wait_all();  // this warp's output stores have completed
   } else {
     operand_loop(sm, p, tmem, tid - 384, abort);
   }

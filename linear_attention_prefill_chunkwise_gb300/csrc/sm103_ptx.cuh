@@ -245,6 +245,20 @@ __device__ __forceinline__ void tmem_ld_16x256b(uint32_t taddr, uint32_t (&r)[4]
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// 16x256b shape, four repetitions along the columns (32 columns), waiting for completion: for
+// repetition r, thread t receives lane base + t/4 in r[4r], r[4r+1] (columns c + 8r + 2 (t%4),
+// + 1) and lane base + 8 + t/4 in r[4r+2], r[4r+3] (same columns).
+__device__ __forceinline__ void tmem_ld_16x256b_x4(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
 // Store 16 consecutive 32-bit columns of the warp's 32 lanes and wait for completion.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&u)[16]) {
   asm volatile(

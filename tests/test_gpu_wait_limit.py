@@ -24,9 +24,10 @@ torch = pytest.importorskip("torch")
 def _short_limit_library():
     from linear_attention_prefill_chunkwise_gb300 import build as b
     lib = ctypes.CDLL(b.build(wait_limit_ns=100))
-    vp, fp, ip = ctypes.c_void_p, ctypes.POINTER(ctypes.c_float), ctypes.c_void_p
-    lib.la_prefill_fwd.argtypes = [vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp, vp] + [ctypes.c_int] * 10 + \
-        [ctypes.c_int, ip, vp]
+    vp, ip = ctypes.c_void_p, ctypes.c_void_p
+    # q, k, v, slopes, scale, h0, state_indices, cu_seqlens, o, h_final, B, T, N, H, HV, D, V, pool_size,
+    # schedule, dev_error, stream
+    lib.la_prefill_fwd.argtypes = [vp, vp, vp, vp, ctypes.c_float, vp, vp, vp, vp, vp] + [ctypes.c_int] * 9 + [ip, vp]
     lib.la_prefill_fwd.restype = ctypes.c_int
     return lib
 
