@@ -83,8 +83,12 @@ la_status la_prefill_fwd(const void* q, const void* k, const void* v, const floa
   // ---- device
   la_host::DeviceState* dsp = nullptr;
   la_status dst = la_host::current_device(g_dev, &dsp, [] {
-    return cudaFuncSetAttribute(lap::la_prefill_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                smem_bytes());
+    cudaError_t e = cudaFuncSetAttribute(lap::la_prefill_fwd_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes());
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(lap::la_prefill_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               smem_bytes());
+    return e;
   });
   if (dst != LA_OK) return dst;
   la_host::DeviceState& ds = *dsp;
@@ -160,8 +164,15 @@ la_status la_prefill_fwd(const void* q, const void* k, const void* v, const floa
 
   int grid = static_cast<int>(units);
   if (schedule != LA_SCHED_NON_PERSISTENT && grid > ds.sms) grid = ds.sms;
-  lap::la_prefill_fwd_kernel<<<grid, lap::kThreads, smem_bytes(), static_cast<cudaStream_t>(stream)>>>(
-      tm_q, tm_k, tm_v, tm_o, p);
+  // A packed batch of few sequences gets the longest-first schedule (the lengths vary, and a
+  // CTA runs a handful of units); other batches deal units out round robin.
+  const bool listed = packed && N <= lap::kSchedSeqMax && (units + grid - 1) / grid <= lap::kSchedMax;
+  if (listed)
+    lap::la_prefill_fwd_kernel<true><<<grid, lap::kThreads, smem_bytes(), static_cast<cudaStream_t>(stream)>>>(
+        tm_q, tm_k, tm_v, tm_o, p);
+  else
+    lap::la_prefill_fwd_kernel<false><<<grid, lap::kThreads, smem_bytes(), static_cast<cudaStream_t>(stream)>>>(
+        tm_q, tm_k, tm_v, tm_o, p);
   ce = cudaGetLastError();
   if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(ce));
   return LA_OK;

@@ -86,6 +86,13 @@ constexpr uint32_t kColState = 384;   // S (TF32) as the A operand of O_inter: l
 
 constexpr int kTabStride = 68;  // per operand warp: lambda^n for n = 0..64
 
+// Unit schedule of a packed batch (the kernel's kListed instance): sequences ranked by length
+// at kernel start and their units dealt out longest first (see build_schedule).  The host uses
+// it for batches of at most kSchedSeqMax sequences whose CTAs get at most kSchedMax units each;
+// the other instance deals units out round robin.
+constexpr int kSchedMax = 128;
+constexpr int kSchedSeqMax = 256;
+
 struct __align__(1024) QKTiles {
   uint8_t q[2][kTileBytes];  // [64 tokens][64 dims] x 2 halves of D, 128B-swizzled
   uint8_t k[2][kTileBytes];
@@ -121,6 +128,8 @@ struct __align__(1024) SharedStorage {
   uint64_t final_bar[2];         // every MMA of thread A / B retired (teardown)            // every MMA retired (teardown)
   uint32_t tmem_base;
   int abort;
+  int sched_n;                   // kListed: units listed in sched
+  int32_t sched[kSchedMax];      // kListed: this CTA's units in processing order
 };
 
 struct KernelParams {
@@ -244,14 +253,79 @@ __device__ __forceinline__ float* fill_lambda_table(SharedStorage& sm, int warp,
   return tab;
 }
 
-// Number of chunks this CTA processes (all roles walk the same units in the same order).
-__device__ __forceinline__ uint32_t cta_chunk_count(const KernelParams& p) {
+// The walk over this CTA's units, taken identically by every role: round robin (units
+// blockIdx.x, blockIdx.x + gridDim.x, ...) or, in the kListed instance, the CTA's list.
+template <bool kListed>
+struct UnitWalk;
+template <>
+struct UnitWalk<false> {
+  int u;
+  __device__ __forceinline__ UnitWalk(const SharedStorage&, const KernelParams&) : u(blockIdx.x) {}
+  __device__ __forceinline__ bool valid(const SharedStorage&, const KernelParams& p) const { return u < p.num_units; }
+  __device__ __forceinline__ int unit(const SharedStorage&) const { return u; }
+  __device__ __forceinline__ void next() { u += gridDim.x; }
+};
+template <>
+struct UnitWalk<true> {
+  int j, n;
+  __device__ __forceinline__ UnitWalk(const SharedStorage& sm, const KernelParams&) : j(0), n(sm.sched_n) {}
+  __device__ __forceinline__ bool valid(const SharedStorage&, const KernelParams&) const { return j < n; }
+  __device__ __forceinline__ int unit(const SharedStorage& sm) const { return sm.sched[j]; }
+  __device__ __forceinline__ void next() { ++j; }
+};
+
+// Number of chunks this CTA processes.
+template <bool kListed>
+__device__ __forceinline__ uint32_t cta_chunk_count(const SharedStorage& sm, const KernelParams& p) {
   uint32_t n = 0;
-  for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-    const Unit w = decode_unit(p, u);
+  for (UnitWalk<kListed> wk(sm, p); wk.valid(sm, p); wk.next()) {
+    const Unit w = decode_unit(p, wk.unit(sm));
     if (w.run) n += w.nchunks;
   }
   return n;
+}
+
+// The packed batch's schedule (kListed instance), built by the whole CTA before the roles start
+// (with CTA-wide barriers, before any role waits on anything).  Round robin over (sequence,
+// head) units leaves some CTAs with the long sequences of a batch of random lengths; instead the
+// sequences are ranked by length (ties by index; a sequence that will not run counts as empty)
+// and the units in that order are dealt out in a snake: round j gives CTA b the unit of rank
+// j G + b for even j and j G + G - 1 - b for odd j (G = gridDim.x).  Every CTA computes the
+// same ranking from the same cu_seqlens, so each unit runs exactly once, and each unit's
+// arithmetic does not depend on which CTA runs it.  The ranking's scratch is the Q conversion
+// buffer, unused until the roles start.
+__device__ __forceinline__ void build_schedule(SharedStorage& sm, const KernelParams& p, int tid) {
+  const int G = gridDim.x, b = blockIdx.x;
+  const int rounds = (p.num_units + G - 1) / G;  // <= kSchedMax (the host's condition)
+  int32_t* len = reinterpret_cast<int32_t*>(sm.qt[0][0]);
+  int32_t* by_rank = len + kSchedSeqMax;
+  if (tid < p.N) {
+    const int bb = __ldg(p.cu_seqlens + tid), ee = __ldg(p.cu_seqlens + tid + 1);
+    int l = (bb >= 0 && ee >= bb && ee <= p.num_tokens) ? ee - bb : 0;
+    if (l <= p.short_max) l = 0;
+    if (p.state_indices && __ldg(p.state_indices + tid) < 0) l = 0;
+    len[tid] = l;
+  }
+  __syncthreads();
+  if (tid < p.N) {
+    const int l = len[tid];
+    int r = 0;
+    for (int m = 0; m < p.N; ++m) {
+      const int lm = len[m];
+      r += (lm > l || (lm == l && m < tid)) ? 1 : 0;
+    }
+    by_rank[r] = tid;
+  }
+  __syncthreads();
+  for (int j = tid; j < rounds; j += blockDim.x) {
+    const int k = j * G + ((j & 1) ? G - 1 - b : b);
+    sm.sched[j] = k < p.num_units ? by_rank[k / p.HV] * p.HV + k % p.HV : -1;
+  }
+  if (tid == 0) {
+    const int jl = rounds - 1;
+    const int kl = jl * G + ((jl & 1) ? G - 1 - b : b);
+    sm.sched_n = kl < p.num_units ? rounds : rounds - 1;  // only the last round can run past the end
+  }
 }
 
 // ------------------------------------------------------------------------------ roles
@@ -259,18 +333,20 @@ __device__ __forceinline__ uint32_t cta_chunk_count(const KernelParams& p) {
 __device__ __forceinline__ uint64_t desc_at(uint64_t base, uint32_t byte_off) { return base + (byte_off >> 4); }
 
 // The walk of this CTA's chunks by a role that runs ahead of the others.
+template <bool kListed>
 struct ChunkCursor {
-  int u, c, row, hq, hv, nchunks;
+  UnitWalk<kListed> wk;
+  int c, row, hq, hv, nchunks;
   int tail;  // valid rows of the unit's last chunk (1..64)
   bool valid;
   // The current chunk ends inside its 64-row tiles: rows past the sequence's end are there.
   __device__ __forceinline__ bool ragged() const { return c == nchunks - 1 && tail < kChunk; }
 };
-__device__ __forceinline__ void cursor_seek(const KernelParams& p, ChunkCursor& k, int u) {
-  for (; u < p.num_units; u += gridDim.x) {
-    const Unit w = decode_unit(p, u);
+template <bool kListed>
+__device__ __forceinline__ void cursor_seek(const SharedStorage& sm, const KernelParams& p, ChunkCursor<kListed>& k) {
+  for (; k.wk.valid(sm, p); k.wk.next()) {
+    const Unit w = decode_unit(p, k.wk.unit(sm));
     if (w.run && w.nchunks > 0) {
-      k.u = u;
       k.c = 0;
       k.row = w.bos;
       k.hq = w.hq;
@@ -283,17 +359,20 @@ __device__ __forceinline__ void cursor_seek(const KernelParams& p, ChunkCursor& 
   }
   k.valid = false;
 }
-__device__ __forceinline__ void cursor_next(const KernelParams& p, ChunkCursor& k) {
+template <bool kListed>
+__device__ __forceinline__ void cursor_next(const SharedStorage& sm, const KernelParams& p, ChunkCursor<kListed>& k) {
   if (++k.c < k.nchunks) {
     k.row += kChunk;
   } else {
-    cursor_seek(p, k, k.u + gridDim.x);
+    k.wk.next();
+    cursor_seek(sm, p, k);
   }
 }
 
 // TMA and MMA thread B, one polling loop: each pass issues, in this order, every job whose
 // inputs are ready (mbarrier.test_wait, no blocking): dS(i) = V(i)^T Kt(i), scores(i) =
 // Q(i) K(i)^T, and the next Q/K and V loads once their ring slots have been released.
+template <bool kListed>
 __device__ __forceinline__ void tma_mma_loop(SharedStorage& sm, const KernelParams& p, const CUtensorMap* tm_q,
                                              const CUtensorMap* tm_k, const CUtensorMap* tm_v, uint32_t tmem,
                                              volatile int* abort) {
@@ -307,11 +386,11 @@ __device__ __forceinline__ void tma_mma_loop(SharedStorage& sm, const KernelPara
   const uint64_t dkt_hi = sdesc_sw128(smem_u32(sm.kt_hi), kTileBytes, 1024);
   const uint64_t dkt_lo = sdesc_sw128(smem_u32(sm.kt_lo), kTileBytes, 1024);
   const uint32_t t_scores = tmem + kColScores, t_ds = tmem + kColDeltaS;
-  const uint32_t total = cta_chunk_count(p);
+  const uint32_t total = cta_chunk_count<kListed>(sm, p);
   uint32_t n_ds = 0, n_sc = 0, nqk = 0, nv = 0;
-  ChunkCursor cq, cv;
-  cursor_seek(p, cq, blockIdx.x);
-  cv = cq;
+  ChunkCursor<kListed> cq{UnitWalk<kListed>(sm, p)};
+  cursor_seek(sm, p, cq);
+  ChunkCursor<kListed> cv = cq;
   uint64_t last = globaltimer_ns();
   while (n_ds < total || n_sc < total || cq.valid || cv.valid) {
     bool progressed = false;
@@ -365,7 +444,7 @@ __device__ __forceinline__ void tma_mma_loop(SharedStorage& sm, const KernelPara
           tma_load_2d(sm.qk[sq].k[h], tm_k, &sm.qk_full[sq], cq.hq * kDim + 64 * h, cq.row);
         }
         ++nqk;
-        cursor_next(p, cq);
+        cursor_next(sm, p, cq);
         progressed = true;
       }
     }
@@ -389,7 +468,7 @@ __device__ __forceinline__ void tma_mma_loop(SharedStorage& sm, const KernelPara
 #pragma unroll
         for (int h = 0; h < 2; ++h) tma_load_2d(sm.v[sv][h], tm_v, bar, cv.hv * kDim + 64 * h, cv.row);
         ++nv;
-        cursor_next(p, cv);
+        cursor_next(sm, p, cv);
         progressed = true;
       }
     }
@@ -424,6 +503,7 @@ __device__ __forceinline__ void tma_mma_loop(SharedStorage& sm, const KernelPara
 // serial chain of the pipeline):
 //   O_inter(i) = S(i) Qt(i)^T     into O[i%2]: needs Qt(i), O(i-2) read out, S(i) published
 //   O_intra(i) += V(i)^T P(i)^T   needs V(i) and P(i); after O_inter(i) (same thread, in order)
+template <bool kListed>
 __device__ __forceinline__ void mma_o_loop(SharedStorage& sm, const KernelParams& p, uint32_t tmem,
                                            volatile int* abort) {
   constexpr uint32_t id_ointer = idesc_tf32_f32(128, 64, false, false);
@@ -435,7 +515,7 @@ __device__ __forceinline__ void mma_o_loop(SharedStorage& sm, const KernelParams
   const uint64_t dp_hi = sdesc_sw128(smem_u32(sm.p_hi), 16, 1024);
   const uint64_t dp_lo = sdesc_sw128(smem_u32(sm.p_lo), 16, 1024);
   const uint32_t t_state = tmem + kColState;
-  const uint32_t total = cta_chunk_count(p);
+  const uint32_t total = cta_chunk_count<kListed>(sm, p);
   for (uint32_t it = 0; it < total; ++it) {
     const uint32_t sv = it % kVStages, ph = it & 1u, b = it & 1u, bph = (it >> 1) & 1u;
     if (!mbar_wait(&sm.qt_ready[b], bph, abort) || !mbar_wait(&sm.o_free[b], bph ^ 1u, abort) ||
@@ -475,13 +555,14 @@ __device__ __forceinline__ void mma_o_loop(SharedStorage& sm, const KernelParams
 // tensor core reads as TF32, i.e. truncated to 10 mantissa bits; rounding it here instead
 // would cost two more instructions per element on the critical conversion and changes the
 // output by far less than its BF16 step.  Thread t owns token row s = t of the chunk.
+template <bool kListed>
 __device__ __forceinline__ void convert_loop(SharedStorage& sm, const KernelParams& p, int ctid,
                                              volatile int* abort) {
   const int s = ctid;
   uint32_t it = 0;
   bool ok = true;
-  for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-    const Unit w = decode_unit(p, u);
+  for (UnitWalk<kListed> wk(sm, p); wk.valid(sm, p) && ok; wk.next()) {
+    const Unit w = decode_unit(p, wk.unit(sm));
     if (!w.run) continue;
     const float f = p.scale * expf(-__ldg(p.slopes + w.hv) * static_cast<float>(s + 1));  // scale lambda^(s+1)
     const uint64_t ff = f2_pack(f, f);
@@ -514,6 +595,7 @@ __device__ __forceinline__ void convert_loop(SharedStorage& sm, const KernelPara
 }
 
 // Operand warpgroup: Kt = lambda^(L-1-j) k_j and P = A * lambda^(s-j) (causal, tail masked), as BF16 hi/lo.
+template <bool kListed>
 __device__ __forceinline__ void operand_loop(SharedStorage& sm, const KernelParams& p, uint32_t tmem, int otid,
                                              volatile int* abort) {
   const int warp = otid >> 5, lane = otid & 31;
@@ -525,8 +607,8 @@ __device__ __forceinline__ void operand_loop(SharedStorage& sm, const KernelPara
   const int kbox = otid >> 6;              //     and its 64-column box of k
   uint32_t it = 0;
   bool ok = true;
-  for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-    const Unit w = decode_unit(p, u);
+  for (UnitWalk<kListed> wk(sm, p); wk.valid(sm, p) && ok; wk.next()) {
+    const Unit w = decode_unit(p, wk.unit(sm));
     if (!w.run) continue;
     const float* lam = fill_lambda_table(sm, warp, lane, __ldg(p.slopes + w.hv));
     // decay row of P for this thread: scale lambda^(s-j) for j <= s, 0 above the diagonal
@@ -625,6 +707,7 @@ __device__ __forceinline__ void operand_loop(SharedStorage& sm, const KernelPara
 }
 
 // State warpgroups: own S in registers, advance it, publish it to TMEM, write the output.
+template <bool kListed>
 __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams& p, const CUtensorMap* tm_o,
                                           uint32_t tmem, int ctid, volatile int* abort) {
   const int warp = ctid >> 5, lane = ctid & 31;
@@ -651,8 +734,8 @@ __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams&
     mbar_arrive(&sm.s_ready);
   };
 
-  for (int u = blockIdx.x; u < p.num_units && ok; u += gridDim.x) {
-    const Unit w = decode_unit(p, u);
+  for (UnitWalk<kListed> wk(sm, p); wk.valid(sm, p) && ok; wk.next()) {
+    const Unit w = decode_unit(p, wk.unit(sm));
     err |= w.error;
     if (!w.run) continue;
     const float slope = __ldg(p.slopes + w.hv);
@@ -797,6 +880,7 @@ __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams&
   return err;
 }
 
+template <bool kListed>
 __global__ void __launch_bounds__(kThreads, 1)
 la_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -851,19 +935,23 @@ la_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
+  if constexpr (kListed) {
+    build_schedule(sm, p, tid);
+    __syncthreads();
+  }
 
   if (warp == 0) {
-    if (lane == 0) tma_mma_loop(sm, p, &tm_q, &tm_k, &tm_v, tmem, abort);
+    if (lane == 0) tma_mma_loop<kListed>(sm, p, &tm_q, &tm_k, &tm_v, tmem, abort);
   } else if (warp == 1) {
-    if (lane == 0) mma_o_loop(sm, p, tmem, abort);
+    if (lane == 0) mma_o_loop<kListed>(sm, p, tmem, abort);
   } else if (warp < 4) {
-    convert_loop(sm, p, tid - 64, abort);
+    convert_loop<kListed>(sm, p, tid - 64, abort);
   } else if (warp < 12) {
-    const int err = state_loop(sm, p, &tm_o, tmem, tid - 128, abort);
+    const int err = state_loop<kListed>(sm, p, &tm_o, tmem, tid - 128, abort);
     if (err && tid == 128 && p.dev_error) atomicOr(p.dev_error, err);
     if ((tid & 31) == 0) bulk_wait_all();  // this warp's output stores have completed
   } else {
-    operand_loop(sm, p, tmem, tid - 384, abort);
+    operand_loop<kListed>(sm, p, tmem, tid - 384, abort);
   }
 
   tc_fence_before();

@@ -51,6 +51,12 @@ EDGE_CASES = {
     "short_no_h0": dict(lengths=[5, 20, 0, 3, 32], H=1, HV=2, with_h0=False),
     "short_no_final": dict(lengths=[5, 20, 3, 31], H=2, HV=2, want_final=False),
     "fixed_T8_gva_pool": dict(B=4, T=8, H=1, HV=4, pool=6, indices=[5, -1, 0, 3], in_place=True),
+    # packed batches of at most 256 sequences run a longest-first unit schedule; ties in length
+    # are ranked by sequence index, padded sequences count as empty
+    "packed_tied_lengths": dict(lengths=[100] * 6 + [37] * 5 + [300, 0, 100], H=1, HV=2, pool=16,
+                                indices=[0, 1, 2, 3, 4, 5, 6, 7, 8, 9, -1, 11, 12, 13], in_place=True),
+    # more than 256 sequences: round robin
+    "packed_300_sequences": dict(lengths=[(37 * i) % 211 for i in range(300)], H=1, HV=2),
 }
 
 
