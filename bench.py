@@ -448,14 +448,15 @@ def workload_roofline(p):
     live = np.ones(len(lengths), dtype=bool) if p.state_indices is None else p.state_indices >= 0
     toks = int(lengths[live].sum())
     nseq = int(live.sum())
-    state_bytes = p.HV * V * D * 4
-    nbytes = 2 * toks * p.H * D * 2 + 2 * toks * p.HV * V * 2
+    d, v = p.D, p.V
+    state_bytes = p.HV * v * d * 4
+    nbytes = 2 * toks * p.H * d * 2 + 2 * toks * p.HV * v * 2
     if p.h0 is not None:
         nbytes += nseq * state_bytes
     if p.want_final:
         nbytes += nseq * state_bytes
     chunks = int(((lengths[live] + 63) // 64).sum())
-    flops = chunks * p.HV * (4 * 64 * D * V + 4 * 64 * 64 * D)
+    flops = chunks * p.HV * (4 * 64 * d * v + 4 * 64 * 64 * d)
     return toks, nbytes, flops
 
 
@@ -480,18 +481,19 @@ def run_sweep(args):
     def bf(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
 
-    for i in (range(1, 6) if args.sweep_what in ("all", "prefill") else ()):
-        p = W.config(i)
+    extra = [W.custom(seed=3002, B=2, T=8192, H=64, HV=64, D=64, name="D=V=64 fixed MHA B=2 T=8192 H=HV=64, h0 + final state")]
+    for i in (list(range(1, 6)) + extra if args.sweep_what in ("all", "prefill") else ()):
+        p = W.config(i) if isinstance(i, int) else i
         q, k, v = bf(p.q_bits), bf(p.k_bits), bf(p.v_bits)
         sl = torch.from_numpy(p.slopes).to(device)
         h0 = None if p.h0 is None else torch.from_numpy(p.h0).to(device)
         idx = None if p.state_indices is None else torch.from_numpy(p.state_indices).to(device)
         cu = None if p.cu_seqlens is None else torch.from_numpy(p.cu_seqlens).to(device)
-        o = torch.empty((p.tokens, p.HV, V), dtype=torch.bfloat16, device=device)
+        o = torch.empty((p.tokens, p.HV, p.V), dtype=torch.bfloat16, device=device)
         if p.in_place:
             hf = h0
         elif p.want_final:
-            hf = torch.empty((p.pool_size, p.HV, V, D), dtype=torch.float32, device=device)
+            hf = torch.empty((p.pool_size, p.HV, p.V, p.D), dtype=torch.float32, device=device)
         else:
             hf = None
 
@@ -514,7 +516,7 @@ def run_sweep(args):
         ms = statistics.fmean(a.elapsed_time(b) for a, b in times)
         toks, nbytes, flops = workload_roofline(p)
         t_roof = max(nbytes / (hbm * 1e9), flops / (tflops * 1e12))
-        line = {"sweep": True, "workload": i, "name": p.name, "ms": round(ms, 5),
+        line = {"sweep": True, "workload": i if isinstance(i, int) else "d64", "name": p.name, "ms": round(ms, 5),
                 "tokens_per_s": round(toks / (ms / 1e3), 1), "tokens": toks, "alg_bytes": nbytes,
                 "alg_flops": flops, "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
                 "roofline_ms": round(t_roof * 1e3, 5), "frac": round(t_roof * 1e3 / ms, 4),

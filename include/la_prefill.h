@@ -40,7 +40,7 @@ extern "C" {
 typedef enum {
   LA_OK = 0,
   LA_ERR_INVALID_ARGUMENT = 1, /* null required pointer, bad size, misaligned pointer */
-  LA_ERR_UNSUPPORTED = 2,      /* a shape this kernel does not implement (D != 128, ...) */
+  LA_ERR_UNSUPPORTED = 2,      /* a shape this kernel does not implement (D != V, D not 64 or 128, ...) */
   LA_ERR_CUDA = 3              /* a CUDA runtime / driver call failed (launch, no sm_103a device) */
 } la_status;
 
@@ -78,9 +78,9 @@ typedef enum {
  *   dev_error                       nullable device int; see LA_DEV_ERR_* (device-side
  *                                   checks never synchronise with the host)
  *
- * Supported: D == V == 128, HV % H == 0, any N >= 0 and any sequence lengths
- * (including 0 and lengths that are not multiples of 64).  q, k, v, o, h0, h_final
- * must be 16-byte aligned.
+ * Supported: D == V == 128 or D == V == 64 (state [P, HV, D, D]), HV % H == 0, any
+ * N >= 0 and any sequence lengths (including 0 and lengths that are not multiples of 64).
+ * q, k, v, o, h0, h_final must be 16-byte aligned.
  *
  * Returns LA_OK after enqueueing the kernels (or with nothing to do when N == 0 or
  * B*T == 0 and no state is requested).  LA_ERR_INVALID_ARGUMENT and LA_ERR_UNSUPPORTED
@@ -100,17 +100,6 @@ const char* la_last_error(void);
 
 /* Size in bytes of dynamic shared memory the kernel requests per CTA. */
 int la_prefill_smem_bytes(void);
-
-/*
- * Timeline tracing (diagnostics).  A library built with -DLA_TRACE records, for CTA 0
- * and its first 64 chunks, one %globaltimer stamp (ns) per pipeline event and chunk
- * into a caller-owned device buffer of la_prefill_trace_events() uint64 values
- * (event-major: [event][chunk]).  la_prefill_trace_events() returns 0 for a normal
- * build, whose kernel contains no tracing code.  The buffer pointer is process-global
- * and used by every later call until it is reset to NULL.
- */
-int la_prefill_trace_events(void);
-void la_prefill_set_trace_buffer(void* device_buffer);
 
 #ifdef __cplusplus
 }

@@ -26,7 +26,7 @@ DEV_ERR_BAD_SEQLENS = 1
 DEV_ERR_BAD_INDEX = 2
 DEV_ERR_TIMEOUT = 4
 EXPORTED_SYMBOLS = ("la_prefill_fwd", "la_status_string", "la_last_error", "la_prefill_smem_bytes",
-                    "la_prefill_trace_events", "la_prefill_set_trace_buffer", "la_decode_mtp", "la_verify",
+                    "la_decode_mtp", "la_verify",
                     "la_commit", "la_prefill_segmented_workspace", "la_prefill_fwd_segmented",
                     "la_prefill_fwd_segmented_static")
 

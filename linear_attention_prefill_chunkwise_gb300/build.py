@@ -18,7 +18,6 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_NAME = "libla_prefill.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
-TRACE_LIB_PATH = os.path.join(BUILD_DIR, "libla_prefill_trace.so")
 INCLUDE_DIR = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["la_prefill_api.cu", "la_decode_api.cu", "la_segment_api.cu", "la_segment_static_api.cu"]
@@ -44,10 +43,9 @@ def _stale(path: str) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, trace: bool = False, wait_limit_ns: int = 0) -> str:
+def build(force: bool = False, verbose: bool = False, wait_limit_ns: int = 0) -> str:
     """Build the library if any source is newer than it; return its path.
 
-    trace=True builds the timeline-tracing variant (-DLA_TRACE) as a separate file.
     wait_limit_ns > 0 builds the prefill entry point alone, as a separate file, with that
     limit on every pipeline wait instead of one second: ordinary waits then exceed it, so the
     kernels' timeout exit can be exercised on a healthy input."""
@@ -55,7 +53,7 @@ def build(force: bool = False, verbose: bool = False, trace: bool = False, wait_
         out = os.path.join(BUILD_DIR, f"libla_prefill_wait{int(wait_limit_ns)}ns.so")
         sources = ["la_prefill_api.cu"]
     else:
-        out = TRACE_LIB_PATH if trace else LIB_PATH
+        out = LIB_PATH
         sources = SOURCES
     if not force and not _stale(out):
         return out
@@ -65,8 +63,6 @@ def build(force: bool = False, verbose: bool = False, trace: bool = False, wait_
            "-cudart", "static", "-I", INCLUDE_DIR, "-o", tmp] + [os.path.join(CSRC, s) for s in sources]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
-    if trace:
-        cmd.insert(1, "-DLA_TRACE")
     if wait_limit_ns:
         cmd.insert(1, f"-DLA_WAIT_LIMIT_NS={int(wait_limit_ns)}ull")
     res = subprocess.run(cmd, capture_output=True, text=True)

@@ -81,14 +81,15 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// Map over a token-major [rows, heads * 128] BF16 matrix: 64 x 64 boxes (64 tokens x 64
-// dims, 128-byte rows), 128-byte swizzle, the layout the kernels' MMA descriptors expect.
+// Map over a token-major [rows, heads * dim] BF16 matrix (dim = 64 or 128): 64 x 64 boxes (64
+// tokens x 64 dims, 128-byte rows), 128-byte swizzle, the layout the kernels' MMA descriptors
+// expect.
 inline la_status encode_bf16_rows_map(CUtensorMap* map, const void* base, int64_t rows, int64_t heads,
-                                      const char* name) {
+                                      const char* name, int64_t dim = 128) {
   auto enc = tensor_map_encoder();
   if (!enc) return fail(LA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the CUDA driver");
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(heads * 128), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(heads * 128 * 2)};
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(heads * dim), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(heads * dim * 2)};
   const cuuint32_t box[2] = {64, 64};
   const cuuint32_t elem_strides[2] = {1, 1};
   const CUresult r =
@@ -99,13 +100,13 @@ inline la_status encode_bf16_rows_map(CUtensorMap* map, const void* base, int64_
   return LA_OK;
 }
 
-// Map over the token-major [rows, heads * 128] BF16 output for the epilogue's stores: 32 x 32
+// Map over the token-major [rows, heads * dim] BF16 output for the epilogue's stores: 32 x 32
 // boxes (32 tokens x 32 values, 64-byte rows), 64-byte swizzle.
-inline la_status encode_bf16_out_map(CUtensorMap* map, void* base, int64_t rows, int64_t heads) {
+inline la_status encode_bf16_out_map(CUtensorMap* map, void* base, int64_t rows, int64_t heads, int64_t dim) {
   auto enc = tensor_map_encoder();
   if (!enc) return fail(LA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the CUDA driver");
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(heads * 128), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(heads * 128 * 2)};
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(heads * dim), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(heads * dim * 2)};
   const cuuint32_t box[2] = {32, 32};
   const cuuint32_t elem_strides[2] = {1, 1};
   const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, elem_strides,
@@ -122,8 +123,8 @@ inline la_status check_prefill_args(const void* q, const void* k, const void* v,
                                     const void* o, const float* h_final, int B, int T, int N, int H, int HV, int D,
                                     int V, int pool_size, const int* dev_error, bool* nothing_to_do) {
   *nothing_to_do = false;
-  if (D != 128 || V != 128)
-    return fail(LA_ERR_UNSUPPORTED, "only D == V == 128 is implemented (got D=%d, V=%d)", D, V);
+  if (D != V || (D != 128 && D != 64))
+    return fail(LA_ERR_UNSUPPORTED, "only D == V == 128 and D == V == 64 are implemented (got D=%d, V=%d)", D, V);
   if (H <= 0 || HV <= 0) return fail(LA_ERR_INVALID_ARGUMENT, "H and HV must be positive (got %d, %d)", H, HV);
   if (HV % H != 0) return fail(LA_ERR_UNSUPPORTED, "HV (%d) must be a multiple of H (%d)", HV, H);
   if (B < 0 || T < 0 || N < 0) return fail(LA_ERR_INVALID_ARGUMENT, "B, T, N must be >= 0");
@@ -136,7 +137,7 @@ inline la_status check_prefill_args(const void* q, const void* k, const void* v,
   if (tokens + 64 > INT32_MAX) return fail(LA_ERR_UNSUPPORTED, "B*T too large (%lld)", (long long)tokens);
   const int64_t units = static_cast<int64_t>(N) * HV;
   if (units > INT32_MAX) return fail(LA_ERR_UNSUPPORTED, "N*HV too large (%lld)", (long long)units);
-  if (static_cast<int64_t>(HV) * 128 * 2 > (int64_t(1) << 39))
+  if (static_cast<int64_t>(HV) * D * 2 > (int64_t(1) << 39))
     return fail(LA_ERR_UNSUPPORTED, "HV too large for a tensor map stride");
   if (N == 0) {
     *nothing_to_do = true;

@@ -26,8 +26,6 @@ namespace {
 using la_host::fail;
 using la_host::g_last_error;
 
-unsigned long long* g_trace = nullptr;  // device buffer for timeline tracing builds
-
 // Per-device facts looked up once: SM count, and the kernel's shared-memory attribute set.
 la_host::DeviceState g_dev[la_host::kMaxDevices];
 
@@ -56,16 +54,6 @@ const char* la_last_error(void) { return g_last_error; }
 
 int la_prefill_smem_bytes(void) { return smem_bytes(); }
 
-int la_prefill_trace_events(void) {
-#ifdef LA_TRACE
-  return lap::kTrEvents * lap::kTraceChunks;
-#else
-  return 0;
-#endif
-}
-
-void la_prefill_set_trace_buffer(void* device_buffer) { g_trace = static_cast<unsigned long long*>(device_buffer); }
-
 la_status la_prefill_fwd(const void* q, const void* k, const void* v, const float* slopes, float scale,
                          const float* h0, const int32_t* state_indices, const int32_t* cu_seqlens, void* o,
                          float* h_final, int B, int T, int N, int H, int HV, int D, int V, int pool_size,
@@ -83,11 +71,11 @@ la_status la_prefill_fwd(const void* q, const void* k, const void* v, const floa
   // ---- device
   la_host::DeviceState* dsp = nullptr;
   la_status dst = la_host::current_device(g_dev, &dsp, [] {
-    cudaError_t e = cudaFuncSetAttribute(lap::la_prefill_fwd_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes());
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(lap::la_prefill_fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               smem_bytes());
+    const cudaFuncAttribute attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+    cudaError_t e = cudaFuncSetAttribute(lap::la_prefill_fwd_kernel<false, 128>, attr, smem_bytes());
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(lap::la_prefill_fwd_kernel<true, 128>, attr, smem_bytes());
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(lap::la_prefill_fwd_kernel<false, 64>, attr, smem_bytes());
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(lap::la_prefill_fwd_kernel<true, 64>, attr, smem_bytes());
     return e;
   });
   if (dst != LA_OK) return dst;
@@ -102,16 +90,17 @@ la_status la_prefill_fwd(const void* q, const void* k, const void* v, const floa
   memset(&tm_o, 0, sizeof(tm_o));
   if (tokens > 0) {
     la_status st;
-    if ((st = la_host::encode_bf16_rows_map(&tm_q, q, tokens, H, "q")) != LA_OK) return st;
-    if ((st = la_host::encode_bf16_rows_map(&tm_k, k, tokens, H, "k")) != LA_OK) return st;
-    if ((st = la_host::encode_bf16_rows_map(&tm_v, v, tokens, HV, "v")) != LA_OK) return st;
-    if ((st = la_host::encode_bf16_out_map(&tm_o, o, tokens, HV)) != LA_OK) return st;
+    if ((st = la_host::encode_bf16_rows_map(&tm_q, q, tokens, H, "q", D)) != LA_OK) return st;
+    if ((st = la_host::encode_bf16_rows_map(&tm_k, k, tokens, H, "k", D)) != LA_OK) return st;
+    if ((st = la_host::encode_bf16_rows_map(&tm_v, v, tokens, HV, "v", D)) != LA_OK) return st;
+    if ((st = la_host::encode_bf16_out_map(&tm_o, o, tokens, HV, D)) != LA_OK) return st;
   }
 
+  // The tokenwise kernel holds a 128 x 128 state: with D = 64 every sequence takes the chunkwise one.
   const bool packed = cu_seqlens != nullptr;
-  const bool split = packed && tokens <= static_cast<int64_t>(kSplitAvg) * N;
-  const bool run_tokenwise = split || (!packed && T <= kShortMax);
-  const bool run_chunkwise = packed || T > kShortMax;
+  const bool split = D == 128 && packed && tokens <= static_cast<int64_t>(kSplitAvg) * N;
+  const bool run_tokenwise = split || (D == 128 && !packed && T <= kShortMax);
+  const bool run_chunkwise = packed || T > kShortMax || D != 128;
   const int pool = la_host::effective_pool_size(h0, h_final, state_indices, pool_size, N);
   if (run_tokenwise) {
     lad::Params tp{};
@@ -150,7 +139,6 @@ la_status la_prefill_fwd(const void* q, const void* k, const void* v, const floa
   p.o = static_cast<__nv_bfloat16*>(o);
   p.h_final = h_final;
   p.dev_error = dev_error;
-  p.trace = g_trace;
   p.scale = scale;
   p.num_tokens = static_cast<int>(tokens);
   p.T = cu_seqlens ? 0 : T;
@@ -167,12 +155,18 @@ la_status la_prefill_fwd(const void* q, const void* k, const void* v, const floa
   // A packed batch of few sequences gets the longest-first schedule (the lengths vary, and a
   // CTA runs a handful of units); other batches deal units out round robin.
   const bool listed = packed && N <= lap::kSchedSeqMax && (units + grid - 1) / grid <= lap::kSchedMax;
-  if (listed)
-    lap::la_prefill_fwd_kernel<true><<<grid, lap::kThreads, smem_bytes(), static_cast<cudaStream_t>(stream)>>>(
-        tm_q, tm_k, tm_v, tm_o, p);
-  else
-    lap::la_prefill_fwd_kernel<false><<<grid, lap::kThreads, smem_bytes(), static_cast<cudaStream_t>(stream)>>>(
-        tm_q, tm_k, tm_v, tm_o, p);
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (D == 128) {
+    if (listed)
+      lap::la_prefill_fwd_kernel<true, 128><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p);
+    else
+      lap::la_prefill_fwd_kernel<false, 128><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p);
+  } else {
+    if (listed)
+      lap::la_prefill_fwd_kernel<true, 64><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p);
+    else
+      lap::la_prefill_fwd_kernel<false, 64><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p);
+  }
   ce = cudaGetLastError();
   if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(ce));
   return LA_OK;

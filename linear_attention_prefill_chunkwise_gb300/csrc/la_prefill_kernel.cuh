@@ -68,7 +68,7 @@
 namespace lap {
 
 constexpr int kChunk = 64;        // tokens per chunk
-constexpr int kDim = 128;         // D = V = 128
+constexpr int kDim = 128;         // largest head dimension D = V (the tile and TMEM layout)
 constexpr int kQKStages = 2;      // Q/K ring depth (released early: after scores, Kt, Qt)
 constexpr int kVStages = 3;       // V ring depth (held until O_intra)
 constexpr int kThreads = 512;
@@ -140,7 +140,6 @@ struct KernelParams {
   __nv_bfloat16* o;
   float* h_final;
   int* dev_error;
-  unsigned long long* trace;  // per-chunk timestamps of CTA 0 (builds with LA_TRACE only)
   float scale;
   int num_tokens;
   int T;          // fixed-length mode sequence length
@@ -198,40 +197,6 @@ __device__ __forceinline__ Unit decode_unit(const KernelParams& p, int u) {
   w.nchunks = (w.len + kChunk - 1) / kChunk;
   return w;
 }
-
-// ---- optional timeline tracing (compiled in with -DLA_TRACE): one %globaltimer stamp
-// per (event, chunk) for the first kTraceChunks chunks of CTA 0, written by one thread of
-// the role that reaches the event.
-enum TraceEvent {
-  kTrProducerIssue = 0,  // producer: stage free, TMA loads issued
-  kTrMmaScores,          // MMA: scores of chunk i issued (one chunk ahead)
-  kTrMmaDeltaS,          // MMA: Kt ready, dS issued
-  kTrMmaOInter,          // MMA: S and Q ready, O_inter issued
-  kTrMmaOIntra,          // MMA: P ready, O_intra issued
-  kTrOperKtStart,        // operand wg: stage loaded, Kt build starts
-  kTrOperKtDone,         // operand wg: Kt published
-  kTrOperScores,         // operand wg: scores available
-  kTrOperPDone,          // operand wg: P published
-  kTrConvDone,           // converter: Qt(i) published
-  kTrStateDeltaS,        // state wgs: dS available
-  kTrStateUpdated,       // state wgs: S advanced in registers, dS released
-  kTrStateOInter,        // state wgs: O_inter(i) complete (S free)
-  kTrStateSReady,        // state wgs: S(i+1) published
-  kTrStateEpilogue,      // state wgs: O(i) stored, accumulators released
-  kTrEvents
-};
-constexpr int kTraceChunks = 64;
-#ifdef LA_TRACE
-#define LA_TRACE_AT(p, ev, it, who)                                                          \
-  do {                                                                                       \
-    if ((who) && (p).trace && blockIdx.x == 0 && (it) < static_cast<uint32_t>(kTraceChunks)) \
-      (p).trace[(ev) * kTraceChunks + (it)] = globaltimer_ns();                              \
-  } while (0)
-#else
-#define LA_TRACE_AT(p, ev, it, who) \
-  do {                              \
-  } while (0)
-#endif
 
 // Byte offset of 16-byte chunk c (0..7) of row r inside a 128-byte-swizzled tile.
 __device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t c) { return r * 128u + ((c ^ (r & 7u)) << 4); }
@@ -372,12 +337,14 @@ __device__ __forceinline__ void cursor_next(const SharedStorage& sm, const Kerne
 // TMA and MMA thread B, one polling loop: each pass issues, in this order, every job whose
 // inputs are ready (mbarrier.test_wait, no blocking): dS(i) = V(i)^T Kt(i), scores(i) =
 // Q(i) K(i)^T, and the next Q/K and V loads once their ring slots have been released.
-template <bool kListed>
+template <bool kListed, int kD>
 __device__ __forceinline__ void tma_mma_loop(SharedStorage& sm, const KernelParams& p, const CUtensorMap* tm_q,
                                              const CUtensorMap* tm_k, const CUtensorMap* tm_v, uint32_t tmem,
                                              volatile int* abort) {
+  static_assert(kD == 64 || kD == 128, "head dimension");
+  constexpr int kHalves = kD / 64;  // 64-wide boxes per head row
   constexpr uint32_t id_scores = idesc_bf16_f32(64, 64, false, false);
-  constexpr uint32_t id_dstate = idesc_bf16_f32(128, 128, true, true);
+  constexpr uint32_t id_dstate = idesc_bf16_f32(128, kD, true, true);
   const uint64_t dq0 = sdesc_sw128(smem_u32(sm.qk[0].q), 16, 1024);
   const uint64_t dk0 = sdesc_sw128(smem_u32(sm.qk[0].k), 16, 1024);
   const uint64_t qk_step = sizeof(QKTiles) >> 4;
@@ -399,7 +366,6 @@ __device__ __forceinline__ void tma_mma_loop(SharedStorage& sm, const KernelPara
       if (mbar_test(&sm.kt_ready, j & 1u) && mbar_test(&sm.v_full[sv], (j / kVStages) & 1u) &&
           mbar_test(&sm.ds_free, (j & 1u) ^ 1u)) {
         tc_fence_after();
-        LA_TRACE_AT(p, kTrMmaDeltaS, j, true);
         const uint64_t v0 = dv0 + sv * v_step;
 #pragma unroll
         for (int part = 0; part < 2; ++part) {
@@ -419,10 +385,9 @@ __device__ __forceinline__ void tma_mma_loop(SharedStorage& sm, const KernelPara
       const uint32_t j = n_sc, sq = j % kQKStages;
       if (mbar_test(&sm.qk_full[sq], (j / kQKStages) & 1u) && (j == 0 || mbar_test(&sm.scores_free, (j - 1) & 1u))) {
         tc_fence_after();
-        LA_TRACE_AT(p, kTrMmaScores, j, true);
         const uint64_t q0 = dq0 + sq * qk_step, k0 = dk0 + sq * qk_step;
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
+        for (int kk = 0; kk < 4 * kHalves; ++kk) {
           const uint32_t off = (kk >> 2) * kTileBytes + (kk & 3) * 32;
           mma_ss(t_scores, desc_at(q0, off), desc_at(k0, off), id_scores, kk > 0);
         }
@@ -435,13 +400,12 @@ __device__ __forceinline__ void tma_mma_loop(SharedStorage& sm, const KernelPara
     if (cq.valid) {
       const uint32_t sq = nqk % kQKStages;
       if (mbar_test(&sm.qk_empty[sq], ((nqk / kQKStages) & 1u) ^ 1u)) {
-        LA_TRACE_AT(p, kTrProducerIssue, nqk, true);
         // a ragged chunk's V tile lands on this stage's barrier as well (see the V load)
-        mbar_arrive_expect_tx(&sm.qk_full[sq], (cq.ragged() ? 6 : 4) * kTileBytes);
+        mbar_arrive_expect_tx(&sm.qk_full[sq], (cq.ragged() ? 3 : 2) * kHalves * kTileBytes);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          tma_load_2d(sm.qk[sq].q[h], tm_q, &sm.qk_full[sq], cq.hq * kDim + 64 * h, cq.row);
-          tma_load_2d(sm.qk[sq].k[h], tm_k, &sm.qk_full[sq], cq.hq * kDim + 64 * h, cq.row);
+        for (int h = 0; h < kHalves; ++h) {
+          tma_load_2d(sm.qk[sq].q[h], tm_q, &sm.qk_full[sq], cq.hq * kD + 64 * h, cq.row);
+          tma_load_2d(sm.qk[sq].k[h], tm_k, &sm.qk_full[sq], cq.hq * kD + 64 * h, cq.row);
         }
         ++nqk;
         cursor_next(sm, p, cq);
@@ -463,10 +427,10 @@ __device__ __forceinline__ void tma_mma_loop(SharedStorage& sm, const KernelPara
           mbar_arrive(bar);
           bar = &sm.qk_full[nv % kQKStages];
         } else {
-          mbar_arrive_expect_tx(bar, 2 * kTileBytes);
+          mbar_arrive_expect_tx(bar, kHalves * kTileBytes);
         }
 #pragma unroll
-        for (int h = 0; h < 2; ++h) tma_load_2d(sm.v[sv][h], tm_v, bar, cv.hv * kDim + 64 * h, cv.row);
+        for (int h = 0; h < kHalves; ++h) tma_load_2d(sm.v[sv][h], tm_v, bar, cv.hv * kD + 64 * h, cv.row);
         ++nv;
         cursor_next(sm, p, cv);
         progressed = true;
@@ -503,7 +467,7 @@ __device__ __forceinline__ void tma_mma_loop(SharedStorage& sm, const KernelPara
 // serial chain of the pipeline):
 //   O_inter(i) = S(i) Qt(i)^T     into O[i%2]: needs Qt(i), O(i-2) read out, S(i) published
 //   O_intra(i) += V(i)^T P(i)^T   needs V(i) and P(i); after O_inter(i) (same thread, in order)
-template <bool kListed>
+template <bool kListed, int kD>
 __device__ __forceinline__ void mma_o_loop(SharedStorage& sm, const KernelParams& p, uint32_t tmem,
                                            volatile int* abort) {
   constexpr uint32_t id_ointer = idesc_tf32_f32(128, 64, false, false);
@@ -522,11 +486,10 @@ __device__ __forceinline__ void mma_o_loop(SharedStorage& sm, const KernelParams
         !mbar_wait(&sm.s_ready, ph, abort))
       break;
     tc_fence_after();
-    LA_TRACE_AT(p, kTrMmaOInter, it, true);
     const uint32_t t_o = tmem + kColO + 64 * b;
     const uint64_t qt0 = dqt0 + b * qt_step;
 #pragma unroll 4
-    for (int kk = 0; kk < 16; ++kk) {
+    for (int kk = 0; kk < kD / 8; ++kk) {
       const uint32_t off = (kk >> 2) * kTileBytes + (kk & 3) * 32;
       mma_tf32_ts(t_o, t_state + kk * 8, desc_at(qt0, off), id_ointer, kk > 0);
     }
@@ -534,7 +497,6 @@ __device__ __forceinline__ void mma_o_loop(SharedStorage& sm, const KernelParams
     mma_commit(&sm.qt_free[b]);
     if (!mbar_wait(&sm.v_full[sv], (it / kVStages) & 1u, abort) || !mbar_wait(&sm.p_ready, ph, abort)) break;
     tc_fence_after();
-    LA_TRACE_AT(p, kTrMmaOIntra, it, true);
     const uint64_t v0 = dv0 + sv * v_step;
 #pragma unroll
     for (int part = 0; part < 2; ++part) {
@@ -555,7 +517,7 @@ __device__ __forceinline__ void mma_o_loop(SharedStorage& sm, const KernelParams
 // tensor core reads as TF32, i.e. truncated to 10 mantissa bits; rounding it here instead
 // would cost two more instructions per element on the critical conversion and changes the
 // output by far less than its BF16 step.  Thread t owns token row s = t of the chunk.
-template <bool kListed>
+template <bool kListed, int kD>
 __device__ __forceinline__ void convert_loop(SharedStorage& sm, const KernelParams& p, int ctid,
                                              volatile int* abort) {
   const int s = ctid;
@@ -574,7 +536,7 @@ __device__ __forceinline__ void convert_loop(SharedStorage& sm, const KernelPara
         break;
       }
 #pragma unroll 1
-      for (int h = 0; h < 2; ++h) {
+      for (int h = 0; h < kD / 64; ++h) {
 #pragma unroll 2
         for (int cc = 0; cc < 8; ++cc) {
           const uint4 x = *reinterpret_cast<const uint4*>(sm.qk[sq].q[h] + swz(s, cc));
@@ -589,13 +551,12 @@ __device__ __forceinline__ void convert_loop(SharedStorage& sm, const KernelPara
       fence_proxy_async_smem();
       mbar_arrive(&sm.qt_ready[b]);
       mbar_arrive(&sm.qk_empty[sq]);
-      LA_TRACE_AT(p, kTrConvDone, it, ctid == 0);
     }
   }
 }
 
 // Operand warpgroup: Kt = lambda^(L-1-j) k_j and P = A * lambda^(s-j) (causal, tail masked), as BF16 hi/lo.
-template <bool kListed>
+template <bool kListed, int kD>
 __device__ __forceinline__ void operand_loop(SharedStorage& sm, const KernelParams& p, uint32_t tmem, int otid,
                                              volatile int* abort) {
   const int warp = otid >> 5, lane = otid & 31;
@@ -625,40 +586,42 @@ __device__ __forceinline__ void operand_loop(SharedStorage& sm, const KernelPara
         ok = false;
         break;
       }
-      LA_TRACE_AT(p, kTrOperKtStart, it, otid == 0);
-      if (krow >= L) {
-        // Rows j >= L of a ragged chunk belong to the next packed sequence (or are the TMA's zero
-        // fill): this thread's K row and V row are zeroed, so that a non-finite value there cannot
-        // reach this sequence (0 * inf is NaN); the V tile of a ragged chunk has landed with the
-        // Q/K stage.
-        uint8_t* kr = sm.qk[sq].k[kbox] + krow * 128;
-        uint8_t* vr = sm.v[it % kVStages][kbox] + krow * 128;
+      // (with D = 64 the second 64-column box of K, V and Kt is unused: V's stays zero, see the
+      // kernel's prologue, and the dS MMA has N = 64)
+      if (kD == 128 || kbox == 0) {
+        if (krow >= L) {
+          // Rows j >= L of a ragged chunk belong to the next packed sequence (or are the TMA's zero
+          // fill): this thread's K row and V row are zeroed, so that a non-finite value there cannot
+          // reach this sequence (0 * inf is NaN); the V tile of a ragged chunk has landed with the
+          // Q/K stage.
+          uint8_t* kr = sm.qk[sq].k[kbox] + krow * 128;
+          uint8_t* vr = sm.v[it % kVStages][kbox] + krow * 128;
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          *reinterpret_cast<uint4*>(kr + 16 * cc) = make_uint4(0, 0, 0, 0);
-          *reinterpret_cast<uint4*>(vr + 16 * cc) = make_uint4(0, 0, 0, 0);
+          for (int cc = 0; cc < 8; ++cc) {
+            *reinterpret_cast<uint4*>(kr + 16 * cc) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(vr + 16 * cc) = make_uint4(0, 0, 0, 0);
+          }
         }
-      }
-      {
-        const float wjf = (krow < L) ? lam[L - 1 - krow] : 0.f;
-        const uint64_t wj = f2_pack(wjf, wjf);
-        const uint8_t* ksrc = sm.qk[sq].k[kbox];
+        {
+          const float wjf = (krow < L) ? lam[L - 1 - krow] : 0.f;
+          const uint64_t wj = f2_pack(wjf, wjf);
+          const uint8_t* ksrc = sm.qk[sq].k[kbox];
 #pragma unroll 2
-        for (int cc = 0; cc < 8; ++cc) {
-          const uint32_t off = swz(krow, cc);
-          const uint4 kx = *reinterpret_cast<const uint4*>(ksrc + off);
-          const uint32_t kw[4] = {kx.x, kx.y, kx.z, kx.w};
-          uint32_t hi[4], lo[4];
+          for (int cc = 0; cc < 8; ++cc) {
+            const uint32_t off = swz(krow, cc);
+            const uint4 kx = *reinterpret_cast<const uint4*>(ksrc + off);
+            const uint32_t kw[4] = {kx.x, kx.y, kx.z, kx.w};
+            uint32_t hi[4], lo[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) split_bf16x2(f2_mul(wj, bf16x2_to_f2(kw[e])), hi[e], lo[e]);
-          *reinterpret_cast<uint4*>(sm.kt_hi[kbox] + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(sm.kt_lo[kbox] + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            for (int e = 0; e < 4; ++e) split_bf16x2(f2_mul(wj, bf16x2_to_f2(kw[e])), hi[e], lo[e]);
+            *reinterpret_cast<uint4*>(sm.kt_hi[kbox] + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *reinterpret_cast<uint4*>(sm.kt_lo[kbox] + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          }
         }
       }
       fence_proxy_async_smem();
       mbar_arrive(&sm.kt_ready);
       mbar_arrive(&sm.qk_empty[sq]);
-      LA_TRACE_AT(p, kTrOperKtDone, it, otid == 0);
 
       // ---- P from the scores: row prow, columns pcol .. pcol + 31 (16x32bx2 loads use all 32 lanes)
       if (!warp_wait(&sm.scores_full, ph, abort)) {
@@ -666,7 +629,6 @@ __device__ __forceinline__ void operand_loop(SharedStorage& sm, const KernelPara
         break;
       }
       tc_fence_after();
-      LA_TRACE_AT(p, kTrOperScores, it, otid == 0);
       float a[2][16];
       tmem_ld16_x2split32(tmem + lane_base + kColScores, a[0]);
       tmem_ld16_x2split32(tmem + lane_base + kColScores + 16, a[1]);
@@ -701,13 +663,12 @@ __device__ __forceinline__ void operand_loop(SharedStorage& sm, const KernelPara
       }
       fence_proxy_async_smem();
       mbar_arrive(&sm.p_ready);
-      LA_TRACE_AT(p, kTrOperPDone, it, otid == 0);
     }
   }
 }
 
 // State warpgroups: own S in registers, advance it, publish it to TMEM, write the output.
-template <bool kListed>
+template <bool kListed, int kD>
 __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams& p, const CUtensorMap* tm_o,
                                           uint32_t tmem, int ctid, volatile int* abort) {
   const int warp = ctid >> 5, lane = ctid & 31;
@@ -715,6 +676,10 @@ __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams&
   const int qd = warp & 3;          // TMEM lane quadrant
   const int vrow = 32 * qd + lane;  // state row / output column v
   const int kbase = 64 * wg;
+  // With D = 64 only rows v < 64 and columns k < 64 of the 128 x 128 layout hold the state: the
+  // second warpgroup's columns are never read (O_inter has K = 64), rows v >= 64 stay zero.
+  const bool k_live = kD == 128 || wg == 0;
+  const bool state_live = kD == 128 || (wg == 0 && qd < 2);
   const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
   float S[64];
   uint32_t it = 0;
@@ -723,12 +688,14 @@ __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams&
 
   // S into its TMEM columns (the TF32 MMA reads its top 10 mantissa bits), then tell the MMA thread.
   auto publish_state = [&]() {
+    if (k_live) {
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-      uint32_t u[16];
+      for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t u[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(S[16 * q4 + i]);
-      tmem_st16(tmem + lane_base + kColState + kbase + 16 * q4, u);
+        for (int i = 0; i < 16; ++i) u[i] = __float_as_uint(S[16 * q4 + i]);
+        tmem_st16(tmem + lane_base + kColState + kbase + 16 * q4, u);
+      }
     }
     tc_fence_before();
     mbar_arrive(&sm.s_ready);
@@ -742,8 +709,8 @@ __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams&
     const float lam_chunk = expf(-slope * static_cast<float>(kChunk));  // lambda^64
 
     // state gather
-    const size_t state_off = ((static_cast<size_t>(w.slot) * p.HV + w.hv) * kDim + vrow) * kDim + kbase;
-    if (p.h0) {
+    const size_t state_off = ((static_cast<size_t>(w.slot) * p.HV + w.hv) * kD + vrow) * kD + kbase;
+    if (p.h0 && state_live) {
       const float4* src = reinterpret_cast<const float4*>(p.h0 + state_off);
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -760,7 +727,7 @@ __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams&
     // The state's TMEM columns are free: the previous chunk's s_free was waited on below.
     if (w.nchunks > 0) publish_state();
 
-    const size_t ostride = static_cast<size_t>(p.HV) * kDim;
+    const size_t ostride = static_cast<size_t>(p.HV) * kD;
     for (int c = 0; c < w.nchunks; ++c, ++it) {
       const uint32_t ph = it & 1u;
       const uint32_t b = it & 1u, bph = (it >> 1) & 1u;
@@ -772,25 +739,26 @@ __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams&
         break;
       }
       tc_fence_after();
-      LA_TRACE_AT(p, kTrStateDeltaS, it, ctid == 0);
       {
         const float lamLf = (L == kChunk) ? lam_chunk : expf(-slope * static_cast<float>(L));
         const uint64_t lamL = f2_pack(lamLf, lamLf);
+        if (k_live) {
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          float d[16];
-          tmem_ld16(tmem + lane_base + kColDeltaS + kbase + 16 * q4, d);
+          for (int q4 = 0; q4 < 4; ++q4) {
+            float d[16];
+            tmem_ld16(tmem + lane_base + kColDeltaS + kbase + 16 * q4, d);
 #pragma unroll
-          for (int i = 0; i < 16; i += 2) {
-            const float2 r = f2_unpack(f2_fma(lamL, f2_pack(S[16 * q4 + i], S[16 * q4 + i + 1]), f2_pack(d[i], d[i + 1])));
-            S[16 * q4 + i] = r.x;
-            S[16 * q4 + i + 1] = r.y;
+            for (int i = 0; i < 16; i += 2) {
+              const float2 r =
+                  f2_unpack(f2_fma(lamL, f2_pack(S[16 * q4 + i], S[16 * q4 + i + 1]), f2_pack(d[i], d[i + 1])));
+              S[16 * q4 + i] = r.x;
+              S[16 * q4 + i + 1] = r.y;
+            }
           }
         }
       }
       tc_fence_before();
       mbar_arrive(&sm.ds_free);
-      LA_TRACE_AT(p, kTrStateUpdated, it, ctid == 0);
 
       // ---- O_inter(i) has read S(i): publish S(i+1)
       if (!warp_wait(&sm.s_free, ph, abort)) {
@@ -798,9 +766,7 @@ __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams&
         break;
       }
       tc_fence_after();
-      LA_TRACE_AT(p, kTrStateOInter, it, ctid == 0);
       if (c + 1 < w.nchunks) publish_state();
-      LA_TRACE_AT(p, kTrStateSReady, it, ctid == 0);
 
       // ---- o = O (the scale is folded into Qt and P): this warp's 32 rows s x 32 values v of the
       //      chunk, staged as BF16 in the chunk's V stage (dS and O_intra, its readers, are done:
@@ -812,8 +778,11 @@ __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams&
       tc_fence_after();
       {
         const uint32_t sv = it % kVStages;
-        uint8_t* stage = sm.v[sv][0] + (wg * 4 + qd) * 2048;  // 32 rows of 64 bytes, 64-byte swizzle
-        const int rows = L - 32 * wg;  // valid rows of this warp's box (may be <= 0 or > 32)
+        // 32 rows of 64 bytes, 64-byte swizzle (D = 64: the four warps with v < 64, in the half of
+        // the stage the V loads use)
+        uint8_t* stage = sm.v[sv][0] + (wg * (kD / 32) + qd) * 2048;
+        // valid rows of this warp's box (may be <= 0 or > 32); none for values v >= D
+        const int rows = (kD == 128 || qd < 2) ? L - 32 * wg : 0;
         // stmatrix.trans: lane l gives row j = l % 8 of matrix m = l / 8; the matrices of one call
         // are (repetition rr, value half h) = (2 k2 + m / 2, m % 2): row sl = 8 rr + j of the box,
         // 16-byte chunk 2 g + h (lanes 16 g .. 16 g + 15 of this warp's quadrant)
@@ -845,14 +814,14 @@ __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams&
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(tm_o, stage, w.hv * kDim + 32 * qd, y0);
+              tma_store_2d(tm_o, stage, w.hv * kD + 32 * qd, y0);
               bulk_commit();
               bulk_wait_read_all();  // the stage is handed back to the V loads below
             }
           } else {
             // a ragged chunk's last rows: copy the valid ones, 16 bytes per lane
             __syncwarp();
-            __nv_bfloat16* orow0 = p.o + static_cast<size_t>(y0) * ostride + static_cast<size_t>(w.hv) * kDim + 32 * qd;
+            __nv_bfloat16* orow0 = p.o + static_cast<size_t>(y0) * ostride + static_cast<size_t>(w.hv) * kD + 32 * qd;
 #pragma unroll
             for (int pass = 0; pass < 4; ++pass) {
               const int sl = pass * 8 + (lane >> 2), ch = lane & 3;
@@ -867,11 +836,10 @@ __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams&
         }
         if (lane == 0) mbar_arrive(&sm.v_empty[sv]);
       }
-      LA_TRACE_AT(p, kTrStateEpilogue, it, ctid == 0);
     }
     if (!ok) break;
     // state scatter
-    if (p.h_final) {
+    if (p.h_final && state_live) {
       float4* dst = reinterpret_cast<float4*>(p.h_final + state_off);
 #pragma unroll
       for (int i = 0; i < 16; ++i) dst[i] = make_float4(S[4 * i], S[4 * i + 1], S[4 * i + 2], S[4 * i + 3]);
@@ -880,7 +848,7 @@ __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams&
   return err;
 }
 
-template <bool kListed>
+template <bool kListed, int kD>
 __global__ void __launch_bounds__(kThreads, 1)
 la_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -931,6 +899,15 @@ la_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_o);
   }
+  if constexpr (kD == 64) {
+    // The MMAs that read V (dS, O_intra) have M = 128 value rows; with D = 64 the V tile's second
+    // 64-column box is never loaded and must hold zeros for the whole kernel.
+    for (int i = tid; i < kVStages * static_cast<int>(kTileBytes / 16); i += kThreads) {
+      const int st = i / static_cast<int>(kTileBytes / 16), e = i % static_cast<int>(kTileBytes / 16);
+      reinterpret_cast<uint4*>(sm.v[st][1])[e] = make_uint4(0, 0, 0, 0);
+    }
+    fence_proxy_async_smem();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -941,17 +918,17 @@ la_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   }
 
   if (warp == 0) {
-    if (lane == 0) tma_mma_loop<kListed>(sm, p, &tm_q, &tm_k, &tm_v, tmem, abort);
+    if (lane == 0) tma_mma_loop<kListed, kD>(sm, p, &tm_q, &tm_k, &tm_v, tmem, abort);
   } else if (warp == 1) {
-    if (lane == 0) mma_o_loop<kListed>(sm, p, tmem, abort);
+    if (lane == 0) mma_o_loop<kListed, kD>(sm, p, tmem, abort);
   } else if (warp < 4) {
-    convert_loop<kListed>(sm, p, tid - 64, abort);
+    convert_loop<kListed, kD>(sm, p, tid - 64, abort);
   } else if (warp < 12) {
-    const int err = state_loop<kListed>(sm, p, &tm_o, tmem, tid - 128, abort);
+    const int err = state_loop<kListed, kD>(sm, p, &tm_o, tmem, tid - 128, abort);
     if (err && tid == 128 && p.dev_error) atomicOr(p.dev_error, err);
     if ((tid & 31) == 0) bulk_wait_all();  // this warp's output stores have completed
   } else {
-    operand_loop<kListed>(sm, p, tmem, tid - 384, abort);
+    operand_loop<kListed, kD>(sm, p, tmem, tid - 384, abort);
   }
 
   tc_fence_before();

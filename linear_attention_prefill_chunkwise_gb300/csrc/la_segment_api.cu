@@ -130,6 +130,7 @@ la_status la_prefill_fwd_segmented(const void* q, const void* k, const void* v, 
   la_status st = la_host::check_prefill_args(q, k, v, slopes, h0, state_indices, cu_seqlens, o, h_final, B, T, N, H,
                                              HV, D, V, pool_size, dev_error, &nothing);
   if (st != LA_OK || nothing) return st;
+  if (D != 128) return fail(LA_ERR_UNSUPPORTED, "the segmented prefill is implemented for D == V == 128 only (got %d)", D);
   // An explicit segment length fixes the plan without the device: the workspace is checked
   // before any device state is touched.
   la_host::DeviceState* ds = nullptr;

@@ -63,7 +63,7 @@ def upload(p: W.Problem, device="cuda", poison_o=True):
     d["h0"] = None if p.h0 is None else torch.from_numpy(p.h0).to(device)
     d["idx"] = None if p.state_indices is None else torch.from_numpy(p.state_indices).to(device)
     d["cu"] = None if p.cu_seqlens is None else torch.from_numpy(p.cu_seqlens).to(device)
-    o = torch.empty((p.tokens, p.HV, W.V), dtype=torch.bfloat16, device=device)
+    o = torch.empty((p.tokens, p.HV, p.V), dtype=torch.bfloat16, device=device)
     if poison_o:
         o.fill_(float("nan"))
     d["o"] = o
@@ -71,7 +71,7 @@ def upload(p: W.Problem, device="cuda", poison_o=True):
         if p.in_place and d["h0"] is not None:
             d["h_final"] = d["h0"]
         else:
-            d["h_final"] = torch.full((p.pool_size, p.HV, W.V, W.D), float("nan"), dtype=torch.float32,
+            d["h_final"] = torch.full((p.pool_size, p.HV, p.V, p.D), float("nan"), dtype=torch.float32,
                                       device=device)
     else:
         d["h_final"] = None
@@ -92,7 +92,7 @@ def oracle_full(p: W.Problem, nthreads=0):
     h0 = None if p.h0 is None else p.h0.astype(np.float64)
     hf_init = None
     if p.want_final:
-        hf_init = h0.copy() if (p.in_place and h0 is not None) else np.full((p.pool_size, p.HV, W.V, W.D), np.nan)
+        hf_init = h0.copy() if (p.in_place and h0 is not None) else np.full((p.pool_size, p.HV, p.V, p.D), np.nan)
     return oracle.tokenwise(p.q(), p.k(), p.v(), p.slopes, p.scale, h0=h0, state_indices=p.state_indices,
                             cu_seqlens=p.cu_seqlens, T=None if p.cu_seqlens is not None else p.T,
                             h_final=hf_init, want_state=p.want_final, nthreads=nthreads)
@@ -115,8 +115,8 @@ def oracle_unit(p: W.Problem, n, hv):
     h0 = None if p.h0 is None else p.h0[slot:slot + 1, hv:hv + 1].astype(np.float64)
     L = b - a
     if L == 0:
-        hf = np.zeros((W.V, W.D)) if h0 is None else h0[0, 0].copy()
-        return np.zeros((0, W.V)), hf
+        hf = np.zeros((p.V, p.D)) if h0 is None else h0[0, 0].copy()
+        return np.zeros((0, p.V)), hf
     o, hf = oracle.tokenwise(W.bf16_to_f32(p.q_bits[a:b, hq:hq + 1]), W.bf16_to_f32(p.k_bits[a:b, hq:hq + 1]),
                              W.bf16_to_f32(p.v_bits[a:b, hv:hv + 1]), p.slopes[hv:hv + 1], p.scale, h0=h0, T=L)
     return o[:, 0], hf[0, 0]

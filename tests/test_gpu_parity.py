@@ -186,9 +186,14 @@ def test_two_streams_concurrent_equals_serial():
 
 def test_rejected_shapes_return_status_without_launch():
     import linear_attention_prefill_chunkwise_gb300 as lap
-    q = torch.zeros((64, 1, 64), dtype=torch.bfloat16, device="cuda")
-    v = torch.zeros((64, 1, 64), dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros((64, 1, 32), dtype=torch.bfloat16, device="cuda")  # D = V = 32: not implemented
+    v = torch.zeros((64, 1, 32), dtype=torch.bfloat16, device="cuda")
     sl = torch.ones(1, dtype=torch.float32, device="cuda")
+    with pytest.raises(lap.LaError) as e:
+        lap.la_prefill_fwd(q, q, v, sl, 1.0, seq_len=64)
+    assert e.value.name == "LA_ERR_UNSUPPORTED"
+    q = torch.zeros((64, 1, 64), dtype=torch.bfloat16, device="cuda")  # D = 64 with V = 128
+    v = torch.zeros((64, 1, 128), dtype=torch.bfloat16, device="cuda")
     with pytest.raises(lap.LaError) as e:
         lap.la_prefill_fwd(q, q, v, sl, 1.0, seq_len=64)
     assert e.value.name == "LA_ERR_UNSUPPORTED"

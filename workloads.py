@@ -67,6 +67,8 @@ class Problem:
     want_final: bool = True
     in_place: bool = False              # final states scattered into the h0 pool
     extra: dict = field(default_factory=dict)
+    D: int = 128                        # q/k head dimension
+    V: int = 128                        # value head dimension
 
     @property
     def tokens(self) -> int:
@@ -97,20 +99,21 @@ class Problem:
         return np.full(self.B, self.T, dtype=np.int64)
 
 
-def make_qkv(rng, tokens, H, HV):
-    q = bf16_bits(_unit_rows(rng, (tokens, H, D)))
-    k = bf16_bits(_unit_rows(rng, (tokens, H, D)))
-    v = bf16_bits(rng.standard_normal((tokens, HV, V), dtype=np.float32))
+def make_qkv(rng, tokens, H, HV, d=D, v_dim=V):
+    q = bf16_bits(_unit_rows(rng, (tokens, H, d)))
+    k = bf16_bits(_unit_rows(rng, (tokens, H, d)))
+    v = bf16_bits(rng.standard_normal((tokens, HV, v_dim), dtype=np.float32))
     return q, k, v
 
 
-def make_states(rng, P, HV, std=0.02):
-    return (rng.standard_normal((P, HV, V, D), dtype=np.float32) * np.float32(std)).astype(np.float32)
+def make_states(rng, P, HV, std=0.02, d=D, v_dim=V):
+    return (rng.standard_normal((P, HV, v_dim, d), dtype=np.float32) * np.float32(std)).astype(np.float32)
 
 
 def custom(seed, lengths=None, B=None, T=None, H=4, HV=4, scale=None, with_h0=True,
-           pool=None, indices=None, want_final=True, in_place=False, slopes=None, name="custom"):
-    """A small problem of any shape: fixed (B, T) or packed (``lengths``)."""
+           pool=None, indices=None, want_final=True, in_place=False, slopes=None, name="custom", D=D):
+    """A small problem of any shape: fixed (B, T) or packed (``lengths``); head dimension
+    D = V (128 or 64)."""
     rng = np.random.default_rng(seed)
     if lengths is not None:
         lengths = np.asarray(lengths, dtype=np.int64)
@@ -124,13 +127,14 @@ def custom(seed, lengths=None, B=None, T=None, H=4, HV=4, scale=None, with_h0=Tr
         tokens = B * T
         N = B
         Bv, Tv = B, T
-    q, k, v = make_qkv(rng, tokens, H, HV)
+    d = D
+    q, k, v = make_qkv(rng, tokens, H, HV, d, d)
     sl = slopes_for(HV) if slopes is None else np.asarray(slopes, dtype=np.float32)
-    sc = 1.0 / math.sqrt(D) if scale is None else scale
+    sc = 1.0 / math.sqrt(d) if scale is None else scale
     P = pool if pool is not None else N
-    h0 = make_states(rng, P, HV) if with_h0 else None
+    h0 = make_states(rng, P, HV, d=d, v_dim=d) if with_h0 else None
     idx = None if indices is None else np.asarray(indices, dtype=np.int32)
-    return Problem(name, q, k, v, sl, sc, H, HV, Bv, Tv, cu, idx, h0, want_final, in_place)
+    return Problem(name, q, k, v, sl, sc, H, HV, Bv, Tv, cu, idx, h0, want_final, in_place, D=d, V=d)
 
 
 def config(i: int) -> Problem:
