@@ -11,6 +11,8 @@ Contents:
     Description), evaluated token by token, and in the chunkwise form
     (intra (QK^T masked by the causal decay) V + inter lambda^(s+1) Q S, one
     state advance per chunk).
+  * ``backward`` -- gradients of a scalar loss through the same recurrence (dq, dk, dv and
+    dh0 from dL/do and dL/dh_final), one forward and one reverse sweep per unit.
   * ``closed_form`` -- the direct O(T^2) sum printed on page "[LA] Lightning
     Attention MTP decode + KVBuffer parallel verify / commit", Description
     ("Closed form used by verify"):
@@ -65,6 +67,9 @@ def _load():
             lib.la_oracle_tokenwise.restype = ctypes.c_int
             lib.la_oracle_chunked.argtypes = common + [ctypes.c_int, ctypes.c_int]
             lib.la_oracle_chunked.restype = ctypes.c_int
+            lib.la_oracle_backward.argtypes = [fp, fp, fp, fp, ctypes.c_double, dp, fp, dp, ip, ip] + \
+                [ctypes.c_int] * 7 + [dp, dp, dp, dp, ctypes.c_int]
+            lib.la_oracle_backward.restype = ctypes.c_int
             lib.la_oracle_max_threads.argtypes = []
             lib.la_oracle_max_threads.restype = ctypes.c_int
             _lib = lib
@@ -177,3 +182,45 @@ def closed_form(q, k, v, slope, scale, h0=None):
     for i in range(T):
         hT = hT + lam ** (T - 1 - i) * np.outer(v[i], k[i])
     return o, hT
+
+
+def backward(q, k, v, slopes, scale, dout, h0=None, dh_final=None, state_indices=None, cu_seqlens=None,
+             T=None, want_dh0=True, nthreads=0):
+    """Gradients of a scalar loss L through the recurrence, FP64 (``la_oracle.c``,
+    la_oracle_backward): given dout = dL/do [tokens, HV, V] and dh_final = dL/dh_final
+    [P, HV, V, D] (or None = 0), returns (dq [tokens, H, D], dk [tokens, H, D],
+    dv [tokens, HV, V], dh0 [P, HV, V, D] or None).  Rows of padded sequences and unselected
+    slots are NaN."""
+    q, k, v, slopes, dout = _f32(q), _f32(k), _f32(v), _f32(slopes), _f32(dout)
+    h0 = None if h0 is None else np.ascontiguousarray(h0, dtype=np.float64)
+    dh_final = None if dh_final is None else np.ascontiguousarray(dh_final, dtype=np.float64)
+    tokens, H, D = q.shape
+    _, HV, V = v.shape
+    if cu_seqlens is not None:
+        cu_seqlens = np.ascontiguousarray(cu_seqlens, dtype=np.int32)
+        N = cu_seqlens.shape[0] - 1
+        T = 0
+    else:
+        if T is None:
+            raise ValueError("fixed-length mode needs T")
+        N = tokens // T if T > 0 else 0
+    if state_indices is not None:
+        state_indices = np.ascontiguousarray(state_indices, dtype=np.int32)
+        pool = next((a.shape[0] for a in (h0, dh_final) if a is not None), int(state_indices.max(initial=-1)) + 1)
+    else:
+        pool = N
+    dq = np.full((tokens, H, D), np.nan)
+    dk = np.full((tokens, H, D), np.nan)
+    dv = np.full((tokens, HV, V), np.nan)
+    dh0 = np.full((pool, HV, V, D), np.nan) if want_dh0 else None
+    lib = _load()
+    rc = lib.la_oracle_backward(_ptr(q, ctypes.c_float), _ptr(k, ctypes.c_float), _ptr(v, ctypes.c_float),
+                                _ptr(slopes, ctypes.c_float), float(scale), _ptr(h0, ctypes.c_double),
+                                _ptr(dout, ctypes.c_float), _ptr(dh_final, ctypes.c_double),
+                                _ptr(state_indices, ctypes.c_int32), _ptr(cu_seqlens, ctypes.c_int32),
+                                int(N), int(T), int(H), int(HV), int(D), int(V), int(pool),
+                                _ptr(dq, ctypes.c_double), _ptr(dk, ctypes.c_double), _ptr(dv, ctypes.c_double),
+                                _ptr(dh0, ctypes.c_double), int(nthreads))
+    if rc != 0:
+        raise ValueError(f"oracle rejected the problem: {ERRORS.get(rc, rc)}")
+    return dq, dk, dv, dh0

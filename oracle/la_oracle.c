@@ -330,6 +330,162 @@ int la_oracle_chunked(const float *q, const float *k, const float *v, const floa
     return run(&p, chunk, nthreads);
 }
 
+/* ---- backward: gradients of a scalar loss through the recurrence ----------
+ *
+ * The forward pass (tokens t = 0 .. L-1 of one sequence and value head, S_{-1} = h0):
+ *     S_t = lambda S_{t-1} + v_t k_t^T        (S stored [V][K])
+ *     o_t = scale S_t q_t                     h_final = S_{L-1}
+ * Given dout_t = dL/do_t and dh_final = dL/dh_final (or 0), the chain rule gives
+ *     dq_t = scale S_t^T dout_t
+ *     G_t  = dL/dS_t = scale dout_t q_t^T + lambda G_{t+1},   G_L = dh_final
+ *     dk_t = G_t^T v_t,    dv_t = G_t k_t,    dh0 = lambda G_0
+ * (an empty sequence passes dh_final through: dh0 = dh_final).  With value heads sharing a
+ * q/k head, dq and dk of that head are the sums over its value heads.  One forward sweep
+ * per unit carries S and gives dq; one reverse sweep carries G and gives dk, dv, dh0.
+ */
+static void unit_backward(const lao_problem *p, const float *dout, const double *dh_final, double *dq, double *dk,
+                          double *dv, double *dh0, int n, int hv, double *M, double *acc)
+{
+    const int D = p->D, V = p->V, H = p->H, HV = p->HV;
+    const int hq = hv / (HV / H);
+    const double lam = exp(-(double)p->slopes[hv]);
+    int64_t bos, len;
+    seq_bounds(p, n, &bos, &len);
+    const int64_t slot = slot_of(p, n);
+    /* forward sweep: M[v][k] = S_t, dq_t += scale S_t^T dout_t */
+    if (p->h0) {
+        const double *src = p->h0 + ((size_t)slot * HV + hv) * (size_t)V * D;
+        memcpy(M, src, sizeof(double) * (size_t)V * D);
+    } else {
+        memset(M, 0, sizeof(double) * (size_t)V * D);
+    }
+    for (int64_t t = 0; t < len; ++t) {
+        const float *kt = p->k + ((size_t)(bos + t) * H + hq) * D;
+        const float *vt = p->v + ((size_t)(bos + t) * HV + hv) * V;
+        const float *dot = dout + ((size_t)(bos + t) * HV + hv) * V;
+        for (int vv = 0; vv < V; ++vv) {
+            double *row = M + (size_t)vv * D;
+            for (int kk = 0; kk < D; ++kk)
+                row[kk] = lam * row[kk] + (double)vt[vv] * (double)kt[kk];
+        }
+        double *dqt = dq + ((size_t)(bos + t) * H + hq) * D;
+        for (int kk = 0; kk < D; ++kk)
+            acc[kk] = 0.0;
+        for (int vv = 0; vv < V; ++vv) {
+            const double g = (double)dot[vv];
+            const double *row = M + (size_t)vv * D;
+            for (int kk = 0; kk < D; ++kk)
+                acc[kk] = acc[kk] + row[kk] * g;
+        }
+        for (int kk = 0; kk < D; ++kk)
+            dqt[kk] = dqt[kk] + p->scale * acc[kk];
+    }
+    /* reverse sweep: M[v][k] = G_t */
+    if (dh_final) {
+        const double *src = dh_final + ((size_t)slot * HV + hv) * (size_t)V * D;
+        memcpy(M, src, sizeof(double) * (size_t)V * D);
+    } else {
+        memset(M, 0, sizeof(double) * (size_t)V * D);
+    }
+    for (int64_t t = len - 1; t >= 0; --t) {
+        const float *qt = p->q + ((size_t)(bos + t) * H + hq) * D;
+        const float *kt = p->k + ((size_t)(bos + t) * H + hq) * D;
+        const float *vt = p->v + ((size_t)(bos + t) * HV + hv) * V;
+        const float *dot = dout + ((size_t)(bos + t) * HV + hv) * V;
+        /* G_t = scale dout_t q_t^T + lambda G_{t+1} (M holds lambda-free G_{t+1} here) */
+        for (int vv = 0; vv < V; ++vv) {
+            const double g = p->scale * (double)dot[vv];
+            double *row = M + (size_t)vv * D;
+            for (int kk = 0; kk < D; ++kk)
+                row[kk] = row[kk] + g * (double)qt[kk];
+        }
+        /* dk_t += G_t^T v_t, dv_t = G_t k_t */
+        double *dkt = dk + ((size_t)(bos + t) * H + hq) * D;
+        for (int kk = 0; kk < D; ++kk)
+            acc[kk] = 0.0;
+        for (int vv = 0; vv < V; ++vv) {
+            const double x = (double)vt[vv];
+            const double *row = M + (size_t)vv * D;
+            for (int kk = 0; kk < D; ++kk)
+                acc[kk] = acc[kk] + row[kk] * x;
+        }
+        for (int kk = 0; kk < D; ++kk)
+            dkt[kk] = dkt[kk] + acc[kk];
+        double *dvt = dv + ((size_t)(bos + t) * HV + hv) * V;
+        for (int vv = 0; vv < V; ++vv) {
+            const double *row = M + (size_t)vv * D;
+            double d = 0.0;
+            for (int kk = 0; kk < D; ++kk)
+                d = d + row[kk] * (double)kt[kk];
+            dvt[vv] = d;
+        }
+        /* carry lambda G_t to the previous token */
+        for (size_t e = 0; e < (size_t)V * D; ++e)
+            M[e] = lam * M[e];
+    }
+    if (dh0) {
+        double *dst = dh0 + ((size_t)slot * HV + hv) * (size_t)V * D;
+        memcpy(dst, M, sizeof(double) * (size_t)V * D);
+    }
+}
+
+/*
+ * Arguments as la_oracle_tokenwise, plus (host pointers, row-major, caller-owned):
+ *   dout       float [tokens, HV, V]      dL/do (BF16 values upcast)
+ *   dh_final   double [P, HV, V, D] or NULL   dL/dh_final (zero when NULL)
+ *   dq, dk     double [tokens, H, D]      rows of padded sequences untouched
+ *   dv         double [tokens, HV, V]     rows of padded sequences untouched
+ *   dh0        double [P, HV, V, D] or NULL; only the selected slots written
+ */
+int la_oracle_backward(const float *q, const float *k, const float *v, const float *slopes, double scale,
+                       const double *h0, const float *dout, const double *dh_final,
+                       const int32_t *state_indices, const int32_t *cu_seqlens, int N, int T, int H, int HV,
+                       int D, int V, int pool_size, double *dq, double *dk, double *dv, double *dh0, int nthreads)
+{
+    lao_problem p = {q, k, v, slopes, h0, state_indices, cu_seqlens, scale,
+                     N, T, H, HV, D, V, pool_size, NULL, NULL};
+    int rc = validate(&p);
+    if (rc != LAO_OK)
+        return rc;
+    const int G = HV / H;
+    const int64_t groups = (int64_t)N * H; /* one (sequence, q/k head) per task: no shared writes */
+    int failed = 0;
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads) reduction(| : failed)
+#endif
+    {
+        double *M = (double *)malloc(sizeof(double) * (size_t)V * D);
+        double *acc = (double *)malloc(sizeof(double) * (size_t)(D > V ? D : V));
+        const int ok = M && acc;
+        if (!ok)
+            failed = 1;
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int64_t u = 0; u < groups; ++u) {
+            if (!ok)
+                continue;
+            const int n = (int)(u / H), hq = (int)(u % H);
+            if (slot_of(&p, n) < 0)
+                continue; /* padded sequence: nothing read, nothing written */
+            int64_t bos, len;
+            seq_bounds(&p, n, &bos, &len);
+            for (int64_t t = 0; t < len; ++t) {
+                memset(dq + ((size_t)(bos + t) * H + hq) * D, 0, sizeof(double) * (size_t)D);
+                memset(dk + ((size_t)(bos + t) * H + hq) * D, 0, sizeof(double) * (size_t)D);
+            }
+            for (int g = 0; g < G; ++g)
+                unit_backward(&p, dout, dh_final, dq, dk, dv, dh0, n, hq * G + g, M, acc);
+        }
+        free(M);
+        free(acc);
+    }
+    (void)nthreads;
+    return failed ? LAO_NO_MEMORY : LAO_OK;
+}
+
 int la_oracle_max_threads(void)
 {
 #ifdef _OPENMP

@@ -287,3 +287,95 @@ def test_bf16_output_floor_tiny_workload():
     ob = W.bf16_to_f32(W.bf16_bits(o.astype(np.float32))).astype(np.float64)
     floor = rel(ob, o)
     assert 5e-4 < floor < 2e-3, floor
+
+
+# ---- backward: the oracle's gradients against finite differences of its forward pass ----
+#
+# L = sum_t o_t . dout_t + sum over selected slots of h_final . dh_final is linear in every
+# single element of q, k, v and h0 (o_t is a sum of products with one factor from each of
+# q, k, v, or of q and h0), so a central difference with any step is exact up to rounding.
+
+def _fd_loss(q, k, v, sl, scale, h0, idx, cu, dout, dhf):
+    o, hf = oracle.tokenwise(q, k, v, sl, scale, h0=h0, state_indices=idx, cu_seqlens=cu,
+                             h_final=np.zeros_like(h0))
+    sel = [int(s) for s in idx if s >= 0]
+    live_rows = ~np.isnan(o[:, 0, 0])
+    return float(np.sum(o[live_rows] * dout[live_rows])) + float(np.sum(hf[sel] * dhf[sel]))
+
+
+def test_backward_matches_finite_differences_of_the_forward():
+    rng = np.random.default_rng(71)
+    lengths = [3, 0, 4, 2]
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    tok, H, HV, D, V, P = int(cu[-1]), 1, 2, 3, 2, 6
+    q = rng.standard_normal((tok, H, D)).astype(np.float32)
+    k = rng.standard_normal((tok, H, D)).astype(np.float32)
+    v = rng.standard_normal((tok, HV, V)).astype(np.float32)
+    dout = rng.standard_normal((tok, HV, V)).astype(np.float32)
+    sl = np.array([0.3, 1.1], np.float32)
+    h0 = rng.standard_normal((P, HV, V, D))
+    dhf = rng.standard_normal((P, HV, V, D))
+    idx = np.array([4, 1, -1, 0], np.int32)  # sequence 2 padded
+    scale = 0.75
+    dq, dk, dv, dh0 = oracle.backward(q, k, v, sl, scale, dout, h0=h0, dh_final=dhf, state_indices=idx,
+                                      cu_seqlens=cu)
+    base = (q, k, v, sl, scale, h0, idx, cu, dout, dhf)
+    eps = 0.5  # exact in float32; L is linear in each element
+
+    def fd(pos, index):
+        # the steps actually taken (x +- eps rounds in float32): L is linear in the element, so
+        # the difference quotient over the exact step is the derivative
+        args = list(base)
+        x = args[pos].copy()
+        x0 = float(x[index])
+        x[index] = x0 + eps
+        up = float(x[index])
+        args[pos] = x
+        lp = _fd_loss(*args)
+        x[index] = x0 - eps
+        dn = float(x[index])
+        lm = _fd_loss(*args)
+        return (lp - lm) / (up - dn)
+
+    live = np.ones(tok, bool)
+    live[cu[2]:cu[3]] = False
+    for name, pos, grad in (("q", 0, dq), ("k", 1, dk), ("v", 2, dv)):
+        for index in np.ndindex(*grad.shape):
+            if not live[index[0]]:
+                assert np.isnan(grad[index]), f"d{name} written for a padded row"
+                continue
+            ref = fd(pos, index)
+            assert abs(grad[index] - ref) <= 1e-9 * (1 + abs(ref)), (name, index, grad[index], ref)
+    for slot in range(P):
+        for index in np.ndindex(HV, V, D):
+            if slot not in (4, 1, 0):
+                assert np.isnan(dh0[(slot,) + index]), "dh0 written for an unselected slot"
+                continue
+            ref = fd(5, (slot,) + index)
+            assert abs(dh0[(slot,) + index] - ref) <= 1e-9 * (1 + abs(ref)), ("h0", slot, index)
+
+
+def test_backward_lambda_one_matches_masked_linear_attention_gradients():
+    # slope 0: o = scale (tril(Q K^T) V + Q h0^T) and h_final = h0 + V^T K, whose gradients are
+    # plain masked matrix products
+    rng = np.random.default_rng(72)
+    T, D, V = 9, 5, 4
+    q = rng.standard_normal((T, 1, D)).astype(np.float32)
+    k = rng.standard_normal((T, 1, D)).astype(np.float32)
+    v = rng.standard_normal((T, 1, V)).astype(np.float32)
+    dout = rng.standard_normal((T, 1, V)).astype(np.float32)
+    h0 = rng.standard_normal((1, 1, V, D))
+    dhf = rng.standard_normal((1, 1, V, D))
+    scale = 0.6
+    dq, dk, dv, dh0 = oracle.backward(q, k, v, np.zeros(1, np.float32), scale, dout, h0=h0, dh_final=dhf, T=T)
+    Q, K, Vm, dO = (x[:, 0].astype(np.float64) for x in (q, k, v, dout))
+    Mk = np.tril(np.ones((T, T)))
+    H0, dHf = h0[0, 0], dhf[0, 0]
+    dq_ref = scale * (Mk * (dO @ Vm.T)) @ K + scale * dO @ H0
+    dk_ref = scale * (Mk * (dO @ Vm.T)).T @ Q + Vm @ dHf
+    dv_ref = scale * (Mk * (Q @ K.T)).T @ dO + K @ dHf.T
+    dh0_ref = scale * dO.T @ Q + dHf
+    assert np.allclose(dq[:, 0], dq_ref, rtol=1e-12, atol=1e-12)
+    assert np.allclose(dk[:, 0], dk_ref, rtol=1e-12, atol=1e-12)
+    assert np.allclose(dv[:, 0], dv_ref, rtol=1e-12, atol=1e-12)
+    assert np.allclose(dh0[0, 0], dh0_ref, rtol=1e-12, atol=1e-12)
