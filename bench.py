@@ -528,6 +528,8 @@ def run_sweep(args):
         run_decode_sweep(args, device, stream, flush, hbm, hbm_kind)
     if args.sweep_what in ("all", "segmented"):
         run_segment_sweep(args, device, stream, flush, hbm, hbm_kind, tflops, tf_kind)
+    if args.sweep_what in ("all", "backward"):
+        run_backward_sweep(args, device, stream, flush, hbm, hbm_kind)
 
 
 def run_decode_sweep(args, device, stream, flush, hbm, hbm_kind):
@@ -657,6 +659,59 @@ def run_segment_sweep(args, device, stream, flush, hbm, hbm_kind, tflops, tf_kin
                           "steps": args.sweep_steps, "l2": "flushed between launches (256 MB write)"}), flush=True)
 
 
+def run_backward_sweep(args, device, stream, flush, hbm, hbm_kind):
+    """The backward pass (la_prefill_bwd) on the bench shape B=2, T=8192, H=HV=64, D=V=128 with
+    h0, dL/do and dL/dh_final given and dh0 returned.  Algorithmic bytes: q, k, v, dout read and
+    dq, dk, dv written once, h0 and dh_final read and dh0 written once; the three forward runs,
+    the token reversals and the state transposes it is built from move more."""
+    import numpy as np
+    import torch
+
+    import linear_attention_prefill_chunkwise_gb300 as lap
+    import workloads as W
+
+    p = W.config(2)
+    rng = np.random.default_rng(4402)
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+    q, k, v = bf(p.q_bits), bf(p.k_bits), bf(p.v_bits)
+    dout = bf(W.bf16_bits(rng.standard_normal(p.v_bits.shape, dtype=np.float32)))
+    sl = torch.from_numpy(p.slopes).to(device)
+    h0 = torch.from_numpy(p.h0).to(device)
+    dhf = torch.randn(h0.shape, generator=torch.Generator(device=device).manual_seed(4403), device=device) * 0.1
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    dh0 = torch.empty_like(h0)
+    ws = torch.empty(lap.la_prefill_bwd_workspace(B, T, H, D, B, True, True), dtype=torch.uint8, device=device)
+
+    def call():
+        lap.la_prefill_bwd(q, k, v, sl, p.scale, dout, h0=h0, dh_final=dhf, dq=dq, dk=dk, dv=dv, dh0=dh0, seq_len=T,
+                           workspace=ws, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            call()
+        times = []
+        for _ in range(args.sweep_steps):
+            flush.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            call()
+            e1.record(stream)
+            times.append((e0, e1))
+    torch.cuda.synchronize(device)
+    ms = statistics.fmean(a.elapsed_time(b) for a, b in times)
+    nbytes = 7 * TOKENS * HV * V * 2 + 3 * B * HV * V * D * 4
+    t_roof = nbytes / (hbm * 1e9)
+    print(json.dumps({"sweep": True, "op": "la_prefill_bwd", "workload": WORKLOAD + ", dL/do and dL/dh_final in, dh0 out",
+                      "ms": round(ms, 5), "tokens_per_s": round(TOKENS / (ms / 1e3), 1), "alg_bytes": nbytes,
+                      "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1), "roofline_ms": round(t_roof * 1e3, 5),
+                      "frac": round(t_roof * 1e3 / ms, 4), "bound": "hbm",
+                      "peaks": {"hbm_gbs": hbm, "hbm_source": hbm_kind}, "steps": args.sweep_steps,
+                      "l2": "flushed between launches (256 MB write)"}), flush=True)
+
+
 def cpu_baseline(p, heads):
     """The FP64 oracle on the host cores over a bounded sample: both sequences, all T tokens,
     the first `heads` of the 64 heads.  Reported in full-workload tokens/s (a token = all 64 heads)."""
@@ -743,7 +798,7 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="time every workload (1..5) instead, one JSON line each (not the headline line)")
     ap.add_argument("--sweep-steps", type=int, default=50)
-    ap.add_argument("--sweep-what", choices=["all", "prefill", "decode", "segmented"], default="all",
+    ap.add_argument("--sweep-what", choices=["all", "prefill", "decode", "segmented", "backward"], default="all",
                     help="with --sweep: the five prefill workloads, the speculative-decoding ops, the "
                          "segmented prefill on few-chain batches, or all of them")
     args = ap.parse_args()

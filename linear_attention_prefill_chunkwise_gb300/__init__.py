@@ -1,6 +1,7 @@
 """GB300 (sm_103a) Lightning Attention chunkwise prefill and speculative-decoding ops.
 
-``la_prefill_fwd`` (include/la_prefill.h), ``la_prefill_fwd_segmented``,
+``la_prefill_fwd`` (include/la_prefill.h), ``la_prefill_bwd`` (include/la_backward.h),
+``la_prefill_fwd_segmented``,
 ``la_prefill_fwd_segmented_static`` and ``la_prefill_segmented_workspace``
 (include/la_segment.h) and ``la_decode_mtp``,
 ``la_verify``, ``la_commit`` (include/la_decode.h) are thin ctypes bindings of the C
@@ -17,7 +18,8 @@ import threading
 
 from . import build as _build
 
-__all__ = ["la_prefill_fwd", "la_prefill_fwd_segmented", "la_prefill_fwd_segmented_static",
+__all__ = ["la_prefill_fwd", "la_prefill_fwd_segmented", "la_prefill_fwd_segmented_static", "la_prefill_bwd",
+           "la_prefill_bwd_workspace",
            "la_prefill_segmented_workspace", "la_decode_mtp", "la_verify", "la_commit", "LaError", "load_library", "SCHEDULES", "DEV_ERR_BAD_SEQLENS",
            "DEV_ERR_BAD_INDEX", "DEV_ERR_TIMEOUT", "EXPORTED_SYMBOLS"]
 
@@ -28,7 +30,7 @@ DEV_ERR_TIMEOUT = 4
 EXPORTED_SYMBOLS = ("la_prefill_fwd", "la_status_string", "la_last_error", "la_prefill_smem_bytes",
                     "la_decode_mtp", "la_verify",
                     "la_commit", "la_prefill_segmented_workspace", "la_prefill_fwd_segmented",
-                    "la_prefill_fwd_segmented_static")
+                    "la_prefill_fwd_segmented_static", "la_prefill_bwd_workspace", "la_prefill_bwd")
 
 _lock = threading.Lock()
 _lib = None
@@ -79,6 +81,11 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.la_prefill_fwd_segmented_static.argtypes = [vp, vp, vp, fp, ctypes.c_float, fp, i32p, i32p, vp,
                                                             fp] + [ctypes.c_int] * 9 + [vp, vp]
             lib.la_prefill_fwd_segmented_static.restype = ctypes.c_int
+            lib.la_prefill_bwd_workspace.argtypes = [ctypes.c_int] * 7 + [vp]
+            lib.la_prefill_bwd_workspace.restype = ctypes.c_int
+            lib.la_prefill_bwd.argtypes = [vp, vp, vp, fp, ctypes.c_float, fp, vp, fp, i32p, i32p, vp, vp, vp, fp] + \
+                [ctypes.c_int] * 8 + [vp, ctypes.c_size_t, vp, vp]
+            lib.la_prefill_bwd.restype = ctypes.c_int
             _lib = lib
         return _lib
 
@@ -241,6 +248,56 @@ def la_prefill_fwd_segmented_static(q, k, v, slopes, scale, h0=None, state_indic
     if st != 0:
         _raise(lib, st)
     return o
+
+
+def la_prefill_bwd_workspace(B, T, H, D, pool_size, has_h0, has_dh_final):
+    """Bytes of device workspace la_prefill_bwd needs for these sizes."""
+    lib = load_library()
+    nbytes = ctypes.c_size_t(0)
+    st = lib.la_prefill_bwd_workspace(int(B), int(T), int(H), int(D), int(pool_size), int(bool(has_h0)),
+                                      int(bool(has_dh_final)), ctypes.byref(nbytes))
+    if st != 0:
+        _raise(lib, st)
+    return nbytes.value
+
+
+def la_prefill_bwd(q, k, v, slopes, scale, dout, h0=None, dh_final=None, state_indices=None, cu_seqlens=None,
+                   dq=None, dk=None, dv=None, dh0=None, seq_len=None, workspace=None, dev_error=None, stream=None):
+    """Gradients of the prefill (include/la_backward.h): given dout = dL/do [tokens, H, D] BF16
+    and dh_final = dL/dh_final [P, H, D, D] FP32 (or None), returns (dq, dk, dv, dh0) with the
+    layouts of q, k, v and h0 (dh0 only when a tensor is passed in).  One value head per q/k
+    head; the other arguments as la_prefill_fwd.  ``workspace`` is a CUDA uint8 tensor of at
+    least la_prefill_bwd_workspace(...) bytes, allocated here when None."""
+    import torch
+    lib = load_library()
+    _check(dout, "dout", torch.bfloat16, 3)
+    _check(dh_final, "dh_final", torch.float32, 4)
+    _check(dh0, "dh0", torch.float32, 4)
+    if dout is None or dout.shape != v.shape:
+        raise ValueError("dout must have the shape of v")
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for t, name, ref in ((dq, "dq", q), (dk, "dk", k), (dv, "dv", v)):
+        _check(t, name, torch.bfloat16, 3)
+        if t.shape != ref.shape:
+            raise ValueError(f"{name} must have the shape of its input")
+    # the forward's checks and sizes: dv has the layout of o, dh0 (else dh_final) that of h_final
+    _, B, T, N, H, HV, D, V, pool, stream = _prefill_args(q, k, v, slopes, h0, state_indices, cu_seqlens, dv,
+                                                          dh0 if dh0 is not None else dh_final, seq_len, dev_error,
+                                                          stream)
+    if workspace is None:
+        nbytes = la_prefill_bwd_workspace(B, T, H, D, pool, h0 is not None, dh_final is not None)
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    _check(workspace, "workspace", torch.uint8, 1)
+    st = lib.la_prefill_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes), ctypes.c_float(scale), _ptr(h0), _ptr(dout),
+                            _ptr(dh_final), _ptr(state_indices), _ptr(cu_seqlens), _ptr(dq), _ptr(dk), _ptr(dv),
+                            _ptr(dh0), int(B), int(T), int(N), int(H), int(HV), int(D), int(V), int(pool),
+                            _ptr(workspace), ctypes.c_size_t(workspace.numel()), _ptr(dev_error),
+                            ctypes.c_void_p(stream))
+    if st != 0:
+        _raise(lib, st)
+    return dq, dk, dv, dh0
 
 
 def _decode_common(q, k, v, slopes, state, state_indices, T, dev_error, stream):
