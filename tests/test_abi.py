@@ -214,3 +214,42 @@ def test_segmented_no_device_is_reported():
         pytest.skip("a GPU is present")
     assert call_segmented() == LA_CUDA          # workspace fine: the first device query fails
     assert call_segmented(seg=0) == LA_CUDA     # automatic length needs the device
+
+
+def call_backward(**over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, slopes=FAKE, scale=1.0, h0=None, dout=FAKE, dhf=None, idx=None, cu=None,
+             dq=FAKE, dk=FAKE, dv=FAKE, dh0=None, B=2, T=128, N=2, H=2, HV=2, D=128, V=128, P=0, ws=FAKE,
+             wsb=1 << 40, err=None, stream=None)
+    a.update(over)
+    lib = lap.load_library()
+    return lib.la_prefill_bwd(a["q"], a["k"], a["v"], a["slopes"], ctypes.c_float(a["scale"]), a["h0"], a["dout"],
+                              a["dhf"], a["idx"], a["cu"], a["dq"], a["dk"], a["dv"], a["dh0"], a["B"], a["T"],
+                              a["N"], a["H"], a["HV"], a["D"], a["V"], a["P"], a["ws"], a["wsb"], a["err"],
+                              a["stream"])
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(H=1, HV=2), LA_UNSUPPORTED),           # one value head per q/k head only
+    (dict(D=64), LA_UNSUPPORTED),                # D != V
+    (dict(D=256, V=256), LA_UNSUPPORTED),
+    (dict(dout=None), LA_INVALID),
+    (dict(dk=FAKE + 2), LA_INVALID),             # misaligned
+    (dict(dhf=FAKE, scale=0.0, h0=FAKE, P=2), LA_INVALID),  # dh_final needs scale != 0
+    (dict(wsb=1024), LA_INVALID),                # workspace too small
+    (dict(ws=FAKE + 16), LA_INVALID),            # workspace not 256-byte aligned
+    (dict(N=3), LA_INVALID),
+])
+def test_backward_host_validation(over, status):
+    assert call_backward(**over) == status
+    assert lap.load_library().la_last_error() != b""
+
+
+def test_backward_empty_batch_is_a_no_op():
+    assert call_backward(N=0, B=0) == LA_OK
+
+
+def test_backward_workspace_size():
+    # six reversed [tokens, H, D] BF16 tensors, a transposed h0 and two forms of dh_final
+    nbytes = lap.la_prefill_bwd_workspace(2, 8192, 64, 128, 2, True, True)
+    assert nbytes == 6 * 2 * 8192 * 64 * 128 * 2 + 3 * 2 * 64 * 128 * 128 * 4
+    assert lap.la_prefill_bwd_workspace(1, 100, 2, 64, 0, False, False) == 6 * ((100 * 2 * 64 * 2 + 255) // 256 * 256)
