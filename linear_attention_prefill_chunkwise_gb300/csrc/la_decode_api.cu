@@ -39,8 +39,9 @@ la_status launch(const lad::Params& p, void* stream) {
   la_host::DeviceState* ds = nullptr;
   la_status st = la_host::current_device(g_dev, &ds, [] { return cudaSuccess; });
   if (st != LA_OK) return st;
-  const int grid = p.B * p.HV * lad::kSplit;
-  lad::la_tokenwise_kernel<kMode><<<grid, lad::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(p);
+  const int grid = lad::tokenwise_grid(p.B * p.HV * lad::kSplit, ds->sms);
+  lad::la_tokenwise_kernel<kMode>
+      <<<grid, lad::kThreads, lad::tokenwise_smem_bytes(), static_cast<cudaStream_t>(stream)>>>(p);
   const cudaError_t ce = cudaGetLastError();
   if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(ce));
   return LA_OK;

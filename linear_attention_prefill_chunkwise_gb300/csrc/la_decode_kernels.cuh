@@ -7,16 +7,19 @@
 // (request, value head) unit costs one read of its 64 KB FP32 state, T token updates and,
 // for decode and commit, one write of the state: the work is bound by the state traffic.
 // Each row of the state evolves, and gives its output, independently of the others, so a
-// unit is split over kSplit CTAs of 128 threads that each keep 64 state rows in registers
-// (more, smaller CTAs per SM overlap one CTA's state load with another's arithmetic).
-// Thread t of part h owns the 4 x 16 block of state rows v = 64 h + 4 (t / 8) .. +3 and
-// columns k = 16 (t % 8) .. +15, and for every token
+// unit is split over kSplit parts of 64 state rows, each held in the registers of one 128-thread
+// CTA.  The CTAs are persistent (kCtasPerSm per SM) and walk their parts; while a CTA applies
+// the tokens of one part, a single bulk copy brings the next part's 32 KB state slice into
+// shared memory, so every state load but the first overlaps arithmetic.  Thread t owns state
+// rows v = 64 h + 4 (t / 8) .. +3 and, of each, the four 16-byte column chunks
+// k = 32 m + 4 (t % 8) .. +3 (m = 0..3), and for every token
 //     S[v][k] = lambda S[v][k] + v_t[v] k_t[k]              (FP32, fused multiply-add)
 //     o_t[v]  = scale sum_k S[v][k] q_t[k]                    (8 column-group partial sums,
 //                                                             added across lanes t^1, t^2, t^4)
-// with the tokens' q, k, v staged in shared memory as FP32, 16 tokens at a time.  Each staged
-// k or q value feeds four rows, which keeps the shared-memory traffic per FMA low; the column
-// groups are padded to 20 floats so that the 8 groups a warp reads sit in distinct banks.
+// with the tokens' q, k, v staged in shared memory as FP32, 8 tokens at a time.  Each staged k
+// or q value feeds four rows, which keeps the shared-memory traffic per FMA low; the strided
+// column chunks make a warp read 128 contiguous bytes of a row at a time, from the staged
+// tokens and from the state slice alike, without bank conflicts.
 // The three operations run this same per-token code, so a commit of all T tokens leaves
 // bitwise the state a decode leaves, and verify's outputs are bitwise decode's.
 //
@@ -43,7 +46,6 @@ constexpr int kDim = 128;   // D = V = 128
 constexpr int kSplit = 2;                 // CTAs per (request, value head)
 constexpr int kRows = kDim / kSplit;      // state rows per CTA
 constexpr int kThreads = kRows / 4 * 8;   // 4 rows x 16 columns per thread
-constexpr int kTileT = 16;  // tokens staged in shared memory per pass
 
 enum Mode : int { kDecode = 0, kVerify = 1, kCommit = 2, kPrefill = 3 };
 
@@ -78,173 +80,254 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& x, float (&f)[8]) {
   }
 }
 
-constexpr int kGroupStride = 20;  // floats per staged 16-column group (16 + 4 padding)
+// Persistent form: a CTA walks its units (unit u = blockIdx.x + j gridDim.x; unit = (request,
+// value head, part)) and, while it applies the tokens of one unit, a single bulk copy brings the
+// next unit's 32 KB state slice into shared memory, so the state load of every unit but the
+// first overlaps the arithmetic of the previous one.  Thread t of a CTA owns rows
+// vbase + 4 (t / 8) .. + 3 and, of each row, the four 16-byte chunks of columns
+// 32 m + 4 (t % 8) .. + 3 (m = 0..3): a warp then reads 128 contiguous bytes per row from the
+// staged slice, the staged k and q, and writes 128 contiguous bytes per row of the state, all
+// without bank conflicts.
+constexpr int kTileTok = 8;  // tokens staged in shared memory per pass
+constexpr uint32_t kSliceBytes = kRows * kDim * 4;
+constexpr int kCtasPerSm = 4;
+
+struct __align__(128) TokSmem {
+  float pre[kRows * kDim];       // the next unit's state slice (bulk copy)
+  float ks[kTileTok][kDim];      // staged k (commit: from the KV buffer)
+  float qs[kTileTok][kDim];      // staged q
+  float vs[kTileTok][kRows];     // staged v, this CTA's rows
+  uint64_t bar;                  // slice landed (transaction bytes)
+  int abort;
+};
+
+__host__ __device__ constexpr int tokenwise_smem_bytes() { return static_cast<int>(sizeof(TokSmem)) + 128; }
+// Persistent grid: every unit of work, or kCtasPerSm CTAs per SM when there are more units.
+inline int tokenwise_grid(int units, int sms) { return units < sms * kCtasPerSm ? units : sms * kCtasPerSm; }
+
+// One unit's decoded description, identical for every thread of the CTA.
+struct TokUnit {
+  int b, hv, hq, part, slot, ntok;
+  size_t row0;
+  bool run, load, bad_index;
+};
 
 template <int kMode>
-__global__ void __launch_bounds__(kThreads, 2 * kSplit) la_tokenwise_kernel(const Params p) {
-  __shared__ __align__(16) float ks[kTileT][8 * kGroupStride];
-  __shared__ __align__(16) float qs[kTileT][8 * kGroupStride];
-  __shared__ __align__(16) float vs[kTileT][kRows];
-
-  const int unit = blockIdx.x / kSplit;  // b * HV + hv
-  const int part = blockIdx.x - unit * kSplit;
-  const int vbase = part * kRows;        // first state row (value index) of this CTA
-  const int b = unit / p.HV;
-  const int hv = unit - b * p.HV;
-  const int hq = hv / p.G;
-  int slot = b;
+__device__ __forceinline__ TokUnit tok_unit(const Params& p, int u) {
+  TokUnit w;
+  const int unit = u / kSplit;
+  w.part = u - unit * kSplit;
+  w.b = unit / p.HV;
+  w.hv = unit - w.b * p.HV;
+  w.hq = w.hv / p.G;
+  w.run = true;
+  w.bad_index = false;
+  w.slot = w.b;
   if (p.state_indices) {
-    slot = __ldg(p.state_indices + b);
-    if (slot < 0) return;  // padded request: nothing read or written
-    if (slot >= p.pool_size) {
-      if (threadIdx.x == 0 && p.dev_error) atomicOr(p.dev_error, 2);  // LA_DEV_ERR_BAD_INDEX
-      return;
-    }
+    w.slot = __ldg(p.state_indices + w.b);
+    w.bad_index = w.slot >= p.pool_size;
+    if (w.slot < 0 || w.bad_index) w.run = false;  // padded (nothing read or written), or a bad index
   }
-  int ntok = p.T;
-  size_t row0 = static_cast<size_t>(b) * p.T;  // first token row of this unit
+  w.ntok = p.T;
+  w.row0 = static_cast<size_t>(w.b) * p.T;
   if (kMode == kPrefill) {
     if (p.cu_seqlens) {
-      const int bb = __ldg(p.cu_seqlens + b), ee = __ldg(p.cu_seqlens + b + 1);
-      if (bb < 0 || ee < bb || ee > p.num_tokens) return;  // flagged by the chunkwise kernel
-      row0 = bb;
-      ntok = ee - bb;
+      const int bb = __ldg(p.cu_seqlens + w.b), ee = __ldg(p.cu_seqlens + w.b + 1);
+      if (bb < 0 || ee < bb || ee > p.num_tokens) w.run = false;  // flagged by the chunkwise kernel
+      w.row0 = bb;
+      w.ntok = ee - bb;
     }
-    if (ntok > p.short_max) return;  // the chunkwise kernel's unit
+    if (w.ntok > p.short_max) w.run = false;  // the chunkwise kernel's unit
   }
-  if (kMode == kCommit) {
-    ntok = min(max(__ldg(p.accepted_len + b), 0), p.T);
-    if (ntok == 0) return;  // nothing accepted: the state stays as it is
+  if (kMode == kCommit && w.run) {
+    w.ntok = min(max(__ldg(p.accepted_len + w.b), 0), p.T);
+    if (w.ntok == 0) w.run = false;  // nothing accepted: the state stays as it is
   }
+  w.load = w.run && (kMode != kPrefill || p.h0 != nullptr);
+  return w;
+}
 
+template <int kMode>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) la_tokenwise_kernel(const Params p) {
+  extern __shared__ uint8_t tok_raw[];
+  TokSmem& sm = *reinterpret_cast<TokSmem*>((reinterpret_cast<uintptr_t>(tok_raw) + 127) & ~uintptr_t(127));
   const int t = threadIdx.x;
-  const int cg = t & 7, rg = t >> 3;  // columns 16 cg .. +15, rows vbase + 4 rg .. +3
-  const float lam = expf(-__ldg(p.slopes + hv));
-  const uint64_t lam2 = f2_pack(lam, lam);
-
-  // ---- state block: S[r][j] pairs = (S[v + r][16 cg + 2 j], S[v + r][16 cg + 2 j + 1]), v = vbase + 4 rg
-  uint64_t S[4][8];
-  const size_t soff = ((static_cast<size_t>(slot) * p.HV + hv) * kDim + vbase + 4 * rg) * kDim + 16 * cg;
+  const int cg = t & 7, rg = t >> 3;  // chunks 32 m + 4 cg, rows vbase + 4 rg .. +3
+  const int units = p.B * p.HV * kSplit;
   const float* s_in = (kMode == kPrefill) ? p.h0 : p.state;
   float* s_out = (kMode == kPrefill) ? p.h_final : p.state;
-  if (kMode != kPrefill || s_in) {
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float4 x = __ldg(reinterpret_cast<const float4*>(s_in + soff + r * kDim) + i);
-        S[r][2 * i] = f2_pack(x.x, x.y);
-        S[r][2 * i + 1] = f2_pack(x.z, x.w);
-      }
-  } else {
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) S[r][j] = f2_pack(0.f, 0.f);
+  volatile int* abort = &sm.abort;
+  if (t == 0) {
+    lap::mbar_init(&sm.bar, 1);
+    sm.abort = 0;
+    lap::fence_mbar_init();
   }
+  __syncthreads();
 
-  const size_t qk_tok = static_cast<size_t>(p.H) * kDim;   // elements between tokens of q / k
-  const size_t v_tok = static_cast<size_t>(p.HV) * kDim;   // ... of v / o
-  for (int t0 = 0; t0 < ntok; t0 += kTileT) {
-    const int nt = min(kTileT, ntok - t0);
-    __syncthreads();  // the previous tile has been consumed
-    // Stage tokens t0 .. t0 + nt - 1: 16 bytes (8 values) per thread and array per step.
-    for (int e = t; e < nt * (kDim / 8); e += kThreads) {
-      const int i = e >> 4, c = e & 15;              // token, 8-value chunk (column group c / 2)
-      const int kpos = (c >> 1) * kGroupStride + 8 * (c & 1);
-      const bool vmine = c / (kRows / 8) == part;    // values 8c .. 8c + 7 are rows of this CTA
-      uint4 kx, vx = make_uint4(0u, 0u, 0u, 0u);
-      if (kMode == kCommit) {
-        const size_t brow = static_cast<size_t>(slot) * p.T + t0 + i;
-        kx = __ldg(reinterpret_cast<const uint4*>(p.kbuf + (brow * p.H + hq) * kDim) + c);
-        if (vmine) vx = __ldg(reinterpret_cast<const uint4*>(p.vbuf + (brow * p.HV + hv) * kDim) + c);
-      } else {
-        const size_t row = row0 + t0 + i;
-        kx = __ldg(reinterpret_cast<const uint4*>(p.k + row * qk_tok + static_cast<size_t>(hq) * kDim) + c);
-        if (vmine) vx = __ldg(reinterpret_cast<const uint4*>(p.v + row * v_tok + static_cast<size_t>(hv) * kDim) + c);
-        const uint4 qx = __ldg(reinterpret_cast<const uint4*>(p.q + row * qk_tok + static_cast<size_t>(hq) * kDim) + c);
-        float f[8];
-        bf16x8_to_f32(qx, f);
-        reinterpret_cast<float4*>(&qs[i][kpos])[0] = make_float4(f[0], f[1], f[2], f[3]);
-        reinterpret_cast<float4*>(&qs[i][kpos])[1] = make_float4(f[4], f[5], f[6], f[7]);
-        if (kMode == kVerify && p.kbuf) {  // the KV buffer copy (k once per q/k head, by part 0)
-          const size_t brow = static_cast<size_t>(slot) * p.T + t0 + i;
-          if (hv % p.G == 0 && part == 0)
-            reinterpret_cast<uint4*>(p.kbuf + (brow * p.H + hq) * kDim)[c] = kx;
-          if (vmine) reinterpret_cast<uint4*>(p.vbuf + (brow * p.HV + hv) * kDim)[c] = vx;
-        }
-      }
-      float f[8];
-      bf16x8_to_f32(kx, f);
-      reinterpret_cast<float4*>(&ks[i][kpos])[0] = make_float4(f[0], f[1], f[2], f[3]);
-      reinterpret_cast<float4*>(&ks[i][kpos])[1] = make_float4(f[4], f[5], f[6], f[7]);
-      if (vmine) {
-        bf16x8_to_f32(vx, f);
-        reinterpret_cast<float4*>(&vs[i][8 * c - vbase])[0] = make_float4(f[0], f[1], f[2], f[3]);
-        reinterpret_cast<float4*>(&vs[i][8 * c - vbase])[1] = make_float4(f[4], f[5], f[6], f[7]);
-      }
+  auto slice_of = [&](const TokUnit& w) {
+    return (static_cast<size_t>(w.slot) * p.HV + w.hv) * kDim * kDim + static_cast<size_t>(w.part) * kRows * kDim;
+  };
+  auto prefetch = [&](const TokUnit& w) {  // thread 0
+    lap::mbar_arrive_expect_tx(&sm.bar, kSliceBytes);
+    lap::bulk_copy_g2s(sm.pre, s_in + slice_of(w), kSliceBytes, &sm.bar);
+  };
+  // the first unit from u on (this CTA's stride) that runs; a bad state index is flagged
+  auto seek = [&](int u, TokUnit& w) {
+    for (; u < units; u += gridDim.x) {
+      w = tok_unit<kMode>(p, u);
+      if (w.bad_index && t == 0 && p.dev_error) atomicOr(p.dev_error, 2);  // LA_DEV_ERR_BAD_INDEX
+      if (w.run) return u;
     }
-    __syncthreads();
+    return units;
+  };
 
-    for (int i = 0; i < nt; ++i) {
-      const float4 vv = *reinterpret_cast<const float4*>(&vs[i][4 * rg]);
-      const float vr[4] = {vv.x, vv.y, vv.z, vv.w};
-      uint64_t kk[8];
-      {
-        const float4* kr = reinterpret_cast<const float4*>(&ks[i][cg * kGroupStride]);
+  TokUnit cur;
+  int u = seek(blockIdx.x, cur);
+  uint32_t phase = 0;
+  bool pending = false;  // a slice copy is in flight
+  if (u < units && cur.load && t == 0) prefetch(cur);
+  pending = u < units && cur.load;
+  while (u < units) {
+    TokUnit nxt;
+    const int un = seek(u + gridDim.x, nxt);
+    const int vbase = cur.part * kRows;
+    const float lam = expf(-__ldg(p.slopes + cur.hv));
+    const uint64_t lam2 = f2_pack(lam, lam);
+
+    // ---- this unit's state slice: S[r][2 m + h] = the pair (e = 2 h, 2 h + 1) of chunk m of row r
+    uint64_t S[4][8];
+    if (cur.load) {
+      // a bounded wait, its outcome agreed by the whole CTA before anyone leaves the loop
+      if (!__syncthreads_and(lap::mbar_wait(&sm.bar, phase, abort))) break;
+      phase ^= 1u;
+      pending = false;
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float4 x = kr[j];
-          kk[2 * j] = f2_pack(x.x, x.y);
-          kk[2 * j + 1] = f2_pack(x.z, x.w);
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const float4 x = *reinterpret_cast<const float4*>(&sm.pre[(4 * rg + r) * kDim + 32 * m + 4 * cg]);
+          S[r][2 * m] = f2_pack(x.x, x.y);
+          S[r][2 * m + 1] = f2_pack(x.z, x.w);
+        }
+    } else {
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) S[r][j] = f2_pack(0.f, 0.f);
+    }
+    __syncthreads();  // every thread holds its part of the slice: the buffer is free
+    if (un < units && nxt.load) {
+      if (t == 0) prefetch(nxt);
+      pending = true;
+    }
+
+    const size_t qk_tok = static_cast<size_t>(p.H) * kDim;
+    const size_t v_tok = static_cast<size_t>(p.HV) * kDim;
+    for (int t0 = 0; t0 < cur.ntok; t0 += kTileTok) {
+      const int nt = min(kTileTok, cur.ntok - t0);
+      __syncthreads();  // the previous tile has been consumed
+      // stage tokens t0 .. t0 + nt - 1: 16 bytes (8 values) per thread and array per step
+      for (int e = t; e < nt * (kDim / 8); e += kThreads) {
+        const int i = e >> 4, c = e & 15;            // token, 8-value chunk
+        const bool vmine = c / (kRows / 8) == cur.part;  // values 8c .. 8c + 7 are rows of this CTA
+        uint4 kx, vx = make_uint4(0u, 0u, 0u, 0u);
+        if (kMode == kCommit) {
+          const size_t brow = static_cast<size_t>(cur.slot) * p.T + t0 + i;
+          kx = __ldg(reinterpret_cast<const uint4*>(p.kbuf + (brow * p.H + cur.hq) * kDim) + c);
+          if (vmine) vx = __ldg(reinterpret_cast<const uint4*>(p.vbuf + (brow * p.HV + cur.hv) * kDim) + c);
+        } else {
+          const size_t row = cur.row0 + t0 + i;
+          kx = __ldg(reinterpret_cast<const uint4*>(p.k + row * qk_tok + static_cast<size_t>(cur.hq) * kDim) + c);
+          if (vmine)
+            vx = __ldg(reinterpret_cast<const uint4*>(p.v + row * v_tok + static_cast<size_t>(cur.hv) * kDim) + c);
+          const uint4 qx =
+              __ldg(reinterpret_cast<const uint4*>(p.q + row * qk_tok + static_cast<size_t>(cur.hq) * kDim) + c);
+          float f[8];
+          bf16x8_to_f32(qx, f);
+          reinterpret_cast<float4*>(&sm.qs[i][8 * c])[0] = make_float4(f[0], f[1], f[2], f[3]);
+          reinterpret_cast<float4*>(&sm.qs[i][8 * c])[1] = make_float4(f[4], f[5], f[6], f[7]);
+          if (kMode == kVerify && p.kbuf) {  // the KV buffer copy (k once per q/k head, by part 0)
+            const size_t brow = static_cast<size_t>(cur.slot) * p.T + t0 + i;
+            if (cur.hv % p.G == 0 && cur.part == 0)
+              reinterpret_cast<uint4*>(p.kbuf + (brow * p.H + cur.hq) * kDim)[c] = kx;
+            if (vmine) reinterpret_cast<uint4*>(p.vbuf + (brow * p.HV + cur.hv) * kDim)[c] = vx;
+          }
+        }
+        float f[8];
+        bf16x8_to_f32(kx, f);
+        reinterpret_cast<float4*>(&sm.ks[i][8 * c])[0] = make_float4(f[0], f[1], f[2], f[3]);
+        reinterpret_cast<float4*>(&sm.ks[i][8 * c])[1] = make_float4(f[4], f[5], f[6], f[7]);
+        if (vmine) {
+          bf16x8_to_f32(vx, f);
+          reinterpret_cast<float4*>(&sm.vs[i][8 * c - vbase])[0] = make_float4(f[0], f[1], f[2], f[3]);
+          reinterpret_cast<float4*>(&sm.vs[i][8 * c - vbase])[1] = make_float4(f[4], f[5], f[6], f[7]);
         }
       }
-      // S = lambda S + v_t[v] k_t
+      __syncthreads();
+
+      for (int i = 0; i < nt; ++i) {
+        const float4 vv = *reinterpret_cast<const float4*>(&sm.vs[i][4 * rg]);
+        const float vr[4] = {vv.x, vv.y, vv.z, vv.w};
+        uint64_t kk[8];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const uint64_t v2 = f2_pack(vr[r], vr[r]);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) S[r][j] = f2_fma(v2, kk[j], f2_mul(lam2, S[r][j]));
-      }
-      if (kMode != kCommit) {
-        // o_t[v] = scale S[v] . q_t over this thread's 16 columns, then across the 8 groups
-        uint64_t qq[8];
-        const float4* qr = reinterpret_cast<const float4*>(&qs[i][cg * kGroupStride]);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float4 x = qr[j];
-          qq[2 * j] = f2_pack(x.x, x.y);
-          qq[2 * j + 1] = f2_pack(x.z, x.w);
+        for (int m = 0; m < 4; ++m) {
+          const float4 x = *reinterpret_cast<const float4*>(&sm.ks[i][32 * m + 4 * cg]);
+          kk[2 * m] = f2_pack(x.x, x.y);
+          kk[2 * m + 1] = f2_pack(x.z, x.w);
         }
-        float dot[4];
+        // S = lambda S + v_t[v] k_t
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          uint64_t acc = f2_pack(0.f, 0.f);
+          const uint64_t v2 = f2_pack(vr[r], vr[r]);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) acc = f2_fma(S[r][j], qq[j], acc);
-          const float2 a2 = f2_unpack(acc);
-          dot[r] = a2.x + a2.y;
+          for (int j = 0; j < 8; ++j) S[r][j] = f2_fma(v2, kk[j], f2_mul(lam2, S[r][j]));
         }
+        if (kMode != kCommit) {
+          // o_t[v] = scale S[v] . q_t over this thread's 16 columns, then across the 8 lanes of the row group
+          uint64_t qq[8];
 #pragma unroll
-        for (int m = 1; m < 8; m <<= 1)
+          for (int m = 0; m < 4; ++m) {
+            const float4 x = *reinterpret_cast<const float4*>(&sm.qs[i][32 * m + 4 * cg]);
+            qq[2 * m] = f2_pack(x.x, x.y);
+            qq[2 * m + 1] = f2_pack(x.z, x.w);
+          }
+          float dot[4];
 #pragma unroll
-          for (int r = 0; r < 4; ++r) dot[r] += __shfl_xor_sync(0xffffffffu, dot[r], m);
-        if (cg < 4)  // lane group cg writes row vbase + 4 rg + cg
-          p.o[(row0 + t0 + i) * v_tok + static_cast<size_t>(hv) * kDim + vbase + 4 * rg + cg] =
-              __float2bfloat16_rn(p.scale * (cg == 0 ? dot[0] : cg == 1 ? dot[1] : cg == 2 ? dot[2] : dot[3]));
+          for (int r = 0; r < 4; ++r) {
+            uint64_t acc = f2_pack(0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc = f2_fma(S[r][j], qq[j], acc);
+            const float2 a2 = f2_unpack(acc);
+            dot[r] = a2.x + a2.y;
+          }
+#pragma unroll
+          for (int m = 1; m < 8; m <<= 1)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) dot[r] += __shfl_xor_sync(0xffffffffu, dot[r], m);
+          if (cg < 4)  // lane group cg writes row vbase + 4 rg + cg
+            p.o[(cur.row0 + t0 + i) * v_tok + static_cast<size_t>(cur.hv) * kDim + vbase + 4 * rg + cg] =
+                __float2bfloat16_rn(p.scale * (cg == 0 ? dot[0] : cg == 1 ? dot[1] : cg == 2 ? dot[2] : dot[3]));
+        }
       }
     }
-  }
 
-  if (kMode != kVerify && (kMode != kPrefill || s_out)) {
+    if (kMode != kVerify && (kMode != kPrefill || s_out)) {
+      float* dst = s_out + slice_of(cur);
 #pragma unroll
-    for (int r = 0; r < 4; ++r)
+      for (int r = 0; r < 4; ++r)
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 a = f2_unpack(S[r][2 * i]), c = f2_unpack(S[r][2 * i + 1]);
-        reinterpret_cast<float4*>(s_out + soff + r * kDim)[i] = make_float4(a.x, a.y, c.x, c.y);
-      }
+        for (int m = 0; m < 4; ++m) {
+          const float2 a = f2_unpack(S[r][2 * m]), c = f2_unpack(S[r][2 * m + 1]);
+          *reinterpret_cast<float4*>(dst + (4 * rg + r) * kDim + 32 * m + 4 * cg) = make_float4(a.x, a.y, c.x, c.y);
+        }
+    }
+    u = un;
+    cur = nxt;
   }
+  // no copy may still be landing in shared memory when the CTA exits
+  if (pending) lap::mbar_wait_drain(&sm.bar, phase);
+  __syncthreads();
+  if (t == 0 && sm.abort && p.dev_error) atomicOr(p.dev_error, 4);  // LA_DEV_ERR_TIMEOUT
 }
 
 }  // namespace lad

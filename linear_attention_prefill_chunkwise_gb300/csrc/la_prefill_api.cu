@@ -125,7 +125,8 @@ la_status la_prefill_fwd(const void* q, const void* k, const void* v, const floa
     tp.short_max = kShortMax;
     if (units * lad::kSplit > INT32_MAX) return fail(LA_ERR_UNSUPPORTED, "N*HV too large (%lld)", (long long)units);
     lad::la_tokenwise_kernel<lad::kPrefill>
-        <<<static_cast<int>(units * lad::kSplit), lad::kThreads, 0, static_cast<cudaStream_t>(stream)>>>(tp);
+        <<<lad::tokenwise_grid(static_cast<int>(units * lad::kSplit), ds.sms), lad::kThreads,
+           lad::tokenwise_smem_bytes(), static_cast<cudaStream_t>(stream)>>>(tp);
     ce = cudaGetLastError();
     if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "tokenwise kernel launch failed: %s", cudaGetErrorString(ce));
   }

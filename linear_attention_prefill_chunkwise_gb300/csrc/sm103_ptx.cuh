@@ -159,6 +159,14 @@ __device__ __forceinline__ void bulk_copy_s2g(void* gdst, const void* ssrc, uint
                "r"(smem_u32(ssrc)), "r"(bytes)
                : "memory");
 }
+// Bulk (non-tensor) asynchronous copy of `bytes` (a multiple of 16, both addresses 16-byte
+// aligned) from global to shared memory, completion signalled on `bar` as transaction bytes.
+__device__ __forceinline__ void bulk_copy_g2s(void* sdst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(sdst)),
+               "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until every committed bulk copy of this thread has finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
