@@ -14,8 +14,10 @@
 // rows v = 64 h + 4 (t / 8) .. +3 and, of each, the four 16-byte column chunks
 // k = 32 m + 4 (t % 8) .. +3 (m = 0..3), and for every token
 //     S[v][k] = lambda S[v][k] + v_t[v] k_t[k]              (FP32, fused multiply-add)
-//     o_t[v]  = scale sum_k S[v][k] q_t[k]                    (8 column-group partial sums,
-//                                                             added across lanes t^1, t^2, t^4)
+//     o_t[v]  = scale sum_k S[v][k] q_t[k]                    (the 8 lanes of a row group hold
+//                                                             partial sums of 4 rows; a reduce-
+//                                                             scatter over lanes t^4, t^2, t^1
+//                                                             leaves each row's total in 2 lanes)
 // with the tokens' q, k, v staged in shared memory as FP32, 8 tokens at a time.  Each staged k
 // or q value feeds four rows, which keeps the shared-memory traffic per FMA low; the strided
 // column chunks make a warp read 128 contiguous bytes of a row at a time, from the staged
@@ -300,13 +302,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) la_tokenwise_kernel(cons
             const float2 a2 = f2_unpack(acc);
             dot[r] = a2.x + a2.y;
           }
-#pragma unroll
-          for (int m = 1; m < 8; m <<= 1)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) dot[r] += __shfl_xor_sync(0xffffffffu, dot[r], m);
-          if (cg < 4)  // lane group cg writes row vbase + 4 rg + cg
-            p.o[(cur.row0 + t0 + i) * v_tok + static_cast<size_t>(cur.hv) * kDim + vbase + 4 * rg + cg] =
-                __float2bfloat16_rn(p.scale * (cg == 0 ? dot[0] : cg == 1 ? dot[1] : cg == 2 ? dot[2] : dot[3]));
+          // reduce-scatter over the 8 lanes of the row group: lanes with bit 2 of cg keep rows
+          // {2, 3} (else {0, 1}), bit 1 picks one of the two, bit 0 pairs lanes; lane cg ends
+          // with the total of row 2 (cg >> 2) + ((cg >> 1) & 1), written by the even lanes
+          const bool b2 = cg & 4, b1 = cg & 2;
+          const float s0 = b2 ? dot[0] : dot[2], s1 = b2 ? dot[1] : dot[3];
+          float k0 = (b2 ? dot[2] : dot[0]) + __shfl_xor_sync(0xffffffffu, s0, 4);
+          float k1 = (b2 ? dot[3] : dot[1]) + __shfl_xor_sync(0xffffffffu, s1, 4);
+          float kx = (b1 ? k1 : k0) + __shfl_xor_sync(0xffffffffu, b1 ? k0 : k1, 2);
+          kx += __shfl_xor_sync(0xffffffffu, kx, 1);
+          if (!(cg & 1))
+            p.o[(cur.row0 + t0 + i) * v_tok + static_cast<size_t>(cur.hv) * kDim + vbase + 4 * rg +
+                (2 * (cg >> 2) + ((cg >> 1) & 1))] = __float2bfloat16_rn(p.scale * kx);
         }
       }
     }
