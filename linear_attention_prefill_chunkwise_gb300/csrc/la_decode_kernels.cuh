@@ -18,7 +18,11 @@
 //                                                             partial sums of 4 rows; a reduce-
 //                                                             scatter over lanes t^4, t^2, t^1
 //                                                             leaves each row's total in 2 lanes)
-// with the tokens' q, k, v staged in shared memory as FP32, 8 tokens at a time.  Each staged k
+// with the tokens' q, k, v staged in shared memory as FP32, 8 tokens at a time.  Where
+// lambda^-8 stays small (slope <= 2.5) the registers hold, within a tile of 8 tokens starting
+// at t0, S'_i = S_(t0 + i) / lambda^(i+1): then S'_i = S'_(i-1) + (lambda^-(i+1) v_i[v]) k_i[k]
+// is one fused multiply-add per element and token, o_i = scale lambda^(i+1) S'_i q_i, and the
+// tile ends with S = lambda^nt S'.  (The same sum, in another rounding order.)  Each staged k
 // or q value feeds four rows, which keeps the shared-memory traffic per FMA low; the strided
 // column chunks make a warp read 128 contiguous bytes of a row at a time, from the staged
 // tokens and from the state slice alike, without bank conflicts.
@@ -99,6 +103,8 @@ struct __align__(128) TokSmem {
   float ks[kTileTok][kDim];      // staged k (commit: from the KV buffer)
   float qs[kTileTok][kDim];      // staged q
   float vs[kTileTok][kRows];     // staged v, this CTA's rows
+  float linv[kTileTok];          // lambda^-(i+1) of the tile's token i (rescaled update)
+  float lpow[kTileTok];          // lambda^(i+1)
   uint64_t bar;                  // slice landed (transaction bytes)
   int abort;
 };
@@ -193,8 +199,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) la_tokenwise_kernel(cons
     TokUnit nxt;
     const int un = seek(u + gridDim.x, nxt);
     const int vbase = cur.part * kRows;
-    const float lam = expf(-__ldg(p.slopes + cur.hv));
+    const float slope = __ldg(p.slopes + cur.hv);
+    const float lam = expf(-slope);
     const uint64_t lam2 = f2_pack(lam, lam);
+    const bool resc = slope * kTileTok <= 20.f;  // the rescaled update (lambda^-8 <= e^20)
 
     // ---- this unit's state slice: S[r][2 m + h] = the pair (e = 2 h, 2 h + 1) of chunk m of row r
     uint64_t S[4][8];
@@ -265,11 +273,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) la_tokenwise_kernel(cons
           reinterpret_cast<float4*>(&sm.vs[i][8 * c - vbase])[1] = make_float4(f[4], f[5], f[6], f[7]);
         }
       }
+      if (t < nt) {
+        sm.linv[t] = resc ? expf(slope * (t + 1)) : 1.f;
+        sm.lpow[t] = resc ? expf(-slope * (t + 1)) : 1.f;
+      }
       __syncthreads();
 
       for (int i = 0; i < nt; ++i) {
         const float4 vv = *reinterpret_cast<const float4*>(&sm.vs[i][4 * rg]);
-        const float vr[4] = {vv.x, vv.y, vv.z, vv.w};
+        const float vf = sm.linv[i];
+        const float vr[4] = {vv.x * vf, vv.y * vf, vv.z * vf, vv.w * vf};
         uint64_t kk[8];
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
@@ -278,11 +291,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) la_tokenwise_kernel(cons
           kk[2 * m + 1] = f2_pack(x.z, x.w);
         }
         // S = lambda S + v_t[v] k_t
+        if (!resc) {
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) S[r][j] = f2_mul(lam2, S[r][j]);
+        }
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
           const uint64_t v2 = f2_pack(vr[r], vr[r]);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) S[r][j] = f2_fma(v2, kk[j], f2_mul(lam2, S[r][j]));
+          for (int j = 0; j < 8; ++j) S[r][j] = f2_fma(v2, kk[j], S[r][j]);
         }
         if (kMode != kCommit) {
           // o_t[v] = scale S[v] . q_t over this thread's 16 columns, then across the 8 lanes of the row group
@@ -313,8 +332,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) la_tokenwise_kernel(cons
           kx += __shfl_xor_sync(0xffffffffu, kx, 1);
           if (!(cg & 1))
             p.o[(cur.row0 + t0 + i) * v_tok + static_cast<size_t>(cur.hv) * kDim + vbase + 4 * rg +
-                (2 * (cg >> 2) + ((cg >> 1) & 1))] = __float2bfloat16_rn(p.scale * kx);
+                (2 * (cg >> 2) + ((cg >> 1) & 1))] = __float2bfloat16_rn(p.scale * sm.lpow[i] * kx);
         }
+      }
+      if (resc) {
+        const float ln = sm.lpow[nt - 1];
+        const uint64_t ln2 = f2_pack(ln, ln);
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) S[r][j] = f2_mul(ln2, S[r][j]);
       }
     }
 
