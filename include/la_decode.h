@@ -11,10 +11,15 @@
  *   la_decode_mtp  over the T draft tokens t = 0 .. T-1 of the request:
  *                      S = lambda S + v_t^T k_t ;  o_t = scale S q_t
  *                  and S is written back to state[slot][hv] (the pool is updated in place).
- *   la_verify      the same outputs o_t, t = 0 .. T-1, which equal the closed form
+ *   la_verify      the same outputs o_t, t = 0 .. T-1, by the closed form ("Closed form used
+ *                  by verify")
  *                      o_t = lambda^(t+1) scale (S q_t) + sum_{i<=t} lambda^(t-i) scale (q_t . k_i) v_i
  *                  with the pool left untouched; optionally k_t, v_t are copied into a
- *                  pooled KV buffer at the request's slot for a later commit.
+ *                  pooled KV buffer at the request's slot for a later commit.  For T <= 8 the
+ *                  products S q_t run on the tensor cores with S and q_t as TF32 operands (the
+ *                  pages' verify kernel also multiplies the state by q in TF32), so the outputs
+ *                  equal la_decode_mtp's within that rounding; for T > 8 verify runs decode's
+ *                  tokenwise recurrence and its outputs are bitwise decode's.
  *   la_commit      with L = accepted_len[b] (0 <= L <= T) taken from that KV buffer:
  *                      S = lambda^L S + sum_{i<L} lambda^(L-1-i) v_i^T k_i   (L = 0: no-op)
  *                  written back to state[slot][hv].  With L == T the committed state is

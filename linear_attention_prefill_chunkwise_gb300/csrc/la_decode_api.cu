@@ -1,6 +1,8 @@
 // la_decode_api.cu -- host side of the C ABI declared in include/la_decode.h: argument
-// validation and one launch per call (lad::kSplit CTAs per (request, value head)).  Nothing here
-// allocates device memory, reads device memory or synchronises with the host.
+// validation and one launch per call: the tokenwise kernel (lad::kSplit CTAs per (request,
+// value head)) for decode, commit and long verifies, the tensor-core closed-form kernel for
+// verifies of at most lav::kMaxTok tokens.  Nothing here allocates device memory, reads device
+// memory or synchronises with the host.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -8,6 +10,7 @@
 #include "../../include/la_decode.h"
 #include "la_decode_kernels.cuh"
 #include "la_host_common.h"
+#include "la_verify_kernel.cuh"
 
 namespace {
 
@@ -34,10 +37,16 @@ la_status check_shapes(int B, int T, int H, int HV, int D, int V, int pool_size,
   return LA_OK;
 }
 
+// One-time setup per device: the closed-form verify kernel's shared memory exceeds the default.
+cudaError_t setup_kernels() {
+  return cudaFuncSetAttribute(lav::la_verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              lav::verify_smem_bytes());
+}
+
 template <int kMode>
 la_status launch(const lad::Params& p, void* stream) {
   la_host::DeviceState* ds = nullptr;
-  la_status st = la_host::current_device(g_dev, &ds, [] { return cudaSuccess; });
+  la_status st = la_host::current_device(g_dev, &ds, setup_kernels);
   if (st != LA_OK) return st;
   const int grid = lad::tokenwise_grid(p.B * p.HV * lad::kSplit, ds->sms);
   lad::la_tokenwise_kernel<kMode>
@@ -111,7 +120,40 @@ la_status la_verify(const void* q, const void* k, const void* v, const float* sl
   p.o = static_cast<__nv_bfloat16*>(o);
   p.kbuf = static_cast<__nv_bfloat16*>(kbuf);
   p.vbuf = static_cast<__nv_bfloat16*>(vbuf);
-  return launch<lad::kVerify>(p, stream);
+  if (T > lav::kMaxTok || static_cast<int64_t>(pool_size) * HV * 128 > INT32_MAX) return launch<lad::kVerify>(p, stream);
+
+  // the closed form on the tensor cores
+  la_host::DeviceState* ds = nullptr;
+  st = la_host::current_device(g_dev, &ds, setup_kernels);
+  if (st != LA_OK) return st;
+  CUtensorMap tm_s, tm_q, tm_k, tm_v;
+  const int64_t rows = static_cast<int64_t>(B) * T;
+  if ((st = la_host::encode_f32_state_map(&tm_s, state, static_cast<int64_t>(pool_size) * HV * 128)) != LA_OK ||
+      (st = la_host::encode_bf16_token_map(&tm_q, q, rows, H, lav::kMaxTok, "q")) != LA_OK ||
+      (st = la_host::encode_bf16_token_map(&tm_k, k, rows, H, lav::kMaxTok, "k")) != LA_OK ||
+      (st = la_host::encode_bf16_token_map(&tm_v, v, rows, HV, lav::kMaxTok, "v")) != LA_OK)
+    return st;
+  lav::Params vp{};
+  vp.slopes = slopes;
+  vp.state_indices = state_indices;
+  vp.o = p.o;
+  vp.kbuf = p.kbuf;
+  vp.vbuf = p.vbuf;
+  vp.dev_error = dev_error;
+  vp.scale = scale;
+  vp.B = B;
+  vp.T = T;
+  vp.H = H;
+  vp.HV = HV;
+  vp.G = HV / H;
+  vp.pool_size = pool_size;
+  const int units = B * HV;
+  const int grid = units < ds->sms ? units : ds->sms;
+  lav::la_verify_tc_kernel<<<grid, lav::kThreads, lav::verify_smem_bytes(), static_cast<cudaStream_t>(stream)>>>(
+      tm_s, tm_q, tm_k, tm_v, vp);
+  const cudaError_t ce = cudaGetLastError();
+  if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(ce));
+  return LA_OK;
 }
 
 la_status la_commit(float* state, const int32_t* state_indices, const void* kbuf, const void* vbuf,

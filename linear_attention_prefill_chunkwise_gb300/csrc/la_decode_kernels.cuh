@@ -27,7 +27,8 @@
 // column chunks make a warp read 128 contiguous bytes of a row at a time, from the staged
 // tokens and from the state slice alike, without bank conflicts.
 // The three operations run this same per-token code, so a commit of all T tokens leaves
-// bitwise the state a decode leaves, and verify's outputs are bitwise decode's.
+// bitwise the state a decode leaves, and verify's outputs (requests of more than 8 tokens; the
+// shorter ones go to the tensor-core closed form of la_verify_kernel.cuh) are bitwise decode's.
 //
 // A fourth mode serves the prefill of short sequences (at most short_max tokens; the
 // chunkwise prefill kernel takes the others): bounds from cu_seqlens or n T, the initial
