@@ -8,16 +8,19 @@
 // operand (N = 16 columns, T of them used), both as TF32 (the pages' verify kernel also
 // multiplies h0 by q in TF32), accumulated in FP32 in tensor memory.
 //
-// One persistent CTA per SM walks the units u = blockIdx.x + j gridDim.x:
-//   warp 4 (one thread)   TMA loads: each unit's state slice as four 128 x 32 FP32 boxes,
+// One persistent CTA per SM walks the units u = blockIdx.x + n gridDim.x:
+//   warp 8 (one thread)   TMA loads: each unit's state slice as four 128 x 32 FP32 boxes,
 //                         128-byte swizzled (the canonical K-major operand layout), into a
 //                         3-stage ring, and the request's q, k, v rows (8 x 128 BF16 each)
-//                         into a 2-stage ring;
-//   warps 0-3             per unit: q to FP32 in the B operand's swizzled layout; one thread
+//                         into the 2-stage ring of the group that takes the unit;
+//   warps 0-3, 4-7        two compute groups, on the units with n even and odd: per unit, q to
+//                         FP32 in the group's 8 rows of the B operand (swizzled); one thread
 //                         issues the 16 MMAs (K = 8 each); meanwhile the scores
 //                         A[i][j] = scale lambda^(i-j) q_i . k_j (j <= i) on the CUDA cores;
 //                         then thread v (= TMEM lane v) reads row v of S q, adds the intra
-//                         terms and stores o_t[v]; the draft k, v go to the KV buffer.
+//                         terms and stores o_t[v]; the draft k, v go to the KV buffer.  Each
+//                         group's chain of waits is long next to its arithmetic; two of them
+//                         keep twice the state loads in flight.
 // Every wait is bounded (sm103_ptx.cuh); a timeout sets LA_DEV_ERR_TIMEOUT, drains this CTA's
 // copies and MMAs in flight and frees tensor memory before the CTA exits.
 #pragma once
@@ -33,16 +36,16 @@ namespace lav {
 constexpr int kDim = 128;
 constexpr int kMaxTok = 8;        // draft tokens per request on this path
 constexpr int kN = 16;            // the MMA's N (q rows kMaxTok .. 15 of the operand stay zero)
-constexpr int kStStages = 3;      // state ring
-constexpr int kTkStages = 2;      // token ring
-constexpr int kCompute = 128;     // warps 0-3, one TMEM lane per thread
-constexpr int kThreads = kCompute + 32;
+constexpr int kGroups = 2;        // compute groups, each on its own units (alternately)
+constexpr int kStStages = 3;      // state ring (shared by the groups, in unit order)
+constexpr int kTkStages = 2;      // token ring of each group
+constexpr int kCompute = 128;     // threads of a group: 4 warps, one TMEM lane per thread
+constexpr int kThreads = kGroups * kCompute + 32;
 constexpr uint32_t kStateBox = 128 * 32 * 4;  // 128 rows x 32 FP32 columns
 constexpr uint32_t kStateBytes = 4 * kStateBox;
 constexpr uint32_t kBBox = kN * 128;          // kN rows x 32 FP32 columns
 constexpr uint32_t kTokBytes = kMaxTok * kDim * 2;
-constexpr uint32_t kTmemCols = 32;
-constexpr uint32_t kBarCompute = 1;  // named barrier of warps 0-3
+constexpr uint32_t kTmemCols = 32;  // group g's accumulator: columns kN g .. kN g + kN - 1
 
 struct Params {
   const float* slopes;           // [HV]
@@ -56,17 +59,19 @@ struct Params {
 };
 
 struct __align__(1024) Smem {
-  uint8_t st[kStStages][kStateBytes];                // state slices: box c = columns 32c .. 32c+31
-  uint8_t bt[4][kBBox];                              // q as FP32, [kN t][128 k] in 4 boxes of 32 k
-  __nv_bfloat16 tk[kTkStages][3][kMaxTok][kDim];     // q, k, v rows of the request's tokens
-  float A[kMaxTok][kMaxTok];                         // scale lambda^(i-j) q_i . k_j, j <= i
-  float dec[kMaxTok + 1];                            // lambda^m, m = 0 .. kMaxTok
+  uint8_t st[kStStages][kStateBytes];                     // state slices: box c = columns 32c .. 32c+31
+  uint8_t bt[4][kBBox];                                   // q as FP32, [kN t][128 k] in 4 boxes of 32 k:
+                                                          // rows 8g .. 8g+7 are group g's tokens
+  __nv_bfloat16 tk[kGroups][kTkStages][3][kMaxTok][kDim];  // q, k, v rows of a request's tokens
+  float A[kGroups][kMaxTok][kMaxTok];                     // scale lambda^(i-j) q_i . k_j, j <= i
+  float dec[kGroups][kMaxTok + 1];                        // lambda^m, m = 0 .. kMaxTok
   uint64_t st_full[kStStages], st_empty[kStStages];
-  uint64_t tk_full[kTkStages], tk_empty[kTkStages];
-  uint64_t mma_bar, final_bar;
+  uint64_t tk_full[kGroups][kTkStages], tk_empty[kGroups][kTkStages];
+  uint64_t mma_bar[kGroups], final_bar[kGroups];
   uint32_t tmem_base;
   int abort;
 };
+static_assert(kGroups * kMaxTok == kN, "the groups' q rows fill the MMA's N");
 
 __host__ __device__ constexpr int verify_smem_bytes() { return static_cast<int>(sizeof(Smem)) + 1024; }
 
@@ -123,15 +128,17 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& x, float (&f)[8]) {
   }
 }
 
-// The load thread: every unit's state slice and token rows, in the consumers' order.
+// The load thread: every unit's state slice (ring stage n % 3 for the CTA's n-th unit) and
+// token rows (group n % 2's ring, stage (n / 2) % 2), in the consumers' order.
 __device__ __forceinline__ void load_loop(Smem& sm, const Params& p, const CUtensorMap* tm_s,
                                           const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                           volatile int* abort) {
   const int units = p.B * p.HV;
-  uint32_t n_st = 0, n_tk = 0;
+  uint32_t n_st = 0, n_tk0 = 0, n_tk1 = 0;  // units loaded, in all and per group
   int slot = 0;
   for (int u = seek(p, blockIdx.x, units, true, slot); u < units; u = seek(p, u + gridDim.x, units, true, slot)) {
     const int b = u / p.HV, hv = u - b * p.HV, hq = hv / p.G;
+    const int g = n_st % kGroups;
     const uint32_t s = n_st % kStStages;
     if (!lap::mbar_wait(&sm.st_empty[s], ((n_st / kStStages) & 1u) ^ 1u, abort)) break;
     lap::mbar_arrive_expect_tx(&sm.st_full[s], kStateBytes);
@@ -139,14 +146,15 @@ __device__ __forceinline__ void load_loop(Smem& sm, const Params& p, const CUten
 #pragma unroll
     for (int c = 0; c < 4; ++c) lap::tma_load_2d(sm.st[s] + c * kStateBox, tm_s, &sm.st_full[s], 32 * c, y);
     ++n_st;
-    const uint32_t s2 = n_tk % kTkStages;
-    if (!lap::mbar_wait(&sm.tk_empty[s2], ((n_tk / kTkStages) & 1u) ^ 1u, abort)) break;
-    lap::mbar_arrive_expect_tx(&sm.tk_full[s2], 3 * kTokBytes);
+    const uint32_t j = g ? n_tk1 : n_tk0, s2 = j % kTkStages;
+    if (!lap::mbar_wait(&sm.tk_empty[g][s2], ((j / kTkStages) & 1u) ^ 1u, abort)) break;
+    uint64_t* bar = &sm.tk_full[g][s2];
+    lap::mbar_arrive_expect_tx(bar, 3 * kTokBytes);
     const int32_t row = b * p.T;
-    lap::tma_load_2d(sm.tk[s2][0], tm_q, &sm.tk_full[s2], hq * kDim, row);
-    lap::tma_load_2d(sm.tk[s2][1], tm_k, &sm.tk_full[s2], hq * kDim, row);
-    lap::tma_load_2d(sm.tk[s2][2], tm_v, &sm.tk_full[s2], hv * kDim, row);
-    ++n_tk;
+    lap::tma_load_2d(sm.tk[g][s2][0], tm_q, bar, hq * kDim, row);
+    lap::tma_load_2d(sm.tk[g][s2][1], tm_k, bar, hq * kDim, row);
+    lap::tma_load_2d(sm.tk[g][s2][2], tm_v, bar, hv * kDim, row);
+    if (g) ++n_tk1; else ++n_tk0;
   }
   // Teardown, also after an abort: a load is issued only after the previous one into its slot
   // was consumed, so the last loads of each ring are the only ones that can still be in flight.
@@ -154,45 +162,57 @@ __device__ __forceinline__ void load_loop(Smem& sm, const Params& p, const CUten
     const uint32_t j = n_st - 1 - i;
     lap::mbar_wait_drain(&sm.st_full[j % kStStages], (j / kStStages) & 1u);
   }
-  for (uint32_t i = 0; i < kTkStages && i < n_tk; ++i) {
-    const uint32_t j = n_tk - 1 - i;
-    lap::mbar_wait_drain(&sm.tk_full[j % kTkStages], (j / kTkStages) & 1u);
+  for (int g = 0; g < kGroups; ++g) {
+    const uint32_t n_tk = g ? n_tk1 : n_tk0;
+    for (uint32_t i = 0; i < kTkStages && i < n_tk; ++i) {
+      const uint32_t j = n_tk - 1 - i;
+      lap::mbar_wait_drain(&sm.tk_full[g][j % kTkStages], (j / kTkStages) & 1u);
+    }
   }
 }
 
-// Warps 0-3: thread t is TMEM lane t and value row t of every unit.
-__device__ __forceinline__ void compute_loop(Smem& sm, const Params& p, uint32_t tmem, volatile int* abort) {
-  const int t = threadIdx.x;
+// Compute group g (warps 4g .. 4g+3): thread t is TMEM lane t and value row t of the group's
+// units, the CTA's units n with n % 2 == g.  The groups meet only in the state ring and in the
+// B operand, of which each writes its own 8 rows (the other group's rows give MMA columns that
+// are not read).
+__device__ __forceinline__ void compute_loop(Smem& sm, const Params& p, uint32_t tmem_base, int g,
+                                             volatile int* abort) {
+  const int t = threadIdx.x - kCompute * g;
+  const uint32_t bar_id = 1 + g;  // the group's named barrier
   const int units = p.B * p.HV;
   const int T = p.T;
+  const uint32_t tmem = tmem_base + kN * g;
   constexpr uint32_t idesc = lap::idesc_tf32_f32(128, kN, false, false);
   const uint64_t da0 = lap::sdesc_sw128(lap::smem_u32(sm.st[0]), 16, 1024);
   const uint64_t db0 = lap::sdesc_sw128(lap::smem_u32(sm.bt[0]), 16, 1024);
   const size_t v_tok = static_cast<size_t>(p.HV) * kDim;
-  uint32_t n = 0;
+  uint32_t n = 0, j = 0;  // the CTA's unit count, this group's unit count
   int slot = 0;
   for (int u = seek(p, blockIdx.x, units, false, slot); u < units;
        u = seek(p, u + gridDim.x, units, false, slot), ++n) {
+    if (static_cast<int>(n % kGroups) != g) continue;
     const int b = u / p.HV, hv = u - b * p.HV, hq = hv / p.G;
-    const uint32_t s = n % kStStages, s2 = n % kTkStages;
-    const bool got = lap::mbar_wait(&sm.tk_full[s2], (n / kTkStages) & 1u, abort);
-    if (!bar_and(kBarCompute, kCompute, got)) break;
+    const uint32_t s = n % kStStages, s2 = j % kTkStages;
+    const bool got = lap::mbar_wait(&sm.tk_full[g][s2], (j / kTkStages) & 1u, abort);
+    if (!bar_and(bar_id, kCompute, got)) break;
+    const __nv_bfloat16(*tk)[kMaxTok][kDim] = sm.tk[g][s2];
 
-    // q rows as FP32 into the B operand: thread t converts 8 values (row t / 16, chunk t % 16) and
-    // writes them as two 16-byte chunks of box (t % 16) / 4, swizzled by the row.
+    // q rows as FP32 into rows 8g .. 8g+7 of the B operand: thread t converts 8 values (token
+    // t / 16, chunk t % 16) and writes them as two 16-byte chunks of box (t % 16) / 4, swizzled by
+    // the operand row.
     {
-      const int row = t >> 4, ch = t & 15;
+      const int i = t >> 4, ch = t & 15, row = kMaxTok * g + i;
       float f[8];
-      bf16x8_to_f32(*reinterpret_cast<const uint4*>(&sm.tk[s2][0][row][8 * ch]), f);
+      bf16x8_to_f32(*reinterpret_cast<const uint4*>(&tk[0][i][8 * ch]), f);
       uint8_t* rp = sm.bt[ch >> 2] + row * 128;
       const int c0 = 2 * (ch & 3);
       *reinterpret_cast<float4*>(rp + ((c0 ^ (row & 7)) << 4)) = make_float4(f[0], f[1], f[2], f[3]);
       *reinterpret_cast<float4*>(rp + (((c0 + 1) ^ (row & 7)) << 4)) = make_float4(f[4], f[5], f[6], f[7]);
     }
     const float slope = __ldg(p.slopes + hv);
-    if (t <= kMaxTok) sm.dec[t] = t == 0 ? 1.f : expf(-slope * t);
+    if (t <= kMaxTok) sm.dec[g][t] = t == 0 ? 1.f : expf(-slope * t);
     lap::fence_proxy_async_smem();
-    lap::named_bar_sync(kBarCompute, kCompute);
+    lap::named_bar_sync(bar_id, kCompute);
 
     if (t == 0) {
       // S q for the unit's tokens: 16 MMAs along K (8 columns each; 4 per 32-column box)
@@ -204,19 +224,19 @@ __device__ __forceinline__ void compute_loop(Smem& sm, const Params& p, uint32_t
           mma_tf32_ss(tmem, desc_at(da, (kk >> 2) * kStateBox + (kk & 3) * 32),
                       desc_at(db0, (kk >> 2) * kBBox + (kk & 3) * 32), idesc, kk > 0);
         lap::mma_commit(&sm.st_empty[s]);
-        lap::mma_commit(&sm.mma_bar);
+        lap::mma_commit(&sm.mma_bar[g]);
       }
     }
 
     // scores while the MMAs run: two threads per pair (i, j) = (t / 16, t / 2 % 8), 64 columns
     // each, their 16-byte chunks rotated by t so that a shared-memory phase hits 8 bank groups
     {
-      const int i = t >> 4, j = (t >> 1) & 7, h = t & 1;
-      const bool live = j <= i && i < T;
+      const int i = t >> 4, jj = (t >> 1) & 7, h = t & 1;
+      const bool live = jj <= i && i < T;
       float d0 = 0.f, d1 = 0.f;
       if (live) {
-        const __nv_bfloat16* qr = &sm.tk[s2][0][i][64 * h];
-        const __nv_bfloat16* kr = &sm.tk[s2][1][j][64 * h];
+        const __nv_bfloat16* qr = &tk[0][i][64 * h];
+        const __nv_bfloat16* kr = &tk[1][jj][64 * h];
 #pragma unroll
         for (int cc = 0; cc < 8; ++cc) {
           const int c = 8 * ((cc + t) & 7);
@@ -232,24 +252,24 @@ __device__ __forceinline__ void compute_loop(Smem& sm, const Params& p, uint32_t
       }
       float d = d0 + d1;
       d += __shfl_xor_sync(0xffffffffu, d, 1);
-      if (live && h == 0) sm.A[i][j] = p.scale * sm.dec[i - j] * d;
+      if (live && h == 0) sm.A[g][i][jj] = p.scale * sm.dec[g][i - jj] * d;
     }
 
-    const bool done = lap::mbar_wait(&sm.mma_bar, n & 1u, abort);
-    if (!bar_and(kBarCompute, kCompute, done)) break;
+    const bool done = lap::mbar_wait(&sm.mma_bar[g], j & 1u, abort);
+    if (!bar_and(bar_id, kCompute, done)) break;
     lap::tc_fence_after();
     float acc[16];
     lap::tmem_ld16(tmem + ((static_cast<uint32_t>(t) & ~31u) << 16), acc);  // row t: (S q_c)[t], c = 0..15
     float vj[kMaxTok];
 #pragma unroll
-    for (int j = 0; j < kMaxTok; ++j) vj[j] = __bfloat162float(sm.tk[s2][2][j][t]);
+    for (int jj = 0; jj < kMaxTok; ++jj) vj[jj] = __bfloat162float(tk[2][jj][t]);
     __nv_bfloat16* orow = p.o + static_cast<size_t>(b) * T * v_tok + static_cast<size_t>(hv) * kDim + t;
 #pragma unroll
     for (int i = 0; i < kMaxTok; ++i) {
       if (i < T) {
-        float o = p.scale * sm.dec[i + 1] * acc[i];
+        float o = p.scale * sm.dec[g][i + 1] * (g ? acc[kMaxTok + i] : acc[i]);
 #pragma unroll
-        for (int j = 0; j <= i; ++j) o = fmaf(sm.A[i][j], vj[j], o);
+        for (int jj = 0; jj <= i; ++jj) o = fmaf(sm.A[g][i][jj], vj[jj], o);
         orow[static_cast<size_t>(i) * v_tok] = __float2bfloat16_rn(o);
       }
     }
@@ -259,19 +279,20 @@ __device__ __forceinline__ void compute_loop(Smem& sm, const Params& p, uint32_t
         const size_t brow = static_cast<size_t>(slot) * T + i;
         if (hv % p.G == 0)
           reinterpret_cast<uint4*>(p.kbuf + (brow * p.H + hq) * kDim)[c] =
-              *reinterpret_cast<const uint4*>(&sm.tk[s2][1][i][8 * c]);
+              *reinterpret_cast<const uint4*>(&tk[1][i][8 * c]);
         reinterpret_cast<uint4*>(p.vbuf + (brow * p.HV + hv) * kDim)[c] =
-            *reinterpret_cast<const uint4*>(&sm.tk[s2][2][i][8 * c]);
+            *reinterpret_cast<const uint4*>(&tk[2][i][8 * c]);
       }
     }
     // the token stage and the accumulator are free once every thread is past this point
     lap::tc_fence_before();
-    lap::named_bar_sync(kBarCompute, kCompute);
-    if (t == 0) lap::mbar_arrive(&sm.tk_empty[s2]);
+    lap::named_bar_sync(bar_id, kCompute);
+    if (t == 0) lap::mbar_arrive(&sm.tk_empty[g][s2]);
+    ++j;
   }
-  if (t == 0) {  // every MMA issued has retired before tensor memory is released
-    lap::mma_commit(&sm.final_bar);
-    lap::mbar_wait_drain(&sm.final_bar, 0);
+  if (t == 0) {  // every MMA this group issued has retired before tensor memory is released
+    lap::mma_commit(&sm.final_bar[g]);
+    lap::mbar_wait_drain(&sm.final_bar[g], 0);
   }
 }
 
@@ -287,17 +308,19 @@ la_verify_tc_kernel(const __grid_constant__ CUtensorMap tm_s, const __grid_const
     lap::tmem_alloc(&sm.tmem_base, kTmemCols);
     lap::tmem_relinquish();
   }
-  if (tid == kCompute) {
+  if (tid == kGroups * kCompute) {
     for (int i = 0; i < kStStages; ++i) {
       lap::mbar_init(&sm.st_full[i], 1);
       lap::mbar_init(&sm.st_empty[i], 1);
     }
-    for (int i = 0; i < kTkStages; ++i) {
-      lap::mbar_init(&sm.tk_full[i], 1);
-      lap::mbar_init(&sm.tk_empty[i], 1);
+    for (int g = 0; g < kGroups; ++g) {
+      for (int i = 0; i < kTkStages; ++i) {
+        lap::mbar_init(&sm.tk_full[g][i], 1);
+        lap::mbar_init(&sm.tk_empty[g][i], 1);
+      }
+      lap::mbar_init(&sm.mma_bar[g], 1);
+      lap::mbar_init(&sm.final_bar[g], 1);
     }
-    lap::mbar_init(&sm.mma_bar, 1);
-    lap::mbar_init(&sm.final_bar, 1);
     sm.abort = 0;
     lap::fence_mbar_init();
     lap::tma_prefetch_desc(&tm_s);
@@ -305,7 +328,7 @@ la_verify_tc_kernel(const __grid_constant__ CUtensorMap tm_s, const __grid_const
     lap::tma_prefetch_desc(&tm_k);
     lap::tma_prefetch_desc(&tm_v);
   }
-  // rows kMaxTok .. kN-1 of the B operand are never written again: zero them (and the rest) once
+  // the B operand starts at zero (a group's MMAs read the other group's rows too)
   for (int i = tid; i < static_cast<int>(sizeof(sm.bt) / 16); i += kThreads)
     reinterpret_cast<uint4*>(&sm.bt[0][0])[i] = make_uint4(0u, 0u, 0u, 0u);
   lap::fence_proxy_async_smem();
@@ -314,8 +337,8 @@ la_verify_tc_kernel(const __grid_constant__ CUtensorMap tm_s, const __grid_const
   lap::tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
-  if (warp < 4) {
-    compute_loop(sm, p, tmem, abort);
+  if (warp < 4 * kGroups) {
+    compute_loop(sm, p, tmem, warp >> 2, abort);
   } else if ((tid & 31) == 0) {
     load_loop(sm, p, &tm_s, &tm_q, &tm_k, &tm_v, abort);
   }
