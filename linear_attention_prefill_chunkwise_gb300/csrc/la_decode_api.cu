@@ -20,6 +20,41 @@ using la_host::fail;
 
 la_host::DeviceState g_dev[la_host::kMaxDevices];
 
+// Map over a pool of FP32 states viewed as [rows, 128] (rows = slots x heads x 128 value rows):
+// 32 x 128 boxes (32 columns = 128 bytes, 128 rows), 128-byte swizzle, the K-major operand
+// layout of a TF32 tensor-core product.
+la_status encode_f32_state_map(CUtensorMap* map, const void* base, int64_t rows) {
+  auto enc = la_host::tensor_map_encoder();
+  if (!enc) return fail(LA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the CUDA driver");
+  const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {128 * 4};
+  const cuuint32_t box[2] = {32, 128};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
+                         elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(LA_ERR_CUDA, "cuTensorMapEncodeTiled(state) failed with CUresult %d", (int)r);
+  return LA_OK;
+}
+
+// Map over a token-major [rows, heads * 128] BF16 matrix with boxes of `box_rows` tokens x 128
+// values (one head's row), unswizzled: a request's draft tokens of one head in one copy.
+la_status encode_bf16_token_map(CUtensorMap* map, const void* base, int64_t rows, int64_t heads,
+                                       int box_rows, const char* name) {
+  auto enc = la_host::tensor_map_encoder();
+  if (!enc) return fail(LA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the CUDA driver");
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(heads * 128), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(heads * 128 * 2)};
+  const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t elem_strides[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+                         elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(LA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", name, (int)r);
+  return LA_OK;
+}
+
+
 // Shape checks shared by the three entry points.
 la_status check_shapes(int B, int T, int H, int HV, int D, int V, int pool_size, const int32_t* state_indices) {
   if (D != lad::kDim || V != lad::kDim)
@@ -128,10 +163,10 @@ la_status la_verify(const void* q, const void* k, const void* v, const float* sl
   if (st != LA_OK) return st;
   CUtensorMap tm_s, tm_q, tm_k, tm_v;
   const int64_t rows = static_cast<int64_t>(B) * T;
-  if ((st = la_host::encode_f32_state_map(&tm_s, state, static_cast<int64_t>(pool_size) * HV * 128)) != LA_OK ||
-      (st = la_host::encode_bf16_token_map(&tm_q, q, rows, H, lav::kMaxTok, "q")) != LA_OK ||
-      (st = la_host::encode_bf16_token_map(&tm_k, k, rows, H, lav::kMaxTok, "k")) != LA_OK ||
-      (st = la_host::encode_bf16_token_map(&tm_v, v, rows, HV, lav::kMaxTok, "v")) != LA_OK)
+  if ((st = encode_f32_state_map(&tm_s, state, static_cast<int64_t>(pool_size) * HV * 128)) != LA_OK ||
+      (st = encode_bf16_token_map(&tm_q, q, rows, H, lav::kMaxTok, "q")) != LA_OK ||
+      (st = encode_bf16_token_map(&tm_k, k, rows, H, lav::kMaxTok, "k")) != LA_OK ||
+      (st = encode_bf16_token_map(&tm_v, v, rows, HV, lav::kMaxTok, "v")) != LA_OK)
     return st;
   lav::Params vp{};
   vp.slopes = slopes;

@@ -116,40 +116,6 @@ inline la_status encode_bf16_out_map(CUtensorMap* map, void* base, int64_t rows,
   return LA_OK;
 }
 
-// Map over a pool of FP32 states viewed as [rows, 128] (rows = slots x heads x 128 value rows):
-// 32 x 128 boxes (32 columns = 128 bytes, 128 rows), 128-byte swizzle, the K-major operand
-// layout of a TF32 tensor-core product.
-inline la_status encode_f32_state_map(CUtensorMap* map, const void* base, int64_t rows) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return fail(LA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the CUDA driver");
-  const cuuint64_t dims[2] = {128, static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {128 * 4};
-  const cuuint32_t box[2] = {32, 128};
-  const cuuint32_t elem_strides[2] = {1, 1};
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box,
-                         elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(LA_ERR_CUDA, "cuTensorMapEncodeTiled(state) failed with CUresult %d", (int)r);
-  return LA_OK;
-}
-
-// Map over a token-major [rows, heads * 128] BF16 matrix with boxes of `box_rows` tokens x 128
-// values (one head's row), unswizzled: a request's draft tokens of one head in one copy.
-inline la_status encode_bf16_token_map(CUtensorMap* map, const void* base, int64_t rows, int64_t heads,
-                                       int box_rows, const char* name) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return fail(LA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the CUDA driver");
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(heads * 128), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(heads * 128 * 2)};
-  const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
-  const cuuint32_t elem_strides[2] = {1, 1};
-  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-                         elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(LA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with CUresult %d", name, (int)r);
-  return LA_OK;
-}
-
 // Argument checks of a prefill call (la_prefill_fwd's contract): shapes, modes, pointers,
 // alignment and the state pool.  Sets *nothing_to_do when the call has no work.
 inline la_status check_prefill_args(const void* q, const void* k, const void* v, const float* slopes,
