@@ -10,12 +10,14 @@
  *     G_t  = dL/dS_t = scale dout_t q_t^T + lambda G_{t+1},   G_{L-1} = scale dout q^T + dh_final
  *     dk_t = G_t^T v_t,   dv_t = G_t k_t,   dh0 = lambda G_0   (dh0 = dh_final when L = 0)
  * Each of dq, dv and dk is itself the forward recurrence on rearranged inputs, so the call runs
- * the chunkwise forward kernel three times:
+ * the chunkwise kernel three times:
  *     dq = forward(q' = dout, k' = v, v' = k, h0' = h0^T)                          in token order
- *     dv = forward(q' = k, k' = q, v' = dout, h0' = dh_final / (lambda scale))     in reversed order
- *     dk = forward(q' = v, k' = dout, v' = q, h0' = (dh_final / (lambda scale))^T) in reversed order
- * where reversed order reverses the tokens of each sequence (cu_seqlens are unchanged), and
- * dh0 = lambda scale times the final state of the dv run.  (The forward pass decays its initial
+ *     dv = forward(q' = k, k' = q, v' = dout, h0' = dh_final / (lambda scale))     in reverse order
+ *     dk = forward(q' = v, k' = dout, v' = q, h0' = (dh_final / (lambda scale))^T) in reverse order
+ * where reverse order runs the recurrence over each sequence from its last token to its first,
+ * on the tokens in place (the kernel's reverse instance: chunks from last to first, the causal
+ * mask and the decay exponents of a chunk mirrored), and dh0 = lambda scale times the final
+ * state of the dv run.  (The forward pass decays its initial
  * state by lambda^(t+1) at token t, the gradient of the final state enters G undecayed at the
  * last token: hence the 1 / lambda.)  For a head with slope > 64 (lambda < e^-64) the reversed
  * runs start from zero and dh_final's term, which is below FP32 resolution at every token but
@@ -35,8 +37,9 @@ extern "C" {
 
 /*
  * Bytes of device workspace la_prefill_bwd needs for these sizes (has_h0 / has_dh_final: 0 or
- * 1): four reversed copies of the inputs and two reversed gradients (tokens x H x D BF16
- * each), a transposed copy of h0, and the scaled (and transposed) dh_final.  Host only.
+ * 1): a transposed copy of h0 and the scaled (and transposed) dh_final, P x H states of D x D
+ * FP32 each; 0 when neither is given.  B and T are accepted for the call's shape and do not
+ * change the size.  Host only.
  */
 la_status la_prefill_bwd_workspace(int B, int T, int H, int D, int pool_size, int has_h0, int has_dh_final,
                                    size_t* bytes);
@@ -53,8 +56,8 @@ la_status la_prefill_bwd_workspace(int B, int T, int H, int D, int pool_size, in
  *   dq, dk, dv bf16 [B*T, H, D]
  *   dh0       fp32  [P, H, D, D]    nullable (not computed)
  * workspace: device memory of at least la_prefill_bwd_workspace(...) bytes, 256-byte aligned,
- * owned by the caller, not read before it is written; calls sharing one workspace must not
- * overlap on the GPU.
+ * owned by the caller, not read before it is written (nullable when that size is 0); calls
+ * sharing one workspace must not overlap on the GPU.
  *
  * Supported: H == HV (one value head per q/k head), D == V == 128 or 64, any N >= 0 and any
  * sequence lengths; 16-byte aligned tensors.  Other shapes return LA_ERR_UNSUPPORTED and

@@ -24,7 +24,7 @@ SOURCES = ["la_prefill_api.cu", "la_decode_api.cu", "la_segment_api.cu", "la_seg
            "la_backward_api.cu"]
 DEPENDS = ["la_prefill_api.cu", "la_prefill_kernel.cuh", "sm103_ptx.cuh", "la_decode_api.cu", "la_decode_kernels.cuh",
            "la_segment_api.cu", "la_segment_kernels.cuh", "la_segment_static_api.cu", "la_host_common.h",
-           "la_backward_api.cu", "la_verify_kernel.cuh"]
+           "la_backward_api.cu", "la_verify_kernel.cuh", "la_prefill_internal.h"]
 HEADERS = ["la_prefill.h", "la_decode.h", "la_segment.h", "la_backward.h"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

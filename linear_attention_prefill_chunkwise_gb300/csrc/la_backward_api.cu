@@ -1,10 +1,10 @@
-// la_backward_api.cu -- host side of include/la_backward.h and its three helper kernels.
+// la_backward_api.cu -- host side of include/la_backward.h and its helper kernels.
 //
-// The backward pass runs the chunkwise forward kernel (la_prefill_fwd) three times on
-// rearranged inputs (the derivation is in include/la_backward.h); what is left to do here is
-// moving data: reversing the tokens of every sequence, transposing and scaling [D x D] states,
-// and the final scaling of dh0.  All three are bandwidth-bound copy kernels; nothing here
-// reads device memory on the host or synchronises.
+// The backward pass runs the chunkwise kernel three times on rearranged inputs (the derivation
+// is in include/la_backward.h): once forward (la_prefill_fwd) and twice in its reverse instance,
+// which walks every sequence from its last token to its first in place.  What is left to do here
+// is transposing and scaling [D x D] states, the final scaling of dh0 and the large-slope
+// fix-up; nothing here reads device memory on the host or synchronises.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -13,72 +13,16 @@
 
 #include "../../include/la_backward.h"
 #include "la_host_common.h"
+#include "la_prefill_internal.h"
 
 namespace labw {
 
 constexpr int kCopyThreads = 256;
-constexpr int kMaxPairs = 4;
-// Largest slope whose 1 / lambda = e^slope scales dh_final into the reversed runs' initial state
+// Largest slope whose 1 / lambda = e^slope scales dh_final into the reverse runs' initial state
 // (e^64 = 6.2e27, far from FP32 overflow); heads with larger slopes start those runs from zero
 // and get dh_final's only non-negligible term, at their sequence's last token, from
 // la_bwd_big_slope_kernel (the others carry lambda^n <= e^-64).
 constexpr float kBigSlope = 64.f;
-
-// Sequence bounds of token row r: [b, e).  Rows outside every sequence (or of a sequence with
-// bounds the forward kernel would reject) map to themselves.
-__device__ __forceinline__ int row_bounds(const int32_t* cu, int N, int T, int tokens, int r, int& b, int& e) {
-  if (!cu) {
-    b = (r / T) * T;
-    e = b + T;
-    return r / T;
-  }
-  int lo = 0, hi = N;  // largest n with cu[n] <= r
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (__ldg(cu + mid) <= r) lo = mid;
-    else hi = mid - 1;
-  }
-  b = lo < N ? __ldg(cu + lo) : r;
-  e = lo < N ? __ldg(cu + lo + 1) : r + 1;
-  if (lo >= N || b < 0 || e < b || e > tokens || r < b || r >= e) {
-    b = r;
-    e = r + 1;
-    return -1;
-  }
-  return lo;
-}
-
-struct ReverseParams {
-  const uint4* src[kMaxPairs];
-  uint4* dst[kMaxPairs];
-  int npairs;
-  int row_vec;  // 16-byte words per token row (heads * D * 2 / 16)
-  const int32_t* cu_seqlens;
-  const int32_t* state_indices;  // outputs only: rows of sequences the forward runs skip are not copied
-  int N, T, tokens, pool;
-  int outputs;
-};
-
-// dst[r] = src[b + e - 1 - r] for every token row r of a sequence [b, e), for up to four
-// tensors of one shape: each sequence's tokens in reversed order, the sequence bounds unchanged.
-__global__ void __launch_bounds__(kCopyThreads) la_reverse_rows_kernel(const ReverseParams p) {
-  for (int r = blockIdx.x; r < p.tokens; r += gridDim.x) {
-    int b, e;
-    const int n = row_bounds(p.cu_seqlens, p.N, p.T, p.tokens, r, b, e);
-    if (p.outputs) {  // the gradients exist only for the rows of sequences the forward runs computed
-      if (n < 0) continue;
-      if (p.state_indices) {
-        const int slot = __ldg(p.state_indices + n);
-        if (slot < 0 || slot >= p.pool) continue;
-      }
-    }
-    const size_t from = static_cast<size_t>(b + e - 1 - r) * p.row_vec, to = static_cast<size_t>(r) * p.row_vec;
-    for (int i = threadIdx.x; i < p.npairs * p.row_vec; i += kCopyThreads) {
-      const int pr = i / p.row_vec, w = i - pr * p.row_vec;
-      p.dst[pr][to + w] = __ldg(p.src[pr] + from + w);
-    }
-  }
-}
 
 // dst[s][b][a] = f * src[s][a][b] (transpose = 1) or dst[s][a][b] = f * src[s][a][b] (transpose
 // = 0) for square [D x D] FP32 matrices, one block per (matrix, 32 x 32 tile); matrix s belongs to
@@ -154,7 +98,7 @@ struct BigSlopeParams {
   int N, T, HV, D, tokens, pool;
 };
 
-// Heads with slope > kBigSlope, when dh_final is given: the reversed runs started from zero, so
+// Heads with slope > kBigSlope, when dh_final is given: the reverse runs started from zero, so
 // the last token's dv and dk lack dh_final's term.  With lambda <= e^-64 every other term of G at
 // that token is below FP32 resolution, so dv = G k and dk = G^T v with G = scale dout q^T +
 // dh_final are recomputed there in FP32 and rounded once; an empty sequence gets dh0 = dh_final.
@@ -212,22 +156,16 @@ __global__ void __launch_bounds__(128) la_bwd_big_slope_kernel(const BigSlopePar
 
 // Workspace layout, every section 256-byte aligned.
 struct Layout {
-  size_t rev[6];  // q_r, k_r, v_r, do_r, dv_r, dk_r
   size_t h0t, dhf, dhft;
   size_t bytes;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-inline Layout layout(int64_t tokens, int H, int D, int pool, bool has_h0, bool has_dhf) {
+inline Layout layout(int H, int D, int pool, bool has_h0, bool has_dhf) {
   Layout l{};
-  const size_t tensor = align256(static_cast<size_t>(tokens) * H * D * 2);
   const size_t states = align256(static_cast<size_t>(pool) * H * D * D * 4);
   size_t off = 0;
-  for (int i = 0; i < 6; ++i) {
-    l.rev[i] = off;
-    off += tensor;
-  }
   l.h0t = off;
   if (has_h0) off += states;
   l.dhf = off;
@@ -266,7 +204,7 @@ la_status la_prefill_bwd_workspace(int B, int T, int H, int D, int pool_size, in
   la_host::g_last_error[0] = '\0';
   if (!bytes) return fail(LA_ERR_INVALID_ARGUMENT, "bytes is null");
   if (B < 0 || T < 0 || H <= 0 || D <= 0 || pool_size < 0) return fail(LA_ERR_INVALID_ARGUMENT, "bad sizes");
-  *bytes = labw::layout(static_cast<int64_t>(B) * T, H, D, pool_size, has_h0 != 0, has_dh_final != 0).bytes;
+  *bytes = labw::layout(H, D, pool_size, has_h0 != 0, has_dh_final != 0).bytes;
   return LA_OK;
 }
 
@@ -296,8 +234,8 @@ la_status la_prefill_bwd(const void* q, const void* k, const void* v, const floa
   if (N == 0) return LA_OK;
   if (tokens == 0 && !dh0) return LA_OK;
   const int pool = (h0 || dh0 || dh_final) ? pool_size : (state_indices ? 0 : N);
-  const labw::Layout lay = labw::layout(tokens, H, D, pool, h0 != nullptr, dh_final != nullptr);
-  if (!workspace || workspace_bytes < lay.bytes)
+  const labw::Layout lay = labw::layout(H, D, pool, h0 != nullptr, dh_final != nullptr);
+  if (lay.bytes > 0 && (!workspace || workspace_bytes < lay.bytes))
     return fail(LA_ERR_INVALID_ARGUMENT, "workspace too small: %zu bytes given, %zu needed", workspace_bytes,
                 lay.bytes);
   if (reinterpret_cast<uintptr_t>(workspace) % 256) return fail(LA_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
@@ -306,8 +244,6 @@ la_status la_prefill_bwd(const void* q, const void* k, const void* v, const floa
   if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(ce));
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  void* rev[6];
-  for (int i = 0; i < 6; ++i) rev[i] = ws + lay.rev[i];
   float* h0t = h0 ? reinterpret_cast<float*>(ws + lay.h0t) : nullptr;
   float* dhf = dh_final ? reinterpret_cast<float*>(ws + lay.dhf) : nullptr;
   float* dhft = dh_final ? reinterpret_cast<float*>(ws + lay.dhft) : nullptr;
@@ -325,26 +261,7 @@ la_status la_prefill_bwd(const void* q, const void* k, const void* v, const floa
     if (st != LA_OK) return st;
   }
 
-  // 2. every sequence's tokens in reversed order
-  labw::ReverseParams rp{};
-  rp.row_vec = H * D * 2 / 16;
-  rp.cu_seqlens = cu_seqlens;
-  rp.state_indices = state_indices;
-  rp.N = N;
-  rp.T = cu_seqlens ? 0 : T;
-  rp.tokens = static_cast<int>(tokens);
-  rp.pool = la_host::effective_pool_size(h0, dh0, state_indices, pool_size, N);
-  const int rgrid = static_cast<int>(tokens < 4096 ? (tokens > 0 ? tokens : 1) : 4096);
-  if (tokens > 0) {
-    const void* srcs[4] = {q, k, v, dout};
-    rp.npairs = 4;
-    for (int i = 0; i < 4; ++i) {
-      rp.src[i] = static_cast<const uint4*>(srcs[i]);
-      rp.dst[i] = static_cast<uint4*>(rev[i]);
-    }
-    labw::la_reverse_rows_kernel<<<rgrid, labw::kCopyThreads, 0, s>>>(rp);
-    if ((st = launched("token reversal")) != LA_OK) return st;
-  }
+  // 2. dh_final / (lambda scale), as it is and transposed: the reverse runs' initial states
   if (dh_final && pool > 0) {
     labw::la_transpose_states_kernel<<<tgrid, tblock, 0, s>>>(dh_final, dhf, D, slopes, HV, scale, 0);
     if ((st = launched("state scaling")) != LA_OK) return st;
@@ -352,26 +269,17 @@ la_status la_prefill_bwd(const void* q, const void* k, const void* v, const floa
     if ((st = launched("state transpose")) != LA_OK) return st;
   }
 
-  // 3. dv (and dh0): the reversed recurrence with (q, k, v) -> (k, q, dout) from dh_final / scale
-  st = la_prefill_fwd(rev[1], rev[0], rev[3], slopes, scale, dhf, state_indices, cu_seqlens, rev[4], dh0, B, T, N, H,
-                      HV, D, V, pool_size, LA_SCHED_AUTO, dev_error, stream);
+  // 3. dv (and dh0): the recurrence run backwards with (q, k, v) -> (k, q, dout)
+  st = la_internal::prefill_reverse(k, q, dout, slopes, scale, dhf, state_indices, cu_seqlens, dv, dh0, B, T, N, H,
+                                    HV, D, V, pool_size, dev_error, stream);
   if (st != LA_OK) return st;
-  // 4. dk: the reversed recurrence with (q, k, v) -> (v, dout, q) from (dh_final / scale)^T
+  // 4. dk: the recurrence run backwards with (q, k, v) -> (v, dout, q)
   if (tokens > 0) {
-    st = la_prefill_fwd(rev[2], rev[3], rev[0], slopes, scale, dhft, state_indices, cu_seqlens, rev[5], nullptr, B, T,
-                        N, H, HV, D, V, pool_size, LA_SCHED_AUTO, dev_error, stream);
+    st = la_internal::prefill_reverse(v, dout, q, slopes, scale, dhft, state_indices, cu_seqlens, dk, nullptr, B, T,
+                                      N, H, HV, D, V, pool_size, dev_error, stream);
     if (st != LA_OK) return st;
-    // 5. dv and dk back in token order (rows of skipped sequences untouched)
-    rp.npairs = 2;
-    rp.outputs = 1;
-    rp.src[0] = static_cast<const uint4*>(rev[4]);
-    rp.dst[0] = static_cast<uint4*>(dv);
-    rp.src[1] = static_cast<const uint4*>(rev[5]);
-    rp.dst[1] = static_cast<uint4*>(dk);
-    labw::la_reverse_rows_kernel<<<rgrid, labw::kCopyThreads, 0, s>>>(rp);
-    if ((st = launched("token reversal")) != LA_OK) return st;
   }
-  // 6. dh0 = scale lambda G_0 / scale
+  // 5. dh0 = scale lambda G_0 / scale
   if (dh0) {
     labw::Dh0Params dp{};
     dp.dh0 = dh0;
@@ -388,7 +296,7 @@ la_status la_prefill_bwd(const void* q, const void* k, const void* v, const floa
     labw::la_finish_dh0_kernel<<<static_cast<unsigned>(N) * HV, labw::kCopyThreads, 0, s>>>(dp);
     if ((st = launched("dh0")) != LA_OK) return st;
   }
-  // 7. heads with slopes beyond kBigSlope: dh_final's last-token term
+  // 6. heads with slopes beyond kBigSlope: dh_final's last-token term
   if (dh_final) {
     labw::BigSlopeParams bp{};
     bp.q = static_cast<const __nv_bfloat16*>(q);

@@ -19,6 +19,7 @@
 #include "../../include/la_prefill.h"
 #include "la_decode_kernels.cuh"
 #include "la_host_common.h"
+#include "la_prefill_internal.h"
 #include "la_prefill_kernel.cuh"
 
 namespace {
@@ -35,6 +36,17 @@ int smem_bytes() { return static_cast<int>(sizeof(lap::SharedStorage)) + 1024; }
 constexpr int kShortMax = 32;
 // Packed batches with at most this many tokens per sequence on average are split.
 constexpr int kSplitAvg = 64;
+
+cudaError_t setup_kernels() {
+  const cudaFuncAttribute attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  cudaError_t e = cudaFuncSetAttribute(lap::la_prefill_fwd_kernel<false, 128>, attr, smem_bytes());
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(lap::la_prefill_fwd_kernel<true, 128>, attr, smem_bytes());
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(lap::la_prefill_fwd_kernel<false, 64>, attr, smem_bytes());
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(lap::la_prefill_fwd_kernel<true, 64>, attr, smem_bytes());
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(lap::la_prefill_fwd_kernel<false, 128, true>, attr, smem_bytes());
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(lap::la_prefill_fwd_kernel<false, 64, true>, attr, smem_bytes());
+  return e;
+}
 
 }  // namespace
 
@@ -70,14 +82,7 @@ la_status la_prefill_fwd(const void* q, const void* k, const void* v, const floa
 
   // ---- device
   la_host::DeviceState* dsp = nullptr;
-  la_status dst = la_host::current_device(g_dev, &dsp, [] {
-    const cudaFuncAttribute attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
-    cudaError_t e = cudaFuncSetAttribute(lap::la_prefill_fwd_kernel<false, 128>, attr, smem_bytes());
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(lap::la_prefill_fwd_kernel<true, 128>, attr, smem_bytes());
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(lap::la_prefill_fwd_kernel<false, 64>, attr, smem_bytes());
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(lap::la_prefill_fwd_kernel<true, 64>, attr, smem_bytes());
-    return e;
-  });
+  la_status dst = la_host::current_device(g_dev, &dsp, setup_kernels);
   if (dst != LA_OK) return dst;
   la_host::DeviceState& ds = *dsp;
   cudaError_t ce;
@@ -174,3 +179,59 @@ la_status la_prefill_fwd(const void* q, const void* k, const void* v, const floa
 }
 
 }  // extern "C"
+
+namespace la_internal {
+
+la_status prefill_reverse(const void* q, const void* k, const void* v, const float* slopes, float scale,
+                          const float* h0, const int32_t* state_indices, const int32_t* cu_seqlens, void* o,
+                          float* h_final, int B, int T, int N, int H, int HV, int D, int V, int pool_size,
+                          int* dev_error, void* stream) {
+  bool nothing = false;
+  la_status st = la_host::check_prefill_args(q, k, v, slopes, h0, state_indices, cu_seqlens, o, h_final, B, T, N, H,
+                                             HV, D, V, pool_size, dev_error, &nothing);
+  if (st != LA_OK || nothing) return st;
+  const int64_t tokens = static_cast<int64_t>(B) * T;
+  const int64_t units = static_cast<int64_t>(N) * HV;
+  la_host::DeviceState* dsp = nullptr;
+  if ((st = la_host::current_device(g_dev, &dsp, setup_kernels)) != LA_OK) return st;
+  CUtensorMap tm_q, tm_k, tm_v, tm_o;
+  memset(&tm_q, 0, sizeof(tm_q));
+  memset(&tm_k, 0, sizeof(tm_k));
+  memset(&tm_v, 0, sizeof(tm_v));
+  memset(&tm_o, 0, sizeof(tm_o));
+  if (tokens > 0) {
+    if ((st = la_host::encode_bf16_rows_map(&tm_q, q, tokens, H, "q", D)) != LA_OK) return st;
+    if ((st = la_host::encode_bf16_rows_map(&tm_k, k, tokens, H, "k", D)) != LA_OK) return st;
+    if ((st = la_host::encode_bf16_rows_map(&tm_v, v, tokens, HV, "v", D)) != LA_OK) return st;
+    if ((st = la_host::encode_bf16_out_map(&tm_o, o, tokens, HV, D)) != LA_OK) return st;
+  }
+  lap::KernelParams p;
+  p.slopes = slopes;
+  p.h0 = h0;
+  p.state_indices = state_indices;
+  p.cu_seqlens = cu_seqlens;
+  p.o = static_cast<__nv_bfloat16*>(o);
+  p.h_final = h_final;
+  p.dev_error = dev_error;
+  p.scale = scale;
+  p.num_tokens = static_cast<int>(tokens);
+  p.T = cu_seqlens ? 0 : T;
+  p.N = N;
+  p.H = H;
+  p.HV = HV;
+  p.G = HV / H;
+  p.pool_size = la_host::effective_pool_size(h0, h_final, state_indices, pool_size, N);
+  p.num_units = static_cast<int>(units);
+  p.short_max = -1;  // every sequence, however short, runs here
+  const int grid = static_cast<int>(units < dsp->sms ? units : dsp->sms);
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (D == 128)
+    lap::la_prefill_fwd_kernel<false, 128, true><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p);
+  else
+    lap::la_prefill_fwd_kernel<false, 64, true><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p);
+  const cudaError_t ce = cudaGetLastError();
+  if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(ce));
+  return LA_OK;
+}
+
+}  // namespace la_internal

@@ -297,23 +297,34 @@ __device__ __forceinline__ void build_schedule(SharedStorage& sm, const KernelPa
 
 __device__ __forceinline__ uint64_t desc_at(uint64_t base, uint32_t byte_off) { return base + (byte_off >> 4); }
 
+// Index in its sequence of a unit's c-th processed chunk: the chunks of a sequence run in order
+// or, in the reverse instance (kRev), from the last to the first.  The partition into 64-token
+// chunks is the same either way: only the sequence's last chunk can be ragged.
+template <bool kRev>
+__device__ __forceinline__ int seq_chunk(int c, int nchunks) { return kRev ? nchunks - 1 - c : c; }
+template <bool kRev>
+__device__ __forceinline__ int chunk_rows(const Unit& w, int c) {
+  return min(kChunk, w.len - seq_chunk<kRev>(c, w.nchunks) * kChunk);
+}
+
 // The walk of this CTA's chunks by a role that runs ahead of the others.
-template <bool kListed>
+template <bool kListed, bool kRev>
 struct ChunkCursor {
   UnitWalk<kListed> wk;
   int c, row, hq, hv, nchunks;
   int tail;  // valid rows of the unit's last chunk (1..64)
   bool valid;
   // The current chunk ends inside its 64-row tiles: rows past the sequence's end are there.
-  __device__ __forceinline__ bool ragged() const { return c == nchunks - 1 && tail < kChunk; }
+  __device__ __forceinline__ bool ragged() const { return seq_chunk<kRev>(c, nchunks) == nchunks - 1 && tail < kChunk; }
 };
-template <bool kListed>
-__device__ __forceinline__ void cursor_seek(const SharedStorage& sm, const KernelParams& p, ChunkCursor<kListed>& k) {
+template <bool kListed, bool kRev>
+__device__ __forceinline__ void cursor_seek(const SharedStorage& sm, const KernelParams& p,
+                                            ChunkCursor<kListed, kRev>& k) {
   for (; k.wk.valid(sm, p); k.wk.next()) {
     const Unit w = decode_unit(p, k.wk.unit(sm));
     if (w.run && w.nchunks > 0) {
       k.c = 0;
-      k.row = w.bos;
+      k.row = w.bos + (kRev ? kChunk * (w.nchunks - 1) : 0);
       k.hq = w.hq;
       k.hv = w.hv;
       k.nchunks = w.nchunks;
@@ -324,10 +335,11 @@ __device__ __forceinline__ void cursor_seek(const SharedStorage& sm, const Kerne
   }
   k.valid = false;
 }
-template <bool kListed>
-__device__ __forceinline__ void cursor_next(const SharedStorage& sm, const KernelParams& p, ChunkCursor<kListed>& k) {
+template <bool kListed, bool kRev>
+__device__ __forceinline__ void cursor_next(const SharedStorage& sm, const KernelParams& p,
+                                            ChunkCursor<kListed, kRev>& k) {
   if (++k.c < k.nchunks) {
-    k.row += kChunk;
+    k.row += kRev ? -kChunk : kChunk;
   } else {
     k.wk.next();
     cursor_seek(sm, p, k);
@@ -337,7 +349,7 @@ __device__ __forceinline__ void cursor_next(const SharedStorage& sm, const Kerne
 // TMA and MMA thread B, one polling loop: each pass issues, in this order, every job whose
 // inputs are ready (mbarrier.test_wait, no blocking): dS(i) = V(i)^T Kt(i), scores(i) =
 // Q(i) K(i)^T, and the next Q/K and V loads once their ring slots have been released.
-template <bool kListed, int kD>
+template <bool kListed, int kD, bool kRev>
 __device__ __forceinline__ void tma_mma_loop(SharedStorage& sm, const KernelParams& p, const CUtensorMap* tm_q,
                                              const CUtensorMap* tm_k, const CUtensorMap* tm_v, uint32_t tmem,
                                              volatile int* abort) {
@@ -355,9 +367,9 @@ __device__ __forceinline__ void tma_mma_loop(SharedStorage& sm, const KernelPara
   const uint32_t t_scores = tmem + kColScores, t_ds = tmem + kColDeltaS;
   const uint32_t total = cta_chunk_count<kListed>(sm, p);
   uint32_t n_ds = 0, n_sc = 0, nqk = 0, nv = 0;
-  ChunkCursor<kListed> cq{UnitWalk<kListed>(sm, p)};
+  ChunkCursor<kListed, kRev> cq{UnitWalk<kListed>(sm, p)};
   cursor_seek(sm, p, cq);
-  ChunkCursor<kListed> cv = cq;
+  ChunkCursor<kListed, kRev> cv = cq;
   uint64_t last = globaltimer_ns();
   while (n_ds < total || n_sc < total || cq.valid || cv.valid) {
     bool progressed = false;
@@ -517,7 +529,7 @@ __device__ __forceinline__ void mma_o_loop(SharedStorage& sm, const KernelParams
 // tensor core reads as TF32, i.e. truncated to 10 mantissa bits; rounding it here instead
 // would cost two more instructions per element on the critical conversion and changes the
 // output by far less than its BF16 step.  Thread t owns token row s = t of the chunk.
-template <bool kListed, int kD>
+template <bool kListed, int kD, bool kRev>
 __device__ __forceinline__ void convert_loop(SharedStorage& sm, const KernelParams& p, int ctid,
                                              volatile int* abort) {
   const int s = ctid;
@@ -526,9 +538,17 @@ __device__ __forceinline__ void convert_loop(SharedStorage& sm, const KernelPara
   for (UnitWalk<kListed> wk(sm, p); wk.valid(sm, p) && ok; wk.next()) {
     const Unit w = decode_unit(p, wk.unit(sm));
     if (!w.run) continue;
-    const float f = p.scale * expf(-__ldg(p.slopes + w.hv) * static_cast<float>(s + 1));  // scale lambda^(s+1)
-    const uint64_t ff = f2_pack(f, f);
+    // scale lambda^(s+1): row s is s + 1 tokens past the state; in the reverse instance the state
+    // enters a chunk of L tokens after its last one, L - s tokens from row s (rows s >= L are
+    // never stored: 0)
+    const float slope = __ldg(p.slopes + w.hv);
+    const float f = p.scale * expf(-slope * static_cast<float>(kRev ? kChunk - s : s + 1));
+    const float ftail = kRev && s < w.len - kChunk * (w.nchunks - 1)
+                            ? p.scale * expf(-slope * static_cast<float>(w.len - kChunk * (w.nchunks - 1) - s))
+                            : 0.f;
     for (int c = 0; c < w.nchunks; ++c, ++it) {
+      const float fc = (kRev && chunk_rows<kRev>(w, c) < kChunk) ? ftail : f;
+      const uint64_t ff = f2_pack(fc, fc);
       const uint32_t sq = it % kQKStages, qph = (it / kQKStages) & 1u;
       const uint32_t b = it & 1u, bph = (it >> 1) & 1u;
       if (!warp_wait(&sm.qk_full[sq], qph, abort) || !warp_wait(&sm.qt_free[b], bph ^ 1u, abort)) {
@@ -555,8 +575,10 @@ __device__ __forceinline__ void convert_loop(SharedStorage& sm, const KernelPara
   }
 }
 
-// Operand warpgroup: Kt = lambda^(L-1-j) k_j and P = A * lambda^(s-j) (causal, tail masked), as BF16 hi/lo.
-template <bool kListed, int kD>
+// Operand warpgroup: Kt = lambda^(L-1-j) k_j and P = A * lambda^(s-j) (causal, tail masked), as BF16 hi/lo;
+// in the reverse instance Kt = lambda^j k_j and P = A * lambda^(j-s) for j >= s (the recurrence
+// run from a chunk's last token to its first).
+template <bool kListed, int kD, bool kRev>
 __device__ __forceinline__ void operand_loop(SharedStorage& sm, const KernelParams& p, uint32_t tmem, int otid,
                                              volatile int* abort) {
   const int warp = otid >> 5, lane = otid & 31;
@@ -575,11 +597,16 @@ __device__ __forceinline__ void operand_loop(SharedStorage& sm, const KernelPara
     // decay row of P for this thread: scale lambda^(s-j) for j <= s, 0 above the diagonal
     float drow[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) drow[i] = (pcol + i <= prow) ? p.scale * lam[max(prow - pcol - i, 0)] : 0.f;
+    for (int i = 0; i < 32; ++i) {
+      if (kRev)
+        drow[i] = (pcol + i >= prow) ? p.scale * lam[max(pcol + i - prow, 0)] : 0.f;
+      else
+        drow[i] = (pcol + i <= prow) ? p.scale * lam[max(prow - pcol - i, 0)] : 0.f;
+    }
     for (int c = 0; c < w.nchunks; ++c, ++it) {
       const uint32_t sq = it % kQKStages, qph = (it / kQKStages) & 1u;
       const uint32_t ph = it & 1u;
-      const int L = min(kChunk, w.len - c * kChunk);
+      const int L = chunk_rows<kRev>(w, c);
 
       // ---- Kt: same swizzled layout as the K tile
       if (!warp_wait(&sm.qk_full[sq], qph, abort) || !warp_wait(&sm.kt_free, ph ^ 1u, abort)) {
@@ -603,7 +630,7 @@ __device__ __forceinline__ void operand_loop(SharedStorage& sm, const KernelPara
           }
         }
         {
-          const float wjf = (krow < L) ? lam[L - 1 - krow] : 0.f;
+          const float wjf = (krow < L) ? lam[kRev ? krow : L - 1 - krow] : 0.f;
           const uint64_t wj = f2_pack(wjf, wjf);
           const uint8_t* ksrc = sm.qk[sq].k[kbox];
 #pragma unroll 2
@@ -668,7 +695,7 @@ __device__ __forceinline__ void operand_loop(SharedStorage& sm, const KernelPara
 }
 
 // State warpgroups: own S in registers, advance it, publish it to TMEM, write the output.
-template <bool kListed, int kD>
+template <bool kListed, int kD, bool kRev>
 __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams& p, const CUtensorMap* tm_o,
                                           uint32_t tmem, int ctid, volatile int* abort) {
   const int warp = ctid >> 5, lane = ctid & 31;
@@ -731,7 +758,7 @@ __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams&
     for (int c = 0; c < w.nchunks; ++c, ++it) {
       const uint32_t ph = it & 1u;
       const uint32_t b = it & 1u, bph = (it >> 1) & 1u;
-      const int L = min(kChunk, w.len - c * kChunk);
+      const int L = chunk_rows<kRev>(w, c);
 
       // ---- S(i+1) = lambda^L S(i) + Delta S(i), in registers
       if (!warp_wait(&sm.ds_full, ph, abort)) {
@@ -809,7 +836,7 @@ __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams&
           }
         }
         if (rows > 0) {
-          const int y0 = w.bos + c * kChunk + 32 * wg;
+          const int y0 = w.bos + seq_chunk<kRev>(c, w.nchunks) * kChunk + 32 * wg;
           if (rows >= 32) {
             fence_proxy_async_smem();
             __syncwarp();
@@ -848,7 +875,7 @@ __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams&
   return err;
 }
 
-template <bool kListed, int kD>
+template <bool kListed, int kD, bool kRev = false>
 __global__ void __launch_bounds__(kThreads, 1)
 la_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -918,17 +945,17 @@ la_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   }
 
   if (warp == 0) {
-    if (lane == 0) tma_mma_loop<kListed, kD>(sm, p, &tm_q, &tm_k, &tm_v, tmem, abort);
+    if (lane == 0) tma_mma_loop<kListed, kD, kRev>(sm, p, &tm_q, &tm_k, &tm_v, tmem, abort);
   } else if (warp == 1) {
     if (lane == 0) mma_o_loop<kListed, kD>(sm, p, tmem, abort);
   } else if (warp < 4) {
-    convert_loop<kListed, kD>(sm, p, tid - 64, abort);
+    convert_loop<kListed, kD, kRev>(sm, p, tid - 64, abort);
   } else if (warp < 12) {
-    const int err = state_loop<kListed, kD>(sm, p, &tm_o, tmem, tid - 128, abort);
+    const int err = state_loop<kListed, kD, kRev>(sm, p, &tm_o, tmem, tid - 128, abort);
     if (err && tid == 128 && p.dev_error) atomicOr(p.dev_error, err);
     if ((tid & 31) == 0) bulk_wait_all();  // this warp's output stores have completed
   } else {
-    operand_loop<kListed, kD>(sm, p, tmem, tid - 384, abort);
+    operand_loop<kListed, kD, kRev>(sm, p, tmem, tid - 384, abort);
   }
 
   tc_fence_before();

@@ -235,7 +235,7 @@ def call_backward(**over):
     (dict(dout=None), LA_INVALID),
     (dict(dk=FAKE + 2), LA_INVALID),             # misaligned
     (dict(dhf=FAKE, scale=0.0, h0=FAKE, P=2), LA_INVALID),  # dh_final needs scale != 0
-    (dict(wsb=1024), LA_INVALID),                # workspace too small
+    (dict(wsb=1024, h0=FAKE, P=2), LA_INVALID),  # workspace too small (it holds h0 transposed)
     (dict(ws=FAKE + 16), LA_INVALID),            # workspace not 256-byte aligned
     (dict(N=3), LA_INVALID),
 ])
@@ -249,7 +249,17 @@ def test_backward_empty_batch_is_a_no_op():
 
 
 def test_backward_workspace_size():
-    # six reversed [tokens, H, D] BF16 tensors, a transposed h0 and two forms of dh_final
+    # a transposed h0 and two forms of dh_final, P x H states of D x D FP32 each; nothing else
     nbytes = lap.la_prefill_bwd_workspace(2, 8192, 64, 128, 2, True, True)
-    assert nbytes == 6 * 2 * 8192 * 64 * 128 * 2 + 3 * 2 * 64 * 128 * 128 * 4
-    assert lap.la_prefill_bwd_workspace(1, 100, 2, 64, 0, False, False) == 6 * ((100 * 2 * 64 * 2 + 255) // 256 * 256)
+    assert nbytes == 3 * 2 * 64 * 128 * 128 * 4
+    assert lap.la_prefill_bwd_workspace(2, 8192, 64, 128, 2, True, False) == 2 * 64 * 128 * 128 * 4
+    assert lap.la_prefill_bwd_workspace(1, 100, 2, 64, 3, False, True) == 2 * 3 * 2 * 64 * 64 * 4
+    assert lap.la_prefill_bwd_workspace(1, 100, 2, 64, 0, False, False) == 0
+
+
+def test_backward_without_states_needs_no_workspace():
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # past every host check (no workspace needed without h0 and dh_final): the device query fails
+    assert call_backward(ws=None, wsb=0) == LA_CUDA

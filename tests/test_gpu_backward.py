@@ -130,3 +130,27 @@ def test_backward_refuses_gva():
         lap.la_prefill_bwd(q, k, v, torch.from_numpy(p.slopes).cuda(), p.scale, to_torch_bf16(dout, "cuda"),
                            cu_seqlens=torch.from_numpy(p.cu_seqlens).cuda())
     assert e.value.name == "LA_ERR_UNSUPPORTED"
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_backward_nonfinite_sequence_does_not_reach_its_neighbours(D):
+    """A packed sequence whose q, k, v and dout hold infinities and NaNs leaves the gradients of
+    every other sequence bitwise as they are with finite values there: the reverse runs read,
+    in a sequence's last (ragged) chunk, rows of the next sequence, which must stay out."""
+    import dataclasses
+    p, dout, dhf = _grad_problem(4405, D=D, lengths=[70, 100, 45, 130], H=2, HV=2, pool=6, indices=[4, 1, 5, 0])
+    clean = _run(p, dout, dhf)
+    a, b = int(p.cu_seqlens[1]), int(p.cu_seqlens[2])
+    bits = {n: getattr(p, n).copy() for n in ("q_bits", "k_bits", "v_bits")}
+    inf, nan, ninf = np.uint16(0x7F80), np.uint16(0x7FC0), np.uint16(0xFF80)
+    bits["q_bits"][a] = ninf
+    bits["k_bits"][a + 3, :, :5] = inf
+    bits["v_bits"][b - 1] = nan
+    dout_bad = dout.copy()
+    dout_bad[a + 50] = inf
+    bad = _run(dataclasses.replace(p, **bits), dout_bad, dhf)
+    keep = np.r_[0:a, b:p.tokens]
+    for name, x, y in zip(("dq", "dk", "dv"), clean[:3], bad[:3]):
+        assert np.array_equal(x[keep].view(np.uint32), y[keep].view(np.uint32)), f"{name} of a neighbour changed"
+    slots = [4, 5, 0]  # the other sequences' slots
+    assert np.array_equal(clean[3][slots].view(np.uint32), bad[3][slots].view(np.uint32)), "dh0 of a neighbour changed"
