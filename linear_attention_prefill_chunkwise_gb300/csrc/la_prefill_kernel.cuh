@@ -888,6 +888,19 @@ la_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   const int lane = tid & 31;
   volatile int* abort = &sm.abort;
 
+  if (p.short_max >= 0) {
+    // Launched beside the tokenwise kernel for a packed batch of short sequences: unless some
+    // sequence is longer than short_max (or has bounds this kernel must report), every CTA
+    // leaves before taking any resource.
+    bool work = false;
+    for (int n = tid; n < p.N && !work; n += kThreads) {
+      const int b = __ldg(p.cu_seqlens + n), e = __ldg(p.cu_seqlens + n + 1);
+      const bool bad = b < 0 || e < b || e > p.num_tokens;
+      work = bad || (e - b > p.short_max && (!p.state_indices || __ldg(p.state_indices + n) >= 0));
+    }
+    if (!__syncthreads_or(work)) return;
+  }
+
   if (warp == 1) {
     tmem_alloc(&sm.tmem_base, kTmemCols);
     tmem_relinquish();
