@@ -523,6 +523,8 @@ def run_sweep(args):
                 "bound": "hbm" if nbytes / (hbm * 1e9) >= flops / (tflops * 1e12) else "tensor",
                 "peaks": {"hbm_gbs": hbm, "hbm_source": hbm_kind, "bf16_tflops": tflops, "tflops_source": tf_kind},
                 "steps": args.sweep_steps, "l2": "flushed between launches (256 MB write)"}
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = oracle_forward_baseline(p, ms)
         print(json.dumps(line), flush=True)
     if args.sweep_what in ("all", "decode"):
         run_decode_sweep(args, device, stream, flush, hbm, hbm_kind)
@@ -571,6 +573,15 @@ def run_decode_sweep(args, device, stream, flush, hbm, hbm_kind):
         "la_commit": (lambda: lap.la_commit(pool, kbuf, vbuf, acc, sl, state_indices=idx, stream=stream),
                       2 * state_b + kv_b),
     }
+    # the oracle's recurrence over the same requests and draft tokens (decode's outputs and states;
+    # verify's outputs; commit's states with every token accepted): one CPU time for the three
+    if not args.no_cpu_baseline:
+        import oracle
+        threads = oracle.max_threads()
+        t0 = time.perf_counter()
+        oracle.tokenwise(p.q(), p.k(), p.v(), p.slopes, p.scale, h0=p.h0.astype(np.float64),
+                         state_indices=p.state_indices, cu_seqlens=p.cu_seqlens, nthreads=threads)
+        cpu_ms = (time.perf_counter() - t0) * 1e3
     for name, (fn, nbytes) in ops.items():
         with torch.cuda.stream(stream):
             for _ in range(3):
@@ -586,12 +597,18 @@ def run_decode_sweep(args, device, stream, flush, hbm, hbm_kind):
         torch.cuda.synchronize(device)
         ms = statistics.fmean(a.elapsed_time(b) for a, b in times)
         t_roof = nbytes / (hbm * 1e9)
-        print(json.dumps({"sweep": True, "op": name, "workload": "B=128 requests x T=8 draft tokens, H=HV=64, "
-                          "256-slot pool, 16 padded", "ms": round(ms, 5), "tokens_per_s": round(toks / (ms / 1e3), 1),
-                          "alg_bytes": nbytes, "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
-                          "roofline_ms": round(t_roof * 1e3, 5), "frac": round(t_roof * 1e3 / ms, 4), "bound": "hbm",
-                          "peaks": {"hbm_gbs": hbm, "hbm_source": hbm_kind}, "steps": args.sweep_steps,
-                          "l2": "flushed between launches (256 MB write)"}), flush=True)
+        line = {"sweep": True, "op": name, "workload": "B=128 requests x T=8 draft tokens, H=HV=64, "
+                "256-slot pool, 16 padded", "ms": round(ms, 5), "tokens_per_s": round(toks / (ms / 1e3), 1),
+                "alg_bytes": nbytes, "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
+                "roofline_ms": round(t_roof * 1e3, 5), "frac": round(t_roof * 1e3 / ms, 4), "bound": "hbm",
+                "peaks": {"hbm_gbs": hbm, "hbm_source": hbm_kind}, "steps": args.sweep_steps,
+                "l2": "flushed between launches (256 MB write)"}
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = {"ms": round(cpu_ms, 2), "cores": threads, "kind": "oracle",
+                                    "gpu_speedup": round(cpu_ms / ms, 1),
+                                    "sample": "every request and head, all 8 tokens (FP64 tokenwise recurrence, "
+                                              "OpenMP over (request, head))"}
+        print(json.dumps(line), flush=True)
 
 
 SEGMENT_WORKLOADS = (
@@ -647,6 +664,7 @@ def run_segment_sweep(args, device, stream, flush, hbm, hbm_kind, tflops, tf_kin
                                                             seq_len=T, segment_len=0, workspace=ws, stream=stream))
         toks, nbytes, flops = workload_roofline(p)
         t_roof = max(nbytes / (hbm * 1e9), flops / (tflops * 1e12))
+        cpu = None if args.no_cpu_baseline else oracle_forward_baseline(p, ms_seg)
         print(json.dumps({"sweep": True, "op": "la_prefill_fwd_segmented", "workload": name, "segment_len": seg,
                           "chains": B * HV, "workspace_bytes": nbytes_ws, "ms": round(ms_seg, 5),
                           "ms_plain": round(ms_plain, 5), "speedup_vs_plain": round(ms_plain / ms_seg, 3),
@@ -656,14 +674,15 @@ def run_segment_sweep(args, device, stream, flush, hbm, hbm_kind, tflops, tf_kin
                           "frac_plain": round(t_roof * 1e3 / ms_plain, 4),
                           "peaks": {"hbm_gbs": hbm, "hbm_source": hbm_kind, "bf16_tflops": tflops,
                                     "tflops_source": tf_kind},
-                          "steps": args.sweep_steps, "l2": "flushed between launches (256 MB write)"}), flush=True)
+                          "steps": args.sweep_steps, "l2": "flushed between launches (256 MB write)",
+                          **({} if cpu is None else {"cpu_baseline": cpu})}), flush=True)
 
 
 def run_backward_sweep(args, device, stream, flush, hbm, hbm_kind):
     """The backward pass (la_prefill_bwd) on the bench shape B=2, T=8192, H=HV=64, D=V=128 with
     h0, dL/do and dL/dh_final given and dh0 returned.  Algorithmic bytes: q, k, v, dout read and
-    dq, dk, dv written once, h0 and dh_final read and dh0 written once; the three forward runs,
-    the token reversals and the state transposes it is built from move more."""
+    dq, dk, dv written once, h0 and dh_final read and dh0 written once; the three chunkwise runs
+    and the state transposes it is built from move more."""
     import numpy as np
     import torch
 
@@ -704,12 +723,46 @@ def run_backward_sweep(args, device, stream, flush, hbm, hbm_kind):
     ms = statistics.fmean(a.elapsed_time(b) for a, b in times)
     nbytes = 7 * TOKENS * HV * V * 2 + 3 * B * HV * V * D * 4
     t_roof = nbytes / (hbm * 1e9)
-    print(json.dumps({"sweep": True, "op": "la_prefill_bwd", "workload": WORKLOAD + ", dL/do and dL/dh_final in, dh0 out",
-                      "ms": round(ms, 5), "tokens_per_s": round(TOKENS / (ms / 1e3), 1), "alg_bytes": nbytes,
-                      "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1), "roofline_ms": round(t_roof * 1e3, 5),
-                      "frac": round(t_roof * 1e3 / ms, 4), "bound": "hbm",
-                      "peaks": {"hbm_gbs": hbm, "hbm_source": hbm_kind}, "steps": args.sweep_steps,
-                      "l2": "flushed between launches (256 MB write)"}), flush=True)
+    line = {"sweep": True, "op": "la_prefill_bwd", "workload": WORKLOAD + ", dL/do and dL/dh_final in, dh0 out",
+            "ms": round(ms, 5), "tokens_per_s": round(TOKENS / (ms / 1e3), 1), "alg_bytes": nbytes,
+            "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1), "roofline_ms": round(t_roof * 1e3, 5),
+            "frac": round(t_roof * 1e3 / ms, 4), "bound": "hbm",
+            "peaks": {"hbm_gbs": hbm, "hbm_source": hbm_kind}, "steps": args.sweep_steps,
+            "l2": "flushed between launches (256 MB write)"}
+    if not args.no_cpu_baseline:
+        # the oracle's backward over both sequences and the first 8 of the 64 heads, scaled
+        import oracle
+        nh = 8
+        threads = oracle.max_threads()
+        dout_h = W.bf16_to_f32(dout.view(torch.int16).cpu().numpy().view(np.uint16))
+        t0 = time.perf_counter()
+        oracle.backward(p.q()[:, :nh], p.k()[:, :nh], p.v()[:, :nh], p.slopes[:nh], p.scale, dout_h[:, :nh],
+                        h0=p.h0[:, :nh].astype(np.float64), dh_final=dhf[:, :nh].cpu().numpy().astype(np.float64),
+                        T=T, nthreads=threads)
+        cpu_ms = (time.perf_counter() - t0) * 1e3 * HV / nh
+        line["cpu_baseline"] = {"ms": round(cpu_ms, 2), "cores": threads, "kind": "oracle",
+                                "gpu_speedup": round(cpu_ms / ms, 1),
+                                "sample": f"B=2 x T=8192 tokens x {nh} of {HV} heads, scaled to all heads (FP64 "
+                                          "forward and reverse sweeps, OpenMP over (sequence, head))"}
+    print(json.dumps(line), flush=True)
+
+
+def oracle_forward_baseline(p, gpu_ms, sample="the whole workload"):
+    """The FP64 oracle's tokenwise recurrence on the host cores over workload ``p`` (every
+    sequence and head, its initial states and pool): the CPU time of the same call beside the
+    GPU's."""
+    import numpy as np
+
+    import oracle
+    threads = oracle.max_threads()
+    h0 = None if p.h0 is None else p.h0.astype(np.float64)
+    t0 = time.perf_counter()
+    oracle.tokenwise(p.q(), p.k(), p.v(), p.slopes, p.scale, h0=h0, state_indices=p.state_indices,
+                     cu_seqlens=p.cu_seqlens, T=None if p.cu_seqlens is not None else p.T, want_state=p.want_final,
+                     nthreads=threads)
+    ms = (time.perf_counter() - t0) * 1e3
+    return {"ms": round(ms, 2), "cores": threads, "kind": "oracle", "gpu_speedup": round(ms / gpu_ms, 1),
+            "sample": f"{sample} (FP64 tokenwise recurrence, OpenMP over (sequence, head))"}
 
 
 def cpu_baseline(p, heads):
