@@ -140,6 +140,32 @@ def test_device_error_word_bad_seqlens_and_index():
     assert err.item() == lap.DEV_ERR_BAD_INDEX
 
 
+def test_device_error_word_all_short_batch():
+    """A packed batch of sequences of at most 32 tokens runs in the tokenwise kernel, and the
+    chunkwise kernel launched beside it returns at once unless a sequence is long or its bounds
+    are bad: bad bounds are still reported, a bad index too, and the valid sequences computed."""
+    import linear_attention_prefill_chunkwise_gb300 as lap
+    p = W.custom(seed=19, lengths=[5, 20, 31, 12], H=2, HV=2, pool=6, indices=[3, 0, 5, 1])
+    d = upload(p)
+    run_gpu(p, d)
+    torch.cuda.synchronize()
+    compare_full(p, d, "all short packed")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bad_cu = d["cu"].clone()
+    bad_cu[2] = bad_cu[1] - 1  # sequence 1 has negative length
+    lap.la_prefill_fwd(d["q"], d["k"], d["v"], d["slopes"], p.scale, h0=d["h0"], state_indices=d["idx"],
+                       cu_seqlens=bad_cu, o=d["o"], h_final=d["h_final"], dev_error=err)
+    torch.cuda.synchronize()
+    assert err.item() & lap.DEV_ERR_BAD_SEQLENS
+    err.zero_()
+    bad_idx = d["idx"].clone()
+    bad_idx[2] = 6  # == pool size
+    lap.la_prefill_fwd(d["q"], d["k"], d["v"], d["slopes"], p.scale, h0=d["h0"], state_indices=bad_idx,
+                       cu_seqlens=d["cu"], o=d["o"], h_final=d["h_final"], dev_error=err)
+    torch.cuda.synchronize()
+    assert err.item() == lap.DEV_ERR_BAD_INDEX
+
+
 def test_cuda_graph_capture_and_replay_deterministic():
     p = W.custom(seed=13, lengths=[1, 100, 64, 257], H=2, HV=2, pool=6, indices=[5, 0, 3, -1])
     d = upload(p)
