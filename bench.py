@@ -702,7 +702,7 @@ def run_backward_sweep(args, device, stream, flush, hbm, hbm_kind):
     dhf = torch.randn(h0.shape, generator=torch.Generator(device=device).manual_seed(4403), device=device) * 0.1
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     dh0 = torch.empty_like(h0)
-    ws = torch.empty(lap.la_prefill_bwd_workspace(B, T, H, D, B, True, True), dtype=torch.uint8, device=device)
+    ws = torch.empty(lap.la_prefill_bwd_workspace(B, T, H, HV, D, B, True, True), dtype=torch.uint8, device=device)
 
     def call():
         lap.la_prefill_bwd(q, k, v, sl, p.scale, dout, h0=h0, dh_final=dhf, dq=dq, dk=dk, dv=dv, dh0=dh0, seq_len=T,

@@ -81,7 +81,7 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.la_prefill_fwd_segmented_static.argtypes = [vp, vp, vp, fp, ctypes.c_float, fp, i32p, i32p, vp,
                                                             fp] + [ctypes.c_int] * 9 + [vp, vp]
             lib.la_prefill_fwd_segmented_static.restype = ctypes.c_int
-            lib.la_prefill_bwd_workspace.argtypes = [ctypes.c_int] * 7 + [vp]
+            lib.la_prefill_bwd_workspace.argtypes = [ctypes.c_int] * 8 + [vp]
             lib.la_prefill_bwd_workspace.restype = ctypes.c_int
             lib.la_prefill_bwd.argtypes = [vp, vp, vp, fp, ctypes.c_float, fp, vp, fp, i32p, i32p, vp, vp, vp, fp] + \
                 [ctypes.c_int] * 8 + [vp, ctypes.c_size_t, vp, vp]
@@ -250,11 +250,11 @@ def la_prefill_fwd_segmented_static(q, k, v, slopes, scale, h0=None, state_indic
     return o
 
 
-def la_prefill_bwd_workspace(B, T, H, D, pool_size, has_h0, has_dh_final):
+def la_prefill_bwd_workspace(B, T, H, HV, D, pool_size, has_h0, has_dh_final):
     """Bytes of device workspace la_prefill_bwd needs for these sizes."""
     lib = load_library()
     nbytes = ctypes.c_size_t(0)
-    st = lib.la_prefill_bwd_workspace(int(B), int(T), int(H), int(D), int(pool_size), int(bool(has_h0)),
+    st = lib.la_prefill_bwd_workspace(int(B), int(T), int(H), int(HV), int(D), int(pool_size), int(bool(has_h0)),
                                       int(bool(has_dh_final)), ctypes.byref(nbytes))
     if st != 0:
         _raise(lib, st)
@@ -263,11 +263,11 @@ def la_prefill_bwd_workspace(B, T, H, D, pool_size, has_h0, has_dh_final):
 
 def la_prefill_bwd(q, k, v, slopes, scale, dout, h0=None, dh_final=None, state_indices=None, cu_seqlens=None,
                    dq=None, dk=None, dv=None, dh0=None, seq_len=None, workspace=None, dev_error=None, stream=None):
-    """Gradients of the prefill (include/la_backward.h): given dout = dL/do [tokens, H, D] BF16
-    and dh_final = dL/dh_final [P, H, D, D] FP32 (or None), returns (dq, dk, dv, dh0) with the
-    layouts of q, k, v and h0 (dh0 only when a tensor is passed in).  One value head per q/k
-    head; the other arguments as la_prefill_fwd.  ``workspace`` is a CUDA uint8 tensor of at
-    least la_prefill_bwd_workspace(...) bytes, allocated here when None."""
+    """Gradients of the prefill (include/la_backward.h): given dout = dL/do [tokens, HV, D] BF16
+    and dh_final = dL/dh_final [P, HV, D, D] FP32 (or None), returns (dq, dk, dv, dh0) with the
+    layouts of q, k, v and h0 (dh0 only when a tensor is passed in).  HV a multiple of H (GVA);
+    the other arguments as la_prefill_fwd.  ``workspace`` is a CUDA uint8 tensor of at least
+    la_prefill_bwd_workspace(...) bytes, allocated here when None."""
     import torch
     lib = load_library()
     _check(dout, "dout", torch.bfloat16, 3)
@@ -287,7 +287,7 @@ def la_prefill_bwd(q, k, v, slopes, scale, dout, h0=None, dh_final=None, state_i
                                                           dh0 if dh0 is not None else dh_final, seq_len, dev_error,
                                                           stream)
     if workspace is None:
-        nbytes = la_prefill_bwd_workspace(B, T, H, D, pool, h0 is not None, dh_final is not None)
+        nbytes = la_prefill_bwd_workspace(B, T, H, HV, D, pool, h0 is not None, dh_final is not None)
         workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
     _check(workspace, "workspace", torch.uint8, 1)
     st = lib.la_prefill_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes), ctypes.c_float(scale), _ptr(h0), _ptr(dout),

@@ -65,15 +65,12 @@ struct Dh0Params {
 // Sequences the forward kernels skipped are skipped too.
 __global__ void __launch_bounds__(kCopyThreads) la_finish_dh0_kernel(const Dh0Params p) {
   const int n = blockIdx.x / p.HV, hv = blockIdx.x - n * p.HV;
-  int len = p.T;
   if (p.cu_seqlens) {
     const int b = __ldg(p.cu_seqlens + n), e = __ldg(p.cu_seqlens + n + 1);
     if (b < 0 || e < b || e > p.tokens) return;
-    len = e - b;
   }
   const int slot = p.state_indices ? __ldg(p.state_indices + n) : n;
   if (slot < 0 || slot >= p.pool) return;
-  (void)len;
   const float f = p.scale * expf(-__ldg(p.slopes + hv));
   float4* st = reinterpret_cast<float4*>(p.dh0 + (static_cast<size_t>(slot) * p.HV + hv) * p.D * p.D);
   for (int i = threadIdx.x; i < p.D * p.D / 4; i += kCopyThreads) {
@@ -93,16 +90,19 @@ struct BigSlopeParams {
   const int32_t* state_indices;
   const int32_t* cu_seqlens;
   __nv_bfloat16 *dq, *dk, *dv;
+  float* dk_f32;  // GVA: value head hv's FP32 part of dk ([tokens, HV, D]), summed per group later
   float* dh0;
   float scale;
-  int N, T, HV, D, tokens, pool;
+  int N, T, H, HV, D, tokens, pool;
 };
 
 // Heads with slope > kBigSlope, when dh_final is given: the reverse runs started from zero, so
 // the last token's dv and dk lack dh_final's term.  With lambda <= e^-64 every other term of G at
 // that token is below FP32 resolution, so dv = G k and dk = G^T v with G = scale dout q^T +
-// dh_final are recomputed there in FP32 and rounded once; an empty sequence gets dh0 = dh_final.
-// One block of D threads per (sequence, head); thread i owns value row i of G and key column i.
+// dh_final are recomputed there in FP32 and rounded once (with value heads sharing a q/k head,
+// dk's part of this value head is written in FP32, to be summed over the group); an empty
+// sequence gets dh0 = dh_final.  One block of D threads per (sequence, value head); thread i
+// owns value row i of G and key column i.
 __global__ void __launch_bounds__(128) la_bwd_big_slope_kernel(const BigSlopeParams p) {
   __shared__ float sq[128], sk[128], sv[128], sd[128], red[2][4];
   const int n = blockIdx.x / p.HV, hv = blockIdx.x - n * p.HV, i = threadIdx.x, D = p.D;
@@ -124,8 +124,9 @@ __global__ void __launch_bounds__(128) la_bwd_big_slope_kernel(const BigSlopePar
     return;
   }
   const size_t row = (static_cast<size_t>(e - 1) * p.HV + hv) * D;
-  sq[i] = __bfloat162float(p.q[row + i]);
-  sk[i] = __bfloat162float(p.k[row + i]);
+  const size_t qk_row = (static_cast<size_t>(e - 1) * p.H + hv / (p.HV / p.H)) * D;
+  sq[i] = __bfloat162float(p.q[qk_row + i]);
+  sk[i] = __bfloat162float(p.k[qk_row + i]);
   sv[i] = __bfloat162float(p.v[row + i]);
   sd[i] = __bfloat162float(p.dout[row + i]);
   __syncthreads();
@@ -151,20 +152,93 @@ __global__ void __launch_bounds__(128) la_bwd_big_slope_kernel(const BigSlopePar
     gtv = fmaf(__ldg(G + static_cast<size_t>(j) * D + i), sv[j], gtv);
   }
   p.dv[row + i] = __float2bfloat16_rn(p.scale * qk * sd[i] + gk);
-  p.dk[row + i] = __float2bfloat16_rn(p.scale * dv_dot * sq[i] + gtv);
+  if (p.dk_f32)
+    p.dk_f32[row + i] = p.scale * dv_dot * sq[i] + gtv;
+  else
+    p.dk[qk_row + i] = __float2bfloat16_rn(p.scale * dv_dot * sq[i] + gtv);
+}
+
+// The sequence of token row r (fixed length T, or the packed bounds cu_seqlens), or -1 when the
+// row belongs to no sequence that the chunkwise runs computed (bad bounds, a padded or invalid
+// state index).
+__device__ __forceinline__ int row_sequence(const int32_t* cu, const int32_t* state_indices, int N, int T, int tokens,
+                                            int pool, int r) {
+  int n;
+  if (!cu) {
+    n = r / T;
+  } else {
+    int lo = 0, hi = N - 1;  // the last n with cu[n] <= r
+    if (N <= 0 || __ldg(cu) > r) return -1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (__ldg(cu + mid) <= r) lo = mid;
+      else hi = mid - 1;
+    }
+    n = lo;
+    const int b = __ldg(cu + n), e = __ldg(cu + n + 1);
+    if (b < 0 || e < b || e > tokens || r >= e) return -1;
+  }
+  if (state_indices) {
+    const int slot = __ldg(state_indices + n);
+    if (slot < 0 || slot >= pool) return -1;
+  }
+  return n;
+}
+
+// Two FP32 values rounded to BF16 (nearest even), the first in the low half.
+__device__ __forceinline__ uint32_t la_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+struct ReduceParams {
+  const float* part;    // [tokens, HV, D] FP32: each value head's part
+  __nv_bfloat16* dst;   // [tokens, H, D]: the sum over each q/k head's group of HV / H value heads
+  const int32_t* cu_seqlens;
+  const int32_t* state_indices;
+  int N, T, tokens, pool, H, HV, D;
+};
+
+// dst[r][h][d] = bf16(sum over g of part[r][h G + g][d]) for the rows of computed sequences (the
+// others are left as they are), 8 values per thread.
+__global__ void __launch_bounds__(kCopyThreads) la_group_sum_kernel(const ReduceParams p) {
+  const int G = p.HV / p.H, per_row = p.H * p.D / 8;
+  for (int r = blockIdx.x; r < p.tokens; r += gridDim.x) {
+    if (row_sequence(p.cu_seqlens, p.state_indices, p.N, p.T, p.tokens, p.pool, r) < 0) continue;
+    for (int i = threadIdx.x; i < per_row; i += kCopyThreads) {
+      const int h = i / (p.D / 8), d = 8 * (i - h * (p.D / 8));
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int g = 0; g < G; ++g) {
+        const float4* src =
+            reinterpret_cast<const float4*>(p.part + (static_cast<size_t>(r) * p.HV + h * G + g) * p.D + d);
+        const float4 a = __ldg(src), b = __ldg(src + 1);
+        acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+        acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+      }
+      uint4 out;
+      out.x = la_bf16x2(acc[0], acc[1]);
+      out.y = la_bf16x2(acc[2], acc[3]);
+      out.z = la_bf16x2(acc[4], acc[5]);
+      out.w = la_bf16x2(acc[6], acc[7]);
+      *reinterpret_cast<uint4*>(p.dst + (static_cast<size_t>(r) * p.H + h) * p.D + d) = out;
+    }
+  }
 }
 
 // Workspace layout, every section 256-byte aligned.
 struct Layout {
-  size_t h0t, dhf, dhft;
+  size_t h0t, dhf, dhft, part;
   size_t bytes;
 };
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-inline Layout layout(int H, int D, int pool, bool has_h0, bool has_dhf) {
+// pool x HV states of D x D FP32 (h0 transposed, dh_final scaled and its transpose) and, with
+// value heads sharing q/k heads (HV > H), one [tokens, HV, D] FP32 buffer for the parts of dq
+// and dk.
+inline Layout layout(int64_t tokens, int H, int HV, int D, int pool, bool has_h0, bool has_dhf) {
   Layout l{};
-  const size_t states = align256(static_cast<size_t>(pool) * H * D * D * 4);
+  const size_t states = align256(static_cast<size_t>(pool) * HV * D * D * 4);
   size_t off = 0;
   l.h0t = off;
   if (has_h0) off += states;
@@ -172,6 +246,8 @@ inline Layout layout(int H, int D, int pool, bool has_h0, bool has_dhf) {
   if (has_dhf) off += states;
   l.dhft = off;
   if (has_dhf) off += states;
+  l.part = off;
+  if (HV > H) off += align256(static_cast<size_t>(tokens) * HV * D * 4);
   l.bytes = off;
   return l;
 }
@@ -188,8 +264,7 @@ la_status launched(const char* what) {
   return LA_OK;
 }
 
-la_status check_shape(int H, int HV, int D, int V) {
-  if (H != HV) return fail(LA_ERR_UNSUPPORTED, "the backward pass needs H == HV (got H=%d, HV=%d)", H, HV);
+la_status check_shape(int D, int V) {
   if (D != V || (D != 128 && D != 64))
     return fail(LA_ERR_UNSUPPORTED, "the backward pass needs D == V == 128 or 64 (got D=%d, V=%d)", D, V);
   return LA_OK;
@@ -197,14 +272,17 @@ la_status check_shape(int H, int HV, int D, int V) {
 
 }  // namespace
 
+
 extern "C" {
 
-la_status la_prefill_bwd_workspace(int B, int T, int H, int D, int pool_size, int has_h0, int has_dh_final,
+la_status la_prefill_bwd_workspace(int B, int T, int H, int HV, int D, int pool_size, int has_h0, int has_dh_final,
                                    size_t* bytes) {
   la_host::g_last_error[0] = '\0';
   if (!bytes) return fail(LA_ERR_INVALID_ARGUMENT, "bytes is null");
-  if (B < 0 || T < 0 || H <= 0 || D <= 0 || pool_size < 0) return fail(LA_ERR_INVALID_ARGUMENT, "bad sizes");
-  *bytes = labw::layout(H, D, pool_size, has_h0 != 0, has_dh_final != 0).bytes;
+  if (B < 0 || T < 0 || H <= 0 || HV <= 0 || D <= 0 || pool_size < 0)
+    return fail(LA_ERR_INVALID_ARGUMENT, "bad sizes");
+  if (HV % H != 0) return fail(LA_ERR_UNSUPPORTED, "HV (%d) must be a multiple of H (%d)", HV, H);
+  *bytes = labw::layout(static_cast<int64_t>(B) * T, H, HV, D, pool_size, has_h0 != 0, has_dh_final != 0).bytes;
   return LA_OK;
 }
 
@@ -214,7 +292,7 @@ la_status la_prefill_bwd(const void* q, const void* k, const void* v, const floa
                          int H, int HV, int D, int V, int pool_size, void* workspace, size_t workspace_bytes,
                          int* dev_error, void* stream) {
   la_host::g_last_error[0] = '\0';
-  la_status st = check_shape(H, HV, D, V);
+  la_status st = check_shape(D, V);
   if (st != LA_OK) return st;
   // The forward's checks cover q, k, v, slopes, the state pool and the modes; the gradients
   // share the layouts of q (dq, dk) and v (dv, dout), dh_final and dh0 that of h0.
@@ -233,8 +311,9 @@ la_status la_prefill_bwd(const void* q, const void* k, const void* v, const floa
     return fail(LA_ERR_INVALID_ARGUMENT, "pool_size (%d) must be >= N (%d) without state_indices", pool_size, N);
   if (N == 0) return LA_OK;
   if (tokens == 0 && !dh0) return LA_OK;
+  const bool grouped = HV > H;  // value heads share q/k heads: dq and dk are sums over a group
   const int pool = (h0 || dh0 || dh_final) ? pool_size : (state_indices ? 0 : N);
-  const labw::Layout lay = labw::layout(H, D, pool, h0 != nullptr, dh_final != nullptr);
+  const labw::Layout lay = labw::layout(tokens, H, HV, D, pool, h0 != nullptr, dh_final != nullptr);
   if (lay.bytes > 0 && (!workspace || workspace_bytes < lay.bytes))
     return fail(LA_ERR_INVALID_ARGUMENT, "workspace too small: %zu bytes given, %zu needed", workspace_bytes,
                 lay.bytes);
@@ -247,18 +326,42 @@ la_status la_prefill_bwd(const void* q, const void* k, const void* v, const floa
   float* h0t = h0 ? reinterpret_cast<float*>(ws + lay.h0t) : nullptr;
   float* dhf = dh_final ? reinterpret_cast<float*>(ws + lay.dhf) : nullptr;
   float* dhft = dh_final ? reinterpret_cast<float*>(ws + lay.dhft) : nullptr;
+  float* part = grouped ? reinterpret_cast<float*>(ws + lay.part) : nullptr;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const dim3 tgrid(static_cast<unsigned>(pool) * HV, (D / 32) * (D / 32)), tblock(32, 8);
+  const int rgrid = static_cast<int>(tokens < 4096 ? (tokens > 0 ? tokens : 1) : 4096);
+  labw::ReduceParams rp{};
+  rp.cu_seqlens = cu_seqlens;
+  rp.state_indices = state_indices;
+  rp.N = N;
+  rp.T = cu_seqlens ? 0 : T;
+  rp.tokens = static_cast<int>(tokens);
+  rp.pool = la_host::effective_pool_size(h0, dh0, state_indices, pool_size, N);
+  rp.H = H;
+  rp.HV = HV;
+  rp.D = D;
 
-  // 1. dq: the forward recurrence with (q, k, v) -> (dout, v, k) from h0^T
+  // 1. dq: the forward recurrence with (q, k, v) -> (dout, v, k) from h0^T; with value heads
+  //    sharing a q/k head, per value head (q' and k' of HV heads, v' of H) into FP32 parts that
+  //    are summed over each group
   if (h0 && pool > 0) {
     labw::la_transpose_states_kernel<<<tgrid, tblock, 0, s>>>(h0, h0t, D, nullptr, HV, 1.f, 1);
     if ((st = launched("state transpose")) != LA_OK) return st;
   }
   if (tokens > 0) {
-    st = la_prefill_fwd(dout, v, k, slopes, scale, h0t, state_indices, cu_seqlens, dq, nullptr, B, T, N, H, HV, D, V,
-                        pool_size, LA_SCHED_AUTO, dev_error, stream);
-    if (st != LA_OK) return st;
+    if (!grouped) {
+      st = la_prefill_fwd(dout, v, k, slopes, scale, h0t, state_indices, cu_seqlens, dq, nullptr, B, T, N, H, HV, D,
+                          V, pool_size, LA_SCHED_AUTO, dev_error, stream);
+      if (st != LA_OK) return st;
+    } else {
+      st = la_internal::chunkwise(dout, v, k, slopes, scale, h0t, state_indices, cu_seqlens, nullptr, part, nullptr, B,
+                                  T, N, HV, HV, H, D, pool_size, false, dev_error, stream);
+      if (st != LA_OK) return st;
+      rp.part = part;
+      rp.dst = static_cast<__nv_bfloat16*>(dq);
+      labw::la_group_sum_kernel<<<rgrid, labw::kCopyThreads, 0, s>>>(rp);
+      if ((st = launched("group sum")) != LA_OK) return st;
+    }
   }
 
   // 2. dh_final / (lambda scale), as it is and transposed: the reverse runs' initial states
@@ -269,14 +372,15 @@ la_status la_prefill_bwd(const void* q, const void* k, const void* v, const floa
     if ((st = launched("state transpose")) != LA_OK) return st;
   }
 
-  // 3. dv (and dh0): the recurrence run backwards with (q, k, v) -> (k, q, dout)
-  st = la_internal::prefill_reverse(k, q, dout, slopes, scale, dhf, state_indices, cu_seqlens, dv, dh0, B, T, N, H,
-                                    HV, D, V, pool_size, dev_error, stream);
+  // 3. dv (and dh0): the recurrence run backwards with (q, k, v) -> (k, q, dout), per value head
+  st = la_internal::chunkwise(k, q, dout, slopes, scale, dhf, state_indices, cu_seqlens, dv, nullptr, dh0, B, T, N, H,
+                              HV, HV, D, pool_size, true, dev_error, stream);
   if (st != LA_OK) return st;
-  // 4. dk: the recurrence run backwards with (q, k, v) -> (v, dout, q)
+  // 4. dk: the recurrence run backwards with (q, k, v) -> (v, dout, q); grouped: per value head
+  //    into FP32 parts
   if (tokens > 0) {
-    st = la_internal::prefill_reverse(v, dout, q, slopes, scale, dhft, state_indices, cu_seqlens, dk, nullptr, B, T,
-                                      N, H, HV, D, V, pool_size, dev_error, stream);
+    st = la_internal::chunkwise(v, dout, q, slopes, scale, dhft, state_indices, cu_seqlens, grouped ? nullptr : dk,
+                                part, nullptr, B, T, N, HV, HV, H, D, pool_size, true, dev_error, stream);
     if (st != LA_OK) return st;
   }
   // 5. dh0 = scale lambda G_0 / scale
@@ -308,17 +412,26 @@ la_status la_prefill_bwd(const void* q, const void* k, const void* v, const floa
     bp.state_indices = state_indices;
     bp.cu_seqlens = cu_seqlens;
     bp.dk = static_cast<__nv_bfloat16*>(dk);
+    bp.dk_f32 = part;
     bp.dv = static_cast<__nv_bfloat16*>(dv);
     bp.dh0 = dh0;
     bp.scale = scale;
     bp.N = N;
     bp.T = cu_seqlens ? 0 : T;
+    bp.H = H;
     bp.HV = HV;
     bp.D = D;
     bp.tokens = static_cast<int>(tokens);
     bp.pool = pool_size;
     labw::la_bwd_big_slope_kernel<<<static_cast<unsigned>(N) * HV, D, 0, s>>>(bp);
     if ((st = launched("large-slope final state")) != LA_OK) return st;
+  }
+  // 7. grouped: dk as the sum of its value heads' parts
+  if (grouped && tokens > 0) {
+    rp.part = part;
+    rp.dst = static_cast<__nv_bfloat16*>(dk);
+    labw::la_group_sum_kernel<<<rgrid, labw::kCopyThreads, 0, s>>>(rp);
+    if ((st = launched("group sum")) != LA_OK) return st;
   }
   return LA_OK;
 }

@@ -45,6 +45,10 @@ cudaError_t setup_kernels() {
   if (e == cudaSuccess) e = cudaFuncSetAttribute(lap::la_prefill_fwd_kernel<true, 64>, attr, smem_bytes());
   if (e == cudaSuccess) e = cudaFuncSetAttribute(lap::la_prefill_fwd_kernel<false, 128, true>, attr, smem_bytes());
   if (e == cudaSuccess) e = cudaFuncSetAttribute(lap::la_prefill_fwd_kernel<false, 64, true>, attr, smem_bytes());
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(lap::la_prefill_fwd_kernel<false, 128, false, true>, attr, smem_bytes());
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(lap::la_prefill_fwd_kernel<false, 128, true, true>, attr, smem_bytes());
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(lap::la_prefill_fwd_kernel<false, 64, false, true>, attr, smem_bytes());
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(lap::la_prefill_fwd_kernel<false, 64, true, true>, attr, smem_bytes());
   return e;
 }
 
@@ -143,6 +147,7 @@ la_status la_prefill_fwd(const void* q, const void* k, const void* v, const floa
   p.state_indices = state_indices;
   p.cu_seqlens = cu_seqlens;
   p.o = static_cast<__nv_bfloat16*>(o);
+  p.o_f32 = nullptr;
   p.h_final = h_final;
   p.dev_error = dev_error;
   p.scale = scale;
@@ -152,6 +157,7 @@ la_status la_prefill_fwd(const void* q, const void* k, const void* v, const floa
   p.H = H;
   p.HV = HV;
   p.G = HV / H;
+  p.vdiv = 1;
   p.pool_size = pool;
   p.num_units = static_cast<int>(units);
   p.short_max = split ? kShortMax : -1;
@@ -182,13 +188,17 @@ la_status la_prefill_fwd(const void* q, const void* k, const void* v, const floa
 
 namespace la_internal {
 
-la_status prefill_reverse(const void* q, const void* k, const void* v, const float* slopes, float scale,
-                          const float* h0, const int32_t* state_indices, const int32_t* cu_seqlens, void* o,
-                          float* h_final, int B, int T, int N, int H, int HV, int D, int V, int pool_size,
-                          int* dev_error, void* stream) {
+la_status chunkwise(const void* q, const void* k, const void* v, const float* slopes, float scale, const float* h0,
+                    const int32_t* state_indices, const int32_t* cu_seqlens, void* o, float* o_f32, float* h_final,
+                    int B, int T, int N, int H, int HV, int v_heads, int D, int pool_size, bool reverse,
+                    int* dev_error, void* stream) {
+  if (v_heads <= 0 || HV % v_heads != 0)
+    return fail(LA_ERR_UNSUPPORTED, "HV (%d) must be a multiple of v's heads (%d)", HV, v_heads);
+  // the checks of la_prefill_fwd; o (or o_f32) has the layout of the output, h_final of the states
   bool nothing = false;
-  la_status st = la_host::check_prefill_args(q, k, v, slopes, h0, state_indices, cu_seqlens, o, h_final, B, T, N, H,
-                                             HV, D, V, pool_size, dev_error, &nothing);
+  la_status st = la_host::check_prefill_args(q, k, v, slopes, h0, state_indices, cu_seqlens,
+                                             o_f32 ? static_cast<const void*>(o_f32) : o, h_final, B, T, N, H, HV, D,
+                                             D, pool_size, dev_error, &nothing);
   if (st != LA_OK || nothing) return st;
   const int64_t tokens = static_cast<int64_t>(B) * T;
   const int64_t units = static_cast<int64_t>(N) * HV;
@@ -202,8 +212,8 @@ la_status prefill_reverse(const void* q, const void* k, const void* v, const flo
   if (tokens > 0) {
     if ((st = la_host::encode_bf16_rows_map(&tm_q, q, tokens, H, "q", D)) != LA_OK) return st;
     if ((st = la_host::encode_bf16_rows_map(&tm_k, k, tokens, H, "k", D)) != LA_OK) return st;
-    if ((st = la_host::encode_bf16_rows_map(&tm_v, v, tokens, HV, "v", D)) != LA_OK) return st;
-    if ((st = la_host::encode_bf16_out_map(&tm_o, o, tokens, HV, D)) != LA_OK) return st;
+    if ((st = la_host::encode_bf16_rows_map(&tm_v, v, tokens, v_heads, "v", D)) != LA_OK) return st;
+    if (!o_f32 && (st = la_host::encode_bf16_out_map(&tm_o, o, tokens, HV, D)) != LA_OK) return st;
   }
   lap::KernelParams p;
   p.slopes = slopes;
@@ -211,6 +221,7 @@ la_status prefill_reverse(const void* q, const void* k, const void* v, const flo
   p.state_indices = state_indices;
   p.cu_seqlens = cu_seqlens;
   p.o = static_cast<__nv_bfloat16*>(o);
+  p.o_f32 = o_f32;
   p.h_final = h_final;
   p.dev_error = dev_error;
   p.scale = scale;
@@ -220,15 +231,23 @@ la_status prefill_reverse(const void* q, const void* k, const void* v, const flo
   p.H = H;
   p.HV = HV;
   p.G = HV / H;
+  p.vdiv = HV / v_heads;
   p.pool_size = la_host::effective_pool_size(h0, h_final, state_indices, pool_size, N);
   p.num_units = static_cast<int>(units);
   p.short_max = -1;  // every sequence, however short, runs here
   const int grid = static_cast<int>(units < dsp->sms ? units : dsp->sms);
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (D == 128)
-    lap::la_prefill_fwd_kernel<false, 128, true><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p);
-  else
-    lap::la_prefill_fwd_kernel<false, 64, true><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p);
+  const int variant = (D == 128 ? 0 : 4) + (reverse ? 2 : 0) + (o_f32 ? 1 : 0);
+  switch (variant) {
+    case 0: lap::la_prefill_fwd_kernel<false, 128, false, false><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p); break;
+    case 1: lap::la_prefill_fwd_kernel<false, 128, false, true><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p); break;
+    case 2: lap::la_prefill_fwd_kernel<false, 128, true, false><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p); break;
+    case 3: lap::la_prefill_fwd_kernel<false, 128, true, true><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p); break;
+    case 4: lap::la_prefill_fwd_kernel<false, 64, false, false><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p); break;
+    case 5: lap::la_prefill_fwd_kernel<false, 64, false, true><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p); break;
+    case 6: lap::la_prefill_fwd_kernel<false, 64, true, false><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p); break;
+    default: lap::la_prefill_fwd_kernel<false, 64, true, true><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p); break;
+  }
   const cudaError_t ce = cudaGetLastError();
   if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(ce));
   return LA_OK;

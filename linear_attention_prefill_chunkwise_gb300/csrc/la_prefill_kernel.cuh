@@ -145,11 +145,15 @@ struct KernelParams {
   int T;          // fixed-length mode sequence length
   int N;          // sequences
   int H;          // q/k heads
-  int HV;         // value heads
+  int HV;         // value heads (units, states and outputs per sequence)
   int G;          // HV / H
   int pool_size;
   int num_units;  // N * HV
   int short_max;  // sequences of at most this many tokens belong to the tokenwise kernel (-1: none)
+  // kF32Out instance only: the FP32 output ([tokens, HV, D], the layout of o), and v's head of
+  // value head hv, hv / vdiv (v then has HV / vdiv heads)
+  float* o_f32;
+  int vdiv;
 };
 
 // One unit's sequence bounds, state slot and chunk count, decoded identically by every role.
@@ -349,7 +353,7 @@ __device__ __forceinline__ void cursor_next(const SharedStorage& sm, const Kerne
 // TMA and MMA thread B, one polling loop: each pass issues, in this order, every job whose
 // inputs are ready (mbarrier.test_wait, no blocking): dS(i) = V(i)^T Kt(i), scores(i) =
 // Q(i) K(i)^T, and the next Q/K and V loads once their ring slots have been released.
-template <bool kListed, int kD, bool kRev>
+template <bool kListed, int kD, bool kRev, bool kF32Out>
 __device__ __forceinline__ void tma_mma_loop(SharedStorage& sm, const KernelParams& p, const CUtensorMap* tm_q,
                                              const CUtensorMap* tm_k, const CUtensorMap* tm_v, uint32_t tmem,
                                              volatile int* abort) {
@@ -441,8 +445,10 @@ __device__ __forceinline__ void tma_mma_loop(SharedStorage& sm, const KernelPara
         } else {
           mbar_arrive_expect_tx(bar, kHalves * kTileBytes);
         }
+        // (the kF32Out instance may share a V head among vdiv value heads)
+        const int vh = kF32Out ? cv.hv / p.vdiv : cv.hv;
 #pragma unroll
-        for (int h = 0; h < kHalves; ++h) tma_load_2d(sm.v[sv][h], tm_v, bar, cv.hv * kD + 64 * h, cv.row);
+        for (int h = 0; h < kHalves; ++h) tma_load_2d(sm.v[sv][h], tm_v, bar, vh * kD + 64 * h, cv.row);
         ++nv;
         cursor_next(sm, p, cv);
         progressed = true;
@@ -695,7 +701,7 @@ __device__ __forceinline__ void operand_loop(SharedStorage& sm, const KernelPara
 }
 
 // State warpgroups: own S in registers, advance it, publish it to TMEM, write the output.
-template <bool kListed, int kD, bool kRev>
+template <bool kListed, int kD, bool kRev, bool kF32Out>
 __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams& p, const CUtensorMap* tm_o,
                                           uint32_t tmem, int ctid, volatile int* abort) {
   const int warp = ctid >> 5, lane = ctid & 31;
@@ -803,7 +809,39 @@ __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams&
         break;
       }
       tc_fence_after();
-      {
+      if constexpr (kF32Out) {
+        // FP32 output (per-value-head partial sums that the caller adds up): each thread stores the
+        // values tcgen05.ld 16x256b gives it, value rows v = 32 qd + 16 g + lane / 4 (+ 8) and
+        // token rows s = 32 wg + 8 r + 2 (lane % 4) (+ 1) of the chunk, rows s < L only
+        const int ybase = w.bos + seq_chunk<kRev>(c, w.nchunks) * kChunk;
+        const bool vlive = kD == 128 || qd < 2;
+        float* obase = p.o_f32 + static_cast<size_t>(w.hv) * kD;
+#pragma unroll 1
+        for (int g = 0; g < 2; ++g) {
+          uint32_t rg[16];
+          tmem_ld_16x256b_x4(tmem + lane_base + (static_cast<uint32_t>(16 * g) << 16) + kColO + 64 * b + 32 * wg, rg);
+          if (g == 1) {
+            tc_fence_before();
+            mbar_arrive(&sm.o_free[b]);
+          }
+          if (vlive) {
+            const int v1 = 32 * qd + 16 * g + (lane >> 2);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int sl = 32 * wg + 8 * r + 2 * (lane & 3) + e;
+                if (sl < L) {
+                  float* orow = obase + static_cast<size_t>(ybase + sl) * ostride;
+                  orow[v1] = __uint_as_float(rg[4 * r + e]);
+                  orow[v1 + 8] = __uint_as_float(rg[4 * r + 2 + e]);
+                }
+              }
+            }
+          }
+        }
+        if (lane == 0) mbar_arrive(&sm.v_empty[it % kVStages]);
+      } else {
         const uint32_t sv = it % kVStages;
         // 32 rows of 64 bytes, 64-byte swizzle (D = 64: the four warps with v < 64, in the half of
         // the stage the V loads use)
@@ -875,7 +913,7 @@ __device__ __forceinline__ int state_loop(SharedStorage& sm, const KernelParams&
   return err;
 }
 
-template <bool kListed, int kD, bool kRev = false>
+template <bool kListed, int kD, bool kRev = false, bool kF32Out = false>
 __global__ void __launch_bounds__(kThreads, 1)
 la_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -958,13 +996,13 @@ la_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   }
 
   if (warp == 0) {
-    if (lane == 0) tma_mma_loop<kListed, kD, kRev>(sm, p, &tm_q, &tm_k, &tm_v, tmem, abort);
+    if (lane == 0) tma_mma_loop<kListed, kD, kRev, kF32Out>(sm, p, &tm_q, &tm_k, &tm_v, tmem, abort);
   } else if (warp == 1) {
     if (lane == 0) mma_o_loop<kListed, kD>(sm, p, tmem, abort);
   } else if (warp < 4) {
     convert_loop<kListed, kD, kRev>(sm, p, tid - 64, abort);
   } else if (warp < 12) {
-    const int err = state_loop<kListed, kD, kRev>(sm, p, &tm_o, tmem, tid - 128, abort);
+    const int err = state_loop<kListed, kD, kRev, kF32Out>(sm, p, &tm_o, tmem, tid - 128, abort);
     if (err && tid == 128 && p.dev_error) atomicOr(p.dev_error, err);
     if ((tid & 31) == 0) bulk_wait_all();  // this warp's output stores have completed
   } else {

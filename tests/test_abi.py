@@ -229,7 +229,7 @@ def call_backward(**over):
 
 
 @pytest.mark.parametrize("over,status", [
-    (dict(H=1, HV=2), LA_UNSUPPORTED),           # one value head per q/k head only
+    (dict(H=2, HV=3), LA_UNSUPPORTED),           # HV must be a multiple of H
     (dict(D=64), LA_UNSUPPORTED),                # D != V
     (dict(D=256, V=256), LA_UNSUPPORTED),
     (dict(dout=None), LA_INVALID),
@@ -249,12 +249,18 @@ def test_backward_empty_batch_is_a_no_op():
 
 
 def test_backward_workspace_size():
-    # a transposed h0 and two forms of dh_final, P x H states of D x D FP32 each; nothing else
-    nbytes = lap.la_prefill_bwd_workspace(2, 8192, 64, 128, 2, True, True)
+    # a transposed h0 and two forms of dh_final, P x HV states of D x D FP32 each; with HV > H one
+    # [tokens, HV, D] FP32 buffer more for the value heads' parts of dq and dk
+    nbytes = lap.la_prefill_bwd_workspace(2, 8192, 64, 64, 128, 2, True, True)
     assert nbytes == 3 * 2 * 64 * 128 * 128 * 4
-    assert lap.la_prefill_bwd_workspace(2, 8192, 64, 128, 2, True, False) == 2 * 64 * 128 * 128 * 4
-    assert lap.la_prefill_bwd_workspace(1, 100, 2, 64, 3, False, True) == 2 * 3 * 2 * 64 * 64 * 4
-    assert lap.la_prefill_bwd_workspace(1, 100, 2, 64, 0, False, False) == 0
+    assert lap.la_prefill_bwd_workspace(2, 8192, 64, 64, 128, 2, True, False) == 2 * 64 * 128 * 128 * 4
+    assert lap.la_prefill_bwd_workspace(1, 100, 2, 2, 64, 3, False, True) == 2 * 3 * 2 * 64 * 64 * 4
+    assert lap.la_prefill_bwd_workspace(1, 100, 2, 2, 64, 0, False, False) == 0
+    align = lambda x: (x + 255) // 256 * 256
+    assert lap.la_prefill_bwd_workspace(4, 1000, 16, 64, 128, 4, True, False) == \
+        align(4 * 64 * 128 * 128 * 4) + align(4000 * 64 * 128 * 4)
+    with pytest.raises(lap.LaError):
+        lap.la_prefill_bwd_workspace(1, 100, 3, 4, 64, 0, False, False)  # HV not a multiple of H
 
 
 def test_backward_without_states_needs_no_workspace():

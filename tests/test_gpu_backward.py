@@ -90,6 +90,12 @@ BWD_CASES = {
     "lambda_one": dict(lengths=[150, 20], H=2, HV=2, slopes=[0.0, 0.0]),
     "lambda_zero": dict(lengths=[150, 20], H=2, HV=2, slopes=[100.0, 100.0]),
     "short_sequences": dict(lengths=[5, 20, 3, 31, 1, 40, 16], H=2, HV=2),
+    # GVA: dq and dk summed over each q/k head's value heads
+    "gva_fixed_T300": dict(B=2, T=300, H=1, HV=4),
+    "gva_packed_ragged_pool": dict(lengths=[1, 63, 64, 65, 130, 0, 200, 31], H=2, HV=6, pool=11,
+                                   indices=[3, 10, -1, 0, 7, 5, 1, 9]),
+    "gva_short_sequences": dict(lengths=[5, 20, 3, 31, 1, 40, 16], H=2, HV=4),
+    "gva_lambda_zero_and_one": dict(lengths=[150, 20], H=1, HV=4, slopes=[100.0, 0.0, 100.0, 0.5]),
 }
 
 
@@ -122,23 +128,19 @@ def test_backward_is_deterministic():
         assert np.array_equal(x.view(np.uint32), y.view(np.uint32))
 
 
-def test_backward_refuses_gva():
-    import linear_attention_prefill_chunkwise_gb300 as lap
-    p, dout, _ = _grad_problem(4404, lengths=[40], H=1, HV=2)
-    q, k, v = (to_torch_bf16(b, "cuda") for b in (p.q_bits, p.k_bits, p.v_bits))
-    with pytest.raises(lap.LaError) as e:
-        lap.la_prefill_bwd(q, k, v, torch.from_numpy(p.slopes).cuda(), p.scale, to_torch_bf16(dout, "cuda"),
-                           cu_seqlens=torch.from_numpy(p.cu_seqlens).cuda())
-    assert e.value.name == "LA_ERR_UNSUPPORTED"
+def test_backward_gva_long_sequence():
+    # B=1, T=4096, H=4 q/k heads with HV=16 value heads, h0 and dh_final: every unit within bounds
+    p, dout, dhf = _grad_problem(4406, B=1, T=4096, H=4, HV=16)
+    _compare(p, dout, dhf, "backward GVA B=1 T=4096 H=4 HV=16")
 
 
-@pytest.mark.parametrize("D", [128, 64])
-def test_backward_nonfinite_sequence_does_not_reach_its_neighbours(D):
+@pytest.mark.parametrize("D,HV", [(128, 2), (64, 2), (128, 4)])
+def test_backward_nonfinite_sequence_does_not_reach_its_neighbours(D, HV):
     """A packed sequence whose q, k, v and dout hold infinities and NaNs leaves the gradients of
     every other sequence bitwise as they are with finite values there: the reverse runs read,
     in a sequence's last (ragged) chunk, rows of the next sequence, which must stay out."""
     import dataclasses
-    p, dout, dhf = _grad_problem(4405, D=D, lengths=[70, 100, 45, 130], H=2, HV=2, pool=6, indices=[4, 1, 5, 0])
+    p, dout, dhf = _grad_problem(4405, D=D, lengths=[70, 100, 45, 130], H=2, HV=HV, pool=6, indices=[4, 1, 5, 0])
     clean = _run(p, dout, dhf)
     a, b = int(p.cu_seqlens[1]), int(p.cu_seqlens[2])
     bits = {n: getattr(p, n).copy() for n in ("q_bits", "k_bits", "v_bits")}
