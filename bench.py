@@ -679,72 +679,84 @@ def run_segment_sweep(args, device, stream, flush, hbm, hbm_kind, tflops, tf_kin
 
 
 def run_backward_sweep(args, device, stream, flush, hbm, hbm_kind):
-    """The backward pass (la_prefill_bwd) on the bench shape B=2, T=8192, H=HV=64, D=V=128 with
-    h0, dL/do and dL/dh_final given and dh0 returned.  Algorithmic bytes: q, k, v, dout read and
-    dq, dk, dv written once, h0 and dh_final read and dh0 written once; the three chunkwise runs
-    and the state transposes it is built from move more."""
+    """The backward pass (la_prefill_bwd) with dL/do and dL/dh_final given and dh0 returned, on
+    the bench shape (B=2, T=8192, H=HV=64, h0 given) and on the GVA shape of workload 4 (B=4,
+    T=16384, H=16 q/k heads, HV=64 value heads, no h0).  Algorithmic bytes: q, k, dq, dk once per
+    q/k head, v, dout, dv once per value head, h0 (when given), dh_final and dh0 once; the three
+    chunkwise runs, the state transposes and (GVA) the FP32 parts of dq and dk move more."""
     import numpy as np
     import torch
 
     import linear_attention_prefill_chunkwise_gb300 as lap
     import workloads as W
 
-    p = W.config(2)
-    rng = np.random.default_rng(4402)
-
     def bf(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
 
-    q, k, v = bf(p.q_bits), bf(p.k_bits), bf(p.v_bits)
-    dout = bf(W.bf16_bits(rng.standard_normal(p.v_bits.shape, dtype=np.float32)))
-    sl = torch.from_numpy(p.slopes).to(device)
-    h0 = torch.from_numpy(p.h0).to(device)
-    dhf = torch.randn(h0.shape, generator=torch.Generator(device=device).manual_seed(4403), device=device) * 0.1
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-    dh0 = torch.empty_like(h0)
-    ws = torch.empty(lap.la_prefill_bwd_workspace(B, T, H, HV, D, B, True, True), dtype=torch.uint8, device=device)
+    for cfg, seed in ((2, 4402), (4, 4404)):
+        p = W.config(cfg)
+        Bp, Tp, Hp, HVp = p.B, p.T, p.H, p.HV
+        G = HVp // Hp
+        rng = np.random.default_rng(seed)
+        q, k, v = bf(p.q_bits), bf(p.k_bits), bf(p.v_bits)
+        dout = bf(W.bf16_bits(rng.standard_normal(p.v_bits.shape, dtype=np.float32)))
+        sl = torch.from_numpy(p.slopes).to(device)
+        h0 = None if p.h0 is None else torch.from_numpy(p.h0).to(device)
+        dhf = torch.randn((Bp, HVp, V, D), generator=torch.Generator(device=device).manual_seed(seed + 1),
+                          device=device) * 0.1
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        dh0 = torch.empty_like(dhf)
+        ws = torch.empty(max(lap.la_prefill_bwd_workspace(Bp, Tp, Hp, HVp, D, Bp, h0 is not None, True), 256),
+                         dtype=torch.uint8, device=device)
 
-    def call():
-        lap.la_prefill_bwd(q, k, v, sl, p.scale, dout, h0=h0, dh_final=dhf, dq=dq, dk=dk, dv=dv, dh0=dh0, seq_len=T,
-                           workspace=ws, stream=stream)
+        def call():
+            lap.la_prefill_bwd(q, k, v, sl, p.scale, dout, h0=h0, dh_final=dhf, dq=dq, dk=dk, dv=dv, dh0=dh0,
+                               seq_len=Tp, workspace=ws, stream=stream)
 
-    with torch.cuda.stream(stream):
-        for _ in range(3):
-            call()
-        times = []
-        for _ in range(args.sweep_steps):
-            flush.fill_(1)
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            call()
-            e1.record(stream)
-            times.append((e0, e1))
-    torch.cuda.synchronize(device)
-    ms = statistics.fmean(a.elapsed_time(b) for a, b in times)
-    nbytes = 7 * TOKENS * HV * V * 2 + 3 * B * HV * V * D * 4
-    t_roof = nbytes / (hbm * 1e9)
-    line = {"sweep": True, "op": "la_prefill_bwd", "workload": WORKLOAD + ", dL/do and dL/dh_final in, dh0 out",
-            "ms": round(ms, 5), "tokens_per_s": round(TOKENS / (ms / 1e3), 1), "alg_bytes": nbytes,
-            "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1), "roofline_ms": round(t_roof * 1e3, 5),
-            "frac": round(t_roof * 1e3 / ms, 4), "bound": "hbm",
-            "peaks": {"hbm_gbs": hbm, "hbm_source": hbm_kind}, "steps": args.sweep_steps,
-            "l2": "flushed between launches (256 MB write)"}
-    if not args.no_cpu_baseline:
-        # the oracle's backward over both sequences and the first 8 of the 64 heads, scaled
-        import oracle
-        nh = 8
-        threads = oracle.max_threads()
-        dout_h = W.bf16_to_f32(dout.view(torch.int16).cpu().numpy().view(np.uint16))
-        t0 = time.perf_counter()
-        oracle.backward(p.q()[:, :nh], p.k()[:, :nh], p.v()[:, :nh], p.slopes[:nh], p.scale, dout_h[:, :nh],
-                        h0=p.h0[:, :nh].astype(np.float64), dh_final=dhf[:, :nh].cpu().numpy().astype(np.float64),
-                        T=T, nthreads=threads)
-        cpu_ms = (time.perf_counter() - t0) * 1e3 * HV / nh
-        line["cpu_baseline"] = {"ms": round(cpu_ms, 2), "cores": threads, "kind": "oracle",
-                                "gpu_speedup": round(cpu_ms / ms, 1),
-                                "sample": f"B=2 x T=8192 tokens x {nh} of {HV} heads, scaled to all heads (FP64 "
-                                          "forward and reverse sweeps, OpenMP over (sequence, head))"}
-    print(json.dumps(line), flush=True)
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                call()
+            times = []
+            for _ in range(args.sweep_steps):
+                flush.fill_(1)
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                call()
+                e1.record(stream)
+                times.append((e0, e1))
+        torch.cuda.synchronize(device)
+        ms = statistics.fmean(a.elapsed_time(b) for a, b in times)
+        toks = Bp * Tp
+        nbytes = 4 * toks * Hp * D * 2 + 3 * toks * HVp * V * 2 + (2 + (h0 is not None)) * Bp * HVp * V * D * 4
+        t_roof = nbytes / (hbm * 1e9)
+        line = {"sweep": True, "op": "la_prefill_bwd",
+                "workload": (WORKLOAD if cfg == 2 else p.name) + ", dL/do and dL/dh_final in, dh0 out",
+                "ms": round(ms, 5), "tokens_per_s": round(toks / (ms / 1e3), 1), "alg_bytes": nbytes,
+                "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1), "roofline_ms": round(t_roof * 1e3, 5),
+                "frac": round(t_roof * 1e3 / ms, 4), "bound": "hbm",
+                "peaks": {"hbm_gbs": hbm, "hbm_source": hbm_kind}, "steps": args.sweep_steps,
+                "l2": "flushed between launches (256 MB write)"}
+        if not args.no_cpu_baseline:
+            # the oracle's backward over every sequence and the first q/k heads (with their value
+            # heads, 8 or so), scaled to all heads
+            import oracle
+            nq = max(1, 8 // G)
+            nv = nq * G
+            threads = oracle.max_threads()
+            dout_h = W.bf16_to_f32(dout.view(torch.int16).cpu().numpy().view(np.uint16))
+            t0 = time.perf_counter()
+            oracle.backward(p.q()[:, :nq], p.k()[:, :nq], p.v()[:, :nv], p.slopes[:nv], p.scale, dout_h[:, :nv],
+                            h0=None if p.h0 is None else p.h0[:, :nv].astype(np.float64),
+                            dh_final=dhf[:, :nv].cpu().numpy().astype(np.float64), T=Tp, nthreads=threads)
+            cpu_ms = (time.perf_counter() - t0) * 1e3 * HVp / nv
+            line["cpu_baseline"] = {"ms": round(cpu_ms, 2), "cores": threads, "kind": "oracle",
+                                    "gpu_speedup": round(cpu_ms / ms, 1),
+                                    "sample": f"B={Bp} x T={Tp} tokens x {nv} of {HVp} value heads ({nq} of {Hp} "
+                                              "q/k heads), scaled to all heads (FP64 forward and reverse sweeps, "
+                                              "OpenMP over (sequence, q/k head))"}
+        print(json.dumps(line), flush=True)
+        del q, k, v, dout, dq, dk, dv, dh0, dhf, h0, ws
+        torch.cuda.empty_cache()
 
 
 def oracle_forward_baseline(p, gpu_ms, sample="the whole workload"):
