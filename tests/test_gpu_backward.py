@@ -156,3 +156,35 @@ def test_backward_nonfinite_sequence_does_not_reach_its_neighbours(D, HV):
         assert np.array_equal(x[keep].view(np.uint32), y[keep].view(np.uint32)), f"{name} of a neighbour changed"
     slots = [4, 5, 0]  # the other sequences' slots
     assert np.array_equal(clean[3][slots].view(np.uint32), bad[3][slots].view(np.uint32)), "dh0 of a neighbour changed"
+
+
+def test_backward_gva_in_a_cuda_graph():
+    """The whole GVA backward (chunkwise runs, FP32 parts, group sums, state kernels) captured in
+    one CUDA graph replays bitwise like the eager call: no host synchronisation, no allocation."""
+    import linear_attention_prefill_chunkwise_gb300 as lap
+    p, dout, dhf = _grad_problem(4407, lengths=[90, 40, 130], H=1, HV=2, pool=4, indices=[3, 0, 1])
+    eager = _run(p, dout, dhf)
+    dev = "cuda"
+    q, k, v = (to_torch_bf16(b, dev) for b in (p.q_bits, p.k_bits, p.v_bits))
+    sl = torch.from_numpy(p.slopes).to(dev)
+    h0 = torch.from_numpy(p.h0).to(dev)
+    dh_final = torch.from_numpy(dhf).to(dev)
+    idx = torch.from_numpy(p.state_indices).to(dev)
+    cu = torch.from_numpy(p.cu_seqlens).to(dev)
+    do = to_torch_bf16(dout, dev)
+    dq, dk, dv = (torch.full_like(t, float("nan")) for t in (q, k, v))
+    dh0 = torch.full((p.pool_size, p.HV, p.V, p.D), float("nan"), dtype=torch.float32, device=dev)
+    nbytes = lap.la_prefill_bwd_workspace(1, p.tokens, p.H, p.HV, p.D, p.pool_size, True, True)
+    ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        lap.la_prefill_bwd(q, k, v, sl, p.scale, do, h0=h0, dh_final=dh_final, state_indices=idx, cu_seqlens=cu,
+                           dq=dq, dk=dk, dv=dv, dh0=dh0, workspace=ws)
+    for _ in range(3):
+        for t in (dq, dk, dv, dh0):
+            t.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        for got, want in zip((dq, dk, dv, dh0), eager):
+            assert np.array_equal(got.float().cpu().numpy().view(np.uint32), want.view(np.uint32))

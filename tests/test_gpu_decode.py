@@ -227,3 +227,42 @@ def test_verify_without_kv_buffer_and_bad_index_flag():
     assert bool(torch.isnan(o2[T:2 * T].float()).all())  # the skipped request's rows are not written
     keep = np.r_[0:T, 2 * T:4 * T]
     assert torch.equal(o2[keep].view(torch.int16), o[keep].view(torch.int16))
+
+
+def test_verify_and_commit_in_a_cuda_graph():
+    """Verify (tensor-core closed form) and commit captured in one CUDA graph replay bitwise like
+    the eager calls: neither synchronises with the host nor allocates."""
+    import torch
+    import linear_attention_prefill_chunkwise_gb300 as lap
+    c = make_case(seed=5040, B=12, T=8, H=2, HV=4, P=16, n_pad=2)
+    B, T, H, HV, P = c["B"], c["T"], c["H"], c["HV"], c["P"]
+    d = upload(c)
+    pool0 = d["pool"].clone()
+    acc = torch.from_numpy(np.random.default_rng(5041).integers(0, T + 1, B).astype(np.int32)).cuda()
+
+    def buffers():
+        return (torch.full((B * T, HV, W.V), float("nan"), dtype=torch.bfloat16, device="cuda"),
+                torch.zeros((P, T, H, W.D), dtype=torch.bfloat16, device="cuda"),
+                torch.zeros((P, T, HV, W.V), dtype=torch.bfloat16, device="cuda"), pool0.clone())
+
+    def calls(o, kbuf, vbuf, pool):
+        lap.la_verify(d["q"], d["k"], d["v"], d["slopes"], c["scale"], pool, T, state_indices=d["idx"], o=o,
+                      kbuf=kbuf, vbuf=vbuf)
+        lap.la_commit(pool, kbuf, vbuf, acc, d["slopes"], state_indices=d["idx"])
+
+    ref = buffers()
+    calls(*ref)
+    torch.cuda.synchronize()
+    bufs = buffers()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        calls(*bufs)
+    rows = live_rows(c)
+    for _ in range(3):
+        bufs[3].copy_(pool0)
+        bufs[0].fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(bufs[0][rows].view(torch.int16), ref[0][rows].view(torch.int16))
+        assert torch.equal(bufs[3].view(torch.int32), ref[3].view(torch.int32))
