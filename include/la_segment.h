@@ -20,7 +20,11 @@
  * Cost: pass 1 reads K and V of every segment but the last once more, so it pays off only
  * when the batch has far fewer chains than SMs.  With segment_len == 0 the library decides:
  * it runs la_prefill_fwd unchanged (no workspace used) unless N * HV is at most half the SM
- * count, and otherwise picks S so that the segments fill the SMs about once.
+ * count, and otherwise picks S so that the segments fill the SMs about once.  When that gives
+ * two segments per fixed-length sequence, the automatic plan instead cuts the first half of
+ * each sequence into two segments of the resolved length and keeps the second half as one
+ * longer last segment: pass 1 (which the last segment does not need) then runs twice as many
+ * units of half the length.
  *
  * Every pointer is a DEVICE pointer owned by the caller.  The call allocates nothing, never
  * synchronises with the host and enqueues its kernels (6 at most) on `stream`.

@@ -27,6 +27,7 @@ size_t align_up(size_t x) { return (x + kWsAlign - 1) & ~(kWsAlign - 1); }
 // Segment length and workspace layout of one call.
 struct SegPlan {
   int S = 0;             // 0: no segmentation (la_prefill_fwd runs unchanged)
+  int S_last = 0;        // > 0: each sequence's last segment is its last S_last tokens (plan kernel)
   int64_t nseg_max = 0;  // upper bound of the segment count
   size_t off_states = 0, off_seg_cu = 0, off_seg_slot = 0, off_seg_flags = 0, off_seq_seg0 = 0, off_seq_slot = 0;
   size_t bytes = 0;
@@ -43,7 +44,7 @@ la_status make_plan(int B, int T, int N, int HV, bool packed, int segment_len, i
   const int64_t tokens = static_cast<int64_t>(B) * T;
   const int64_t units = static_cast<int64_t>(N) * HV;
   if (N == 0 || tokens == 0) return LA_OK;
-  int64_t S = segment_len;
+  int64_t S = segment_len, S_last = 0;
   if (S == 0) {
     // Segment only when the chains fill at most half of the SMs, and then aim at about one
     // segment per SM: the extra pass over K and V costs more than a nearly full GPU gains.
@@ -51,6 +52,14 @@ la_status make_plan(int B, int T, int N, int HV, bool packed, int segment_len, i
     if (!packed) {
       const int64_t m = sms / units;  // segments per sequence
       S = (T + m - 1) / m;
+      // Two segments per sequence leave the local-state pass (one unit per sequence and head)
+      // on at most half of the SMs: cut the first segment in two instead, so that twice as many
+      // shorter local states run in parallel, and keep the last segment, which needs none, at
+      // full length (the prefill's longest unit, and so its time, is unchanged).
+      if (m == 2 && T >= 4 * las::kChunk) {
+        S_last = (S + las::kChunk - 1) / las::kChunk * las::kChunk;
+        S = ((T - S_last + 1) / 2 + las::kChunk - 1) / las::kChunk * las::kChunk;
+      }
     } else {
       S = (tokens * HV + sms - 1) / sms;
     }
@@ -59,12 +68,15 @@ la_status make_plan(int B, int T, int N, int HV, bool packed, int segment_len, i
   }
   // no sequence is longer than one segment: nothing to gain
   if ((!packed && S >= T) || (packed && S >= tokens)) return LA_OK;
-  const int64_t nseg = packed ? N + tokens / S : static_cast<int64_t>(B) * ((T + S - 1) / S);
+  const int64_t nseg = packed ? N + tokens / S
+                              : static_cast<int64_t>(B) *
+                                    (S_last > 0 ? ((T > S_last ? T - S_last : 0) + S - 1) / S + 1 : (T + S - 1) / S);
   if (nseg >= INT32_MAX || nseg * HV > INT32_MAX)
     return fail(LA_ERR_UNSUPPORTED, "too many segments (%lld x %d heads); use a longer segment_len", (long long)nseg,
                 HV);
   SegPlan p;
   p.S = static_cast<int>(S);
+  p.S_last = static_cast<int>(S_last);
   p.nseg_max = nseg;
   size_t off = 0;
   p.off_states = off;
@@ -182,6 +194,7 @@ la_status la_prefill_fwd_segmented(const void* q, const void* k, const void* v, 
   pp.T = cu_seqlens ? 0 : T;
   pp.tokens = static_cast<int>(tokens);
   pp.S = pl.S;
+  pp.S_last = pl.S_last;
   pp.nseg_max = nseg;
   pp.pool_size = la_host::effective_pool_size(h0, h_final, state_indices, pool_size, N);
   las::la_segment_plan_kernel<<<1, las::kPlanThreads, 0, s>>>(pp);

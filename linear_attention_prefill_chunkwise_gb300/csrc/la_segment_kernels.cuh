@@ -52,12 +52,16 @@ struct PlanParams {
   int32_t* seq_seg0;   // [N + 1] first segment of each sequence
   int32_t* seq_slot;   // [N] the sequence's state slot when it runs, else -1
   int N, T, tokens, S, nseg_max, pool_size;
+  int S_last;  // > 0: each sequence's last segment is its last S_last tokens, the rest cut into S
 };
 
 constexpr int kPlanThreads = 1024;
 
 // Sequence n owns max(1, ceil(L_n / S)) consecutive segments; segment j covers tokens
-// [bos + j S, min(bos + (j + 1) S, eos)).  A skipped sequence (padded, bad bounds, bad index)
+// [bos + j S, min(bos + (j + 1) S, eos)).  With S_last > 0 the last segment is the sequence's
+// last min(L_n, S_last) tokens and the E = L_n - S_last before it (if any) are cut into
+// ceil(E / S) segments of S from the start: short segments whose local states run in parallel,
+// one long one that needs none.  A skipped sequence (padded, bad bounds, bad index)
 // owns one segment with slot -1 so that the segment bounds stay one contiguous prefix array.
 // Segment g's end is written by g itself (seg_cu[g + 1]), so every entry has one writer.
 __global__ void __launch_bounds__(kPlanThreads, 1) la_segment_plan_kernel(const PlanParams p) {
@@ -99,7 +103,10 @@ __global__ void __launch_bounds__(kPlanThreads, 1) la_segment_plan_kernel(const 
         if (slot >= p.pool_size) err |= 2;  // LA_DEV_ERR_BAD_INDEX
       }
       run = !bad && slot >= 0 && slot < p.pool_size;
-      cnt = run ? max(1, (len + p.S - 1) / p.S) : 1;
+      if (p.S_last > 0)
+        cnt = run ? (max(len - p.S_last, 0) + p.S - 1) / p.S + 1 : 1;
+      else
+        cnt = run ? max(1, (len + p.S - 1) / p.S) : 1;
     }
     // exclusive scan of cnt over the block
     long long x = cnt;
@@ -134,7 +141,8 @@ __global__ void __launch_bounds__(kPlanThreads, 1) la_segment_plan_kernel(const 
         for (int j = 0; j < cnt; ++j) {
           const int g = static_cast<int>(g0) + j;
           const bool last = j == cnt - 1;
-          p.seg_cu[g + 1] = last ? (run ? bos + len : eos) : bos + (j + 1) * p.S;
+          const int early_end = p.S_last > 0 ? min((j + 1) * p.S, len - p.S_last) : (j + 1) * p.S;
+          p.seg_cu[g + 1] = last ? (run ? bos + len : eos) : bos + early_end;
           p.seg_slot[g] = run ? g : -1;
           p.seg_flags[g] = (run && !last) ? 1 : 0;
         }

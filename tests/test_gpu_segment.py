@@ -62,6 +62,20 @@ def test_segmented_auto_length_full():
     compare_full(p, d, f"segmented auto S={seg}")
 
 
+def test_segmented_auto_short_first_segments_full():
+    """B=1, T=4096, H=HV=64: two segments per chain would leave the local-state pass on 64
+    SMs, so the automatic plan cuts the first half of each chain in two and keeps a long last
+    segment; every unit against the oracle."""
+    import linear_attention_prefill_chunkwise_gb300 as lap
+    p = W.custom(seed=81, B=1, T=4096, H=64, HV=64)
+    nbytes, seg = lap.la_prefill_segmented_workspace(1, 4096, 1, 64, False, 0)
+    if seg == 0:
+        pytest.skip("this device has too few SMs for 64 chains to be segmented")
+    d = upload(p)
+    run_seg(p, d, 0)
+    compare_full(p, d, f"segmented auto short first segments S={seg}")
+
+
 def test_segmented_long_few_heads_sampled():
     """B=1, T=65536, H=HV=8 (a tensor-parallel shard of a 64-head layer), automatic length."""
     p = W.custom(seed=78, B=1, T=65536, H=8, HV=8)
