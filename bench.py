@@ -115,12 +115,12 @@ class ClockSampler:
                    0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
     SMI_FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
                   "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+                  "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,temperature.gpu")
 
     def __init__(self, gpu_uuid: str, period_s: float = 0.001):
         self.uuid = gpu_uuid
         self.period = period_s
-        self.samples = []  # (perf_counter, sm_mhz, max_mhz, power_w, reason names)
+        self.samples = []  # (perf_counter, sm_mhz, max_mhz, power_w, reason names[, temperature_c])
         self.source = None
         self.t0 = self.t1 = None
         self._stop = None
@@ -142,7 +142,7 @@ class ClockSampler:
 
     def _nvml_loop(self, lib, h, reasons_fn):
         import ctypes
-        sm, mx, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        sm, mx, pw, rs, tc = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong(), ctypes.c_uint()
         while not self._stop.is_set():
             ok = (lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(sm)) == 0 and
                   lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0)
@@ -150,7 +150,8 @@ class ClockSampler:
                 power = pw.value / 1000.0 if lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw)) == 0 else None
                 names = [n for bit, n in self.REASON_BITS.items() if reasons_fn(h, ctypes.byref(rs)) == 0
                          and rs.value & bit]
-                self.samples.append((time.perf_counter(), float(sm.value), float(mx.value), power, names))
+                temp = float(tc.value) if lib.nvmlDeviceGetTemperature(h, 0, ctypes.byref(tc)) == 0 else None
+                self.samples.append((time.perf_counter(), float(sm.value), float(mx.value), power, names, temp))
             self._stop.wait(self.period)
 
     # ---- nvidia-smi fallback
@@ -162,8 +163,9 @@ class ClockSampler:
             try:
                 names = [n for n, val in zip(["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
                                               "sw_power_cap"], parts[5:9]) if val.lower().startswith("active")]
+                temp = float(parts[9]) if len(parts) > 9 and parts[9].replace(".", "", 1).isdigit() else None
                 self.samples.append((time.perf_counter(), float(parts[1]), float(parts[2]), float(parts[3]),
-                                     names))
+                                     names, temp))
             except ValueError:
                 continue
 
@@ -214,9 +216,10 @@ class ClockSampler:
                     "source": self.source}
         reasons = sorted({n for s in inside for n in s[4]})
         power = [s[3] for s in inside if s[3] is not None]
+        temps = [s[5] for s in inside if len(s) > 5 and s[5] is not None]
         return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": max(s[2] for s in inside),
                 "reasons": reasons, "power_w_median": statistics.median(power) if power else None,
-                "samples": len(inside), "source": self.source}
+                "temperature_c_max": max(temps) if temps else None, "samples": len(inside), "source": self.source}
 
 
 def gpu_id_for_smi(device) -> str:

@@ -96,5 +96,9 @@ def test_clock_summary_keeps_only_the_timed_window_and_reports_reasons():
     s = c.summary()
     assert s["samples"] == 3 and s["sm_mhz"] == 2010.0 and s["sm_max_mhz"] == 2070.0
     assert s["reasons"] == ["sw_power_cap"]
-    c.t0, c.t1 = 2.1, 3.0  # a window with no sample is reported as such, not guessed
+    assert s["temperature_c_max"] is None  # these samples carry no temperature
+    c.samples = [(1.0, 2070.0, 2070.0, 900.0, [], 51.0), (1.5, 2070.0, 2070.0, 950.0, [], 58.0),
+                 (3.0, 2070.0, 2070.0, 950.0, [], 90.0)]                  # the last one after it
+    assert c.summary()["temperature_c_max"] == 58.0
+    c.t0, c.t1 = 2.1, 2.9  # a window with no sample is reported as such, not guessed
     assert c.summary()["reasons"] == ["unavailable"]
