@@ -59,6 +59,11 @@ def call(**over):
     (dict(D=256, V=256), LA_UNSUPPORTED),
     (dict(D=32, V=32), LA_UNSUPPORTED),
     (dict(D=64, V=64, N=3), LA_INVALID),         # D = V = 64 passes the shape check
+    # size limits: token rows (TMA coordinates) and units must stay within int32
+    (dict(B=1, T=2**31 - 64, N=1), LA_UNSUPPORTED),
+    (dict(B=2**16, T=2**15, N=2**16), LA_UNSUPPORTED),
+    (dict(cu=FAKE, B=1, T=1000, N=2**30, HV=4, H=4), LA_UNSUPPORTED),
+    (dict(B=2**20, T=1, N=2**20, H=2**12, HV=2**12), LA_UNSUPPORTED),  # N * HV units
     (dict(H=3, HV=4), LA_UNSUPPORTED),
     (dict(H=0), LA_INVALID),
     (dict(N=-1), LA_INVALID),

@@ -288,3 +288,46 @@ def test_nonfinite_sequence_does_not_reach_its_neighbours(path):
         h_one = da["h_final"].view(torch.int32).cpu().numpy()
         assert np.array_equal(o_all[a:b], o_one), f"{path}: sequence {n} output differs from running it alone"
         assert np.array_equal(h_all[n], h_one[0]), f"{path}: sequence {n} final state differs from running it alone"
+
+
+def test_rows_past_two_to_the_31_elements():
+    """A packed batch of 2^20 tokens with 32 heads: q, k, v and o each hold 2^32 elements (8 GiB).
+    Its first sequence is padded (never read or written); the second, the last 100 tokens, lies
+    past element 2^31 of every tensor, so its loads, stores and state slots exercise 64-bit
+    offsets: outputs and final state against the oracle, the padded rows and slot untouched."""
+    import oracle
+    import linear_attention_prefill_chunkwise_gb300 as lap
+    from harness import check_output, check_state, to_torch_bf16
+    tokens, H, HV, L = 1 << 20, 32, 32, 100
+    assert (tokens - L) * HV * 128 > 2 ** 31
+    dev = "cuda"
+    rng = np.random.default_rng(31)
+    qb, kb, vb = W.make_qkv(rng, L, H, HV)
+    h0_np = W.make_states(rng, 2, HV)
+    slopes = W.slopes_for(HV)
+    scale = 1.0 / np.sqrt(128.0)
+    q = torch.empty((tokens, H, 128), dtype=torch.bfloat16, device=dev)
+    k = torch.empty_like(q)
+    v = torch.empty((tokens, HV, 128), dtype=torch.bfloat16, device=dev)
+    q[-L:] = to_torch_bf16(qb, dev)
+    k[-L:] = to_torch_bf16(kb, dev)
+    v[-L:] = to_torch_bf16(vb, dev)
+    o = torch.full((tokens, HV, 128), float("nan"), dtype=torch.bfloat16, device=dev)
+    h0 = torch.from_numpy(h0_np).to(dev)
+    hf = torch.full_like(h0, float("nan"))
+    idx = torch.tensor([-1, 1], dtype=torch.int32, device=dev)
+    cu = torch.tensor([0, tokens - L, tokens], dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    lap.la_prefill_fwd(q, k, v, torch.from_numpy(slopes).to(dev), scale, h0=h0, state_indices=idx, cu_seqlens=cu,
+                       o=o, h_final=hf, dev_error=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    o_ref, h_ref = oracle.tokenwise(W.bf16_to_f32(qb), W.bf16_to_f32(kb), W.bf16_to_f32(vb), slopes, scale,
+                                    h0=h0_np[1:2].astype(np.float64), cu_seqlens=np.array([0, L], dtype=np.int32))
+    check_output(o[-L:].float().cpu().numpy(), o_ref, "rows past 2^31 elements")
+    check_state(hf[1].cpu().numpy(), h_ref[0], "state of the sequence past 2^31 elements")
+    assert bool(torch.isnan(hf[0]).all())
+    for r in (0, tokens // 2, tokens - L - 1):
+        assert bool(torch.isnan(o[r].float()).all())
+    del q, k, v, o
+    torch.cuda.empty_cache()
