@@ -4,23 +4,25 @@
 //     o_t = lambda^(t+1) scale (S q_t) + sum_(j <= t) lambda^(t-j) scale (q_t . k_j) v_j,
 // evaluated without materialising any intermediate state.  Per (request, value head) the work
 // is one read of the 64 KB FP32 state S and one small product S [q_0 .. q_(T-1)], which runs on
-// the tensor cores: S is the A operand (M = 128 value rows, K = 128), the request's q rows the B
-// operand (N = 16 columns, T of them used), both as TF32 (the pages' verify kernel also
+// the tensor cores: S is the A operand (M = 128 value rows, K = 128), the request's q rows part of
+// the B operand (N = 32 columns, T of the unit's 8 used), both as TF32 (the pages' verify kernel also
 // multiplies h0 by q in TF32), accumulated in FP32 in tensor memory.
 //
 // One persistent CTA per SM walks the units u = blockIdx.x + n gridDim.x:
-//   warp 8 (one thread)   TMA loads: each unit's state slice as four 128 x 32 FP32 boxes,
+//   warp 12 (one thread)  TMA loads: each unit's state slice as four 128 x 32 FP32 boxes,
 //                         128-byte swizzled (the canonical K-major operand layout), into a
-//                         3-stage ring, and the request's q, k, v rows (8 x 128 BF16 each)
+//                         2-stage ring, and the request's q, k, v rows (8 x 128 BF16 each)
 //                         into the 2-stage ring of the group that takes the unit;
-//   warps 0-3, 4-7        two compute groups, on the units with n even and odd: per unit, q to
-//                         FP32 in the group's 8 rows of the B operand (swizzled); one thread
+//   warps 0-3, 4-7, 8-11  three compute groups, group g on the units n with n % 3 == g: per
+//                         unit, q to FP32 in the group's 8 rows of the B operand (swizzled); one thread
 //                         issues the 16 MMAs (K = 8 each); meanwhile the scores
 //                         A[i][j] = scale lambda^(i-j) q_i . k_j (j <= i) on the CUDA cores;
 //                         then thread v (= TMEM lane v) reads row v of S q, adds the intra
 //                         terms and stores o_t[v]; the draft k, v go to the KV buffer.  Each
-//                         group's chain of waits is long next to its arithmetic; two of them
-//                         keep twice the state loads in flight.
+//                         group's chain of waits is long next to its arithmetic; three of them
+//                         keep three units' state loads in flight (one group: 0.123 ms, two:
+//                         0.107, three: 0.103 on 128 requests x 8 tokens x 64 heads; four: no
+//                         better).
 // Every wait is bounded (sm103_ptx.cuh); a timeout sets LA_DEV_ERR_TIMEOUT, drains this CTA's
 // copies and MMAs in flight and frees tensor memory before the CTA exits.
 #pragma once
@@ -35,9 +37,9 @@ namespace lav {
 
 constexpr int kDim = 128;
 constexpr int kMaxTok = 8;        // draft tokens per request on this path
-constexpr int kN = 16;            // the MMA's N (q rows kMaxTok .. 15 of the operand stay zero)
-constexpr int kGroups = 2;        // compute groups, each on its own units (alternately)
-constexpr int kStStages = 3;      // state ring (shared by the groups, in unit order)
+constexpr int kN = 32;            // the MMA's N: the groups' q rows (rows kGroups * kMaxTok .. 31 stay zero)
+constexpr int kGroups = 3;        // compute groups, each on its own units (in turn)
+constexpr int kStStages = 2;      // state ring (shared by the groups, in unit order)
 constexpr int kTkStages = 2;      // token ring of each group
 constexpr int kCompute = 128;     // threads of a group: 4 warps, one TMEM lane per thread
 constexpr int kThreads = kGroups * kCompute + 32;
@@ -45,7 +47,7 @@ constexpr uint32_t kStateBox = 128 * 32 * 4;  // 128 rows x 32 FP32 columns
 constexpr uint32_t kStateBytes = 4 * kStateBox;
 constexpr uint32_t kBBox = kN * 128;          // kN rows x 32 FP32 columns
 constexpr uint32_t kTokBytes = kMaxTok * kDim * 2;
-constexpr uint32_t kTmemCols = 32;  // group g's accumulator: columns kN g .. kN g + kN - 1
+constexpr uint32_t kTmemCols = 128;  // group g's accumulator: columns kN g .. kN g + kN - 1 (power of 2)
 
 struct Params {
   const float* slopes;           // [HV]
@@ -71,7 +73,7 @@ struct __align__(1024) Smem {
   uint32_t tmem_base;
   int abort;
 };
-static_assert(kGroups * kMaxTok == kN, "the groups' q rows fill the MMA's N");
+static_assert(kGroups * kMaxTok <= kN, "the groups' q rows fit the MMA's N");
 
 __host__ __device__ constexpr int verify_smem_bytes() { return static_cast<int>(sizeof(Smem)) + 1024; }
 
@@ -128,13 +130,13 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& x, float (&f)[8]) {
   }
 }
 
-// The load thread: every unit's state slice (ring stage n % 3 for the CTA's n-th unit) and
-// token rows (group n % 2's ring, stage (n / 2) % 2), in the consumers' order.
+// The load thread: every unit's state slice (ring stage n % kStStages for the CTA's n-th unit) and
+// token rows (group n % kGroups's ring, stage (n / kGroups) % kTkStages), in the consumers' order.
 __device__ __forceinline__ void load_loop(Smem& sm, const Params& p, const CUtensorMap* tm_s,
                                           const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                                           volatile int* abort) {
   const int units = p.B * p.HV;
-  uint32_t n_st = 0, n_tk0 = 0, n_tk1 = 0;  // units loaded, in all and per group
+  uint32_t n_st = 0, n_tk[kGroups] = {};  // units loaded, in all and per group
   int slot = 0;
   for (int u = seek(p, blockIdx.x, units, true, slot); u < units; u = seek(p, u + gridDim.x, units, true, slot)) {
     const int b = u / p.HV, hv = u - b * p.HV, hq = hv / p.G;
@@ -146,7 +148,7 @@ __device__ __forceinline__ void load_loop(Smem& sm, const Params& p, const CUten
 #pragma unroll
     for (int c = 0; c < 4; ++c) lap::tma_load_2d(sm.st[s] + c * kStateBox, tm_s, &sm.st_full[s], 32 * c, y);
     ++n_st;
-    const uint32_t j = g ? n_tk1 : n_tk0, s2 = j % kTkStages;
+    const uint32_t j = n_tk[g], s2 = j % kTkStages;
     if (!lap::mbar_wait(&sm.tk_empty[g][s2], ((j / kTkStages) & 1u) ^ 1u, abort)) break;
     uint64_t* bar = &sm.tk_full[g][s2];
     lap::mbar_arrive_expect_tx(bar, 3 * kTokBytes);
@@ -154,7 +156,7 @@ __device__ __forceinline__ void load_loop(Smem& sm, const Params& p, const CUten
     lap::tma_load_2d(sm.tk[g][s2][0], tm_q, bar, hq * kDim, row);
     lap::tma_load_2d(sm.tk[g][s2][1], tm_k, bar, hq * kDim, row);
     lap::tma_load_2d(sm.tk[g][s2][2], tm_v, bar, hv * kDim, row);
-    if (g) ++n_tk1; else ++n_tk0;
+    ++n_tk[g];
   }
   // Teardown, also after an abort: a load is issued only after the previous one into its slot
   // was consumed, so the last loads of each ring are the only ones that can still be in flight.
@@ -163,17 +165,17 @@ __device__ __forceinline__ void load_loop(Smem& sm, const Params& p, const CUten
     lap::mbar_wait_drain(&sm.st_full[j % kStStages], (j / kStStages) & 1u);
   }
   for (int g = 0; g < kGroups; ++g) {
-    const uint32_t n_tk = g ? n_tk1 : n_tk0;
-    for (uint32_t i = 0; i < kTkStages && i < n_tk; ++i) {
-      const uint32_t j = n_tk - 1 - i;
+    const uint32_t n_tkg = n_tk[g];
+    for (uint32_t i = 0; i < kTkStages && i < n_tkg; ++i) {
+      const uint32_t j = n_tkg - 1 - i;
       lap::mbar_wait_drain(&sm.tk_full[g][j % kTkStages], (j / kTkStages) & 1u);
     }
   }
 }
 
 // Compute group g (warps 4g .. 4g+3): thread t is TMEM lane t and value row t of the group's
-// units, the CTA's units n with n % 2 == g.  The groups meet only in the state ring and in the
-// B operand, of which each writes its own 8 rows (the other group's rows give MMA columns that
+// units, the CTA's units n with n % kGroups == g.  The groups meet only in the state ring and in the
+// B operand, of which each writes its own 8 rows (the other groups' rows give MMA columns that
 // are not read).
 __device__ __forceinline__ void compute_loop(Smem& sm, const Params& p, uint32_t tmem_base, int g,
                                              volatile int* abort) {
@@ -259,7 +261,8 @@ __device__ __forceinline__ void compute_loop(Smem& sm, const Params& p, uint32_t
     if (!bar_and(bar_id, kCompute, done)) break;
     lap::tc_fence_after();
     float acc[16];
-    lap::tmem_ld16(tmem + ((static_cast<uint32_t>(t) & ~31u) << 16), acc);  // row t: (S q_c)[t], c = 0..15
+    const uint32_t col0 = (kMaxTok * g) & ~15u;  // the 16 columns holding this group's 8
+    lap::tmem_ld16(tmem + ((static_cast<uint32_t>(t) & ~31u) << 16) + col0, acc);  // row t: (S q_c)[t], c = 0..15
     float vj[kMaxTok];
 #pragma unroll
     for (int jj = 0; jj < kMaxTok; ++jj) vj[jj] = __bfloat162float(tk[2][jj][t]);
@@ -267,7 +270,7 @@ __device__ __forceinline__ void compute_loop(Smem& sm, const Params& p, uint32_t
 #pragma unroll
     for (int i = 0; i < kMaxTok; ++i) {
       if (i < T) {
-        float o = p.scale * sm.dec[g][i + 1] * (g ? acc[kMaxTok + i] : acc[i]);
+        float o = p.scale * sm.dec[g][i + 1] * (kMaxTok * g - col0 ? acc[kMaxTok + i] : acc[i]);
 #pragma unroll
         for (int jj = 0; jj <= i; ++jj) o = fmaf(sm.A[g][i][jj], vj[jj], o);
         orow[static_cast<size_t>(i) * v_tok] = __float2bfloat16_rn(o);
