@@ -78,11 +78,10 @@ CASES = {
 }
 
 
-@pytest.mark.parametrize("name", sorted(CASES))
-def test_decode_mtp_matches_oracle(name):
+def check_decode_mtp(c, name):
+    """la_decode_mtp on case c against the oracle: outputs, advanced slots, untouched rest."""
     import torch
     import linear_attention_prefill_chunkwise_gb300 as lap
-    c = make_case(**CASES[name])
     d = upload(c)
     o = torch.full((c["B"] * c["T"], c["HV"], W.V), float("nan"), dtype=torch.bfloat16, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -103,11 +102,12 @@ def test_decode_mtp_matches_oracle(name):
     assert np.array_equal(pool[untouched], c["pool"][untouched])
 
 
-@pytest.mark.parametrize("name", sorted(CASES))
-def test_verify_then_commit(name):
+def check_verify_then_commit(c, name, seed):
+    """la_verify then la_commit of a random accepted prefix (0 and T included) on case c: the
+    outputs against the oracle and decode, the KV buffer, the committed slots against the
+    oracle, bitwise where nothing or everything is accepted, and the untouched rest."""
     import torch
     import linear_attention_prefill_chunkwise_gb300 as lap
-    c = make_case(**CASES[name])
     B, T, H, HV, P = c["B"], c["T"], c["H"], c["HV"], c["P"]
     d = upload(c)
     # decode on a copy of the pool: the reference for verify's outputs and a full commit's state
@@ -138,7 +138,7 @@ def test_verify_then_commit(name):
     o_ref, _, _ = oracle_run(c)
     check_output(o.float().cpu().numpy()[rows], o_ref[rows], f"{name} verify o")
     # commit a random accepted prefix per request (0 and T included)
-    rng = np.random.default_rng(c["B"] * 131 + T)
+    rng = np.random.default_rng(seed)
     acc = rng.integers(0, T + 1, B).astype(np.int32)
     acc[0] = T
     if B > 1:
@@ -161,6 +161,17 @@ def test_verify_then_commit(name):
             assert np.array_equal(pool[s], dec[s])
     untouched = np.setdiff1d(np.arange(P), sel)
     assert np.array_equal(pool[untouched], c["pool"][untouched])
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_decode_mtp_matches_oracle(name):
+    check_decode_mtp(make_case(**CASES[name]), name)
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_verify_then_commit(name):
+    c = make_case(**CASES[name])
+    check_verify_then_commit(c, name, c["B"] * 131 + c["T"])
 
 
 def test_decode_without_indices_and_bad_index_flag():

@@ -102,3 +102,31 @@ def test_random_backward(seed):
     dout = W.bf16_bits(rng.standard_normal((p.tokens, p.HV, p.V), dtype=np.float32))
     dhf = (rng.standard_normal((p.pool_size, p.HV, p.V, p.D), dtype=np.float32) * np.float32(0.1)) if with_dhf else None
     _compare(p, dout, dhf, f"random backward {seed} {kw}", want_dh0=bool(seed % 3))
+
+
+def _draw_decode(seed):
+    """Arguments of test_gpu_decode.make_case for one random speculative-decoding batch: up to
+    40 requests of 1 to 17 draft tokens (both sides of the tensor-core verify's 8-token limit),
+    GVA groups, a pool larger than the batch with padded requests, and mixed special slopes."""
+    rng = np.random.default_rng(31000 + seed)
+    H = int(rng.integers(1, 5))
+    HV = H * int(rng.integers(1, 4))
+    B = int(rng.integers(1, 41))
+    T = int(rng.choice([1, 2, 3, 4, 5, 7, 8, 9, 12, 16, 17]))
+    kw = dict(seed=32000 + seed, B=B, T=T, H=H, HV=HV, P=B + int(rng.integers(0, 9)),
+              n_pad=int(rng.integers(0, B // 4 + 1)))
+    if rng.random() < 0.4:
+        sl = W.slopes_for(HV).astype(np.float32)
+        special = rng.random(HV) < 0.5
+        sl[special] = rng.choice([0.0, 1e-4, 0.7, 5.0, 40.0, 200.0], size=int(special.sum())).astype(np.float32)
+        kw["slopes"] = [float(x) for x in sl]
+    return kw
+
+
+@pytest.mark.parametrize("seed", range(32))
+def test_random_decode_ops(seed):
+    from test_gpu_decode import check_decode_mtp, check_verify_then_commit, make_case
+    kw = _draw_decode(seed)
+    c = make_case(**kw)
+    check_decode_mtp(c, f"random decode {seed} {kw}")
+    check_verify_then_commit(c, f"random verify/commit {seed} {kw}", 33000 + seed)
