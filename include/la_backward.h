@@ -65,7 +65,9 @@ la_status la_prefill_bwd_workspace(int B, int T, int H, int HV, int D, int pool_
  * Supported: HV a multiple of H (GVA: the G = HV / H value heads of a q/k head each contribute
  * to its dq and dk, which are summed in FP32 over the group before the one rounding to BF16),
  * D == V == 128 or 64, any N >= 0 and any sequence lengths; 16-byte aligned tensors.  Other shapes return LA_ERR_UNSUPPORTED and
- * launch nothing; invalid arguments LA_ERR_INVALID_ARGUMENT.  Device-side errors (bad
+ * launch nothing; invalid arguments LA_ERR_INVALID_ARGUMENT, among them outputs (dq, dk, dv,
+ * dh0, the workspace, dev_error) that share memory with an input or with each other (address
+ * ranges checked on the host).  Device-side errors (bad
  * cu_seqlens, bad state indices) set bits in *dev_error as for la_prefill_fwd.  The call
  * enqueues its kernels on `stream` and never synchronises with the host.
  */

@@ -41,6 +41,9 @@
  *   accepted_len int32 [B]            tokens to commit per request, clamped to [0, T]
  *   dev_error device int, nullable    LA_DEV_ERR_BAD_INDEX when a slot >= P (request skipped)
  * Supported: D == V == 128, HV % H == 0, T >= 1 (any B >= 0); 16-byte aligned pointers.
+ * What a call writes (o, kbuf, vbuf; the pool in decode and commit; dev_error) may share no
+ * memory with what it reads or with another of its outputs: LA_ERR_INVALID_ARGUMENT (address
+ * ranges checked on the host; pool and KV buffer span P slots with state_indices, B without).
  * Returns LA_OK after enqueueing (or with nothing to do when B == 0); any other status means
  * nothing was launched.
  */

@@ -80,7 +80,10 @@ typedef enum {
  *
  * Supported: D == V == 128 or D == V == 64 (state [P, HV, D, D]), HV % H == 0, any
  * N >= 0 and any sequence lengths (including 0 and lengths that are not multiples of 64).
- * q, k, v, o, h0, h_final must be 16-byte aligned.
+ * q, k, v, o, h0, h_final must be 16-byte aligned.  The outputs (o, h_final, dev_error) may
+ * share no memory with an input or with each other (the kernels read ahead of their stores),
+ * except that h_final may be h0 itself; the host checks the address ranges (the state ranges
+ * span P slots with state_indices, N without) and returns LA_ERR_INVALID_ARGUMENT.
  *
  * Returns LA_OK after enqueueing the kernels (or with nothing to do when N == 0 or
  * B*T == 0 and no state is requested).  LA_ERR_INVALID_ARGUMENT and LA_ERR_UNSUPPORTED

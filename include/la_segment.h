@@ -73,8 +73,9 @@ la_status la_prefill_segmented_workspace(int B, int T, int N, int HV, int packed
  *
  * Device-side errors go to *dev_error as for la_prefill_fwd; bounds whose segments would not
  * fit the workspace (overlapping cu_seqlens ranges) also set LA_DEV_ERR_BAD_SEQLENS and
- * skip the sequences concerned.  Returns LA_OK after enqueueing; LA_ERR_INVALID_ARGUMENT /
- * LA_ERR_UNSUPPORTED with nothing enqueued; LA_ERR_CUDA if a launch failed (earlier passes
+ * skip the sequences concerned.  The buffers follow la_prefill_fwd's rule on overlap, and the
+ * workspace may share no memory with any of them.  Returns LA_OK after enqueueing;
+ * LA_ERR_INVALID_ARGUMENT / LA_ERR_UNSUPPORTED with nothing enqueued; LA_ERR_CUDA if a launch failed (earlier passes
  * may then have been enqueued).
  */
 la_status la_prefill_fwd_segmented(const void* q, const void* k, const void* v, const float* slopes, float scale,

@@ -318,6 +318,27 @@ la_status la_prefill_bwd(const void* q, const void* k, const void* v, const floa
     return fail(LA_ERR_INVALID_ARGUMENT, "workspace too small: %zu bytes given, %zu needed", workspace_bytes,
                 lay.bytes);
   if (reinterpret_cast<uintptr_t>(workspace) % 256) return fail(LA_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
+  {
+    // q, k, v, dout, slopes, h0, dh_final and the index arrays are read; the gradients, the
+    // workspace and dev_error are written, and none of these may share memory with another
+    const uint64_t tk = static_cast<uint64_t>(tokens);
+    const uint64_t bq = tk * H * D * 2, bv = tk * HV * V * 2;
+    const uint64_t slots = state_indices ? static_cast<uint64_t>(pool_size) : static_cast<uint64_t>(N);
+    const uint64_t bst = slots * HV * static_cast<uint64_t>(V) * D * 4;
+    const la_host::Span ins[] = {{q, bq, "q"},
+                                 {k, bq, "k"},
+                                 {v, bv, "v"},
+                                 {dout, bv, "dout"},
+                                 {slopes, static_cast<uint64_t>(HV) * 4, "slopes"},
+                                 {h0, bst, "h0"},
+                                 {dh_final, bst, "dh_final"},
+                                 {state_indices, static_cast<uint64_t>(N) * 4, "state_indices"},
+                                 {cu_seqlens, cu_seqlens ? static_cast<uint64_t>(N + 1) * 4 : 0, "cu_seqlens"}};
+    const la_host::Span outs[] = {{dq, bq, "dq"},   {dk, bq, "dk"},
+                                  {dv, bv, "dv"},   {dh0, bst, "dh0"},
+                                  {workspace, lay.bytes, "workspace"}, {dev_error, 4, "dev_error"}};
+    if ((st = la_host::check_disjoint(outs, 6, ins, 9)) != LA_OK) return st;
+  }
   int dev = 0;
   cudaError_t ce = cudaGetDevice(&dev);
   if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(ce));

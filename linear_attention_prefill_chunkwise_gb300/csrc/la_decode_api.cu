@@ -108,6 +108,25 @@ lad::Params base_params(const float* slopes, float scale, float* state, const in
   return p;
 }
 
+// Byte sizes of a speculative-decoding call's buffers (the state pool and the KV buffer hold
+// pool_size slots with state_indices, else one per request).
+struct Sizes {
+  uint64_t q, v, state, kbuf, vbuf, slopes, per_request;
+};
+Sizes sizes(int B, int T, int H, int HV, int D, int V, int pool_size, const int32_t* state_indices) {
+  const uint64_t rows = static_cast<uint64_t>(B) * T;
+  const uint64_t slots = state_indices ? static_cast<uint64_t>(pool_size) : static_cast<uint64_t>(B);
+  Sizes z;
+  z.q = rows * H * D * 2;
+  z.v = rows * HV * V * 2;
+  z.state = slots * HV * static_cast<uint64_t>(V) * D * 4;
+  z.kbuf = slots * T * H * D * 2;
+  z.vbuf = slots * T * HV * V * 2;
+  z.slopes = static_cast<uint64_t>(HV) * 4;
+  z.per_request = static_cast<uint64_t>(B) * 4;
+  return z;
+}
+
 }  // namespace
 
 extern "C" {
@@ -124,6 +143,13 @@ la_status la_decode_mtp(const void* q, const void* k, const void* v, const float
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(state) || !aligned4(slopes) ||
       !aligned4(dev_error))
     return fail(LA_ERR_INVALID_ARGUMENT, "q, k, v, o, state must be 16-byte and slopes, dev_error 4-byte aligned");
+  {
+    const Sizes z = sizes(B, T, H, HV, D, V, pool_size, state_indices);
+    const la_host::Span ins[] = {{q, z.q, "q"}, {k, z.q, "k"}, {v, z.v, "v"}, {slopes, z.slopes, "slopes"},
+                                 {state_indices, z.per_request, "state_indices"}};
+    const la_host::Span outs[] = {{o, z.v, "o"}, {state, z.state, "state"}, {dev_error, 4, "dev_error"}};
+    if ((st = la_host::check_disjoint(outs, 3, ins, 5)) != LA_OK) return st;
+  }
   lad::Params p = base_params(slopes, scale, state, state_indices, dev_error, B, T, H, HV, pool_size);
   p.q = static_cast<const __nv_bfloat16*>(q);
   p.k = static_cast<const __nv_bfloat16*>(k);
@@ -147,6 +173,14 @@ la_status la_verify(const void* q, const void* k, const void* v, const float* sl
       !aligned16(vbuf) || !aligned4(slopes) || !aligned4(dev_error))
     return fail(LA_ERR_INVALID_ARGUMENT,
                 "q, k, v, o, state, kbuf, vbuf must be 16-byte and slopes, dev_error 4-byte aligned");
+  {
+    const Sizes z = sizes(B, T, H, HV, D, V, pool_size, state_indices);
+    const la_host::Span ins[] = {{q, z.q, "q"},           {k, z.q, "k"}, {v, z.v, "v"}, {slopes, z.slopes, "slopes"},
+                                 {state, z.state, "state"}, {state_indices, z.per_request, "state_indices"}};
+    const la_host::Span outs[] = {{o, z.v, "o"}, {kbuf, z.kbuf, "kbuf"}, {vbuf, z.vbuf, "vbuf"},
+                                  {dev_error, 4, "dev_error"}};
+    if ((st = la_host::check_disjoint(outs, 4, ins, 6)) != LA_OK) return st;
+  }
   lad::Params p = base_params(slopes, scale, const_cast<float*>(state), state_indices, dev_error, B, T, H, HV,
                               pool_size);
   p.q = static_cast<const __nv_bfloat16*>(q);
@@ -204,6 +238,16 @@ la_status la_commit(float* state, const int32_t* state_indices, const void* kbuf
       !aligned4(dev_error))
     return fail(LA_ERR_INVALID_ARGUMENT,
                 "state, kbuf, vbuf must be 16-byte and accepted_len, slopes, dev_error 4-byte aligned");
+  {
+    const Sizes z = sizes(B, T, H, HV, D, V, pool_size, state_indices);
+    const la_host::Span ins[] = {{kbuf, z.kbuf, "kbuf"},
+                                 {vbuf, z.vbuf, "vbuf"},
+                                 {accepted_len, z.per_request, "accepted_len"},
+                                 {slopes, z.slopes, "slopes"},
+                                 {state_indices, z.per_request, "state_indices"}};
+    const la_host::Span outs[] = {{state, z.state, "state"}, {dev_error, 4, "dev_error"}};
+    if ((st = la_host::check_disjoint(outs, 2, ins, 5)) != LA_OK) return st;
+  }
   lad::Params p = base_params(slopes, 0.f, state, state_indices, dev_error, B, T, H, HV, pool_size);
   p.kbuf = const_cast<__nv_bfloat16*>(static_cast<const __nv_bfloat16*>(kbuf));
   p.vbuf = const_cast<__nv_bfloat16*>(static_cast<const __nv_bfloat16*>(vbuf));

@@ -30,6 +30,60 @@ inline la_status fail(la_status st, const char* fmt, ...) {
 inline bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 inline bool aligned4(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 3u) == 0; }
 
+// A caller's buffer as a byte range (a null pointer or an empty range holds no byte).
+struct Span {
+  const void* p;
+  uint64_t bytes;
+  const char* name;
+};
+
+// Outputs may share no byte with an input or with another output: the kernels read their
+// inputs ahead of their stores and write their states after their last read, so an overlap
+// is a race, not an in-place update.  A buffer that a call updates in place (the state pool)
+// is listed once, as an output.  Only addresses are compared; nothing is read.
+inline la_status check_disjoint(const Span* outs, int n_out, const Span* ins, int n_in) {
+  auto meet = [](const Span& a, const Span& b) {
+    if (!a.p || !b.p || a.bytes == 0 || b.bytes == 0) return false;
+    const uint64_t x = reinterpret_cast<uintptr_t>(a.p), y = reinterpret_cast<uintptr_t>(b.p);
+    return x < y + b.bytes && y < x + a.bytes;
+  };
+  for (int i = 0; i < n_out; ++i) {
+    for (int j = 0; j < n_in; ++j)
+      if (meet(outs[i], ins[j]))
+        return fail(LA_ERR_INVALID_ARGUMENT, "%s overlaps %s (an output may share no memory with an input)",
+                    outs[i].name, ins[j].name);
+    for (int j = 0; j < i; ++j)
+      if (meet(outs[i], outs[j]))
+        return fail(LA_ERR_INVALID_ARGUMENT, "%s overlaps %s (outputs may share no memory)", outs[i].name,
+                    outs[j].name);
+  }
+  return LA_OK;
+}
+
+// The buffers of a prefill call (la_prefill_fwd and the segmented entry points): q, k, v,
+// slopes, h0, state_indices and cu_seqlens are read; o, h_final and dev_error are written;
+// h_final may be h0 itself (an in-place pool), which then counts as an output only.
+inline la_status check_prefill_disjoint(const void* q, const void* k, const void* v, const float* slopes,
+                                        const float* h0, const int32_t* state_indices, const int32_t* cu_seqlens,
+                                        const void* o, const float* h_final, const int* dev_error, int B, int T,
+                                        int N, int H, int HV, int D, int V, int pool_size,
+                                        const void* workspace = nullptr, uint64_t workspace_bytes = 0) {
+  const uint64_t tokens = static_cast<uint64_t>(B) * static_cast<uint64_t>(T);
+  const uint64_t bq = tokens * H * D * 2, bv = tokens * HV * V * 2;
+  const uint64_t slots = state_indices ? static_cast<uint64_t>(pool_size) : static_cast<uint64_t>(N);
+  const uint64_t bst = slots * HV * static_cast<uint64_t>(V) * D * 4;
+  const Span ins[] = {{q, bq, "q"},
+                      {k, bq, "k"},
+                      {v, bv, "v"},
+                      {slopes, static_cast<uint64_t>(HV) * 4, "slopes"},
+                      {h0 == h_final ? nullptr : h0, bst, "h0"},
+                      {state_indices, static_cast<uint64_t>(N) * 4, "state_indices"},
+                      {cu_seqlens, cu_seqlens ? static_cast<uint64_t>(N + 1) * 4 : 0, "cu_seqlens"}};
+  const Span outs[] = {{o, bv, "o"}, {h_final, bst, "h_final"}, {dev_error, 4, "dev_error"},
+                       {workspace, workspace_bytes, "workspace"}};
+  return check_disjoint(outs, 4, ins, 7);
+}
+
 // SM count and compute capability of the current device, looked up once per device, plus
 // an optional one-time setup step (a kernel attribute) run with it.
 constexpr int kMaxDevices = 64;

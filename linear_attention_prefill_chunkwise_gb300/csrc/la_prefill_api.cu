@@ -81,6 +81,9 @@ la_status la_prefill_fwd(const void* q, const void* k, const void* v, const floa
   la_status st0 = la_host::check_prefill_args(q, k, v, slopes, h0, state_indices, cu_seqlens, o, h_final, B, T, N,
                                               H, HV, D, V, pool_size, dev_error, &nothing);
   if (st0 != LA_OK || nothing) return st0;
+  st0 = la_host::check_prefill_disjoint(q, k, v, slopes, h0, state_indices, cu_seqlens, o, h_final, dev_error, B, T,
+                                        N, H, HV, D, V, pool_size);
+  if (st0 != LA_OK) return st0;
   const int64_t tokens = static_cast<int64_t>(B) * T;
   const int64_t units = static_cast<int64_t>(N) * HV;
 

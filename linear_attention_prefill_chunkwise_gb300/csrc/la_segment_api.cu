@@ -161,6 +161,9 @@ la_status la_prefill_fwd_segmented(const void* q, const void* k, const void* v, 
                 pl.bytes);
   if (reinterpret_cast<uintptr_t>(workspace) % kWsAlign)
     return fail(LA_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
+  st = la_host::check_prefill_disjoint(q, k, v, slopes, h0, state_indices, cu_seqlens, o, h_final, dev_error, B, T, N,
+                                       H, HV, D, V, pool_size, workspace, pl.bytes);
+  if (st != LA_OK) return st;
   if (!ds && (st = segment_device(&ds)) != LA_OK) return st;
 
   const int64_t tokens = static_cast<int64_t>(B) * T;

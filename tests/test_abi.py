@@ -41,10 +41,14 @@ def test_library_loads_and_exports_every_declared_symbol():
 
 
 FAKE = 0x10000  # never dereferenced: every call below is rejected on the host
+# distinct fake buffers, 2^40 bytes apart, so that the check that outputs share no memory with
+# inputs or with each other passes unless a case sets two of them to overlap
+(Q, K, VV, SL, H0, O, HF, IDX, CU, ERR, WS, DOUT, DQ, DK, DV, DH0, DHF, KB, VB, ACC, ST) = (
+    FAKE + (i + 1) * (1 << 40) for i in range(21))
 
 
 def call(**over):
-    args = dict(q=FAKE, k=FAKE, v=FAKE, slopes=FAKE, scale=1.0, h0=None, idx=None, cu=None, o=FAKE, hf=None,
+    args = dict(q=Q, k=K, v=VV, slopes=SL, scale=1.0, h0=None, idx=None, cu=None, o=O, hf=None,
                 B=2, T=128, N=2, H=2, HV=2, D=128, V=128, P=0, sched=0, err=None, stream=None)
     args.update(over)
     a = args
@@ -82,6 +86,34 @@ def test_host_validation(over, status):
     assert lap.load_library().la_last_error() != b""
 
 
+# B=2, T=128, H=HV=2, D=128: q, k, v and o are 128 KiB each, a state slot 128 KiB (2 heads)
+@pytest.mark.parametrize("over", [
+    dict(o=Q),                                   # o is q
+    dict(o=VV + 128 * 1024 - 16),                # o starts inside v's last 16 bytes
+    dict(o=K - 128 * 1024 + 16),                 # o ends inside k
+    dict(o=SL - 64),                             # o covers slopes
+    dict(hf=VV + 4096, P=2),                     # h_final inside v
+    dict(h0=H0, hf=H0 + 65536, P=2),             # h_final overlaps h0 without being h0
+    dict(hf=O + 1024, P=2),                      # the two outputs overlap
+    dict(err=O + 16),                            # dev_error inside o
+    dict(cu=O + 32, B=1, T=256, N=2),            # cu_seqlens inside o
+    dict(idx=HF + 16, hf=HF, P=4),               # state_indices inside h_final
+])
+def test_outputs_may_not_overlap_inputs(over):
+    assert call(**over) == LA_INVALID
+    assert b"overlaps" in lap.load_library().la_last_error()
+
+
+def test_in_place_pool_is_not_an_overlap():
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # h_final == h0 (an in-place pool) passes every host check; without a device the call then
+    # fails on the device query, not on the overlap check
+    assert call(h0=H0, hf=H0, P=2) == LA_CUDA
+    assert call(h0=H0, hf=H0, idx=IDX, P=8) == LA_CUDA
+
+
 def test_empty_batch_is_a_no_op():
     assert call(N=0, B=0) == LA_OK
     assert call(cu=FAKE, B=1, T=0, N=1) == LA_OK  # no tokens and no state requested
@@ -105,8 +137,8 @@ def test_product_path_does_not_touch_the_oracle():
 
 
 def call_decode(fn="la_decode_mtp", **over):
-    a = dict(q=FAKE, k=FAKE, v=FAKE, slopes=FAKE, scale=1.0, state=FAKE, idx=None, o=FAKE, kbuf=None, vbuf=None,
-             acc=FAKE, B=2, T=8, H=2, HV=2, D=128, V=128, P=2, err=None, stream=None)
+    a = dict(q=Q, k=K, v=VV, slopes=SL, scale=1.0, state=ST, idx=None, o=O, kbuf=None, vbuf=None,
+             acc=ACC, B=2, T=8, H=2, HV=2, D=128, V=128, P=2, err=None, stream=None)
     a.update(over)
     lib = lap.load_library()
     ints = (a["B"], a["T"], a["H"], a["HV"], a["D"], a["V"], a["P"])
@@ -138,6 +170,23 @@ def call_decode(fn="la_decode_mtp", **over):
 def test_decode_host_validation(fn, over, status):
     assert call_decode(fn, **over) == status
     assert lap.load_library().la_last_error() != b""
+
+
+# B=2, T=8, H=HV=2: q, k, v and o are 8 KiB each, a pool slot 128 KiB, a KV-buffer slot 8 KiB
+@pytest.mark.parametrize("fn,over", [
+    ("la_decode_mtp", dict(o=VV)),               # o is v
+    ("la_decode_mtp", dict(state=Q + 4096)),     # the pool overlaps q
+    ("la_decode_mtp", dict(o=ST + 16)),          # o inside the pool
+    ("la_decode_mtp", dict(err=ST + 16)),        # dev_error inside the pool
+    ("la_verify", dict(kbuf=K, vbuf=VB)),        # the KV buffer is the draft k itself
+    ("la_verify", dict(kbuf=KB, vbuf=KB + 1024)),  # the two KV buffers overlap
+    ("la_verify", dict(kbuf=KB, vbuf=VB, o=ST - 16)),  # o ends inside the pool (read here)
+    ("la_commit", dict(kbuf=ST, vbuf=VB)),       # the pool overlaps the KV buffer it reads
+    ("la_commit", dict(kbuf=KB, vbuf=VB, acc=ST + 64)),
+])
+def test_decode_outputs_may_not_overlap_inputs(fn, over):
+    assert call_decode(fn, **over) == LA_INVALID
+    assert b"overlaps" in lap.load_library().la_last_error()
 
 
 def test_decode_empty_batch_is_a_no_op():
@@ -184,8 +233,8 @@ def test_segmented_workspace_rejects_bad_segment_len(seg):
 
 
 def call_segmented(**over):
-    a = dict(q=FAKE, k=FAKE, v=FAKE, slopes=FAKE, scale=1.0, h0=None, idx=None, cu=None, o=FAKE, hf=None,
-             B=2, T=1000, N=2, H=2, HV=2, D=128, V=128, P=0, seg=128, ws=FAKE, wsb=1 << 30, err=None, stream=None)
+    a = dict(q=Q, k=K, v=VV, slopes=SL, scale=1.0, h0=None, idx=None, cu=None, o=O, hf=None,
+             B=2, T=1000, N=2, H=2, HV=2, D=128, V=128, P=0, seg=128, ws=WS, wsb=1 << 30, err=None, stream=None)
     a.update(over)
     lib = lap.load_library()
     return lib.la_prefill_fwd_segmented(a["q"], a["k"], a["v"], a["slopes"], ctypes.c_float(a["scale"]), a["h0"],
@@ -209,6 +258,12 @@ def test_segmented_host_validation(over, status):
     assert lap.load_library().la_last_error() != b""
 
 
+def test_segmented_workspace_may_not_overlap_the_buffers():
+    assert call_segmented(ws=O - 256) == LA_INVALID     # the workspace runs into o
+    assert call_segmented(o=Q) == LA_INVALID
+    assert b"overlaps" in lap.load_library().la_last_error()
+
+
 def test_segmented_empty_batch_is_a_no_op():
     assert call_segmented(N=0, B=0, T=0) == LA_OK
 
@@ -222,9 +277,9 @@ def test_segmented_no_device_is_reported():
 
 
 def call_backward(**over):
-    a = dict(q=FAKE, k=FAKE, v=FAKE, slopes=FAKE, scale=1.0, h0=None, dout=FAKE, dhf=None, idx=None, cu=None,
-             dq=FAKE, dk=FAKE, dv=FAKE, dh0=None, B=2, T=128, N=2, H=2, HV=2, D=128, V=128, P=0, ws=FAKE,
-             wsb=1 << 40, err=None, stream=None)
+    a = dict(q=Q, k=K, v=VV, slopes=SL, scale=1.0, h0=None, dout=DOUT, dhf=None, idx=None, cu=None,
+             dq=DQ, dk=DK, dv=DV, dh0=None, B=2, T=128, N=2, H=2, HV=2, D=128, V=128, P=0, ws=WS,
+             wsb=1 << 39, err=None, stream=None)
     a.update(over)
     lib = lap.load_library()
     return lib.la_prefill_bwd(a["q"], a["k"], a["v"], a["slopes"], ctypes.c_float(a["scale"]), a["h0"], a["dout"],
@@ -247,6 +302,19 @@ def call_backward(**over):
 def test_backward_host_validation(over, status):
     assert call_backward(**over) == status
     assert lap.load_library().la_last_error() != b""
+
+
+@pytest.mark.parametrize("over", [
+    dict(dq=DK),                                 # two gradients in one buffer
+    dict(dv=DOUT),                               # dv written over dout
+    dict(dk=K),                                  # dk written over k
+    dict(ws=DQ - 1024, h0=H0, P=2),              # the workspace (h0 transposed) runs into dq
+    dict(dh0=H0, h0=H0, P=2),                    # dh0 written over h0 (read until the end)
+    dict(err=DV + 4),
+])
+def test_backward_outputs_may_not_overlap_inputs(over):
+    assert call_backward(**over) == LA_INVALID
+    assert b"overlaps" in lap.load_library().la_last_error()
 
 
 def test_backward_empty_batch_is_a_no_op():
