@@ -84,9 +84,9 @@ la_status launch(const lad::Params& p, void* stream) {
   la_status st = la_host::current_device(g_dev, &ds, setup_kernels);
   if (st != LA_OK) return st;
   const int grid = lad::tokenwise_grid(p.B * p.HV * lad::kSplit, ds->sms);
-  lad::la_tokenwise_kernel<kMode>
-      <<<grid, lad::kThreads, lad::tokenwise_smem_bytes(), static_cast<cudaStream_t>(stream)>>>(p);
-  const cudaError_t ce = cudaGetLastError();
+  cudaError_t ce = la_host::launch_pdl(lad::la_tokenwise_kernel<kMode>, grid, lad::kThreads,
+                                       lad::tokenwise_smem_bytes(), static_cast<cudaStream_t>(stream), p);
+  if (ce == cudaSuccess) ce = cudaGetLastError();
   if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(ce));
   return LA_OK;
 }
@@ -218,9 +218,9 @@ la_status la_verify(const void* q, const void* k, const void* v, const float* sl
   vp.pool_size = pool_size;
   const int units = B * HV;
   const int grid = units < ds->sms ? units : ds->sms;
-  lav::la_verify_tc_kernel<<<grid, lav::kThreads, lav::verify_smem_bytes(), static_cast<cudaStream_t>(stream)>>>(
-      tm_s, tm_q, tm_k, tm_v, vp);
-  const cudaError_t ce = cudaGetLastError();
+  cudaError_t ce = la_host::launch_pdl(lav::la_verify_tc_kernel, grid, lav::kThreads, lav::verify_smem_bytes(),
+                                       static_cast<cudaStream_t>(stream), tm_s, tm_q, tm_k, tm_v, vp);
+  if (ce == cudaSuccess) ce = cudaGetLastError();
   if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(ce));
   return LA_OK;
 }

@@ -166,6 +166,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) la_tokenwise_kernel(cons
   const float* s_in = (kMode == kPrefill) ? p.h0 : p.state;
   float* s_out = (kMode == kPrefill) ? p.h_final : p.state;
   volatile int* abort = &sm.abort;
+  // launched with programmatic stream serialization (see la_prefill_fwd_kernel)
+  lap::griddep_wait();
+  lap::griddep_launch_dependents();
   if (t == 0) {
     lap::mbar_init(&sm.bar, 1);
     sm.abort = 0;

@@ -11,6 +11,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
+#include <utility>
 
 #include "../../include/la_prefill.h"
 
@@ -29,6 +30,26 @@ inline la_status fail(la_status st, const char* fmt, ...) {
 
 inline bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 inline bool aligned4(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 3u) == 0; }
+
+// A launch with programmatic stream serialization: the grid may be placed on the GPU while the
+// previous kernel in the stream is still finishing, which hides the launch gap between
+// back-to-back calls.  Every kernel launched this way starts with griddepcontrol.wait, so none
+// of its memory accesses happens before that previous kernel has completed.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), int grid, int threads, int smem, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // A caller's buffer as a byte range (a null pointer or an empty range holds no byte).
 struct Span {

@@ -136,10 +136,10 @@ la_status la_prefill_fwd(const void* q, const void* k, const void* v, const floa
     tp.num_tokens = static_cast<int>(tokens);
     tp.short_max = kShortMax;
     if (units * lad::kSplit > INT32_MAX) return fail(LA_ERR_UNSUPPORTED, "N*HV too large (%lld)", (long long)units);
-    lad::la_tokenwise_kernel<lad::kPrefill>
-        <<<lad::tokenwise_grid(static_cast<int>(units * lad::kSplit), ds.sms), lad::kThreads,
-           lad::tokenwise_smem_bytes(), static_cast<cudaStream_t>(stream)>>>(tp);
-    ce = cudaGetLastError();
+    ce = la_host::launch_pdl(lad::la_tokenwise_kernel<lad::kPrefill>,
+                             lad::tokenwise_grid(static_cast<int>(units * lad::kSplit), ds.sms), lad::kThreads,
+                             lad::tokenwise_smem_bytes(), static_cast<cudaStream_t>(stream), tp);
+    if (ce == cudaSuccess) ce = cudaGetLastError();
     if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "tokenwise kernel launch failed: %s", cudaGetErrorString(ce));
   }
   if (!run_chunkwise) return LA_OK;
@@ -171,18 +171,11 @@ la_status la_prefill_fwd(const void* q, const void* k, const void* v, const floa
   // CTA runs a handful of units); other batches deal units out round robin.
   const bool listed = packed && N <= lap::kSchedSeqMax && (units + grid - 1) / grid <= lap::kSchedMax;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  if (D == 128) {
-    if (listed)
-      lap::la_prefill_fwd_kernel<true, 128><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p);
-    else
-      lap::la_prefill_fwd_kernel<false, 128><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p);
-  } else {
-    if (listed)
-      lap::la_prefill_fwd_kernel<true, 64><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p);
-    else
-      lap::la_prefill_fwd_kernel<false, 64><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p);
-  }
-  ce = cudaGetLastError();
+  void (*kernel)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, lap::KernelParams) =
+      D == 128 ? (listed ? lap::la_prefill_fwd_kernel<true, 128> : lap::la_prefill_fwd_kernel<false, 128>)
+               : (listed ? lap::la_prefill_fwd_kernel<true, 64> : lap::la_prefill_fwd_kernel<false, 64>);
+  ce = la_host::launch_pdl(kernel, grid, lap::kThreads, smem_bytes(), cs, tm_q, tm_k, tm_v, tm_o, p);
+  if (ce == cudaSuccess) ce = cudaGetLastError();
   if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(ce));
   return LA_OK;
 }
@@ -241,17 +234,14 @@ la_status chunkwise(const void* q, const void* k, const void* v, const float* sl
   const int grid = static_cast<int>(units < dsp->sms ? units : dsp->sms);
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const int variant = (D == 128 ? 0 : 4) + (reverse ? 2 : 0) + (o_f32 ? 1 : 0);
-  switch (variant) {
-    case 0: lap::la_prefill_fwd_kernel<false, 128, false, false><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p); break;
-    case 1: lap::la_prefill_fwd_kernel<false, 128, false, true><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p); break;
-    case 2: lap::la_prefill_fwd_kernel<false, 128, true, false><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p); break;
-    case 3: lap::la_prefill_fwd_kernel<false, 128, true, true><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p); break;
-    case 4: lap::la_prefill_fwd_kernel<false, 64, false, false><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p); break;
-    case 5: lap::la_prefill_fwd_kernel<false, 64, false, true><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p); break;
-    case 6: lap::la_prefill_fwd_kernel<false, 64, true, false><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p); break;
-    default: lap::la_prefill_fwd_kernel<false, 64, true, true><<<grid, lap::kThreads, smem_bytes(), cs>>>(tm_q, tm_k, tm_v, tm_o, p); break;
-  }
-  const cudaError_t ce = cudaGetLastError();
+  static void (*const kernels[8])(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, lap::KernelParams) = {
+      lap::la_prefill_fwd_kernel<false, 128, false, false>, lap::la_prefill_fwd_kernel<false, 128, false, true>,
+      lap::la_prefill_fwd_kernel<false, 128, true, false>,  lap::la_prefill_fwd_kernel<false, 128, true, true>,
+      lap::la_prefill_fwd_kernel<false, 64, false, false>,  lap::la_prefill_fwd_kernel<false, 64, false, true>,
+      lap::la_prefill_fwd_kernel<false, 64, true, false>,   lap::la_prefill_fwd_kernel<false, 64, true, true>};
+  cudaError_t ce = la_host::launch_pdl(kernels[variant], grid, lap::kThreads, smem_bytes(), cs, tm_q, tm_k, tm_v,
+                                       tm_o, p);
+  if (ce == cudaSuccess) ce = cudaGetLastError();
   if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(ce));
   return LA_OK;
 }

@@ -925,6 +925,11 @@ la_prefill_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
   const int warp = tid >> 5;
   const int lane = tid & 31;
   volatile int* abort = &sm.abort;
+  // Launched with programmatic stream serialization: no global memory is touched before the
+  // previous grid in the stream has completed, and the next grid may be placed once every CTA
+  // of this one is running (it waits the same way).
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (p.short_max >= 0) {
     // Launched beside the tokenwise kernel for a packed batch of short sequences: unless some

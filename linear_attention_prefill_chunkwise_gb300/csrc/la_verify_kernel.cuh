@@ -307,6 +307,9 @@ la_verify_tc_kernel(const __grid_constant__ CUtensorMap tm_s, const __grid_const
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(verify_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5;
   volatile int* abort = &sm.abort;
+  // launched with programmatic stream serialization (see la_prefill_fwd_kernel)
+  lap::griddep_wait();
+  lap::griddep_launch_dependents();
   if (warp == 0) {
     lap::tmem_alloc(&sm.tmem_base, kTmemCols);
     lap::tmem_relinquish();
