@@ -36,11 +36,11 @@ inline bool aligned4(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr)
 // back-to-back calls.  Every kernel launched this way starts with griddepcontrol.wait, so none
 // of its memory accesses happens before that previous kernel has completed.
 template <typename... Params, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(Params...), int grid, int threads, int smem, cudaStream_t stream,
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 threads, int smem, cudaStream_t stream,
                        Args&&... args) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(static_cast<unsigned>(threads));
+  cfg.gridDim = grid;
+  cfg.blockDim = threads;
   cfg.dynamicSmemBytes = static_cast<size_t>(smem);
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

@@ -200,7 +200,7 @@ la_status la_prefill_fwd_segmented(const void* q, const void* k, const void* v, 
   pp.S_last = pl.S_last;
   pp.nseg_max = nseg;
   pp.pool_size = la_host::effective_pool_size(h0, h_final, state_indices, pool_size, N);
-  las::la_segment_plan_kernel<<<1, las::kPlanThreads, 0, s>>>(pp);
+  (void)la_host::launch_pdl(las::la_segment_plan_kernel, 1, las::kPlanThreads, 0, s, pp);
   if ((st = launched("segment plan")) != LA_OK) return st;
 
   // 2. local states of the segments that are not the last of their sequence
@@ -214,7 +214,7 @@ la_status la_prefill_fwd_segmented(const void* q, const void* k, const void* v, 
   sp.G = HV / H;
   sp.num_units = nseg * HV;
   const int grid_a = sp.num_units < ds->sms ? sp.num_units : ds->sms;
-  las::la_segment_state_kernel<<<grid_a, las::kStThreads, state_smem_bytes(), s>>>(tm_k, tm_v, sp);
+  (void)la_host::launch_pdl(las::la_segment_state_kernel, grid_a, las::kStThreads, state_smem_bytes(), s, tm_k, tm_v, sp);
   if ((st = launched("segment state")) != LA_OK) return st;
 
   // 3. initial state of every segment
@@ -228,7 +228,7 @@ la_status la_prefill_fwd_segmented(const void* q, const void* k, const void* v, 
   cp.states = states;
   cp.HV = HV;
   const dim3 grid_c(static_cast<unsigned>(N) * HV, las::kCombSplit);
-  las::la_segment_combine_kernel<<<grid_c, las::kCombThreads, 0, s>>>(cp);
+  (void)la_host::launch_pdl(las::la_segment_combine_kernel, grid_c, las::kCombThreads, 0, s, cp);
   if ((st = launched("segment combine")) != LA_OK) return st;
 
   // 4. the chunkwise prefill of every segment: a packed batch whose state pool is the
@@ -239,7 +239,7 @@ la_status la_prefill_fwd_segmented(const void* q, const void* k, const void* v, 
 
   // 5. final states
   if (h_final) {
-    las::la_segment_final_kernel<<<grid_c, las::kCombThreads, 0, s>>>(cp);
+    (void)la_host::launch_pdl(las::la_segment_final_kernel, grid_c, las::kCombThreads, 0, s, cp);
     if ((st = launched("segment final")) != LA_OK) return st;
   }
   return LA_OK;

@@ -65,6 +65,8 @@ constexpr int kPlanThreads = 1024;
 // owns one segment with slot -1 so that the segment bounds stay one contiguous prefix array.
 // Segment g's end is written by g itself (seg_cu[g + 1]), so every entry has one writer.
 __global__ void __launch_bounds__(kPlanThreads, 1) la_segment_plan_kernel(const PlanParams p) {
+  lap::griddep_wait();  // launched with programmatic stream serialization (la_host::launch_pdl)
+  lap::griddep_launch_dependents();
   // 64-bit counts: with overlapping (invalid) bounds the segment counts can exceed int32
   __shared__ long long warp_tot[kPlanThreads / 32];
   __shared__ long long s_carry;
@@ -372,6 +374,8 @@ __device__ __forceinline__ void st_epilogue(StateSmem& sm, const StateParams& p,
 __global__ void __launch_bounds__(kStThreads, 1)
 la_segment_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const StateParams p) {
+  lap::griddep_wait();  // launched with programmatic stream serialization (la_host::launch_pdl)
+  lap::griddep_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   StateSmem& sm = *reinterpret_cast<StateSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -443,6 +447,8 @@ constexpr int kCombBatch = 8;   // segments whose local states are loaded before
 // H <- h0 (or 0); for each segment i of the sequence: states[i] <- H, then
 // H <- lambda^{L_i} H + Sloc_i (Sloc_i read from states[i] before it is overwritten).
 __global__ void __launch_bounds__(kCombThreads) la_segment_combine_kernel(const CombineParams p) {
+  lap::griddep_wait();  // launched with programmatic stream serialization (la_host::launch_pdl)
+  lap::griddep_launch_dependents();
   const int n = blockIdx.x / p.HV, hv = blockIdx.x - n * p.HV;
   const int slot = __ldg(p.seq_slot + n);
   if (slot < 0) return;
@@ -477,6 +483,8 @@ __global__ void __launch_bounds__(kCombThreads) la_segment_combine_kernel(const 
 // grid (N * HV, kCombSplit): the final state of each running sequence's last segment,
 // left in the workspace by the prefill, copied to h_final[slot].
 __global__ void __launch_bounds__(kCombThreads) la_segment_final_kernel(const CombineParams p) {
+  lap::griddep_wait();  // launched with programmatic stream serialization (la_host::launch_pdl)
+  lap::griddep_launch_dependents();
   const int n = blockIdx.x / p.HV, hv = blockIdx.x - n * p.HV;
   const int slot = __ldg(p.seq_slot + n);
   if (slot < 0) return;
