@@ -103,8 +103,9 @@ la_status segment_device(la_host::DeviceState** ds) {
   });
 }
 
-la_status launched(const char* what) {
-  const cudaError_t ce = cudaGetLastError();
+// The status of a launch: the launch call's own result, else any earlier error it left pending.
+la_status launched(const char* what, cudaError_t launch_result = cudaSuccess) {
+  const cudaError_t ce = launch_result != cudaSuccess ? launch_result : cudaGetLastError();
   if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "%s launch failed: %s", what, cudaGetErrorString(ce));
   return LA_OK;
 }
@@ -200,8 +201,9 @@ la_status la_prefill_fwd_segmented(const void* q, const void* k, const void* v, 
   pp.S_last = pl.S_last;
   pp.nseg_max = nseg;
   pp.pool_size = la_host::effective_pool_size(h0, h_final, state_indices, pool_size, N);
-  (void)la_host::launch_pdl(las::la_segment_plan_kernel, 1, las::kPlanThreads, 0, s, pp);
-  if ((st = launched("segment plan")) != LA_OK) return st;
+  if ((st = launched("segment plan", la_host::launch_pdl(las::la_segment_plan_kernel, 1, las::kPlanThreads, 0, s,
+                                                         pp))) != LA_OK)
+    return st;
 
   // 2. local states of the segments that are not the last of their sequence
   las::StateParams sp;
@@ -214,8 +216,9 @@ la_status la_prefill_fwd_segmented(const void* q, const void* k, const void* v, 
   sp.G = HV / H;
   sp.num_units = nseg * HV;
   const int grid_a = sp.num_units < ds->sms ? sp.num_units : ds->sms;
-  (void)la_host::launch_pdl(las::la_segment_state_kernel, grid_a, las::kStThreads, state_smem_bytes(), s, tm_k, tm_v, sp);
-  if ((st = launched("segment state")) != LA_OK) return st;
+  if ((st = launched("segment state", la_host::launch_pdl(las::la_segment_state_kernel, grid_a, las::kStThreads,
+                                                          state_smem_bytes(), s, tm_k, tm_v, sp))) != LA_OK)
+    return st;
 
   // 3. initial state of every segment
   las::CombineParams cp;
@@ -228,8 +231,9 @@ la_status la_prefill_fwd_segmented(const void* q, const void* k, const void* v, 
   cp.states = states;
   cp.HV = HV;
   const dim3 grid_c(static_cast<unsigned>(N) * HV, las::kCombSplit);
-  (void)la_host::launch_pdl(las::la_segment_combine_kernel, grid_c, las::kCombThreads, 0, s, cp);
-  if ((st = launched("segment combine")) != LA_OK) return st;
+  if ((st = launched("segment combine",
+                     la_host::launch_pdl(las::la_segment_combine_kernel, grid_c, las::kCombThreads, 0, s, cp))) != LA_OK)
+    return st;
 
   // 4. the chunkwise prefill of every segment: a packed batch whose state pool is the
   //    workspace (segment g reads its initial state from slot g and leaves its final one there)
@@ -239,8 +243,9 @@ la_status la_prefill_fwd_segmented(const void* q, const void* k, const void* v, 
 
   // 5. final states
   if (h_final) {
-    (void)la_host::launch_pdl(las::la_segment_final_kernel, grid_c, las::kCombThreads, 0, s, cp);
-    if ((st = launched("segment final")) != LA_OK) return st;
+    if ((st = launched("segment final",
+                       la_host::launch_pdl(las::la_segment_final_kernel, grid_c, las::kCombThreads, 0, s, cp))) != LA_OK)
+      return st;
   }
   return LA_OK;
 }
