@@ -188,6 +188,27 @@ def test_cuda_graph_capture_and_replay_deterministic():
         assert torch.equal(hf[[5, 0, 3]].view(torch.int32), hf_ref[[5, 0, 3]].view(torch.int32))
 
 
+@pytest.mark.parametrize("cfg", [2, 4])
+def test_back_to_back_calls_bitwise(cfg):
+    # Calls on one stream overlap their launches (programmatic stream serialization): each waits
+    # for the previous kernel before touching memory, so back-to-back calls into separate output
+    # buffers must agree bit for bit (GVA: two units per CTA on part of the SMs).
+    p = W.config(cfg)
+    d = upload(p)
+    s = torch.cuda.Stream()
+    outs = []
+    with torch.cuda.stream(s):
+        for _ in range(4):
+            o = torch.empty_like(d["o"])
+            hf = torch.empty_like(d["h_final"])
+            run_gpu(p, {**d, "o": o, "h_final": hf}, stream=s.cuda_stream)
+            outs.append((o, hf))
+    torch.cuda.synchronize()
+    for o, hf in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0][0].view(torch.int16))
+        assert torch.equal(hf.view(torch.int32), outs[0][1].view(torch.int32))
+
+
 def test_two_streams_concurrent_equals_serial():
     pa = W.custom(seed=21, lengths=[300, 70, 1], H=2, HV=2)
     pb = W.custom(seed=22, B=2, T=200, H=1, HV=2)
