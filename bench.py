@@ -485,7 +485,8 @@ def run_sweep(args):
     def bf(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
 
-    extra = [W.custom(seed=3002, B=2, T=8192, H=64, HV=64, D=64, name="D=V=64 fixed MHA B=2 T=8192 H=HV=64, h0 + final state")]
+    extra = [W.custom(seed=3002, B=2, T=8192, H=64, HV=64, D=64, name="D=V=64 fixed MHA B=2 T=8192 H=HV=64, h0 + final state"),
+             short_d64_problem()]
     for i in (list(range(1, 6)) + extra if args.sweep_what in ("all", "prefill") else ()):
         p = W.config(i) if isinstance(i, int) else i
         q, k, v = bf(p.q_bits), bf(p.k_bits), bf(p.v_bits)
@@ -520,7 +521,7 @@ def run_sweep(args):
         ms = statistics.fmean(a.elapsed_time(b) for a, b in times)
         toks, nbytes, flops = workload_roofline(p)
         t_roof = max(nbytes / (hbm * 1e9), flops / (tflops * 1e12))
-        line = {"sweep": True, "workload": i if isinstance(i, int) else "d64", "name": p.name, "ms": round(ms, 5),
+        line = {"sweep": True, "workload": i if isinstance(i, int) else ("d64", "d64_short")[extra.index(i)], "name": p.name, "ms": round(ms, 5),
                 "tokens_per_s": round(toks / (ms / 1e3), 1), "tokens": toks, "alg_bytes": nbytes,
                 "alg_flops": flops, "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
                 "roofline_ms": round(t_roof * 1e3, 5), "frac": round(t_roof * 1e3 / ms, 4),
@@ -538,19 +539,36 @@ def run_sweep(args):
         run_backward_sweep(args, device, stream, flush, hbm, hbm_kind)
 
 
+def short_d64_problem():
+    """The short-continuation workload (128 requests of 8 tokens, H=HV=64, 256-slot pool, 16
+    padded) at D = V = 64."""
+    import numpy as np
+    import workloads as W
+    rng = np.random.default_rng(1105)
+    idx = rng.permutation(256)[:128].astype(np.int32)
+    idx[rng.choice(128, 16, replace=False)] = -1
+    return W.custom(seed=1105, lengths=[8] * 128, H=64, HV=64, D=64, pool=256, indices=idx, in_place=True,
+                    name="D=V=64 short packed N=128 T=8 H=HV=64, 256-slot pool, 16 padded")
+
+
 def run_decode_sweep(args, device, stream, flush, hbm, hbm_kind):
     """The speculative-decoding ops on the short-continuation workload (workloads.config(5):
-    128 requests of 8 draft tokens, H=HV=64, 256-slot pool, 16 padded): MTP decode, verify
-    with the KV-buffer copy, and commit of every accepted token.  Bytes: per live (request,
-    value head) the 64 KB state read (and written, decode and commit), the tokens' q, k
-    (once per q/k head), v and o, and the KV buffer written (verify) or read (commit)."""
+    128 requests of 8 draft tokens, H=HV=64, 256-slot pool, 16 padded), and on the same shape
+    at D = V = 64: MTP decode, verify with the KV-buffer copy, and commit of every accepted
+    token.  Bytes: per live (request, value head) the state (64 KB, or 16 KB at D = 64) read
+    (and written, decode and commit), the tokens' q, k (once per q/k head), v and o, and the
+    KV buffer written (verify) or read (commit)."""
+    for p in (__import__("workloads").config(5), short_d64_problem()):
+        decode_sweep_one(args, p, device, stream, flush, hbm, hbm_kind)
+
+
+def decode_sweep_one(args, p, device, stream, flush, hbm, hbm_kind):
     import numpy as np
     import torch
 
     import linear_attention_prefill_chunkwise_gb300 as lap
-    import workloads as W
 
-    p = W.config(5)
+    D, V = p.D, p.V
     Bq, Tq = p.N, 8
     live = int((p.state_indices >= 0).sum())
     toks = live * Tq
@@ -601,7 +619,7 @@ def run_decode_sweep(args, device, stream, flush, hbm, hbm_kind):
         torch.cuda.synchronize(device)
         ms = statistics.fmean(a.elapsed_time(b) for a, b in times)
         t_roof = nbytes / (hbm * 1e9)
-        line = {"sweep": True, "op": name, "workload": "B=128 requests x T=8 draft tokens, H=HV=64, "
+        line = {"sweep": True, "op": name, "workload": f"B=128 requests x T=8 draft tokens, H=HV=64, D=V={D}, "
                 "256-slot pool, 16 padded", "ms": round(ms, 5), "tokens_per_s": round(toks / (ms / 1e3), 1),
                 "alg_bytes": nbytes, "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
                 "roofline_ms": round(t_roof * 1e3, 5), "frac": round(t_roof * 1e3 / ms, 4), "bound": "hbm",

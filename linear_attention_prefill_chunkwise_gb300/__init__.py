@@ -314,7 +314,7 @@ def _decode_common(q, k, v, slopes, state, state_indices, T, dev_error, stream):
     tokens, H, D = q.shape
     _, HV, V = v.shape
     if k.shape != q.shape or v.shape[0] != tokens or tokens % T:
-        raise ValueError("q, k: [B*T, H, 128]; v: [B*T, HV, 128] with the same B*T")
+        raise ValueError("q, k: [B*T, H, D]; v: [B*T, HV, V] with the same B*T")
     B = tokens // T
     if tuple(state.shape[1:]) != (HV, V, D):
         raise ValueError("state must be [P, HV, V, D]")
@@ -334,7 +334,7 @@ def _raise(lib, st):
 
 def la_decode_mtp(q, k, v, slopes, scale, state, T, state_indices=None, o=None, dev_error=None, stream=None):
     """Multi-token decode: advance each request's pooled state over its T draft tokens (in
-    place) and return the outputs o (bf16 [B*T, HV, 128])."""
+    place) and return the outputs o (bf16 [B*T, HV, V]; D = V = 128 or 64)."""
     import torch
     lib, B, H, HV, pool, stream = _decode_common(q, k, v, slopes, state, state_indices, T, dev_error, stream)
     if o is None:
@@ -349,7 +349,7 @@ def la_decode_mtp(q, k, v, slopes, scale, state, T, state_indices=None, o=None, 
 def la_verify(q, k, v, slopes, scale, state, T, state_indices=None, o=None, kbuf=None, vbuf=None, dev_error=None,
               stream=None):
     """Parallel verify: the outputs of all T draft tokens from the pooled states, which are
-    left untouched; with kbuf/vbuf (bf16 [P, T, H, 128] / [P, T, HV, 128]) the draft k, v
+    left untouched; with kbuf/vbuf (bf16 [P, T, H, D] / [P, T, HV, V]) the draft k, v
     are copied to the request's slot for la_commit.  Returns o."""
     import torch
     lib, B, H, HV, pool, stream = _decode_common(q, k, v, slopes, state, state_indices, T, dev_error, stream)

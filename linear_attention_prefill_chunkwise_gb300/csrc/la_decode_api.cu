@@ -1,7 +1,7 @@
 // la_decode_api.cu -- host side of the C ABI declared in include/la_decode.h: argument
-// validation and one launch per call: the tokenwise kernel (lad::kSplit CTAs per (request,
-// value head)) for decode, commit and long verifies, the tensor-core closed-form kernel for
-// verifies of at most lav::kMaxTok tokens.  Nothing here allocates device memory, reads device
+// validation and one launch per call: the tokenwise kernel (D / 64 CTAs per (request, value
+// head)) for decode, commit and long verifies, the tensor-core closed-form kernel for verifies
+// of at most lav::kMaxTok tokens at D = 128.  Nothing here allocates device memory, reads device
 // memory or synchronises with the host.
 #include <cuda_runtime.h>
 
@@ -57,8 +57,8 @@ la_status encode_bf16_token_map(CUtensorMap* map, const void* base, int64_t rows
 
 // Shape checks shared by the three entry points.
 la_status check_shapes(int B, int T, int H, int HV, int D, int V, int pool_size, const int32_t* state_indices) {
-  if (D != lad::kDim || V != lad::kDim)
-    return fail(LA_ERR_UNSUPPORTED, "only D == V == 128 is implemented (got D=%d, V=%d)", D, V);
+  if (D != V || (D != 128 && D != 64))
+    return fail(LA_ERR_UNSUPPORTED, "only D == V == 128 or 64 is implemented (got D=%d, V=%d)", D, V);
   if (H <= 0 || HV <= 0) return fail(LA_ERR_INVALID_ARGUMENT, "H and HV must be positive (got %d, %d)", H, HV);
   if (HV % H != 0) return fail(LA_ERR_UNSUPPORTED, "HV (%d) must be a multiple of H (%d)", HV, H);
   if (B < 0) return fail(LA_ERR_INVALID_ARGUMENT, "B must be >= 0 (got %d)", B);
@@ -79,13 +79,14 @@ cudaError_t setup_kernels() {
 }
 
 template <int kMode>
-la_status launch(const lad::Params& p, void* stream) {
+la_status launch(const lad::Params& p, int D, void* stream) {
   la_host::DeviceState* ds = nullptr;
   la_status st = la_host::current_device(g_dev, &ds, setup_kernels);
   if (st != LA_OK) return st;
-  const int grid = lad::tokenwise_grid(p.B * p.HV * lad::kSplit, ds->sms);
-  cudaError_t ce = la_host::launch_pdl(lad::la_tokenwise_kernel<kMode>, grid, lad::kThreads,
-                                       lad::tokenwise_smem_bytes(), static_cast<cudaStream_t>(stream), p);
+  const int units = p.B * p.HV * (D == 128 ? lad::split_of<128>() : lad::split_of<64>());
+  cudaError_t ce = la_host::launch_pdl(D == 128 ? lad::la_tokenwise_kernel<kMode, 128> : lad::la_tokenwise_kernel<kMode, 64>,
+                                       lad::tokenwise_grid(units, ds->sms), lad::kThreads, lad::tokenwise_smem_bytes(),
+                                       static_cast<cudaStream_t>(stream), p);
   if (ce == cudaSuccess) ce = cudaGetLastError();
   if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(ce));
   return LA_OK;
@@ -155,7 +156,7 @@ la_status la_decode_mtp(const void* q, const void* k, const void* v, const float
   p.k = static_cast<const __nv_bfloat16*>(k);
   p.v = static_cast<const __nv_bfloat16*>(v);
   p.o = static_cast<__nv_bfloat16*>(o);
-  return launch<lad::kDecode>(p, stream);
+  return launch<lad::kDecode>(p, D, stream);
 }
 
 la_status la_verify(const void* q, const void* k, const void* v, const float* slopes, float scale,
@@ -189,9 +190,10 @@ la_status la_verify(const void* q, const void* k, const void* v, const float* sl
   p.o = static_cast<__nv_bfloat16*>(o);
   p.kbuf = static_cast<__nv_bfloat16*>(kbuf);
   p.vbuf = static_cast<__nv_bfloat16*>(vbuf);
-  if (T > lav::kMaxTok || static_cast<int64_t>(pool_size) * HV * 128 > INT32_MAX) return launch<lad::kVerify>(p, stream);
+  if (D != 128 || T > lav::kMaxTok || static_cast<int64_t>(pool_size) * HV * 128 > INT32_MAX)
+    return launch<lad::kVerify>(p, D, stream);
 
-  // the closed form on the tensor cores
+  // the closed form on the tensor cores (D = 128)
   la_host::DeviceState* ds = nullptr;
   st = la_host::current_device(g_dev, &ds, setup_kernels);
   if (st != LA_OK) return st;
@@ -252,7 +254,7 @@ la_status la_commit(float* state, const int32_t* state_indices, const void* kbuf
   p.kbuf = const_cast<__nv_bfloat16*>(static_cast<const __nv_bfloat16*>(kbuf));
   p.vbuf = const_cast<__nv_bfloat16*>(static_cast<const __nv_bfloat16*>(vbuf));
   p.accepted_len = accepted_len;
-  return launch<lad::kCommit>(p, stream);
+  return launch<lad::kCommit>(p, D, stream);
 }
 
 }  // extern "C"

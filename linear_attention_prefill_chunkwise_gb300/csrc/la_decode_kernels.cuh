@@ -7,12 +7,12 @@
 // (request, value head) unit costs one read of its 64 KB FP32 state, T token updates and,
 // for decode and commit, one write of the state: the work is bound by the state traffic.
 // Each row of the state evolves, and gives its output, independently of the others, so a
-// unit is split over kSplit parts of 64 state rows, each held in the registers of one 128-thread
-// CTA.  The CTAs are persistent (kCtasPerSm per SM) and walk their parts; while a CTA applies
-// the tokens of one part, a single bulk copy brings the next part's 32 KB state slice into
-// shared memory, so every state load but the first overlaps arithmetic.  Thread t owns state
-// rows v = 64 h + 4 (t / 8) .. +3 and, of each, the four 16-byte column chunks
-// k = 32 m + 4 (t % 8) .. +3 (m = 0..3), and for every token
+// unit is split over D / 64 parts of 64 state rows, each held in the registers of one
+// 128-thread CTA.  The CTAs are persistent (kCtasPerSm per SM) and walk their parts; while a CTA
+// applies the tokens of one part, a single bulk copy brings the next part's state slice (32 KB
+// at D = 128, 16 KB at D = 64) into shared memory, so every state load but the first overlaps
+// arithmetic.  Thread t owns state rows v = 64 h + 4 (t / 8) .. +3 and, of each, the D / 32
+// 16-byte column chunks k = 32 m + 4 (t % 8) .. +3 (m = 0 .. D / 32 - 1), and for every token
 //     S[v][k] = lambda S[v][k] + v_t[v] k_t[k]              (FP32, fused multiply-add)
 //     o_t[v]  = scale sum_k S[v][k] q_t[k]                    (the 8 lanes of a row group hold
 //                                                             partial sums of 4 rows; a reduce-
@@ -49,26 +49,29 @@ using lap::f2_mul;
 using lap::f2_pack;
 using lap::f2_unpack;
 
-constexpr int kDim = 128;   // D = V = 128
-constexpr int kSplit = 2;                 // CTAs per (request, value head)
-constexpr int kRows = kDim / kSplit;      // state rows per CTA
-constexpr int kThreads = kRows / 4 * 8;   // 4 rows x 16 columns per thread
+constexpr int kDim = 128;                 // largest D = V (the staging arrays' width)
+constexpr int kRows = 64;                 // state rows per CTA
+constexpr int kSplit = kDim / kRows;      // CTAs per (request, value head) at D = 128
+constexpr int kThreads = kRows / 4 * 8;   // 4 rows x D / 8 columns per thread
+// CTAs per (request, value head) for head dimension kD (D = V = 128 or 64)
+template <int kD>
+__host__ __device__ constexpr int split_of() { return kD / kRows; }
 
 enum Mode : int { kDecode = 0, kVerify = 1, kCommit = 2, kPrefill = 3 };
 
-struct Params {
-  const __nv_bfloat16* q;  // [B*T, H, 128]   (decode, verify)
-  const __nv_bfloat16* k;  // [B*T, H, 128]   (decode, verify)
-  const __nv_bfloat16* v;  // [B*T, HV, 128]  (decode, verify)
+struct Params {  // (D = V = 128 or 64)
+  const __nv_bfloat16* q;  // [B*T, H, D]   (decode, verify)
+  const __nv_bfloat16* k;  // [B*T, H, D]   (decode, verify)
+  const __nv_bfloat16* v;  // [B*T, HV, D]  (decode, verify)
   const float* slopes;     // [HV]
-  float* state;            // [P, HV, 128, 128]
+  float* state;            // [P, HV, D, D]
   const int32_t* state_indices;
-  __nv_bfloat16* o;        // [B*T, HV, 128]  (decode, verify)
-  __nv_bfloat16* kbuf;     // [P, T, H, 128]  (written by verify when given, read by commit)
-  __nv_bfloat16* vbuf;     // [P, T, HV, 128]
+  __nv_bfloat16* o;        // [B*T, HV, D]  (decode, verify)
+  __nv_bfloat16* kbuf;     // [P, T, H, D]  (written by verify when given, read by commit)
+  __nv_bfloat16* vbuf;     // [P, T, HV, D]
   const int32_t* accepted_len;  // [B] (commit)
-  const float* h0;              // [P, HV, 128, 128] or null (prefill: initial states)
-  float* h_final;               // [P, HV, 128, 128] or null (prefill: final states)
+  const float* h0;              // [P, HV, D, D] or null (prefill: initial states)
+  float* h_final;               // [P, HV, D, D] or null (prefill: final states)
   const int32_t* cu_seqlens;    // [B + 1] or null (prefill: packed sequence bounds)
   int* dev_error;
   float scale;
@@ -89,14 +92,13 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& x, float (&f)[8]) {
 
 // Persistent form: a CTA walks its units (unit u = blockIdx.x + j gridDim.x; unit = (request,
 // value head, part)) and, while it applies the tokens of one unit, a single bulk copy brings the
-// next unit's 32 KB state slice into shared memory, so the state load of every unit but the
-// first overlaps the arithmetic of the previous one.  Thread t of a CTA owns rows
-// vbase + 4 (t / 8) .. + 3 and, of each row, the four 16-byte chunks of columns
-// 32 m + 4 (t % 8) .. + 3 (m = 0..3): a warp then reads 128 contiguous bytes per row from the
+// next unit's state slice into shared memory, so the state load of every unit but the first
+// overlaps the arithmetic of the previous one.  Thread t of a CTA owns rows
+// vbase + 4 (t / 8) .. + 3 and, of each row, the D / 32 16-byte chunks of columns
+// 32 m + 4 (t % 8) .. + 3: a warp then reads 128 contiguous bytes per row from the
 // staged slice, the staged k and q, and writes 128 contiguous bytes per row of the state, all
 // without bank conflicts.
 constexpr int kTileTok = 8;  // tokens staged in shared memory per pass
-constexpr uint32_t kSliceBytes = kRows * kDim * 4;
 constexpr int kCtasPerSm = 4;
 
 struct __align__(128) TokSmem {
@@ -121,11 +123,11 @@ struct TokUnit {
   bool run, load, bad_index;
 };
 
-template <int kMode>
+template <int kMode, int kD>
 __device__ __forceinline__ TokUnit tok_unit(const Params& p, int u) {
   TokUnit w;
-  const int unit = u / kSplit;
-  w.part = u - unit * kSplit;
+  const int unit = u / split_of<kD>();
+  w.part = u - unit * split_of<kD>();
   w.b = unit / p.HV;
   w.hv = unit - w.b * p.HV;
   w.hq = w.hv / p.G;
@@ -156,13 +158,19 @@ __device__ __forceinline__ TokUnit tok_unit(const Params& p, int u) {
   return w;
 }
 
-template <int kMode>
+// kD = D = V: 128 (two CTAs of 64 state rows per unit, 16 columns of each row per thread) or 64
+// (one CTA per unit, 8 columns per thread); the staging arrays keep their 128-value width.
+template <int kMode, int kD = kDim>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm) la_tokenwise_kernel(const Params p) {
+  static_assert(kD == 128 || kD == 64, "head dimension");
+  constexpr int kM = kD / 32;             // 16-byte column chunks of a row per thread
+  constexpr int kChunks = kD / 8;         // 8-value chunks of a token row
+  constexpr uint32_t kSlice = kRows * kD * 4;
   extern __shared__ uint8_t tok_raw[];
   TokSmem& sm = *reinterpret_cast<TokSmem*>((reinterpret_cast<uintptr_t>(tok_raw) + 127) & ~uintptr_t(127));
   const int t = threadIdx.x;
   const int cg = t & 7, rg = t >> 3;  // chunks 32 m + 4 cg, rows vbase + 4 rg .. +3
-  const int units = p.B * p.HV * kSplit;
+  const int units = p.B * p.HV * split_of<kD>();
   const float* s_in = (kMode == kPrefill) ? p.h0 : p.state;
   float* s_out = (kMode == kPrefill) ? p.h_final : p.state;
   volatile int* abort = &sm.abort;
@@ -177,16 +185,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) la_tokenwise_kernel(cons
   __syncthreads();
 
   auto slice_of = [&](const TokUnit& w) {
-    return (static_cast<size_t>(w.slot) * p.HV + w.hv) * kDim * kDim + static_cast<size_t>(w.part) * kRows * kDim;
+    return (static_cast<size_t>(w.slot) * p.HV + w.hv) * kD * kD + static_cast<size_t>(w.part) * kRows * kD;
   };
   auto prefetch = [&](const TokUnit& w) {  // thread 0
-    lap::mbar_arrive_expect_tx(&sm.bar, kSliceBytes);
-    lap::bulk_copy_g2s(sm.pre, s_in + slice_of(w), kSliceBytes, &sm.bar);
+    lap::mbar_arrive_expect_tx(&sm.bar, kSlice);
+    lap::bulk_copy_g2s(sm.pre, s_in + slice_of(w), kSlice, &sm.bar);
   };
   // the first unit from u on (this CTA's stride) that runs; a bad state index is flagged
   auto seek = [&](int u, TokUnit& w) {
     for (; u < units; u += gridDim.x) {
-      w = tok_unit<kMode>(p, u);
+      w = tok_unit<kMode, kD>(p, u);
       if (w.bad_index && t == 0 && p.dev_error) atomicOr(p.dev_error, 2);  // LA_DEV_ERR_BAD_INDEX
       if (w.run) return u;
     }
@@ -209,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) la_tokenwise_kernel(cons
     const bool resc = slope * kTileTok <= 20.f;  // the rescaled update (lambda^-8 <= e^20)
 
     // ---- this unit's state slice: S[r][2 m + h] = the pair (e = 2 h, 2 h + 1) of chunk m of row r
-    uint64_t S[4][8];
+    uint64_t S[4][2 * kM];
     if (cur.load) {
       // a bounded wait, its outcome agreed by the whole CTA before anyone leaves the loop
       if (!__syncthreads_and(lap::mbar_wait(&sm.bar, phase, abort))) break;
@@ -218,8 +226,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) la_tokenwise_kernel(cons
 #pragma unroll
       for (int r = 0; r < 4; ++r)
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
-          const float4 x = *reinterpret_cast<const float4*>(&sm.pre[(4 * rg + r) * kDim + 32 * m + 4 * cg]);
+        for (int m = 0; m < kM; ++m) {
+          const float4 x = *reinterpret_cast<const float4*>(&sm.pre[(4 * rg + r) * kD + 32 * m + 4 * cg]);
           S[r][2 * m] = f2_pack(x.x, x.y);
           S[r][2 * m + 1] = f2_pack(x.z, x.w);
         }
@@ -227,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) la_tokenwise_kernel(cons
 #pragma unroll
       for (int r = 0; r < 4; ++r)
 #pragma unroll
-        for (int j = 0; j < 8; ++j) S[r][j] = f2_pack(0.f, 0.f);
+        for (int j = 0; j < 2 * kM; ++j) S[r][j] = f2_pack(0.f, 0.f);
     }
     __syncthreads();  // every thread holds its part of the slice: the buffer is free
     if (un < units && nxt.load) {
@@ -235,27 +243,27 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) la_tokenwise_kernel(cons
       pending = true;
     }
 
-    const size_t qk_tok = static_cast<size_t>(p.H) * kDim;
-    const size_t v_tok = static_cast<size_t>(p.HV) * kDim;
+    const size_t qk_tok = static_cast<size_t>(p.H) * kD;
+    const size_t v_tok = static_cast<size_t>(p.HV) * kD;
     for (int t0 = 0; t0 < cur.ntok; t0 += kTileTok) {
       const int nt = min(kTileTok, cur.ntok - t0);
       __syncthreads();  // the previous tile has been consumed
       // stage tokens t0 .. t0 + nt - 1: 16 bytes (8 values) per thread and array per step
-      for (int e = t; e < nt * (kDim / 8); e += kThreads) {
-        const int i = e >> 4, c = e & 15;            // token, 8-value chunk
+      for (int e = t; e < nt * kChunks; e += kThreads) {
+        const int i = e / kChunks, c = e % kChunks;  // token, 8-value chunk
         const bool vmine = c / (kRows / 8) == cur.part;  // values 8c .. 8c + 7 are rows of this CTA
         uint4 kx, vx = make_uint4(0u, 0u, 0u, 0u);
         if (kMode == kCommit) {
           const size_t brow = static_cast<size_t>(cur.slot) * p.T + t0 + i;
-          kx = __ldg(reinterpret_cast<const uint4*>(p.kbuf + (brow * p.H + cur.hq) * kDim) + c);
-          if (vmine) vx = __ldg(reinterpret_cast<const uint4*>(p.vbuf + (brow * p.HV + cur.hv) * kDim) + c);
+          kx = __ldg(reinterpret_cast<const uint4*>(p.kbuf + (brow * p.H + cur.hq) * kD) + c);
+          if (vmine) vx = __ldg(reinterpret_cast<const uint4*>(p.vbuf + (brow * p.HV + cur.hv) * kD) + c);
         } else {
           const size_t row = cur.row0 + t0 + i;
-          kx = __ldg(reinterpret_cast<const uint4*>(p.k + row * qk_tok + static_cast<size_t>(cur.hq) * kDim) + c);
+          kx = __ldg(reinterpret_cast<const uint4*>(p.k + row * qk_tok + static_cast<size_t>(cur.hq) * kD) + c);
           if (vmine)
-            vx = __ldg(reinterpret_cast<const uint4*>(p.v + row * v_tok + static_cast<size_t>(cur.hv) * kDim) + c);
+            vx = __ldg(reinterpret_cast<const uint4*>(p.v + row * v_tok + static_cast<size_t>(cur.hv) * kD) + c);
           const uint4 qx =
-              __ldg(reinterpret_cast<const uint4*>(p.q + row * qk_tok + static_cast<size_t>(cur.hq) * kDim) + c);
+              __ldg(reinterpret_cast<const uint4*>(p.q + row * qk_tok + static_cast<size_t>(cur.hq) * kD) + c);
           float f[8];
           bf16x8_to_f32(qx, f);
           reinterpret_cast<float4*>(&sm.qs[i][8 * c])[0] = make_float4(f[0], f[1], f[2], f[3]);
@@ -263,8 +271,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) la_tokenwise_kernel(cons
           if (kMode == kVerify && p.kbuf) {  // the KV buffer copy (k once per q/k head, by part 0)
             const size_t brow = static_cast<size_t>(cur.slot) * p.T + t0 + i;
             if (cur.hv % p.G == 0 && cur.part == 0)
-              reinterpret_cast<uint4*>(p.kbuf + (brow * p.H + cur.hq) * kDim)[c] = kx;
-            if (vmine) reinterpret_cast<uint4*>(p.vbuf + (brow * p.HV + cur.hv) * kDim)[c] = vx;
+              reinterpret_cast<uint4*>(p.kbuf + (brow * p.H + cur.hq) * kD)[c] = kx;
+            if (vmine) reinterpret_cast<uint4*>(p.vbuf + (brow * p.HV + cur.hv) * kD)[c] = vx;
           }
         }
         float f[8];
@@ -287,9 +295,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) la_tokenwise_kernel(cons
         const float4 vv = *reinterpret_cast<const float4*>(&sm.vs[i][4 * rg]);
         const float vf = sm.linv[i];
         const float vr[4] = {vv.x * vf, vv.y * vf, vv.z * vf, vv.w * vf};
-        uint64_t kk[8];
+        uint64_t kk[2 * kM];
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
+        for (int m = 0; m < kM; ++m) {
           const float4 x = *reinterpret_cast<const float4*>(&sm.ks[i][32 * m + 4 * cg]);
           kk[2 * m] = f2_pack(x.x, x.y);
           kk[2 * m + 1] = f2_pack(x.z, x.w);
@@ -299,19 +307,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) la_tokenwise_kernel(cons
 #pragma unroll
           for (int r = 0; r < 4; ++r)
 #pragma unroll
-            for (int j = 0; j < 8; ++j) S[r][j] = f2_mul(lam2, S[r][j]);
+            for (int j = 0; j < 2 * kM; ++j) S[r][j] = f2_mul(lam2, S[r][j]);
         }
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
           const uint64_t v2 = f2_pack(vr[r], vr[r]);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) S[r][j] = f2_fma(v2, kk[j], S[r][j]);
+          for (int j = 0; j < 2 * kM; ++j) S[r][j] = f2_fma(v2, kk[j], S[r][j]);
         }
         if (kMode != kCommit) {
-          // o_t[v] = scale S[v] . q_t over this thread's 16 columns, then across the 8 lanes of the row group
-          uint64_t qq[8];
+          // o_t[v] = scale S[v] . q_t over this thread's 4 kM columns, then across the 8 lanes of the row group
+          uint64_t qq[2 * kM];
 #pragma unroll
-          for (int m = 0; m < 4; ++m) {
+          for (int m = 0; m < kM; ++m) {
             const float4 x = *reinterpret_cast<const float4*>(&sm.qs[i][32 * m + 4 * cg]);
             qq[2 * m] = f2_pack(x.x, x.y);
             qq[2 * m + 1] = f2_pack(x.z, x.w);
@@ -321,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) la_tokenwise_kernel(cons
           for (int r = 0; r < 4; ++r) {
             uint64_t acc = f2_pack(0.f, 0.f);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) acc = f2_fma(S[r][j], qq[j], acc);
+            for (int j = 0; j < 2 * kM; ++j) acc = f2_fma(S[r][j], qq[j], acc);
             const float2 a2 = f2_unpack(acc);
             dot[r] = a2.x + a2.y;
           }
@@ -335,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) la_tokenwise_kernel(cons
           float kx = (b1 ? k1 : k0) + __shfl_xor_sync(0xffffffffu, b1 ? k0 : k1, 2);
           kx += __shfl_xor_sync(0xffffffffu, kx, 1);
           if (!(cg & 1))
-            p.o[(cur.row0 + t0 + i) * v_tok + static_cast<size_t>(cur.hv) * kDim + vbase + 4 * rg +
+            p.o[(cur.row0 + t0 + i) * v_tok + static_cast<size_t>(cur.hv) * kD + vbase + 4 * rg +
                 (2 * (cg >> 2) + ((cg >> 1) & 1))] = __float2bfloat16_rn(p.scale * sm.lpow[i] * kx);
         }
       }
@@ -345,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) la_tokenwise_kernel(cons
 #pragma unroll
         for (int r = 0; r < 4; ++r)
 #pragma unroll
-          for (int j = 0; j < 8; ++j) S[r][j] = f2_mul(ln2, S[r][j]);
+          for (int j = 0; j < 2 * kM; ++j) S[r][j] = f2_mul(ln2, S[r][j]);
       }
     }
 
@@ -354,9 +362,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) la_tokenwise_kernel(cons
 #pragma unroll
       for (int r = 0; r < 4; ++r)
 #pragma unroll
-        for (int m = 0; m < 4; ++m) {
+        for (int m = 0; m < kM; ++m) {
           const float2 a = f2_unpack(S[r][2 * m]), c = f2_unpack(S[r][2 * m + 1]);
-          *reinterpret_cast<float4*>(dst + (4 * rg + r) * kDim + 32 * m + 4 * cg) = make_float4(a.x, a.y, c.x, c.y);
+          *reinterpret_cast<float4*>(dst + (4 * rg + r) * kD + 32 * m + 4 * cg) = make_float4(a.x, a.y, c.x, c.y);
         }
     }
     u = un;

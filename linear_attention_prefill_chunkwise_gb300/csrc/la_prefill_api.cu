@@ -32,7 +32,7 @@ la_host::DeviceState g_dev[la_host::kMaxDevices];
 
 int smem_bytes() { return static_cast<int>(sizeof(lap::SharedStorage)) + 1024; }
 
-// Longest sequence the tokenwise kernel takes: up to two of its 16-token staging tiles.
+// Longest sequence the tokenwise kernel takes: up to four of its 8-token staging tiles.
 constexpr int kShortMax = 32;
 // Packed batches with at most this many tokens per sequence on average are split.
 constexpr int kSplitAvg = 64;
@@ -108,11 +108,10 @@ la_status la_prefill_fwd(const void* q, const void* k, const void* v, const floa
     if ((st = la_host::encode_bf16_out_map(&tm_o, o, tokens, HV, D)) != LA_OK) return st;
   }
 
-  // The tokenwise kernel holds a 128 x 128 state: with D = 64 every sequence takes the chunkwise one.
   const bool packed = cu_seqlens != nullptr;
-  const bool split = D == 128 && packed && tokens <= static_cast<int64_t>(kSplitAvg) * N;
-  const bool run_tokenwise = split || (D == 128 && !packed && T <= kShortMax);
-  const bool run_chunkwise = packed || T > kShortMax || D != 128;
+  const bool split = packed && tokens <= static_cast<int64_t>(kSplitAvg) * N;
+  const bool run_tokenwise = split || (!packed && T <= kShortMax);
+  const bool run_chunkwise = packed || T > kShortMax;
   const int pool = la_host::effective_pool_size(h0, h_final, state_indices, pool_size, N);
   if (run_tokenwise) {
     lad::Params tp{};
@@ -135,10 +134,12 @@ la_status la_prefill_fwd(const void* q, const void* k, const void* v, const floa
     tp.pool_size = pool;
     tp.num_tokens = static_cast<int>(tokens);
     tp.short_max = kShortMax;
-    if (units * lad::kSplit > INT32_MAX) return fail(LA_ERR_UNSUPPORTED, "N*HV too large (%lld)", (long long)units);
-    ce = la_host::launch_pdl(lad::la_tokenwise_kernel<lad::kPrefill>,
-                             lad::tokenwise_grid(static_cast<int>(units * lad::kSplit), ds.sms), lad::kThreads,
-                             lad::tokenwise_smem_bytes(), static_cast<cudaStream_t>(stream), tp);
+    const int64_t parts = units * (D == 128 ? lad::split_of<128>() : lad::split_of<64>());
+    if (parts > INT32_MAX) return fail(LA_ERR_UNSUPPORTED, "N*HV too large (%lld)", (long long)units);
+    ce = la_host::launch_pdl(
+        D == 128 ? lad::la_tokenwise_kernel<lad::kPrefill, 128> : lad::la_tokenwise_kernel<lad::kPrefill, 64>,
+        lad::tokenwise_grid(static_cast<int>(parts), ds.sms), lad::kThreads, lad::tokenwise_smem_bytes(),
+        static_cast<cudaStream_t>(stream), tp);
     if (ce == cudaSuccess) ce = cudaGetLastError();
     if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "tokenwise kernel launch failed: %s", cudaGetErrorString(ce));
   }

@@ -3,8 +3,9 @@
 The chunkwise kernel's D = 64 instance uses the D = 128 tile and tensor-memory layout with
 the second 64-wide box of every head row unused: Q, K and V load one box per row, the score
 and O_inter contractions run over K = 64, dS has N = 64, and the state is the top-left 64 x 64
-block of the 128 x 128 register and TMEM layout.  Sequences of every length take the chunkwise
-kernel (the tokenwise kernel holds a 128 x 128 state).  The oracle computes in FP64 at any D.
+block of the 128 x 128 register and TMEM layout.  Short sequences take the tokenwise kernel's
+D = 64 instance (one CTA per (sequence, value head), 8 columns of each state row per thread),
+as at D = 128.  The oracle computes in FP64 at any D.
 """
 import zlib
 
@@ -29,6 +30,11 @@ D64_CASES = {
     "lambda_zero": dict(lengths=[150, 20], H=1, HV=2, slopes=[100.0, 100.0]),
     "long_nine_chunks": dict(lengths=[64 * 9 + 17], H=1, HV=1),
     "short_sequences": dict(lengths=[5, 20, 3, 31, 1, 40], H=2, HV=2),
+    "short_fixed_T32_tokenwise": dict(B=3, T=32, H=2, HV=4),
+    "short_fixed_T1_tokenwise": dict(B=5, T=1, H=1, HV=1),
+    "short_pool_in_place_tokenwise": dict(lengths=[9, 32, 0, 17, 33, 2], H=1, HV=3, pool=9,
+                                          indices=[4, 0, 8, -1, 2, 6], in_place=True),
+    "short_no_h0_tokenwise": dict(B=2, T=24, H=1, HV=2, with_h0=False),
     "many_sequences": dict(lengths=[(37 * i) % 211 for i in range(300)], H=1, HV=2),
 }
 

@@ -24,16 +24,16 @@ from harness import check_output, check_state, to_torch_bf16
 pytestmark = pytest.mark.gpu
 
 
-def make_case(seed, B, T, H, HV, P, n_pad=0, scale=None, slopes=None):
+def make_case(seed, B, T, H, HV, P, n_pad=0, scale=None, slopes=None, D=W.D):
     rng = np.random.default_rng(seed)
-    q, k, v = W.make_qkv(rng, B * T, H, HV)
-    pool = W.make_states(rng, P, HV)
+    q, k, v = W.make_qkv(rng, B * T, H, HV, d=D, v_dim=D)
+    pool = W.make_states(rng, P, HV, d=D, v_dim=D)
     idx = rng.permutation(P)[:B].astype(np.int32)
     if n_pad:
         idx[rng.choice(B, n_pad, replace=False)] = -1
     sl = W.slopes_for(HV) if slopes is None else np.asarray(slopes, dtype=np.float32)
-    sc = 1.0 / math.sqrt(W.D) if scale is None else scale
-    return dict(q=q, k=k, v=v, pool=pool, idx=idx, slopes=sl, scale=sc, B=B, T=T, H=H, HV=HV, P=P)
+    sc = 1.0 / math.sqrt(D) if scale is None else scale
+    return dict(q=q, k=k, v=v, pool=pool, idx=idx, slopes=sl, scale=sc, B=B, T=T, H=H, HV=HV, P=P, D=D)
 
 
 def oracle_run(c, lengths=None):
@@ -75,6 +75,12 @@ CASES = {
                                 slopes=[0.0, 1e-4, 0.7, 5.0, 40.0, 200.0]),
     "T8_gva_pool": dict(seed=5007, B=40, T=8, H=4, HV=16, P=64, n_pad=5),
     "T2_single_request": dict(seed=5008, B=1, T=2, H=1, HV=1, P=1),
+    # D = V = 64: one CTA per (request, value head), and verify always tokenwise
+    "D64_T1": dict(seed=5101, B=5, T=1, H=4, HV=4, P=8, n_pad=1, D=64),
+    "D64_T5_gva_lambda_edges": dict(seed=5102, B=7, T=5, H=2, HV=6, P=11, n_pad=2,
+                                    slopes=[0.0, 1e-4, 0.7, 5.0, 40.0, 200.0], D=64),
+    "D64_T8_gva_pool": dict(seed=5103, B=40, T=8, H=4, HV=16, P=64, n_pad=5, D=64),
+    "D64_T17_tiles": dict(seed=5104, B=3, T=17, H=4, HV=4, P=4, D=64),
 }
 
 
@@ -83,7 +89,7 @@ def check_decode_mtp(c, name):
     import torch
     import linear_attention_prefill_chunkwise_gb300 as lap
     d = upload(c)
-    o = torch.full((c["B"] * c["T"], c["HV"], W.V), float("nan"), dtype=torch.bfloat16, device="cuda")
+    o = torch.full((c["B"] * c["T"], c["HV"], c["D"]), float("nan"), dtype=torch.bfloat16, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     lap.la_decode_mtp(d["q"], d["k"], d["v"], d["slopes"], c["scale"], d["pool"], c["T"], state_indices=d["idx"],
                       o=o, dev_error=err)
@@ -113,16 +119,17 @@ def check_verify_then_commit(c, name, seed):
     # decode on a copy of the pool: the reference for verify's outputs and a full commit's state
     dec_pool = d["pool"].clone()
     o_dec = lap.la_decode_mtp(d["q"], d["k"], d["v"], d["slopes"], c["scale"], dec_pool, T, state_indices=d["idx"])
-    kbuf = torch.zeros((P, T, H, W.D), dtype=torch.bfloat16, device="cuda")
-    vbuf = torch.zeros((P, T, HV, W.V), dtype=torch.bfloat16, device="cuda")
+    kbuf = torch.zeros((P, T, H, c["D"]), dtype=torch.bfloat16, device="cuda")
+    vbuf = torch.zeros((P, T, HV, c["D"]), dtype=torch.bfloat16, device="cuda")
     o = lap.la_verify(d["q"], d["k"], d["v"], d["slopes"], c["scale"], d["pool"], T, state_indices=d["idx"],
                       kbuf=kbuf, vbuf=vbuf)
     torch.cuda.synchronize()
     rows = live_rows(c)
     # verify: pool untouched, KV buffer = the draft k, v at the slot; the outputs match the oracle
-    # (below) and, where verify runs the same tokenwise recurrence as decode (T > 8), are bitwise
-    # decode's; for T <= 8 verify evaluates the closed form with the state as a TF32 operand
-    if T > VERIFY_TC_MAX_T:
+    # (below) and, where verify runs the same tokenwise recurrence as decode (T > 8, or D = 64),
+    # are bitwise decode's; for T <= 8 at D = 128 verify evaluates the closed form with the state
+    # as a TF32 operand
+    if T > VERIFY_TC_MAX_T or c["D"] != 128:
         assert torch.equal(o[rows], o_dec[rows])
     else:
         check_output(o.float().cpu().numpy()[rows], o_dec.float().cpu().numpy()[rows].astype(np.float64),
