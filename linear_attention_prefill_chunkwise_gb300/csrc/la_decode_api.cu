@@ -83,10 +83,14 @@ la_status launch(const lad::Params& p, int D, void* stream) {
   la_host::DeviceState* ds = nullptr;
   la_status st = la_host::current_device(g_dev, &ds, setup_kernels);
   if (st != LA_OK) return st;
-  const int units = p.B * p.HV * (D == 128 ? lad::split_of<128>() : lad::split_of<64>());
-  cudaError_t ce = la_host::launch_pdl(D == 128 ? lad::la_tokenwise_kernel<kMode, 128> : lad::la_tokenwise_kernel<kMode, 64>,
-                                       lad::tokenwise_grid(units, ds->sms), lad::kThreads, lad::tokenwise_smem_bytes(),
-                                       static_cast<cudaStream_t>(stream), p);
+  const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaError_t ce =
+      D == 128 ? la_host::launch_pdl(lad::la_tokenwise_kernel<kMode, 128>,
+                                     lad::tokenwise_grid<128>(p.B * p.HV * lad::split_of<128>(), ds->sms),
+                                     lad::kThreads, lad::tokenwise_smem_bytes<128>(), cs, p)
+               : la_host::launch_pdl(lad::la_tokenwise_kernel<kMode, 64>,
+                                     lad::tokenwise_grid<64>(p.B * p.HV * lad::split_of<64>(), ds->sms),
+                                     lad::kThreads, lad::tokenwise_smem_bytes<64>(), cs, p);
   if (ce == cudaSuccess) ce = cudaGetLastError();
   if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(ce));
   return LA_OK;

@@ -8,7 +8,7 @@
 // for decode and commit, one write of the state: the work is bound by the state traffic.
 // Each row of the state evolves, and gives its output, independently of the others, so a
 // unit is split over D / 64 parts of 64 state rows, each held in the registers of one
-// 128-thread CTA.  The CTAs are persistent (kCtasPerSm per SM) and walk their parts; while a CTA
+// 128-thread CTA.  The CTAs are persistent (ctas_per_sm per SM) and walk their parts; while a CTA
 // applies the tokens of one part, a single bulk copy brings the next part's state slice (32 KB
 // at D = 128, 16 KB at D = 64) into shared memory, so every state load but the first overlaps
 // arithmetic.  Thread t owns state rows v = 64 h + 4 (t / 8) .. +3 and, of each, the D / 32
@@ -99,12 +99,15 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& x, float (&f)[8]) {
 // staged slice, the staged k and q, and writes 128 contiguous bytes per row of the state, all
 // without bank conflicts.
 constexpr int kTileTok = 8;  // tokens staged in shared memory per pass
-constexpr int kCtasPerSm = 4;
+// Resident CTAs per SM: the D = 64 instance holds half the registers and shared memory.
+template <int kD>
+__host__ __device__ constexpr int ctas_per_sm() { return kD == 64 ? 6 : 4; }
 
+template <int kD>
 struct __align__(128) TokSmem {
-  float pre[kRows * kDim];       // the next unit's state slice (bulk copy)
-  float ks[kTileTok][kDim];      // staged k (commit: from the KV buffer)
-  float qs[kTileTok][kDim];      // staged q
+  float pre[kRows * kD];         // the next unit's state slice (bulk copy)
+  float ks[kTileTok][kD];        // staged k (commit: from the KV buffer)
+  float qs[kTileTok][kD];        // staged q
   float vs[kTileTok][kRows];     // staged v, this CTA's rows
   float linv[kTileTok];          // lambda^-(i+1) of the tile's token i (rescaled update)
   float lpow[kTileTok];          // lambda^(i+1)
@@ -112,9 +115,13 @@ struct __align__(128) TokSmem {
   int abort;
 };
 
-__host__ __device__ constexpr int tokenwise_smem_bytes() { return static_cast<int>(sizeof(TokSmem)) + 128; }
-// Persistent grid: every unit of work, or kCtasPerSm CTAs per SM when there are more units.
-inline int tokenwise_grid(int units, int sms) { return units < sms * kCtasPerSm ? units : sms * kCtasPerSm; }
+template <int kD>
+__host__ __device__ constexpr int tokenwise_smem_bytes() { return static_cast<int>(sizeof(TokSmem<kD>)) + 128; }
+// Persistent grid: every unit of work, or ctas_per_sm CTAs per SM when there are more units.
+template <int kD>
+inline int tokenwise_grid(int units, int sms) {
+  return units < sms * ctas_per_sm<kD>() ? units : sms * ctas_per_sm<kD>();
+}
 
 // One unit's decoded description, identical for every thread of the CTA.
 struct TokUnit {
@@ -159,15 +166,15 @@ __device__ __forceinline__ TokUnit tok_unit(const Params& p, int u) {
 }
 
 // kD = D = V: 128 (two CTAs of 64 state rows per unit, 16 columns of each row per thread) or 64
-// (one CTA per unit, 8 columns per thread); the staging arrays keep their 128-value width.
+// (one CTA per unit, 8 columns per thread, twice the CTAs per SM).
 template <int kMode, int kD = kDim>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm) la_tokenwise_kernel(const Params p) {
+__global__ void __launch_bounds__(kThreads, ctas_per_sm<kD>()) la_tokenwise_kernel(const Params p) {
   static_assert(kD == 128 || kD == 64, "head dimension");
   constexpr int kM = kD / 32;             // 16-byte column chunks of a row per thread
   constexpr int kChunks = kD / 8;         // 8-value chunks of a token row
   constexpr uint32_t kSlice = kRows * kD * 4;
   extern __shared__ uint8_t tok_raw[];
-  TokSmem& sm = *reinterpret_cast<TokSmem*>((reinterpret_cast<uintptr_t>(tok_raw) + 127) & ~uintptr_t(127));
+  TokSmem<kD>& sm = *reinterpret_cast<TokSmem<kD>*>((reinterpret_cast<uintptr_t>(tok_raw) + 127) & ~uintptr_t(127));
   const int t = threadIdx.x;
   const int cg = t & 7, rg = t >> 3;  // chunks 32 m + 4 cg, rows vbase + 4 rg .. +3
   const int units = p.B * p.HV * split_of<kD>();

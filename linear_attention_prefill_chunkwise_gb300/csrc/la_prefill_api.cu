@@ -136,10 +136,13 @@ la_status la_prefill_fwd(const void* q, const void* k, const void* v, const floa
     tp.short_max = kShortMax;
     const int64_t parts = units * (D == 128 ? lad::split_of<128>() : lad::split_of<64>());
     if (parts > INT32_MAX) return fail(LA_ERR_UNSUPPORTED, "N*HV too large (%lld)", (long long)units);
-    ce = la_host::launch_pdl(
-        D == 128 ? lad::la_tokenwise_kernel<lad::kPrefill, 128> : lad::la_tokenwise_kernel<lad::kPrefill, 64>,
-        lad::tokenwise_grid(static_cast<int>(parts), ds.sms), lad::kThreads, lad::tokenwise_smem_bytes(),
-        static_cast<cudaStream_t>(stream), tp);
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    ce = D == 128 ? la_host::launch_pdl(lad::la_tokenwise_kernel<lad::kPrefill, 128>,
+                                        lad::tokenwise_grid<128>(static_cast<int>(parts), ds.sms), lad::kThreads,
+                                        lad::tokenwise_smem_bytes<128>(), cs, tp)
+                  : la_host::launch_pdl(lad::la_tokenwise_kernel<lad::kPrefill, 64>,
+                                        lad::tokenwise_grid<64>(static_cast<int>(parts), ds.sms), lad::kThreads,
+                                        lad::tokenwise_smem_bytes<64>(), cs, tp);
     if (ce == cudaSuccess) ce = cudaGetLastError();
     if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "tokenwise kernel launch failed: %s", cudaGetErrorString(ce));
   }
