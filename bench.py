@@ -639,6 +639,7 @@ SEGMENT_WORKLOADS = (
     (2002, 1, 32768, 16, 16, "B=1 T=32768 H=HV=16 (a 4-way head shard)"),
     (2003, 1, 65536, 8, 8, "B=1 T=65536 H=HV=8 (an 8-way head shard)"),
     (2004, 2, 8192, 64, 64, "fixed MHA B=2 T=8192 H=64"),
+    (2005, 1, 32768, 16, 16, "D=V=64: B=1 T=32768 H=HV=16"),
 )
 
 
@@ -672,11 +673,11 @@ def run_segment_sweep(args, device, stream, flush, hbm, hbm_kind, tflops, tf_kin
         return statistics.fmean(a.elapsed_time(b) for a, b in times)
 
     for seed, B, T, H, HV, name in SEGMENT_WORKLOADS:
-        p = W.custom(seed=seed, B=B, T=T, H=H, HV=HV, name=name)
+        p = W.custom(seed=seed, B=B, T=T, H=H, HV=HV, name=name, D=64 if name.startswith("D=V=64") else 128)
         q, k, v = bf(p.q_bits), bf(p.k_bits), bf(p.v_bits)
         sl = torch.from_numpy(p.slopes).to(device)
         h0 = torch.from_numpy(p.h0).to(device)
-        o = torch.empty((p.tokens, HV, V), dtype=torch.bfloat16, device=device)
+        o = torch.empty((p.tokens, HV, p.V), dtype=torch.bfloat16, device=device)
         hf = torch.empty_like(h0)
         nbytes_ws, seg = lap.la_prefill_segmented_workspace(B, T, B, HV, False, 0)
         ws = torch.empty(max(nbytes_ws, 1), dtype=torch.uint8, device=device)

@@ -54,7 +54,8 @@ extern "C" {
  *
  * The workspace holds one FP32 [128 x 128] state per (segment, value head) -- 64 KiB each --
  * plus five int32 tables; the segment count is at most N + floor(B*T / S) (packed) or
- * B * ceil(T / S) (fixed length).
+ * B * ceil(T / S) (fixed length).  The size does not depend on D: a D = V = 64 call keeps its
+ * [64 x 64] states in the first quarter of the same state region.
  */
 la_status la_prefill_segmented_workspace(int B, int T, int N, int HV, int packed, int segment_len, size_t* bytes,
                                          int* resolved_segment_len);
@@ -62,7 +63,7 @@ la_status la_prefill_segmented_workspace(int B, int T, int N, int HV, int packed
 /*
  * la_prefill_fwd_segmented -- la_prefill_fwd over segments of segment_len tokens.
  *
- * Arguments as la_prefill_fwd (no schedule), plus:
+ * Arguments as la_prefill_fwd (no schedule; D == V == 128 or 64), plus:
  *   segment_len      0 = automatic, else a positive multiple of 64 (the same value given to
  *                    la_prefill_segmented_workspace)
  *   workspace        device buffer of at least the queried size, 256-byte aligned; may be

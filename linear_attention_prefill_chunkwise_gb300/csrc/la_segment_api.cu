@@ -21,6 +21,10 @@ la_host::DeviceState g_dev[la_host::kMaxDevices];
 
 int state_smem_bytes() { return static_cast<int>(sizeof(las::StateSmem)) + 1024; }
 
+// The workspace is sized for D = V = 128 states whatever D is (the size query takes no D); a
+// D = 64 call keeps its [nseg, HV, 64, 64] states in the first quarter of that region.
+constexpr int kWsDim = 128;
+
 constexpr size_t kWsAlign = 256;
 size_t align_up(size_t x) { return (x + kWsAlign - 1) & ~(kWsAlign - 1); }
 
@@ -80,7 +84,7 @@ la_status make_plan(int B, int T, int N, int HV, bool packed, int segment_len, i
   p.nseg_max = nseg;
   size_t off = 0;
   p.off_states = off;
-  off = align_up(off + static_cast<size_t>(nseg) * HV * las::kDim * las::kDim * sizeof(float));
+  off = align_up(off + static_cast<size_t>(nseg) * HV * kWsDim * kWsDim * sizeof(float));
   p.off_seg_cu = off;
   off = align_up(off + static_cast<size_t>(nseg + 1) * sizeof(int32_t));
   p.off_seg_slot = off;
@@ -98,8 +102,12 @@ la_status make_plan(int B, int T, int N, int HV, bool packed, int segment_len, i
 
 la_status segment_device(la_host::DeviceState** ds) {
   return la_host::current_device(g_dev, ds, [] {
-    return cudaFuncSetAttribute(las::la_segment_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                state_smem_bytes());
+    cudaError_t e = cudaFuncSetAttribute(las::la_segment_state_kernel<128>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, state_smem_bytes());
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(las::la_segment_state_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               state_smem_bytes());
+    return e;
   });
 }
 
@@ -143,7 +151,6 @@ la_status la_prefill_fwd_segmented(const void* q, const void* k, const void* v, 
   la_status st = la_host::check_prefill_args(q, k, v, slopes, h0, state_indices, cu_seqlens, o, h_final, B, T, N, H,
                                              HV, D, V, pool_size, dev_error, &nothing);
   if (st != LA_OK || nothing) return st;
-  if (D != 128) return fail(LA_ERR_UNSUPPORTED, "the segmented prefill is implemented for D == V == 128 only (got %d)", D);
   // An explicit segment length fixes the plan without the device: the workspace is checked
   // before any device state is touched.
   la_host::DeviceState* ds = nullptr;
@@ -181,8 +188,8 @@ la_status la_prefill_fwd_segmented(const void* q, const void* k, const void* v, 
   CUtensorMap tm_k, tm_v;
   memset(&tm_k, 0, sizeof(tm_k));
   memset(&tm_v, 0, sizeof(tm_v));
-  if ((st = la_host::encode_bf16_rows_map(&tm_k, k, tokens, H, "k")) != LA_OK) return st;
-  if ((st = la_host::encode_bf16_rows_map(&tm_v, v, tokens, HV, "v")) != LA_OK) return st;
+  if ((st = la_host::encode_bf16_rows_map(&tm_k, k, tokens, H, "k", D)) != LA_OK) return st;
+  if ((st = la_host::encode_bf16_rows_map(&tm_v, v, tokens, HV, "v", D)) != LA_OK) return st;
 
   // 1. segment table
   las::PlanParams pp;
@@ -216,8 +223,9 @@ la_status la_prefill_fwd_segmented(const void* q, const void* k, const void* v, 
   sp.G = HV / H;
   sp.num_units = nseg * HV;
   const int grid_a = sp.num_units < ds->sms ? sp.num_units : ds->sms;
-  if ((st = launched("segment state", la_host::launch_pdl(las::la_segment_state_kernel, grid_a, las::kStThreads,
-                                                          state_smem_bytes(), s, tm_k, tm_v, sp))) != LA_OK)
+  if ((st = launched("segment state",
+                     la_host::launch_pdl(D == 128 ? las::la_segment_state_kernel<128> : las::la_segment_state_kernel<64>,
+                                         grid_a, las::kStThreads, state_smem_bytes(), s, tm_k, tm_v, sp))) != LA_OK)
     return st;
 
   // 3. initial state of every segment
@@ -230,9 +238,10 @@ la_status la_prefill_fwd_segmented(const void* q, const void* k, const void* v, 
   cp.seq_slot = seq_slot;
   cp.states = states;
   cp.HV = HV;
-  const dim3 grid_c(static_cast<unsigned>(N) * HV, las::kCombSplit);
+  const dim3 grid_c(static_cast<unsigned>(N) * HV, D == 128 ? las::comb_split<128>() : las::comb_split<64>());
   if ((st = launched("segment combine",
-                     la_host::launch_pdl(las::la_segment_combine_kernel, grid_c, las::kCombThreads, 0, s, cp))) != LA_OK)
+                     la_host::launch_pdl(D == 128 ? las::la_segment_combine_kernel<128> : las::la_segment_combine_kernel<64>,
+                                         grid_c, las::kCombThreads, 0, s, cp))) != LA_OK)
     return st;
 
   // 4. the chunkwise prefill of every segment: a packed batch whose state pool is the
@@ -244,7 +253,8 @@ la_status la_prefill_fwd_segmented(const void* q, const void* k, const void* v, 
   // 5. final states
   if (h_final) {
     if ((st = launched("segment final",
-                       la_host::launch_pdl(las::la_segment_final_kernel, grid_c, las::kCombThreads, 0, s, cp))) != LA_OK)
+                       la_host::launch_pdl(D == 128 ? las::la_segment_final_kernel<128> : las::la_segment_final_kernel<64>,
+                                           grid_c, las::kCombThreads, 0, s, cp))) != LA_OK)
       return st;
   }
   return LA_OK;

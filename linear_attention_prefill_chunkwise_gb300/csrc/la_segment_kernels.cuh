@@ -21,6 +21,8 @@
 //   final     la_segment_final_kernel: the last segment's final state -> h_final
 // Every segment's output is then the unsegmented output: the same chunkwise arithmetic, from
 // the exact initial state up to FP32 rounding.
+// The kernels are templated on the head dimension kD = D = V (128 or 64); the states in the
+// workspace are [kD v][kD k].
 #pragma once
 
 #include <cuda.h>
@@ -37,7 +39,6 @@ using lap::f2_pack;
 using lap::split_bf16x2;
 
 constexpr int kChunk = 64;
-constexpr int kDim = 128;
 constexpr uint32_t kTileBytes = 8192;  // one 64 x 64 BF16 box, 128-byte swizzled rows
 
 // ---------------------------------------------------------------------------- plan
@@ -173,7 +174,7 @@ struct StateParams {
   const float* slopes;
   const int32_t* seg_cu;
   const int32_t* seg_flags;
-  float* states;  // [nseg_max, HV, 128 v, 128 k]
+  float* states;  // [nseg_max, HV, D v, D k]
   int* dev_error;
   int HV, G, num_units;  // num_units = nseg_max * HV, unit u = g * HV + hv
 };
@@ -185,8 +186,8 @@ constexpr int kStEpiThreads = 128;    // warps 12..15: accumulator -> global
 constexpr uint32_t kStTmemCols = 256; // two 128-column accumulators
 
 struct __align__(1024) StateSmem {
-  uint8_t k[kStStages][2][kTileBytes];  // K [64 tokens][64 dims] x 2 halves of D
-  uint8_t v[kStStages][2][kTileBytes];  // V [64 tokens][64 dims] x 2 halves of V
+  uint8_t k[kStStages][2][kTileBytes];  // K [64 tokens][64 dims] x 2 halves of D (D = 64: the first)
+  uint8_t v[kStStages][2][kTileBytes];  // V [64 tokens][64 dims] x 2 halves of V (D = 64: the second zero)
   uint8_t kt_hi[2][2][kTileBytes];      // Kt hi/lo, 2 buffers, same layout as K (MN-major B operand)
   uint8_t kt_lo[2][2][kTileBytes];
   uint64_t full[kStStages];
@@ -226,9 +227,11 @@ __device__ __forceinline__ bool st_warp_wait(uint64_t* bar, uint32_t parity, vol
   return __all_sync(0xffffffffu, ok);
 }
 
-// Warp 0: TMA producer of the K and V chunk tiles.
+// Warp 0: TMA producer of the K and V chunk tiles (kD / 64 boxes of each).
+template <int kD>
 __device__ __forceinline__ void st_producer(StateSmem& sm, const StateParams& p, const CUtensorMap* tm_k,
                                             const CUtensorMap* tm_v, volatile int* abort) {
+  constexpr int kBoxes = kD / 64;
   uint32_t it = 0;
   SegUnit w;
   for (int u = blockIdx.x; next_seg_unit(p, u, w); u += gridDim.x) {
@@ -236,11 +239,11 @@ __device__ __forceinline__ void st_producer(StateSmem& sm, const StateParams& p,
     for (int c = 0; c < w.nchunks; ++c, ++it) {
       const uint32_t s = it % kStStages;
       if (!lap::mbar_wait(&sm.empty[s], ((it / kStStages) & 1u) ^ 1u, abort)) goto drain;
-      lap::mbar_arrive_expect_tx(&sm.full[s], 4 * kTileBytes);
+      lap::mbar_arrive_expect_tx(&sm.full[s], 2 * kBoxes * kTileBytes);
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        lap::tma_load_2d(sm.k[s][h], tm_k, &sm.full[s], hq * kDim + 64 * h, w.bos + c * kChunk);
-        lap::tma_load_2d(sm.v[s][h], tm_v, &sm.full[s], w.hv * kDim + 64 * h, w.bos + c * kChunk);
+      for (int h = 0; h < kBoxes; ++h) {
+        lap::tma_load_2d(sm.k[s][h], tm_k, &sm.full[s], hq * kD + 64 * h, w.bos + c * kChunk);
+        lap::tma_load_2d(sm.v[s][h], tm_v, &sm.full[s], w.hv * kD + 64 * h, w.bos + c * kChunk);
       }
     }
   }
@@ -252,10 +255,12 @@ drain:
   }
 }
 
-// Warp 1, one thread: Sloc[acc] (+)= V^T Kt_hi + V^T Kt_lo, 8 MMAs (M = 128 v, N = 128 k,
-// K = 16 tokens each) per chunk.
+// Warp 1, one thread: Sloc[acc] (+)= V^T Kt_hi + V^T Kt_lo, 8 MMAs (M = 128 v, N = kD k,
+// K = 16 tokens each) per chunk.  With kD = 64, rows v >= 64 of the accumulator come from V's
+// zeroed second box and are not read.
+template <int kD>
 __device__ __forceinline__ void st_mma(StateSmem& sm, const StateParams& p, uint32_t tmem, volatile int* abort) {
-  constexpr uint32_t idesc = lap::idesc_bf16_f32(128, 128, true, true);
+  constexpr uint32_t idesc = lap::idesc_bf16_f32(128, kD, true, true);
   const uint64_t dv0 = lap::sdesc_sw128(lap::smem_u32(sm.v[0]), kTileBytes, 1024);
   const uint64_t v_step = (2 * kTileBytes) >> 4;
   const uint64_t dhi0 = lap::sdesc_sw128(lap::smem_u32(sm.kt_hi[0]), kTileBytes, 1024);
@@ -297,9 +302,12 @@ __device__ __forceinline__ void st_mma(StateSmem& sm, const StateParams& p, uint
 
 // Warps 4..11: Kt_j = lambda^(L-1-j) k_j as a BF16 hi/lo pair, in the K tile's own swizzled
 // layout (an elementwise map, so each 16-byte chunk keeps its position).  Thread bt owns
-// token row bt % 64 of box (bt / 64) % 2 and its 16-byte chunks 4 (bt / 128) .. + 3.
+// token row bt % 64 of box (bt / 64) % 2 and its 16-byte chunks 4 (bt / 128) .. + 3; with
+// kD = 64 the threads of box 1 have nothing to build but still take part in every phase.
+template <int kD>
 __device__ __forceinline__ void st_builder(StateSmem& sm, const StateParams& p, int bt, volatile int* abort) {
   const int row = bt & 63, box = (bt >> 6) & 1, c0 = 4 * (bt >> 7);
+  const bool active = box < kD / 64;
   uint32_t it = 0;
   SegUnit w;
   for (int u = blockIdx.x; next_seg_unit(p, u, w); u += gridDim.x) {
@@ -313,7 +321,8 @@ __device__ __forceinline__ void st_builder(StateSmem& sm, const StateParams& p, 
       const uint8_t* src = sm.k[s][box];
       uint8_t* dhi = sm.kt_hi[b][box];
       uint8_t* dlo = sm.kt_lo[b][box];
-      if (j < w.len) {
+      if (!active) {
+      } else if (j < w.len) {
         const float wj = expf(-slope * static_cast<float>(w.len - 1 - j));
         const uint64_t w2 = f2_pack(wj, wj);
 #pragma unroll
@@ -346,11 +355,14 @@ __device__ __forceinline__ void st_builder(StateSmem& sm, const StateParams& p, 
   }
 }
 
-// Warps 12..15: accumulator rows (lane v) -> states[g][hv][v][:], 512 contiguous bytes per thread.
+// Warps 12..15: accumulator rows (lane v) -> states[g][hv][v][:], 4 kD contiguous bytes per
+// thread (with kD = 64 the warps of rows v >= 64 only take part in the barriers).
+template <int kD>
 __device__ __forceinline__ void st_epilogue(StateSmem& sm, const StateParams& p, uint32_t tmem, int et,
                                             volatile int* abort) {
   const int qd = et >> 5, lane = et & 31;
   const int vrow = 32 * qd + lane;
+  const bool active = 32 * qd < kD;  // warp-uniform
   const uint32_t lane_base = static_cast<uint32_t>(32 * qd) << 16;
   uint32_t ui = 0;
   SegUnit w;
@@ -358,22 +370,26 @@ __device__ __forceinline__ void st_epilogue(StateSmem& sm, const StateParams& p,
     const uint32_t a = ui & 1u;
     if (!st_warp_wait(&sm.acc_full[a], (ui >> 1) & 1u, abort)) return;
     lap::tc_fence_after();
-    float4* dst = reinterpret_cast<float4*>(p.states + ((static_cast<size_t>(w.g) * p.HV + w.hv) * kDim + vrow) * kDim);
+    if (active) {
+      float4* dst = reinterpret_cast<float4*>(p.states + ((static_cast<size_t>(w.g) * p.HV + w.hv) * kD + vrow) * kD);
 #pragma unroll 1
-    for (int q = 0; q < 8; ++q) {
-      float r[16];
-      lap::tmem_ld16(tmem + lane_base + a * 128 + 16 * q, r);
+      for (int q = 0; q < kD / 16; ++q) {
+        float r[16];
+        lap::tmem_ld16(tmem + lane_base + a * 128 + 16 * q, r);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) dst[4 * q + i] = make_float4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+        for (int i = 0; i < 4; ++i) dst[4 * q + i] = make_float4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+      }
     }
     lap::tc_fence_before();
     lap::mbar_arrive(&sm.acc_free[a]);
   }
 }
 
+template <int kD>
 __global__ void __launch_bounds__(kStThreads, 1)
 la_segment_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                         const StateParams p) {
+  static_assert(kD == 128 || kD == 64, "head dimension");
   lap::griddep_wait();  // launched with programmatic stream serialization (la_host::launch_pdl)
   lap::griddep_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
@@ -401,19 +417,28 @@ la_segment_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_c
     lap::tma_prefetch_desc(&tm_k);
     lap::tma_prefetch_desc(&tm_v);
   }
+  if constexpr (kD == 64) {
+    // The MMAs read V as an M = 128 operand; with D = 64 its second box is never loaded and
+    // must hold zeros for the whole kernel.
+    for (int i = tid; i < kStStages * static_cast<int>(kTileBytes / 16); i += kStThreads) {
+      const int st = i / static_cast<int>(kTileBytes / 16), e = i % static_cast<int>(kTileBytes / 16);
+      reinterpret_cast<uint4*>(sm.v[st][1])[e] = make_uint4(0, 0, 0, 0);
+    }
+    lap::fence_proxy_async_smem();
+  }
   lap::tc_fence_before();
   __syncthreads();
   lap::tc_fence_after();
   const uint32_t tmem = sm.tmem_base;
 
   if (warp == 0) {
-    if (lane == 0) st_producer(sm, p, &tm_k, &tm_v, abort);
+    if (lane == 0) st_producer<kD>(sm, p, &tm_k, &tm_v, abort);
   } else if (warp == 1) {
-    if (lane == 0) st_mma(sm, p, tmem, abort);
+    if (lane == 0) st_mma<kD>(sm, p, tmem, abort);
   } else if (warp >= 4 && warp < 12) {
-    st_builder(sm, p, tid - 128, abort);
+    st_builder<kD>(sm, p, tid - 128, abort);
   } else if (warp >= 12) {
-    st_epilogue(sm, p, tmem, tid - 384, abort);
+    st_epilogue<kD>(sm, p, tmem, tid - 384, abort);
   }
 
   lap::tc_fence_before();
@@ -430,22 +455,25 @@ la_segment_state_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_c
 
 struct CombineParams {
   const float* slopes;
-  const float* h0;  // [P, HV, 128, 128] or null
-  float* h_final;   // [P, HV, 128, 128] or null (final kernel)
+  const float* h0;  // [P, HV, D, D] or null
+  float* h_final;   // [P, HV, D, D] or null (final kernel)
   const int32_t* seg_cu;
   const int32_t* seq_seg0;
   const int32_t* seq_slot;
-  float* states;  // [nseg_max, HV, 128, 128]
+  float* states;  // [nseg_max, HV, D, D]
   int HV;
 };
 
 constexpr int kCombThreads = 256;
-constexpr int kCombSplit = 16;  // CTAs per (sequence, head): 16 x 256 threads = the 4096 float4 of a state
+// CTAs per (sequence, head): comb_split x 256 threads = the float4 of a state (16 at D = 128)
+template <int kD>
+__host__ __device__ constexpr int comb_split() { return kD * kD / 4 / kCombThreads; }
 constexpr int kCombBatch = 8;   // segments whose local states are loaded before they are chained
 
-// grid (N * HV, kCombSplit): thread owns one float4 of the [128 x 128] state.
+// grid (N * HV, comb_split): thread owns one float4 of the [kD x kD] state.
 // H <- h0 (or 0); for each segment i of the sequence: states[i] <- H, then
 // H <- lambda^{L_i} H + Sloc_i (Sloc_i read from states[i] before it is overwritten).
+template <int kD>
 __global__ void __launch_bounds__(kCombThreads) la_segment_combine_kernel(const CombineParams p) {
   lap::griddep_wait();  // launched with programmatic stream serialization (la_host::launch_pdl)
   lap::griddep_launch_dependents();
@@ -454,7 +482,7 @@ __global__ void __launch_bounds__(kCombThreads) la_segment_combine_kernel(const 
   if (slot < 0) return;
   const int g0 = __ldg(p.seq_seg0 + n), g1 = __ldg(p.seq_seg0 + n + 1);
   const size_t e = static_cast<size_t>(blockIdx.y) * kCombThreads + threadIdx.x;  // float4 index
-  constexpr size_t kState4 = kDim * kDim / 4;
+  constexpr size_t kState4 = kD * kD / 4;
   float4 H = make_float4(0.f, 0.f, 0.f, 0.f);
   if (p.h0) H = __ldg(reinterpret_cast<const float4*>(p.h0) + (static_cast<size_t>(slot) * p.HV + hv) * kState4 + e);
   const float slope = __ldg(p.slopes + hv);
@@ -480,8 +508,9 @@ __global__ void __launch_bounds__(kCombThreads) la_segment_combine_kernel(const 
   }
 }
 
-// grid (N * HV, kCombSplit): the final state of each running sequence's last segment,
+// grid (N * HV, comb_split): the final state of each running sequence's last segment,
 // left in the workspace by the prefill, copied to h_final[slot].
+template <int kD>
 __global__ void __launch_bounds__(kCombThreads) la_segment_final_kernel(const CombineParams p) {
   lap::griddep_wait();  // launched with programmatic stream serialization (la_host::launch_pdl)
   lap::griddep_launch_dependents();
@@ -490,7 +519,7 @@ __global__ void __launch_bounds__(kCombThreads) la_segment_final_kernel(const Co
   if (slot < 0) return;
   const int glast = __ldg(p.seq_seg0 + n + 1) - 1;
   const size_t e = static_cast<size_t>(blockIdx.y) * kCombThreads + threadIdx.x;
-  constexpr size_t kState4 = kDim * kDim / 4;
+  constexpr size_t kState4 = kD * kD / 4;
   const float4 x = reinterpret_cast<const float4*>(p.states)[(static_cast<size_t>(glast) * p.HV + hv) * kState4 + e];
   reinterpret_cast<float4*>(p.h_final)[(static_cast<size_t>(slot) * p.HV + hv) * kState4 + e] = x;
 }

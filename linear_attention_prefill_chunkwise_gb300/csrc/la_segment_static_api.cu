@@ -64,7 +64,6 @@ la_status la_prefill_fwd_segmented_static(const void* q, const void* k, const vo
   la_status st = la_host::check_prefill_args(q, k, v, slopes, h0, state_indices, cu_seqlens, o, h_final, B, T, N, H,
                                              HV, D, V, pool_size, dev_error, &nothing);
   if (st != LA_OK || nothing) return st;
-  if (D != 128) return fail(LA_ERR_UNSUPPORTED, "the segmented prefill is implemented for D == V == 128 only (got %d)", D);
   size_t need = 0;
   st = la_prefill_segmented_workspace(B, T, N, HV, cu_seqlens != nullptr, segment_len, &need, nullptr);
   if (st != LA_OK) return st;

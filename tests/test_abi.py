@@ -248,7 +248,8 @@ def call_segmented(**over):
 
 @pytest.mark.parametrize("over,status", [
     (dict(D=64), LA_UNSUPPORTED),
-    (dict(D=64, V=64), LA_UNSUPPORTED),  # the segmented path is D = V = 128 only
+    (dict(D=32, V=32), LA_UNSUPPORTED),
+    (dict(D=64, V=64, wsb=1024), LA_INVALID),  # D = V = 64 passes the shape check
     (dict(H=3, HV=4), LA_UNSUPPORTED),
     (dict(N=3), LA_INVALID),
     (dict(seg=100), LA_INVALID),        # not a multiple of 64

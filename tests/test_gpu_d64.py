@@ -5,7 +5,8 @@ the second 64-wide box of every head row unused: Q, K and V load one box per row
 and O_inter contractions run over K = 64, dS has N = 64, and the state is the top-left 64 x 64
 block of the 128 x 128 register and TMEM layout.  Short sequences take the tokenwise kernel's
 D = 64 instance (one CTA per (sequence, value head), 8 columns of each state row per thread),
-as at D = 128.  The oracle computes in FP64 at any D.
+as at D = 128.  The segmented path at D = 64 is tested with the D = 128 cases in
+test_gpu_segment.py.  The oracle computes in FP64 at any D.
 """
 import zlib
 
@@ -77,15 +78,25 @@ def test_d64_persistent_equals_non_persistent_bitwise():
     assert np.array_equal(outs[0][1], outs[1][1])
 
 
-def test_d64_nonfinite_sequence_does_not_reach_its_neighbours():
+def _run_path(path, p, d):
+    import linear_attention_prefill_chunkwise_gb300 as lap
+    if path == "prefill":
+        run_gpu(p, d)
+    else:
+        lap.la_prefill_fwd_segmented(d["q"], d["k"], d["v"], d["slopes"], p.scale, h0=d["h0"], cu_seqlens=d["cu"],
+                                     o=d["o"], h_final=d["h_final"], segment_len=64)
+    torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("path", ["prefill", "segmented"])
+def test_d64_nonfinite_sequence_does_not_reach_its_neighbours(path):
     lengths = [100, 77, 150, 64, 40]
     p = W.custom(seed=3005, lengths=lengths, H=2, HV=2, D=64)
     a, b = int(p.cu_seqlens[2]), int(p.cu_seqlens[3])
     p.k_bits[a:b] = 0x7F80
     p.v_bits[a:b] = 0x7FC0
     d = upload(p)
-    run_gpu(p, d)
-    torch.cuda.synchronize()
+    _run_path(path, p, d)
     o_all = d["o"].view(torch.int16).cpu().numpy()
     for n in (0, 1, 3, 4):
         s, e = int(p.cu_seqlens[n]), int(p.cu_seqlens[n + 1])
@@ -93,18 +104,7 @@ def test_d64_nonfinite_sequence_does_not_reach_its_neighbours():
                        p.scale, p.H, p.HV, 1, e - s, np.array([0, e - s], dtype=np.int32), None,
                        p.h0[n:n + 1].copy(), D=64, V=64)
         da = upload(pa)
-        run_gpu(pa, da)
-        torch.cuda.synchronize()
-        assert np.array_equal(o_all[s:e], da["o"].view(torch.int16).cpu().numpy()), f"sequence {n}"
+        _run_path(path, pa, da)
+        assert np.array_equal(o_all[s:e], da["o"].view(torch.int16).cpu().numpy()), f"{path}: sequence {n}"
         assert np.array_equal(d["h_final"][n].view(torch.int32).cpu().numpy(),
-                              da["h_final"][0].view(torch.int32).cpu().numpy()), f"sequence {n} state"
-
-
-def test_d64_segmented_path_is_refused():
-    import linear_attention_prefill_chunkwise_gb300 as lap
-    p = W.custom(seed=3006, B=1, T=256, H=1, HV=1, D=64)
-    d = upload(p)
-    with pytest.raises(lap.LaError) as e:
-        lap.la_prefill_fwd_segmented(d["q"], d["k"], d["v"], d["slopes"], p.scale, h0=d["h0"], o=d["o"],
-                                     h_final=d["h_final"], seq_len=p.T, segment_len=64)
-    assert e.value.name == "LA_ERR_UNSUPPORTED"
+                              da["h_final"][0].view(torch.int32).cpu().numpy()), f"{path}: sequence {n} state"

@@ -77,8 +77,6 @@ def test_random_prefill(seed):
 def test_random_segmented(seed):
     import linear_attention_prefill_chunkwise_gb300 as lap
     kw, seg = _draw(seed)
-    if kw["D"] != 128:
-        kw["D"] = 128  # the segmented entry point takes D = 128 only
     p = W.custom(seed=seed, name=f"random segmented {seed}", **kw)
     d = upload(p)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")

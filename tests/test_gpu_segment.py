@@ -3,9 +3,9 @@
 The segmented path computes the same outputs and final states as the plain prefill, so
 it is held to the same oracle and the same bounds: small problems in full (segments
 ending inside a chunk, sequences shorter than one segment, empty and padded sequences,
-GVA, in-place pools, no h0 / no final state, lambda = 1 and lambda = 0), a long
-few-head batch with the automatic segment length on sampled units, the device error
-word, and two calls sharing one workspace.
+GVA, in-place pools, no h0 / no final state, lambda = 1 and lambda = 0) at D = V = 128 and
+64, a long few-head batch with the automatic segment length on sampled units, the device
+error word, and two calls sharing one workspace.
 """
 import zlib
 
@@ -42,38 +42,41 @@ CASES = {
 }
 
 
+@pytest.mark.parametrize("D", [128, 64])
 @pytest.mark.parametrize("name", sorted(CASES))
-def test_segmented_full(name):
+def test_segmented_full(name, D):
     kw, seg = CASES[name]
-    p = W.custom(seed=zlib.crc32(name.encode()) % 10000, name=name, **kw)
+    p = W.custom(seed=zlib.crc32(name.encode()) % 10000 + (D != 128), name=name, D=D, **kw)
     d = upload(p)
     run_seg(p, d, seg)
-    compare_full(p, d, f"segmented {name} S={seg}")
+    compare_full(p, d, f"segmented {name} S={seg} D={D}")
 
 
-def test_segmented_auto_length_full():
+@pytest.mark.parametrize("D", [128, 64])
+def test_segmented_auto_length_full(D):
     """B=1, T=16384, H=HV=4: 4 chains, far fewer than SMs, so the automatic length segments."""
     import linear_attention_prefill_chunkwise_gb300 as lap
-    p = W.custom(seed=77, B=1, T=16384, H=4, HV=4)
+    p = W.custom(seed=77, B=1, T=16384, H=4, HV=4, D=D)
     nbytes, seg = lap.la_prefill_segmented_workspace(1, 16384, 1, 4, False, 0)
     assert seg > 0 and seg % 64 == 0 and seg < 16384 and nbytes > 0
     d = upload(p)
     run_seg(p, d, 0)
-    compare_full(p, d, f"segmented auto S={seg}")
+    compare_full(p, d, f"segmented auto S={seg} D={D}")
 
 
-def test_segmented_auto_short_first_segments_full():
+@pytest.mark.parametrize("D", [128, 64])
+def test_segmented_auto_short_first_segments_full(D):
     """B=1, T=4096, H=HV=64: two segments per chain would leave the local-state pass on 64
     SMs, so the automatic plan cuts the first half of each chain in two and keeps a long last
     segment; every unit against the oracle."""
     import linear_attention_prefill_chunkwise_gb300 as lap
-    p = W.custom(seed=81, B=1, T=4096, H=64, HV=64)
+    p = W.custom(seed=81, B=1, T=4096, H=64, HV=64, D=D)
     nbytes, seg = lap.la_prefill_segmented_workspace(1, 4096, 1, 64, False, 0)
     if seg == 0:
         pytest.skip("this device has too few SMs for 64 chains to be segmented")
     d = upload(p)
     run_seg(p, d, 0)
-    compare_full(p, d, f"segmented auto short first segments S={seg}")
+    compare_full(p, d, f"segmented auto short first segments S={seg} D={D}")
 
 
 def test_segmented_long_few_heads_sampled():
