@@ -485,10 +485,15 @@ def run_sweep(args):
     def bf(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
 
-    extra = [W.custom(seed=3002, B=2, T=8192, H=64, HV=64, D=64, name="D=V=64 fixed MHA B=2 T=8192 H=HV=64, h0 + final state"),
-             short_d64_problem()]
-    for i in (list(range(1, 6)) + extra if args.sweep_what in ("all", "prefill") else ()):
-        p = W.config(i) if isinstance(i, int) else i
+    # (label, problem): the five workloads, then the other head dimensions
+    work = [(i, None) for i in range(1, 6)] + [
+        ("d64", W.custom(seed=3002, B=2, T=8192, H=64, HV=64, D=64,
+                         name="D=V=64 fixed MHA B=2 T=8192 H=HV=64, h0 + final state")),
+        ("d64_short", short_d64_problem()),
+        ("d256", W.custom(seed=3010, B=2, T=8192, H=16, HV=16, D=256,
+                          name="D=V=256 fixed B=2 T=8192 H=HV=16, h0 + final state"))]
+    for label, extra_p in (work if args.sweep_what in ("all", "prefill") else ()):
+        p = W.config(label) if extra_p is None else extra_p
         q, k, v = bf(p.q_bits), bf(p.k_bits), bf(p.v_bits)
         sl = torch.from_numpy(p.slopes).to(device)
         h0 = None if p.h0 is None else torch.from_numpy(p.h0).to(device)
@@ -502,9 +507,18 @@ def run_sweep(args):
         else:
             hf = None
 
-        def call():
-            lap.la_prefill_fwd(q, k, v, sl, p.scale, h0=h0, state_indices=idx, cu_seqlens=cu, o=o, h_final=hf,
-                               seq_len=None if cu is not None else p.T, stream=stream)
+        if p.D == 256:
+            ws = torch.empty(lap.la_prefill_d256_workspace(p.B, p.T, p.N, p.HV, h0 is not None or hf is not None),
+                             dtype=torch.uint8, device=device)
+
+            def call():
+                lap.la_prefill_fwd_d256(q, k, v, sl, p.scale, h0=h0, state_indices=idx, cu_seqlens=cu, o=o,
+                                        h_final=hf, seq_len=None if cu is not None else p.T, workspace=ws,
+                                        stream=stream)
+        else:
+            def call():
+                lap.la_prefill_fwd(q, k, v, sl, p.scale, h0=h0, state_indices=idx, cu_seqlens=cu, o=o, h_final=hf,
+                                   seq_len=None if cu is not None else p.T, stream=stream)
 
         with torch.cuda.stream(stream):
             for _ in range(3):
@@ -521,7 +535,7 @@ def run_sweep(args):
         ms = statistics.fmean(a.elapsed_time(b) for a, b in times)
         toks, nbytes, flops = workload_roofline(p)
         t_roof = max(nbytes / (hbm * 1e9), flops / (tflops * 1e12))
-        line = {"sweep": True, "workload": i if isinstance(i, int) else ("d64", "d64_short")[extra.index(i)], "name": p.name, "ms": round(ms, 5),
+        line = {"sweep": True, "workload": label, "name": p.name, "ms": round(ms, 5),
                 "tokens_per_s": round(toks / (ms / 1e3), 1), "tokens": toks, "alg_bytes": nbytes,
                 "alg_flops": flops, "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
                 "roofline_ms": round(t_roof * 1e3, 5), "frac": round(t_roof * 1e3 / ms, 4),

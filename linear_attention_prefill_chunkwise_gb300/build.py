@@ -1,7 +1,7 @@
 """Compile the sm_103a C-ABI library ``libla_prefill.so`` in-tree.
 
-Five translation units (prefill; speculative-decoding ops; segmented prefill; its variant
-with a built-in scratch buffer; backward pass), one ``-gencode`` (sm_103a),
+Six translation units (prefill; speculative-decoding ops; segmented prefill; its variant
+with a built-in scratch buffer; backward pass; D = 256 prefill), one ``-gencode`` (sm_103a),
 static CUDA runtime, no
 link-time dependency on the driver library (the tensor-map encoder is fetched
 through the runtime's driver entry-point query), so the library loads on a
@@ -21,11 +21,11 @@ LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 INCLUDE_DIR = os.path.join(os.path.dirname(HERE), "include")
 
 SOURCES = ["la_prefill_api.cu", "la_decode_api.cu", "la_segment_api.cu", "la_segment_static_api.cu",
-           "la_backward_api.cu"]
+           "la_backward_api.cu", "la_d256_api.cu"]
 DEPENDS = ["la_prefill_api.cu", "la_prefill_kernel.cuh", "sm103_ptx.cuh", "la_decode_api.cu", "la_decode_kernels.cuh",
            "la_segment_api.cu", "la_segment_kernels.cuh", "la_segment_static_api.cu", "la_host_common.h",
-           "la_backward_api.cu", "la_verify_kernel.cuh", "la_prefill_internal.h"]
-HEADERS = ["la_prefill.h", "la_decode.h", "la_segment.h", "la_backward.h"]
+           "la_backward_api.cu", "la_verify_kernel.cuh", "la_prefill_internal.h", "la_d256_api.cu"]
+HEADERS = ["la_prefill.h", "la_decode.h", "la_segment.h", "la_backward.h", "la_d256.h"]
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

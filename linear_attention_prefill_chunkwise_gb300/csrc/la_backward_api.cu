@@ -158,39 +158,6 @@ __global__ void __launch_bounds__(128) la_bwd_big_slope_kernel(const BigSlopePar
     p.dk[qk_row + i] = __float2bfloat16_rn(p.scale * dv_dot * sq[i] + gtv);
 }
 
-// The sequence of token row r (fixed length T, or the packed bounds cu_seqlens), or -1 when the
-// row belongs to no sequence that the chunkwise runs computed (bad bounds, a padded or invalid
-// state index).
-__device__ __forceinline__ int row_sequence(const int32_t* cu, const int32_t* state_indices, int N, int T, int tokens,
-                                            int pool, int r) {
-  int n;
-  if (!cu) {
-    n = r / T;
-  } else {
-    int lo = 0, hi = N - 1;  // the last n with cu[n] <= r
-    if (N <= 0 || __ldg(cu) > r) return -1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (__ldg(cu + mid) <= r) lo = mid;
-      else hi = mid - 1;
-    }
-    n = lo;
-    const int b = __ldg(cu + n), e = __ldg(cu + n + 1);
-    if (b < 0 || e < b || e > tokens || r >= e) return -1;
-  }
-  if (state_indices) {
-    const int slot = __ldg(state_indices + n);
-    if (slot < 0 || slot >= pool) return -1;
-  }
-  return n;
-}
-
-// Two FP32 values rounded to BF16 (nearest even), the first in the low half.
-__device__ __forceinline__ uint32_t la_bf16x2(float lo, float hi) {
-  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&v);
-}
-
 struct ReduceParams {
   const float* part;    // [tokens, HV, D] FP32: each value head's part
   __nv_bfloat16* dst;   // [tokens, H, D]: the sum over each q/k head's group of HV / H value heads
@@ -204,7 +171,7 @@ struct ReduceParams {
 __global__ void __launch_bounds__(kCopyThreads) la_group_sum_kernel(const ReduceParams p) {
   const int G = p.HV / p.H, per_row = p.H * p.D / 8;
   for (int r = blockIdx.x; r < p.tokens; r += gridDim.x) {
-    if (row_sequence(p.cu_seqlens, p.state_indices, p.N, p.T, p.tokens, p.pool, r) < 0) continue;
+    if (la_internal::row_sequence(p.cu_seqlens, p.state_indices, p.N, p.T, p.tokens, p.pool, r) < 0) continue;
     for (int i = threadIdx.x; i < per_row; i += kCopyThreads) {
       const int h = i / (p.D / 8), d = 8 * (i - h * (p.D / 8));
       float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -216,10 +183,10 @@ __global__ void __launch_bounds__(kCopyThreads) la_group_sum_kernel(const Reduce
         acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
       }
       uint4 out;
-      out.x = la_bf16x2(acc[0], acc[1]);
-      out.y = la_bf16x2(acc[2], acc[3]);
-      out.z = la_bf16x2(acc[4], acc[5]);
-      out.w = la_bf16x2(acc[6], acc[7]);
+      out.x = la_internal::bf16x2(acc[0], acc[1]);
+      out.y = la_internal::bf16x2(acc[2], acc[3]);
+      out.z = la_internal::bf16x2(acc[4], acc[5]);
+      out.w = la_internal::bf16x2(acc[6], acc[7]);
       *reinterpret_cast<uint4*>(p.dst + (static_cast<size_t>(r) * p.H + h) * p.D + d) = out;
     }
   }

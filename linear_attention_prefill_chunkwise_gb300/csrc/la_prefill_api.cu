@@ -165,6 +165,7 @@ la_status la_prefill_fwd(const void* q, const void* k, const void* v, const floa
   p.HV = HV;
   p.G = HV / H;
   p.vdiv = 1;
+  p.vfold = 0;
   p.pool_size = pool;
   p.num_units = static_cast<int>(units);
   p.short_max = split ? kShortMax : -1;
@@ -191,9 +192,11 @@ namespace la_internal {
 la_status chunkwise(const void* q, const void* k, const void* v, const float* slopes, float scale, const float* h0,
                     const int32_t* state_indices, const int32_t* cu_seqlens, void* o, float* o_f32, float* h_final,
                     int B, int T, int N, int H, int HV, int v_heads, int D, int pool_size, bool reverse,
-                    int* dev_error, void* stream) {
+                    int* dev_error, void* stream, int v_fold) {
   if (v_heads <= 0 || HV % v_heads != 0)
     return fail(LA_ERR_UNSUPPORTED, "HV (%d) must be a multiple of v's heads (%d)", HV, v_heads);
+  if (v_fold < 0 || (v_fold > 0 && (!o_f32 || v_heads * 2 != HV || HV % (2 * v_fold) != 0)))
+    return fail(LA_ERR_UNSUPPORTED, "bad value-head fold %d (HV %d, v heads %d)", v_fold, HV, v_heads);
   // the checks of la_prefill_fwd; o (or o_f32) has the layout of the output, h_final of the states
   bool nothing = false;
   la_status st = la_host::check_prefill_args(q, k, v, slopes, h0, state_indices, cu_seqlens,
@@ -232,6 +235,7 @@ la_status chunkwise(const void* q, const void* k, const void* v, const float* sl
   p.HV = HV;
   p.G = HV / H;
   p.vdiv = HV / v_heads;
+  p.vfold = v_fold;
   p.pool_size = la_host::effective_pool_size(h0, h_final, state_indices, pool_size, N);
   p.num_units = static_cast<int>(units);
   p.short_max = -1;  // every sequence, however short, runs here

@@ -151,9 +151,12 @@ struct KernelParams {
   int num_units;  // N * HV
   int short_max;  // sequences of at most this many tokens belong to the tokenwise kernel (-1: none)
   // kF32Out instance only: the FP32 output ([tokens, HV, D], the layout of o), and v's head of
-  // value head hv, hv / vdiv (v then has HV / vdiv heads)
+  // value head hv: hv / vdiv (v then has HV / vdiv heads), or with vfold > 0 the index hv
+  // with the digit of weight vfold dropped, (hv / (2 vfold)) vfold + hv % vfold (v then has
+  // HV / 2 heads; the D = 256 decomposition, where that digit is the half of the key dimension)
   float* o_f32;
   int vdiv;
+  int vfold;
 };
 
 // One unit's sequence bounds, state slot and chunk count, decoded identically by every role.
@@ -445,8 +448,8 @@ __device__ __forceinline__ void tma_mma_loop(SharedStorage& sm, const KernelPara
         } else {
           mbar_arrive_expect_tx(bar, kHalves * kTileBytes);
         }
-        // (the kF32Out instance may share a V head among vdiv value heads)
-        const int vh = kF32Out ? cv.hv / p.vdiv : cv.hv;
+        // (the kF32Out instance may share a V head among vdiv value heads, or fold two onto one)
+        const int vh = !kF32Out ? cv.hv : p.vfold ? (cv.hv / (2 * p.vfold)) * p.vfold + cv.hv % p.vfold : cv.hv / p.vdiv;
 #pragma unroll
         for (int h = 0; h < kHalves; ++h) tma_load_2d(sm.v[sv][h], tm_v, bar, vh * kD + 64 * h, cv.row);
         ++nv;

@@ -347,3 +347,51 @@ def test_backward_without_states_needs_no_workspace():
         pytest.skip("a GPU is present")
     # past every host check (no workspace needed without h0 and dh_final): the device query fails
     assert call_backward(ws=None, wsb=0) == LA_CUDA
+
+
+# ---- D = 256 prefill (include/la_d256.h)
+
+def call_d256(**over):
+    a = dict(q=Q, k=K, v=VV, slopes=SL, scale=1.0, h0=None, idx=None, cu=None, o=O, hf=None,
+             B=2, T=128, N=2, H=2, HV=2, D=256, V=256, P=0, ws=WS, wsb=1 << 30, err=None, stream=None)
+    a.update(over)
+    lib = lap.load_library()
+    return lib.la_prefill_fwd_d256(a["q"], a["k"], a["v"], a["slopes"], ctypes.c_float(a["scale"]), a["h0"], a["idx"],
+                                   a["cu"], a["o"], a["hf"], a["B"], a["T"], a["N"], a["H"], a["HV"], a["D"],
+                                   a["V"], a["P"], a["ws"], a["wsb"], a["err"], a["stream"])
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(D=128, V=128), LA_UNSUPPORTED),    # the D = 128 entry point is la_prefill_fwd
+    (dict(V=128), LA_UNSUPPORTED),
+    (dict(D=64, V=64), LA_UNSUPPORTED),
+    (dict(H=3, HV=4), LA_UNSUPPORTED),
+    (dict(N=3), LA_INVALID),                 # fixed length needs N == B
+    (dict(ws=None), LA_INVALID),
+    (dict(wsb=1024), LA_INVALID),            # workspace too small
+    (dict(ws=WS + 16), LA_INVALID),          # not 256-byte aligned
+    (dict(q=Q + 2), LA_INVALID),             # misaligned
+    (dict(h0=H0, P=1), LA_INVALID),          # pool smaller than N without indices
+    (dict(o=Q), LA_INVALID),                 # the output overlaps an input
+    (dict(ws=Q), LA_INVALID),                # the workspace overlaps an input
+])
+def test_d256_host_validation(over, status):
+    assert call_d256(**over) == status
+    assert lap.load_library().la_last_error() != b""
+
+
+def test_d256_nothing_to_do():
+    assert call_d256(N=0, B=0) == LA_OK
+
+
+def test_d256_workspace_size():
+    # FP32 parts: tokens x 4 HV x 128 floats; blocks: N x 4 HV x 128 x 128 floats (with a state)
+    parts = 2 * 8192 * 4 * 16 * 128 * 4
+    blocks = 2 * 4 * 16 * 128 * 128 * 4
+    n0 = lap.la_prefill_d256_workspace(2, 8192, 2, 16, False)
+    n1 = lap.la_prefill_d256_workspace(2, 8192, 2, 16, True)
+    assert parts <= n0 < parts + 4096
+    assert n1 - n0 >= blocks and n1 - n0 < blocks + 4096
+    with pytest.raises(lap.LaError) as e:
+        lap.la_prefill_d256_workspace(-1, 8, 1, 1, False)
+    assert e.value.status == LA_INVALID

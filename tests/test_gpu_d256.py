@@ -1,0 +1,119 @@
+"""Head dimension D = V = 256 (include/la_d256.h) against the FP64 oracle.
+
+la_prefill_fwd_d256 evaluates the 256 x 256 state as four independent 128 x 128 blocks with the
+D = 128 chunkwise kernel and adds the two key halves of every output in FP32 before one rounding.
+The oracle runs the D = 256 recurrence itself, so these cases check the decomposition as well as
+the kernels: ragged and packed batches, a pool in place with padding, GVA, no h0, no final state,
+lambda = 1 and lambda -> 0, a bad state index, isolation from a non-finite neighbour, and two
+calls bitwise equal.
+"""
+import zlib
+
+import numpy as np
+import pytest
+
+import workloads as W
+from harness import compare_full, upload
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+def run_d256(p, d, dev_error=None, workspace=None):
+    import linear_attention_prefill_chunkwise_gb300 as lap
+    return lap.la_prefill_fwd_d256(d["q"], d["k"], d["v"], d["slopes"], p.scale, h0=d["h0"], state_indices=d["idx"],
+                                   cu_seqlens=d["cu"], o=d["o"], h_final=d["h_final"],
+                                   seq_len=None if p.cu_seqlens is not None else p.T, dev_error=dev_error,
+                                   workspace=workspace)
+
+
+D256_CASES = {
+    "fixed_T300": dict(B=2, T=300, H=2, HV=2),
+    "fixed_T64": dict(B=3, T=64, H=1, HV=2),
+    "ragged_pool_in_place_gva": dict(lengths=[1, 63, 64, 65, 130, 0, 200, 31], H=2, HV=4, pool=11,
+                                     indices=[3, 10, -1, 0, 7, 5, 1, 9], in_place=True),
+    "gva_three_heads_per_group": dict(lengths=[150, 77], H=1, HV=3),
+    "pool_out_of_place": dict(lengths=[333, 0, 777], H=1, HV=2, pool=5, indices=[4, 0, -1]),
+    "no_h0": dict(lengths=[70, 3, 129], H=2, HV=2, with_h0=False),
+    "no_final": dict(lengths=[70, 3], H=2, HV=2, want_final=False),
+    "lambda_one": dict(lengths=[150, 20], H=1, HV=2, slopes=[0.0, 0.0]),
+    "lambda_zero": dict(lengths=[150, 20], H=1, HV=2, slopes=[100.0, 100.0]),
+    "long_nine_chunks": dict(lengths=[64 * 9 + 17], H=1, HV=1),
+    "short_sequences": dict(lengths=[5, 20, 3, 31, 1, 40], H=2, HV=2),
+    "empty_sequences_with_final": dict(lengths=[0, 0, 5], H=1, HV=2),
+}
+
+
+@pytest.mark.parametrize("name", sorted(D256_CASES))
+def test_d256_cases_full(name):
+    p = W.custom(seed=zlib.crc32(("d256" + name).encode()) % 10000, name=name, D=256, **D256_CASES[name])
+    d = upload(p)
+    run_d256(p, d)
+    compare_full(p, d, f"D=256 {name}")
+
+
+def test_d256_fixed_b2_t2048_h4_full():
+    p = W.custom(seed=4002, B=2, T=2048, H=4, HV=4, D=256, name="D=256 B=2 T=2048 H=4")
+    d = upload(p)
+    run_d256(p, d)
+    compare_full(p, d, p.name)
+
+
+def test_d256_bad_index_flagged_others_intact():
+    import linear_attention_prefill_chunkwise_gb300 as lap
+    p = W.custom(seed=4003, lengths=[100, 65, 30], H=1, HV=2, D=256, pool=4, indices=[2, 0, 3])
+    d = upload(p)
+    run_d256(p, d)
+    o_ref = d["o"].clone()
+    hf_ref = d["h_final"].clone()
+    d2 = upload(p)
+    d2["idx"] = torch.tensor([2, 9, 3], dtype=torch.int32, device="cuda")  # slot 9 is past the pool
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    run_d256(p, d2, dev_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & lap.DEV_ERR_BAD_INDEX
+    a, b = int(p.cu_seqlens[1]), int(p.cu_seqlens[2])
+    keep = np.r_[0:a, b:p.tokens]
+    assert torch.equal(d2["o"][keep].view(torch.int16), o_ref[keep].view(torch.int16))
+    assert bool(torch.isnan(d2["o"][a:b].float()).all())  # the skipped sequence's rows are not written
+    for slot in (2, 3):
+        assert torch.equal(d2["h_final"][slot].view(torch.int32), hf_ref[slot].view(torch.int32))
+
+
+def test_d256_nonfinite_sequence_does_not_reach_its_neighbours():
+    lengths = [100, 77, 150, 64, 40]
+    p = W.custom(seed=4004, lengths=lengths, H=1, HV=2, D=256)
+    a, b = int(p.cu_seqlens[2]), int(p.cu_seqlens[3])
+    p.k_bits[a:b] = 0x7F80
+    p.v_bits[a:b] = 0x7FC0
+    d = upload(p)
+    run_d256(p, d)
+    torch.cuda.synchronize()
+    o_all = d["o"].view(torch.int16).cpu().numpy()
+    for n in (0, 1, 3, 4):
+        s, e = int(p.cu_seqlens[n]), int(p.cu_seqlens[n + 1])
+        pa = W.Problem("alone", p.q_bits[s:e].copy(), p.k_bits[s:e].copy(), p.v_bits[s:e].copy(), p.slopes,
+                       p.scale, p.H, p.HV, 1, e - s, np.array([0, e - s], dtype=np.int32), None,
+                       p.h0[n:n + 1].copy(), D=256, V=256)
+        da = upload(pa)
+        run_d256(pa, da)
+        torch.cuda.synchronize()
+        assert np.array_equal(o_all[s:e], da["o"].view(torch.int16).cpu().numpy()), f"sequence {n}"
+        assert np.array_equal(d["h_final"][n].view(torch.int32).cpu().numpy(),
+                              da["h_final"][0].view(torch.int32).cpu().numpy()), f"sequence {n} state"
+
+
+def test_d256_two_calls_bitwise_and_garbage_workspace():
+    import linear_attention_prefill_chunkwise_gb300 as lap
+    p = W.custom(seed=4005, lengths=[300, 1, 129], H=2, HV=4, D=256, pool=6, indices=[5, -1, 2])
+    nbytes = lap.la_prefill_d256_workspace(p.B, p.T, p.N, p.HV, True)
+    ws = torch.full((nbytes,), 0x7F, dtype=torch.uint8, device="cuda")  # NaN-like garbage
+    outs = []
+    for _ in range(2):
+        d = upload(p)
+        run_d256(p, d, workspace=ws)
+        torch.cuda.synchronize()
+        outs.append((d["o"].view(torch.int16).clone(), d["h_final"].view(torch.int32).clone()))
+    assert torch.equal(outs[0][0], outs[1][0])
+    assert torch.equal(outs[0][1], outs[1][1])

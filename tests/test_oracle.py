@@ -379,3 +379,33 @@ def test_backward_lambda_one_matches_masked_linear_attention_gradients():
     assert np.allclose(dk[:, 0], dk_ref, rtol=1e-12, atol=1e-12)
     assert np.allclose(dv[:, 0], dv_ref, rtol=1e-12, atol=1e-12)
     assert np.allclose(dh0[0, 0], dh0_ref, rtol=1e-12, atol=1e-12)
+
+
+# ---- the block decomposition the D = 256 prefill relies on ---------------------------
+
+def test_key_and_value_halves_decompose_the_recurrence():
+    """S[v][k] += v_t[v] k_t[k] updates every state element on its own, and q . k splits over
+    any partition of the key dimension, so the recurrence at head dimension D equals the sum over
+    key halves b of the recurrences on (q[b half], k[b half]) from the state columns of that half,
+    with the final state assembled block by block, for each half of the value dimension alike.
+    A slip that mixes the halves (a cross term, one scale or decay applied twice) breaks it."""
+    lengths = [9, 0, 14]
+    q, k, v, slopes, scale, h0, cu = rand_problem(41, lengths, 2, 4, D=12, V=10)
+    o, hf = oracle.tokenwise(q, k, v, slopes, scale, h0=h0, cu_seqlens=cu)
+    half = 6
+    o_sum = np.zeros_like(o)
+    hf_blocks = np.zeros_like(hf)
+    for b in range(2):
+        ks = slice(b * half, (b + 1) * half)
+        for a, vs in enumerate((slice(0, 4), slice(4, 10))):  # uneven value halves: rows are independent
+            ob, hb = oracle.tokenwise(np.ascontiguousarray(q[:, :, ks]), np.ascontiguousarray(k[:, :, ks]),
+                                      np.ascontiguousarray(v[:, :, vs]), slopes, scale,
+                                      h0=np.ascontiguousarray(h0[:, :, vs, ks]), cu_seqlens=cu)
+            o_sum[:, :, vs] += ob
+            hf_blocks[:, :, vs, ks] = hb
+    assert rel(o_sum, o) < 1e-12
+    assert rel(hf_blocks, hf) < 1e-12
+    # one key half alone is far from the whole (the test would catch a dropped half)
+    o_half, _ = oracle.tokenwise(np.ascontiguousarray(q[:, :, :half]), np.ascontiguousarray(k[:, :, :half]), v,
+                                 slopes, scale, h0=np.ascontiguousarray(h0[:, :, :, :half]), cu_seqlens=cu)
+    assert rel(o_half, o) > 0.1
