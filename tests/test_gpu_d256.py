@@ -117,3 +117,40 @@ def test_d256_two_calls_bitwise_and_garbage_workspace():
         outs.append((d["o"].view(torch.int16).clone(), d["h_final"].view(torch.int32).clone()))
     assert torch.equal(outs[0][0], outs[1][0])
     assert torch.equal(outs[0][1], outs[1][1])
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_d256_random(seed):
+    """Random batches (the generator of tests/test_gpu_random.py) at D = V = 256."""
+    from test_gpu_random import _draw
+    kw, _ = _draw(seed)
+    kw["D"] = 256
+    p = W.custom(seed=seed, name=f"random d256 {seed}", **kw)
+    d = upload(p)
+    run_d256(p, d)
+    compare_full(p, d, f"random D=256 {seed} {kw}")
+
+
+def test_d256_in_a_cuda_graph():
+    """The five kernels of one call captured in a CUDA graph replay bitwise like the eager call:
+    the call neither synchronises with the host nor allocates."""
+    import linear_attention_prefill_chunkwise_gb300 as lap
+    p = W.custom(seed=4006, lengths=[200, 0, 65], H=1, HV=2, D=256, pool=4, indices=[3, -1, 1], in_place=True)
+    ref = upload(p)
+    run_d256(p, ref)
+    torch.cuda.synchronize()
+    d = upload(p)
+    h0_init = d["h0"].clone()
+    ws = torch.empty(lap.la_prefill_d256_workspace(p.B, p.T, p.N, p.HV, True), dtype=torch.uint8, device="cuda")
+    run_d256(p, d, workspace=ws)  # warm-up outside the capture (first-call setup)
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        run_d256(p, d, workspace=ws)
+    for _ in range(2):
+        d["h0"].copy_(h0_init)
+        d["o"].fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(d["o"].view(torch.int16), ref["o"].view(torch.int16))
+        assert torch.equal(d["h0"].view(torch.int32), ref["h0"].view(torch.int32))
