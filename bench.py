@@ -553,26 +553,26 @@ def run_sweep(args):
         run_backward_sweep(args, device, stream, flush, hbm, hbm_kind)
 
 
-def short_d64_problem():
-    """The short-continuation workload (128 requests of 8 tokens, H=HV=64, 256-slot pool, 16
-    padded) at D = V = 64."""
+def short_d64_problem(D=64, H=64, seed=1105):
+    """The short-continuation workload (128 requests of 8 tokens, 256-slot pool, 16 padded) at
+    D = V = 64 (H=HV=64), or another head dimension and head count."""
     import numpy as np
     import workloads as W
-    rng = np.random.default_rng(1105)
+    rng = np.random.default_rng(seed)
     idx = rng.permutation(256)[:128].astype(np.int32)
     idx[rng.choice(128, 16, replace=False)] = -1
-    return W.custom(seed=1105, lengths=[8] * 128, H=64, HV=64, D=64, pool=256, indices=idx, in_place=True,
-                    name="D=V=64 short packed N=128 T=8 H=HV=64, 256-slot pool, 16 padded")
+    return W.custom(seed=seed, lengths=[8] * 128, H=H, HV=H, D=D, pool=256, indices=idx, in_place=True,
+                    name=f"D=V={D} short packed N=128 T=8 H=HV={H}, 256-slot pool, 16 padded")
 
 
 def run_decode_sweep(args, device, stream, flush, hbm, hbm_kind):
     """The speculative-decoding ops on the short-continuation workload (workloads.config(5):
     128 requests of 8 draft tokens, H=HV=64, 256-slot pool, 16 padded), and on the same shape
-    at D = V = 64: MTP decode, verify with the KV-buffer copy, and commit of every accepted
+    at D = V = 64, and at D = V = 256 with H=HV=16: MTP decode, verify with the KV-buffer copy, and commit of every accepted
     token.  Bytes: per live (request, value head) the state (64 KB, or 16 KB at D = 64) read
     (and written, decode and commit), the tokens' q, k (once per q/k head), v and o, and the
     KV buffer written (verify) or read (commit)."""
-    for p in (__import__("workloads").config(5), short_d64_problem()):
+    for p in (__import__("workloads").config(5), short_d64_problem(), short_d64_problem(D=256, H=16, seed=1106)):
         decode_sweep_one(args, p, device, stream, flush, hbm, hbm_kind)
 
 
@@ -633,7 +633,7 @@ def decode_sweep_one(args, p, device, stream, flush, hbm, hbm_kind):
         torch.cuda.synchronize(device)
         ms = statistics.fmean(a.elapsed_time(b) for a, b in times)
         t_roof = nbytes / (hbm * 1e9)
-        line = {"sweep": True, "op": name, "workload": f"B=128 requests x T=8 draft tokens, H=HV=64, D=V={D}, "
+        line = {"sweep": True, "op": name, "workload": f"B=128 requests x T=8 draft tokens, H=HV={p.HV}, D=V={D}, "
                 "256-slot pool, 16 padded", "ms": round(ms, 5), "tokens_per_s": round(toks / (ms / 1e3), 1),
                 "alg_bytes": nbytes, "achieved_gbs": round(nbytes / (ms / 1e3) / 1e9, 1),
                 "roofline_ms": round(t_roof * 1e3, 5), "frac": round(t_roof * 1e3 / ms, 4), "bound": "hbm",

@@ -18,8 +18,8 @@
  *                  pooled KV buffer at the request's slot for a later commit.  For T <= 8 the
  *                  products S q_t run on the tensor cores with S and q_t as TF32 operands (the
  *                  pages' verify kernel also multiplies the state by q in TF32), so the outputs
- *                  equal la_decode_mtp's within that rounding; for T > 8, and for D = 64,
- *                  verify runs decode's tokenwise recurrence and its outputs are bitwise
+ *                  equal la_decode_mtp's within that rounding; for T > 8, and for D = 64 and
+ *                  256, verify runs decode's tokenwise recurrence and its outputs are bitwise
  *                  decode's.
  *   la_commit      with L = accepted_len[b] (0 <= L <= T) taken from that KV buffer:
  *                      S = lambda^L S + sum_{i<L} lambda^(L-1-i) v_i^T k_i   (L = 0: no-op)
@@ -41,8 +41,8 @@
  *   vbuf      bf16 [P, T, HV, V]
  *   accepted_len int32 [B]            tokens to commit per request, clamped to [0, T]
  *   dev_error device int, nullable    LA_DEV_ERR_BAD_INDEX when a slot >= P (request skipped)
- * Supported: D == V == 128 or D == V == 64, HV % H == 0, T >= 1 (any B >= 0); 16-byte
- * aligned pointers.
+ * Supported: D == V == 128, 64 or 256, HV % H == 0, T >= 1 (any B >= 0); 16-byte aligned
+ * pointers.
  * What a call writes (o, kbuf, vbuf; the pool in decode and commit; dev_error) may share no
  * memory with what it reads or with another of its outputs: LA_ERR_INVALID_ARGUMENT (address
  * ranges checked on the host; pool and KV buffer span P slots with state_indices, B without).

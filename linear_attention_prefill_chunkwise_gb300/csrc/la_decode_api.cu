@@ -57,13 +57,13 @@ la_status encode_bf16_token_map(CUtensorMap* map, const void* base, int64_t rows
 
 // Shape checks shared by the three entry points.
 la_status check_shapes(int B, int T, int H, int HV, int D, int V, int pool_size, const int32_t* state_indices) {
-  if (D != V || (D != 128 && D != 64))
-    return fail(LA_ERR_UNSUPPORTED, "only D == V == 128 or 64 is implemented (got D=%d, V=%d)", D, V);
+  if (D != V || (D != 128 && D != 64 && D != 256))
+    return fail(LA_ERR_UNSUPPORTED, "only D == V == 128, 64 or 256 is implemented (got D=%d, V=%d)", D, V);
   if (H <= 0 || HV <= 0) return fail(LA_ERR_INVALID_ARGUMENT, "H and HV must be positive (got %d, %d)", H, HV);
   if (HV % H != 0) return fail(LA_ERR_UNSUPPORTED, "HV (%d) must be a multiple of H (%d)", HV, H);
   if (B < 0) return fail(LA_ERR_INVALID_ARGUMENT, "B must be >= 0 (got %d)", B);
   if (T < 1) return fail(LA_ERR_INVALID_ARGUMENT, "T must be >= 1 (got %d)", T);
-  if (static_cast<int64_t>(B) * HV * lad::kSplit > INT32_MAX || static_cast<int64_t>(B) * T > INT32_MAX)
+  if (static_cast<int64_t>(B) * HV * lad::split_of<256>() > INT32_MAX || static_cast<int64_t>(B) * T > INT32_MAX)
     return fail(LA_ERR_UNSUPPORTED, "B*HV or B*T too large");
   if (state_indices ? pool_size <= 0 : pool_size < B)
     return fail(LA_ERR_INVALID_ARGUMENT, "pool_size (%d) must be positive, and >= B (%d) without state_indices",
@@ -72,10 +72,18 @@ la_status check_shapes(int B, int T, int H, int HV, int D, int V, int pool_size,
   return LA_OK;
 }
 
-// One-time setup per device: the closed-form verify kernel's shared memory exceeds the default.
+// One-time setup per device: the shared memory of the closed-form verify kernel and of the
+// tokenwise kernel's D = 256 instances exceeds the default.
 cudaError_t setup_kernels() {
-  return cudaFuncSetAttribute(lav::la_verify_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              lav::verify_smem_bytes());
+  const cudaFuncAttribute attr = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  cudaError_t e = cudaFuncSetAttribute(lav::la_verify_tc_kernel, attr, lav::verify_smem_bytes());
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(lad::la_tokenwise_kernel<lad::kDecode, 256>, attr,
+                                                 lad::tokenwise_smem_bytes<256>());
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(lad::la_tokenwise_kernel<lad::kVerify, 256>, attr,
+                                                 lad::tokenwise_smem_bytes<256>());
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(lad::la_tokenwise_kernel<lad::kCommit, 256>, attr,
+                                                 lad::tokenwise_smem_bytes<256>());
+  return e;
 }
 
 template <int kMode>
@@ -84,13 +92,19 @@ la_status launch(const lad::Params& p, int D, void* stream) {
   la_status st = la_host::current_device(g_dev, &ds, setup_kernels);
   if (st != LA_OK) return st;
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-  cudaError_t ce =
-      D == 128 ? la_host::launch_pdl(lad::la_tokenwise_kernel<kMode, 128>,
-                                     lad::tokenwise_grid<128>(p.B * p.HV * lad::split_of<128>(), ds->sms),
-                                     lad::kThreads, lad::tokenwise_smem_bytes<128>(), cs, p)
-               : la_host::launch_pdl(lad::la_tokenwise_kernel<kMode, 64>,
-                                     lad::tokenwise_grid<64>(p.B * p.HV * lad::split_of<64>(), ds->sms),
-                                     lad::kThreads, lad::tokenwise_smem_bytes<64>(), cs, p);
+  cudaError_t ce;
+  if (D == 128)
+    ce = la_host::launch_pdl(lad::la_tokenwise_kernel<kMode, 128>,
+                             lad::tokenwise_grid<128>(p.B * p.HV * lad::split_of<128>(), ds->sms), lad::kThreads,
+                             lad::tokenwise_smem_bytes<128>(), cs, p);
+  else if (D == 64)
+    ce = la_host::launch_pdl(lad::la_tokenwise_kernel<kMode, 64>,
+                             lad::tokenwise_grid<64>(p.B * p.HV * lad::split_of<64>(), ds->sms), lad::kThreads,
+                             lad::tokenwise_smem_bytes<64>(), cs, p);
+  else
+    ce = la_host::launch_pdl(lad::la_tokenwise_kernel<kMode, 256>,
+                             lad::tokenwise_grid<256>(p.B * p.HV * lad::split_of<256>(), ds->sms), lad::kThreads,
+                             lad::tokenwise_smem_bytes<256>(), cs, p);
   if (ce == cudaSuccess) ce = cudaGetLastError();
   if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(ce));
   return LA_OK;

@@ -49,13 +49,20 @@ using lap::f2_mul;
 using lap::f2_pack;
 using lap::f2_unpack;
 
-constexpr int kDim = 128;                 // largest D = V (the staging arrays' width)
-constexpr int kRows = 64;                 // state rows per CTA
+constexpr int kDim = 128;                 // the default D = V
+constexpr int kRows = 64;                 // state rows per CTA (D = 128 and 64)
 constexpr int kSplit = kDim / kRows;      // CTAs per (request, value head) at D = 128
-constexpr int kThreads = kRows / 4 * 8;   // 4 rows x D / 8 columns per thread
-// CTAs per (request, value head) for head dimension kD (D = V = 128 or 64)
+constexpr int kThreads = 128;             // 4 rows x 4 D / lanes columns per thread
+// State rows per CTA and lanes per row group for head dimension kD (D = V = 64, 128 or 256):
+// at D = 256 a CTA holds 32 rows and a row group of 4 rows spans 16 lanes, so that a thread
+// still owns 4 rows x 16 columns.
 template <int kD>
-__host__ __device__ constexpr int split_of() { return kD / kRows; }
+__host__ __device__ constexpr int rows_of() { return kD == 256 ? 32 : kRows; }
+template <int kD>
+__host__ __device__ constexpr int lanes_of() { return kD == 256 ? 16 : 8; }
+// CTAs per (request, value head)
+template <int kD>
+__host__ __device__ constexpr int split_of() { return kD / rows_of<kD>(); }
 
 enum Mode : int { kDecode = 0, kVerify = 1, kCommit = 2, kPrefill = 3 };
 
@@ -105,10 +112,10 @@ __host__ __device__ constexpr int ctas_per_sm() { return kD == 64 ? 6 : 4; }
 
 template <int kD>
 struct __align__(128) TokSmem {
-  float pre[kRows * kD];         // the next unit's state slice (bulk copy)
+  float pre[rows_of<kD>() * kD]; // the next unit's state slice (bulk copy)
   float ks[kTileTok][kD];        // staged k (commit: from the KV buffer)
   float qs[kTileTok][kD];        // staged q
-  float vs[kTileTok][kRows];     // staged v, this CTA's rows
+  float vs[kTileTok][rows_of<kD>()];  // staged v, this CTA's rows
   float linv[kTileTok];          // lambda^-(i+1) of the tile's token i (rescaled update)
   float lpow[kTileTok];          // lambda^(i+1)
   uint64_t bar;                  // slice landed (transaction bytes)
@@ -165,18 +172,23 @@ __device__ __forceinline__ TokUnit tok_unit(const Params& p, int u) {
   return w;
 }
 
-// kD = D = V: 128 (two CTAs of 64 state rows per unit, 16 columns of each row per thread) or 64
-// (one CTA per unit, 8 columns per thread, twice the CTAs per SM).
+// kD = D = V: 128 (two CTAs of 64 state rows per unit, 16 columns of each row per thread), 64
+// (one CTA per unit, 8 columns per thread, more CTAs per SM) or 256 (eight CTAs of 32 rows per
+// unit, 16 columns of each row per thread, row groups of 16 lanes).
 template <int kMode, int kD = kDim>
 __global__ void __launch_bounds__(kThreads, ctas_per_sm<kD>()) la_tokenwise_kernel(const Params p) {
-  static_assert(kD == 128 || kD == 64, "head dimension");
-  constexpr int kM = kD / 32;             // 16-byte column chunks of a row per thread
+  static_assert(kD == 128 || kD == 64 || kD == 256, "head dimension");
+  constexpr int kR = rows_of<kD>();       // state rows of this CTA
+  constexpr int kLanes = lanes_of<kD>();  // lanes of a row group
+  constexpr int kLaneBits = kLanes == 16 ? 4 : 3;
+  constexpr int kColStride = 4 * kLanes;  // columns between a thread's 16-byte chunks
+  constexpr int kM = kD / kColStride;     // 16-byte column chunks of a row per thread
   constexpr int kChunks = kD / 8;         // 8-value chunks of a token row
-  constexpr uint32_t kSlice = kRows * kD * 4;
+  constexpr uint32_t kSlice = kR * kD * 4;
   extern __shared__ uint8_t tok_raw[];
   TokSmem<kD>& sm = *reinterpret_cast<TokSmem<kD>*>((reinterpret_cast<uintptr_t>(tok_raw) + 127) & ~uintptr_t(127));
   const int t = threadIdx.x;
-  const int cg = t & 7, rg = t >> 3;  // chunks 32 m + 4 cg, rows vbase + 4 rg .. +3
+  const int cg = t & (kLanes - 1), rg = t >> kLaneBits;  // chunks kColStride m + 4 cg, rows vbase + 4 rg .. +3
   const int units = p.B * p.HV * split_of<kD>();
   const float* s_in = (kMode == kPrefill) ? p.h0 : p.state;
   float* s_out = (kMode == kPrefill) ? p.h_final : p.state;
@@ -192,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kD>()) la_tokenwise_kern
   __syncthreads();
 
   auto slice_of = [&](const TokUnit& w) {
-    return (static_cast<size_t>(w.slot) * p.HV + w.hv) * kD * kD + static_cast<size_t>(w.part) * kRows * kD;
+    return (static_cast<size_t>(w.slot) * p.HV + w.hv) * kD * kD + static_cast<size_t>(w.part) * kR * kD;
   };
   auto prefetch = [&](const TokUnit& w) {  // thread 0
     lap::mbar_arrive_expect_tx(&sm.bar, kSlice);
@@ -217,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kD>()) la_tokenwise_kern
   while (u < units) {
     TokUnit nxt;
     const int un = seek(u + gridDim.x, nxt);
-    const int vbase = cur.part * kRows;
+    const int vbase = cur.part * kR;
     const float slope = __ldg(p.slopes + cur.hv);
     const float lam = expf(-slope);
     const uint64_t lam2 = f2_pack(lam, lam);
@@ -234,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kD>()) la_tokenwise_kern
       for (int r = 0; r < 4; ++r)
 #pragma unroll
         for (int m = 0; m < kM; ++m) {
-          const float4 x = *reinterpret_cast<const float4*>(&sm.pre[(4 * rg + r) * kD + 32 * m + 4 * cg]);
+          const float4 x = *reinterpret_cast<const float4*>(&sm.pre[(4 * rg + r) * kD + kColStride * m + 4 * cg]);
           S[r][2 * m] = f2_pack(x.x, x.y);
           S[r][2 * m + 1] = f2_pack(x.z, x.w);
         }
@@ -258,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kD>()) la_tokenwise_kern
       // stage tokens t0 .. t0 + nt - 1: 16 bytes (8 values) per thread and array per step
       for (int e = t; e < nt * kChunks; e += kThreads) {
         const int i = e / kChunks, c = e % kChunks;  // token, 8-value chunk
-        const bool vmine = c / (kRows / 8) == cur.part;  // values 8c .. 8c + 7 are rows of this CTA
+        const bool vmine = c / (kR / 8) == cur.part;  // values 8c .. 8c + 7 are rows of this CTA
         uint4 kx, vx = make_uint4(0u, 0u, 0u, 0u);
         if (kMode == kCommit) {
           const size_t brow = static_cast<size_t>(cur.slot) * p.T + t0 + i;
@@ -305,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kD>()) la_tokenwise_kern
         uint64_t kk[2 * kM];
 #pragma unroll
         for (int m = 0; m < kM; ++m) {
-          const float4 x = *reinterpret_cast<const float4*>(&sm.ks[i][32 * m + 4 * cg]);
+          const float4 x = *reinterpret_cast<const float4*>(&sm.ks[i][kColStride * m + 4 * cg]);
           kk[2 * m] = f2_pack(x.x, x.y);
           kk[2 * m + 1] = f2_pack(x.z, x.w);
         }
@@ -327,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kD>()) la_tokenwise_kern
           uint64_t qq[2 * kM];
 #pragma unroll
           for (int m = 0; m < kM; ++m) {
-            const float4 x = *reinterpret_cast<const float4*>(&sm.qs[i][32 * m + 4 * cg]);
+            const float4 x = *reinterpret_cast<const float4*>(&sm.qs[i][kColStride * m + 4 * cg]);
             qq[2 * m] = f2_pack(x.x, x.y);
             qq[2 * m + 1] = f2_pack(x.z, x.w);
           }
@@ -340,16 +352,22 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kD>()) la_tokenwise_kern
             const float2 a2 = f2_unpack(acc);
             dot[r] = a2.x + a2.y;
           }
-          // reduce-scatter over the 8 lanes of the row group: lanes with bit 2 of cg keep rows
+          // (16-lane row groups: fold the upper 8 lanes onto the lower first)
+          if constexpr (kLanes == 16) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) dot[r] += __shfl_xor_sync(0xffffffffu, dot[r], 8);
+          }
+          // reduce-scatter over 8 lanes of the row group: lanes with bit 2 of cg keep rows
           // {2, 3} (else {0, 1}), bit 1 picks one of the two, bit 0 pairs lanes; lane cg ends
           // with the total of row 2 (cg >> 2) + ((cg >> 1) & 1), written by the even lanes
+          // (of the lower 8, with 16-lane groups)
           const bool b2 = cg & 4, b1 = cg & 2;
           const float s0 = b2 ? dot[0] : dot[2], s1 = b2 ? dot[1] : dot[3];
           float k0 = (b2 ? dot[2] : dot[0]) + __shfl_xor_sync(0xffffffffu, s0, 4);
           float k1 = (b2 ? dot[3] : dot[1]) + __shfl_xor_sync(0xffffffffu, s1, 4);
           float kx = (b1 ? k1 : k0) + __shfl_xor_sync(0xffffffffu, b1 ? k0 : k1, 2);
           kx += __shfl_xor_sync(0xffffffffu, kx, 1);
-          if (!(cg & 1))
+          if (!(cg & 1) && (kLanes == 8 || cg < 8))
             p.o[(cur.row0 + t0 + i) * v_tok + static_cast<size_t>(cur.hv) * kD + vbase + 4 * rg +
                 (2 * (cg >> 2) + ((cg >> 1) & 1))] = __float2bfloat16_rn(p.scale * sm.lpow[i] * kx);
         }
@@ -371,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kD>()) la_tokenwise_kern
 #pragma unroll
         for (int m = 0; m < kM; ++m) {
           const float2 a = f2_unpack(S[r][2 * m]), c = f2_unpack(S[r][2 * m + 1]);
-          *reinterpret_cast<float4*>(dst + (4 * rg + r) * kD + 32 * m + 4 * cg) = make_float4(a.x, a.y, c.x, c.y);
+          *reinterpret_cast<float4*>(dst + (4 * rg + r) * kD + kColStride * m + 4 * cg) = make_float4(a.x, a.y, c.x, c.y);
         }
     }
     u = un;

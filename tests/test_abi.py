@@ -155,8 +155,9 @@ def call_decode(fn="la_decode_mtp", **over):
 @pytest.mark.parametrize("fn,over,status", [
     ("la_decode_mtp", dict(D=64), LA_UNSUPPORTED),        # D != V
     ("la_decode_mtp", dict(D=32, V=32), LA_UNSUPPORTED),
-    ("la_decode_mtp", dict(D=256, V=256), LA_UNSUPPORTED),
+    ("la_decode_mtp", dict(D=512, V=512), LA_UNSUPPORTED),
     ("la_decode_mtp", dict(D=64, V=64, P=1), LA_INVALID),  # D = V = 64 passes the shape check
+    ("la_decode_mtp", dict(D=256, V=256, P=1), LA_INVALID),  # and D = V = 256
     ("la_commit", dict(D=64, V=64, kbuf=FAKE, vbuf=FAKE, acc=None), LA_INVALID),
     ("la_decode_mtp", dict(H=3, HV=4), LA_UNSUPPORTED),
     ("la_decode_mtp", dict(T=0), LA_INVALID),

@@ -81,6 +81,12 @@ CASES = {
                                     slopes=[0.0, 1e-4, 0.7, 5.0, 40.0, 200.0], D=64),
     "D64_T8_gva_pool": dict(seed=5103, B=40, T=8, H=4, HV=16, P=64, n_pad=5, D=64),
     "D64_T17_tiles": dict(seed=5104, B=3, T=17, H=4, HV=4, P=4, D=64),
+    # D = V = 256: eight CTAs of 32 rows per (request, value head), row groups of 16 lanes
+    "D256_T1": dict(seed=5201, B=5, T=1, H=2, HV=2, P=8, n_pad=1, D=256),
+    "D256_T5_gva_lambda_edges": dict(seed=5202, B=7, T=5, H=2, HV=6, P=11, n_pad=2,
+                                     slopes=[0.0, 1e-4, 0.7, 5.0, 40.0, 200.0], D=256),
+    "D256_T8_gva_pool": dict(seed=5203, B=24, T=8, H=2, HV=8, P=32, n_pad=3, D=256),
+    "D256_T17_tiles": dict(seed=5204, B=3, T=17, H=2, HV=2, P=4, D=256),
 }
 
 

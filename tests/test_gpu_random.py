@@ -106,7 +106,7 @@ def _draw_decode(seed):
     """Arguments of test_gpu_decode.make_case for one random speculative-decoding batch: up to
     40 requests of 1 to 17 draft tokens (both sides of the tensor-core verify's 8-token limit),
     GVA groups, a pool larger than the batch with padded requests, mixed special slopes, and
-    D = V = 128 or 64."""
+    D = V = 128, 64 or 256."""
     rng = np.random.default_rng(31000 + seed)
     H = int(rng.integers(1, 5))
     HV = H * int(rng.integers(1, 4))
@@ -119,7 +119,7 @@ def _draw_decode(seed):
         special = rng.random(HV) < 0.5
         sl[special] = rng.choice([0.0, 1e-4, 0.7, 5.0, 40.0, 200.0], size=int(special.sum())).astype(np.float32)
         kw["slopes"] = [float(x) for x in sl]
-    kw["D"] = int(rng.choice([128, 128, 64]))
+    kw["D"] = int(rng.choice([128, 128, 64, 256]))
     return kw
 
 
