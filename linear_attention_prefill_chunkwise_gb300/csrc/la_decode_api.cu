@@ -103,7 +103,7 @@ la_status launch(const lad::Params& p, int D, void* stream) {
                              lad::tokenwise_smem_bytes<64>(), cs, p);
   else
     ce = la_host::launch_pdl(lad::la_tokenwise_kernel<kMode, 256>,
-                             lad::tokenwise_grid<256>(p.B * p.HV * lad::split_of<256>(), ds->sms), lad::kThreads,
+                             lad::tokenwise_grid<256>(p.B * p.HV * lad::split_of<256>(), ds->sms), lad::threads_of<256>(),
                              lad::tokenwise_smem_bytes<256>(), cs, p);
   if (ce == cudaSuccess) ce = cudaGetLastError();
   if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(ce));

@@ -8,11 +8,13 @@
 // for decode and commit, one write of the state: the work is bound by the state traffic.
 // Each row of the state evolves, and gives its output, independently of the others, so a
 // unit is split over D / 64 parts of 64 state rows, each held in the registers of one
-// 128-thread CTA.  The CTAs are persistent (ctas_per_sm per SM) and walk their parts; while a CTA
-// applies the tokens of one part, a single bulk copy brings the next part's state slice (32 KB
-// at D = 128, 16 KB at D = 64) into shared memory, so every state load but the first overlaps
-// arithmetic.  Thread t owns state rows v = 64 h + 4 (t / 8) .. +3 and, of each, the D / 32
-// 16-byte column chunks k = 32 m + 4 (t % 8) .. +3 (m = 0 .. D / 32 - 1), and for every token
+// 128-thread CTA (256 threads at D = 256).  The CTAs are persistent (ctas_per_sm per SM) and
+// walk their parts; while a CTA applies the tokens of one part, a single bulk copy brings the
+// next part's state slice (32 KB at D = 128, 16 KB at D = 64, 64 KB at D = 256) into shared
+// memory, so every state load but the first overlaps arithmetic.  At D = 128 thread t owns state
+// rows v = 64 h + 4 (t / 8) .. +3 and, of each, the four 16-byte column chunks
+// k = 32 m + 4 (t % 8) .. +3 (m = 0..3) (two chunks at D = 64; at D = 256 rows 4 (t / 16) .. +3
+// and chunks 64 m + 4 (t % 16), the row group's 16 lanes folded to 8 first), and for every token
 //     S[v][k] = lambda S[v][k] + v_t[v] k_t[k]              (FP32, fused multiply-add)
 //     o_t[v]  = scale sum_k S[v][k] q_t[k]                    (the 8 lanes of a row group hold
 //                                                             partial sums of 4 rows; a reduce-
@@ -52,14 +54,16 @@ using lap::f2_unpack;
 constexpr int kDim = 128;                 // the default D = V
 constexpr int kRows = 64;                 // state rows per CTA (D = 128 and 64)
 constexpr int kSplit = kDim / kRows;      // CTAs per (request, value head) at D = 128
-constexpr int kThreads = 128;             // 4 rows x 4 D / lanes columns per thread
-// State rows per CTA and lanes per row group for head dimension kD (D = V = 64, 128 or 256):
-// at D = 256 a CTA holds 32 rows and a row group of 4 rows spans 16 lanes, so that a thread
-// still owns 4 rows x 16 columns.
+constexpr int kThreads = 128;             // threads per CTA at D = 128 and 64
+// Lanes per row group and threads per CTA for head dimension kD (D = V = 64, 128 or 256): at
+// D = 256 a row group of 4 rows spans 16 lanes, so that a thread still owns 4 rows x 16
+// columns, and a CTA of 256 threads holds its 64 rows.
 template <int kD>
-__host__ __device__ constexpr int rows_of() { return kD == 256 ? 32 : kRows; }
+__host__ __device__ constexpr int rows_of() { return kRows; }
 template <int kD>
 __host__ __device__ constexpr int lanes_of() { return kD == 256 ? 16 : 8; }
+template <int kD>
+__host__ __device__ constexpr int threads_of() { return kD == 256 ? 256 : kThreads; }
 // CTAs per (request, value head)
 template <int kD>
 __host__ __device__ constexpr int split_of() { return kD / rows_of<kD>(); }
@@ -108,7 +112,7 @@ __device__ __forceinline__ void bf16x8_to_f32(const uint4& x, float (&f)[8]) {
 constexpr int kTileTok = 8;  // tokens staged in shared memory per pass
 // Resident CTAs per SM: the D = 64 instance holds half the registers and shared memory.
 template <int kD>
-__host__ __device__ constexpr int ctas_per_sm() { return kD == 64 ? 6 : 4; }
+__host__ __device__ constexpr int ctas_per_sm() { return kD == 64 ? 6 : kD == 256 ? 2 : 4; }
 
 template <int kD>
 struct __align__(128) TokSmem {
@@ -173,10 +177,10 @@ __device__ __forceinline__ TokUnit tok_unit(const Params& p, int u) {
 }
 
 // kD = D = V: 128 (two CTAs of 64 state rows per unit, 16 columns of each row per thread), 64
-// (one CTA per unit, 8 columns per thread, more CTAs per SM) or 256 (eight CTAs of 32 rows per
-// unit, 16 columns of each row per thread, row groups of 16 lanes).
+// (one CTA per unit, 8 columns per thread, more CTAs per SM) or 256 (four CTAs of 256 threads
+// and 64 rows per unit, 16 columns of each row per thread, row groups of 16 lanes).
 template <int kMode, int kD = kDim>
-__global__ void __launch_bounds__(kThreads, ctas_per_sm<kD>()) la_tokenwise_kernel(const Params p) {
+__global__ void __launch_bounds__(threads_of<kD>(), ctas_per_sm<kD>()) la_tokenwise_kernel(const Params p) {
   static_assert(kD == 128 || kD == 64 || kD == 256, "head dimension");
   constexpr int kR = rows_of<kD>();       // state rows of this CTA
   constexpr int kLanes = lanes_of<kD>();  // lanes of a row group
@@ -268,7 +272,7 @@ __global__ void __launch_bounds__(kThreads, ctas_per_sm<kD>()) la_tokenwise_kern
       const int nt = min(kTileTok, cur.ntok - t0);
       __syncthreads();  // the previous tile has been consumed
       // stage tokens t0 .. t0 + nt - 1: 16 bytes (8 values) per thread and array per step
-      for (int e = t; e < nt * kChunks; e += kThreads) {
+      for (int e = t; e < nt * kChunks; e += threads_of<kD>()) {
         const int i = e / kChunks, c = e % kChunks;  // token, 8-value chunk
         const bool vmine = c / (kR / 8) == cur.part;  // values 8c .. 8c + 7 are rows of this CTA
         uint4 kx, vx = make_uint4(0u, 0u, 0u, 0u);
