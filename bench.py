@@ -491,7 +491,8 @@ def run_sweep(args):
                          name="D=V=64 fixed MHA B=2 T=8192 H=HV=64, h0 + final state")),
         ("d64_short", short_d64_problem()),
         ("d256", W.custom(seed=3010, B=2, T=8192, H=16, HV=16, D=256,
-                          name="D=V=256 fixed B=2 T=8192 H=HV=16, h0 + final state"))]
+                          name="D=V=256 fixed B=2 T=8192 H=HV=16, h0 + final state")),
+        ("d256_short", d256_short_problem())]
     for label, extra_p in (work if args.sweep_what in ("all", "prefill") else ()):
         p = W.config(label) if extra_p is None else extra_p
         q, k, v = bf(p.q_bits), bf(p.k_bits), bf(p.v_bits)
@@ -563,6 +564,18 @@ def short_d64_problem(D=64, H=64, seed=1105):
     idx[rng.choice(128, 16, replace=False)] = -1
     return W.custom(seed=seed, lengths=[8] * 128, H=H, HV=H, D=D, pool=256, indices=idx, in_place=True,
                     name=f"D=V={D} short packed N=128 T=8 H=HV={H}, 256-slot pool, 16 padded")
+
+
+def d256_short_problem():
+    """128 fixed-length sequences of 8 tokens at D = V = 256, H=HV=16, 256-slot pool in place
+    with 16 padded (the tokenwise path of la_prefill_fwd_d256)."""
+    import numpy as np
+    import workloads as W
+    rng = np.random.default_rng(1107)
+    idx = rng.permutation(256)[:128].astype(np.int32)
+    idx[rng.choice(128, 16, replace=False)] = -1
+    return W.custom(seed=1107, B=128, T=8, H=16, HV=16, D=256, pool=256, indices=idx, in_place=True,
+                    name="D=V=256 short fixed B=128 T=8 H=HV=16, 256-slot pool, 16 padded")
 
 
 def run_decode_sweep(args, device, stream, flush, hbm, hbm_kind):

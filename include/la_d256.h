@@ -22,7 +22,9 @@
  *
  * Layouts as la_prefill_fwd with D = V = 256: q, k bf16 [B*T, H, 256]; v, o bf16 [B*T, HV, 256];
  * slopes fp32 [HV]; h0, h_final fp32 [P, HV, 256, 256] (nullable; h_final may be h0).
- * Sequences of every length run the chunkwise kernel (there is no tokenwise path at D = 256).
+ * Fixed-length batches (cu_seqlens null) with T <= 32 run the tokenwise recurrence instead, on
+ * whole 256 x 256 states (the D = 256 instance of the speculative-decoding ops' kernel, see
+ * la_decode.h): BF16 outputs directly, no workspace.
  */
 #ifndef LA_D256_H
 #define LA_D256_H
@@ -51,7 +53,8 @@ la_status la_prefill_d256_workspace(int B, int T, int N, int HV, int has_state, 
  * Arguments as la_prefill_fwd (no schedule; D and V must be 256), plus
  *   workspace        device buffer of at least la_prefill_d256_workspace(B, T, N, HV,
  *                    h0 || h_final) bytes, 256-byte aligned; its contents on entry do not
- *                    matter; it may share no memory with any other argument
+ *                    matter; it may share no memory with any other argument.  Not used (and
+ *                    may be null) for a fixed-length batch with T <= 32
  *   workspace_bytes  its size
  * Device-side errors go to *dev_error as for la_prefill_fwd (a bad state index skips its
  * sequence, bad bounds skip theirs).  Returns LA_OK after enqueueing (or with nothing to do);

@@ -8,14 +8,17 @@
 // of head hq) and v as [tokens, 2HV, 128] (the kernel's value-head fold drops the digit b of u:
 // v head 2 hv + a, the a half of head hv).  Virtual head u evolves the state block
 // S[a half of v][b half of k] from its block of h0 and writes its part of o[.][hv][a half] in
-// FP32; la_d256_sum_kernel adds the parts of b = 0 and 1 and rounds once.  Nothing here reads
-// device memory on the host or synchronises.
+// FP32; la_d256_sum_kernel adds the parts of b = 0 and 1 and rounds once.  Fixed-length batches
+// of at most kShortMax tokens per sequence go to the tokenwise kernel's D = 256 instance instead
+// (whole 256 x 256 states, BF16 outputs, no workspace).  Nothing here reads device memory on the
+// host or synchronises.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
 
 #include "../../include/la_d256.h"
+#include "la_decode_kernels.cuh"
 #include "la_host_common.h"
 #include "la_prefill_internal.h"
 
@@ -24,6 +27,7 @@ namespace la256 {
 constexpr int kThreads = 256;
 constexpr int kHalf = 128;       // the kernel's head dimension
 constexpr int kRowsPerCta = 8;   // rows of a 128 x 128 block per copy CTA (kThreads float4)
+constexpr int kShortMax = 32;    // longest fixed-length sequence taken by the tokenwise kernel
 
 // The value head hv, value half a and key half b of virtual head u (G value heads per q/k head).
 struct Virt {
@@ -155,6 +159,11 @@ inline Layout layout(int64_t tokens, int N, int HV, bool has_state) {
 
 la_host::DeviceState g_dev[la_host::kMaxDevices];
 
+cudaError_t setup_kernels() {
+  return cudaFuncSetAttribute(lad::la_tokenwise_kernel<lad::kPrefill, 256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              lad::tokenwise_smem_bytes<256>());
+}
+
 la_status launched(const char* what) {
   const cudaError_t ce = cudaGetLastError();
   if (ce != cudaSuccess) return la_host::fail(LA_ERR_CUDA, "%s launch failed: %s", what, cudaGetErrorString(ce));
@@ -193,6 +202,43 @@ la_status la_prefill_fwd_d256(const void* q, const void* k, const void* v, const
   if (st != LA_OK || nothing) return st;
   const int64_t tokens = static_cast<int64_t>(B) * T;
   if (static_cast<int64_t>(N) * 4 * HV > INT32_MAX) return fail(LA_ERR_UNSUPPORTED, "4*N*HV too large");
+  la_host::DeviceState* ds = nullptr;
+  const int pool = la_host::effective_pool_size(h0, h_final, state_indices, pool_size, N);
+
+  if (!cu_seqlens && T <= la256::kShortMax) {
+    // short fixed-length sequences: the tokenwise recurrence on whole states, no workspace
+    if ((st = la_host::check_prefill_disjoint(q, k, v, slopes, h0, state_indices, cu_seqlens, o, h_final, dev_error,
+                                              B, T, N, H, HV, D, V, pool_size)) != LA_OK)
+      return st;
+    if ((st = la_host::current_device(la256::g_dev, &ds, la256::setup_kernels)) != LA_OK) return st;
+    lad::Params tp{};
+    tp.q = static_cast<const __nv_bfloat16*>(q);
+    tp.k = static_cast<const __nv_bfloat16*>(k);
+    tp.v = static_cast<const __nv_bfloat16*>(v);
+    tp.slopes = slopes;
+    tp.state_indices = state_indices;
+    tp.o = static_cast<__nv_bfloat16*>(o);
+    tp.h0 = h0;
+    tp.h_final = h_final;
+    tp.dev_error = dev_error;
+    tp.scale = scale;
+    tp.B = N;
+    tp.T = T;
+    tp.H = H;
+    tp.HV = HV;
+    tp.G = HV / H;
+    tp.pool_size = pool;
+    tp.num_tokens = static_cast<int>(tokens);
+    tp.short_max = la256::kShortMax;
+    const int parts = N * HV * lad::split_of<256>();  // <= 4 N HV, checked above
+    cudaError_t ce = la_host::launch_pdl(lad::la_tokenwise_kernel<lad::kPrefill, 256>,
+                                         lad::tokenwise_grid<256>(parts, ds->sms), lad::threads_of<256>(),
+                                         lad::tokenwise_smem_bytes<256>(), static_cast<cudaStream_t>(stream), tp);
+    if (ce == cudaSuccess) ce = cudaGetLastError();
+    if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "tokenwise kernel launch failed: %s", cudaGetErrorString(ce));
+    return LA_OK;
+  }
+
   const bool has_state = h0 || h_final;
   const la256::Layout l = la256::layout(tokens, N, HV, has_state);
   if (!workspace || workspace_bytes < l.bytes)
@@ -202,8 +248,7 @@ la_status la_prefill_fwd_d256(const void* q, const void* k, const void* v, const
   if ((st = la_host::check_prefill_disjoint(q, k, v, slopes, h0, state_indices, cu_seqlens, o, h_final, dev_error, B,
                                             T, N, H, HV, D, V, pool_size, workspace, l.bytes)) != LA_OK)
     return st;
-  la_host::DeviceState* ds = nullptr;
-  if ((st = la_host::current_device(la256::g_dev, &ds, [] { return cudaSuccess; })) != LA_OK) return st;
+  if ((st = la_host::current_device(la256::g_dev, &ds, la256::setup_kernels)) != LA_OK) return st;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* part = reinterpret_cast<float*>(ws + l.part);
@@ -211,7 +256,6 @@ la_status la_prefill_fwd_d256(const void* q, const void* k, const void* v, const
   float* slopes_q = reinterpret_cast<float*>(ws + l.slopes_q);
   int32_t* slot_q = reinterpret_cast<int32_t*>(ws + l.slot_q);
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int pool = la_host::effective_pool_size(h0, h_final, state_indices, pool_size, N);
   const int G = HV / H;
 
   // 1. per-virtual-head slopes, the sequences that run, and the h0 blocks

@@ -42,6 +42,12 @@ D256_CASES = {
     "long_nine_chunks": dict(lengths=[64 * 9 + 17], H=1, HV=1),
     "short_sequences": dict(lengths=[5, 20, 3, 31, 1, 40], H=2, HV=2),
     "empty_sequences_with_final": dict(lengths=[0, 0, 5], H=1, HV=2),
+    # fixed length, T <= 32: the tokenwise kernel's D = 256 instance on whole states
+    "short_fixed_T32_tokenwise": dict(B=3, T=32, H=2, HV=4),
+    "short_fixed_T1_tokenwise": dict(B=4, T=1, H=1, HV=2),
+    "short_fixed_T17_pool_in_place_tokenwise": dict(B=3, T=17, H=1, HV=2, pool=5, indices=[4, -1, 1],
+                                                    in_place=True),
+    "short_fixed_T8_no_h0_tokenwise": dict(B=2, T=8, H=2, HV=2, with_h0=False),
 }
 
 
