@@ -194,6 +194,8 @@ la_status la_prefill_fwd_d256(const void* q, const void* k, const void* v, const
   la_host::g_last_error[0] = '\0';
   if (D != 256 || V != 256)
     return fail(LA_ERR_UNSUPPORTED, "la_prefill_fwd_d256 needs D == V == 256 (got D=%d, V=%d)", D, V);
+  if (H <= 0 || HV <= 0) return fail(LA_ERR_INVALID_ARGUMENT, "H and HV must be positive (got %d, %d)", H, HV);
+  if (HV % H != 0) return fail(LA_ERR_UNSUPPORTED, "HV (%d) must be a multiple of H (%d)", HV, H);
   // la_prefill_fwd's checks on the same memory seen as 2 H q/k and 2 HV value heads of 128
   bool nothing = false;
   la_status st = la_host::check_prefill_args(q, k, v, slopes, h0, state_indices, cu_seqlens, o, h_final, B, T, N,
