@@ -667,6 +667,7 @@ SEGMENT_WORKLOADS = (
     (2003, 1, 65536, 8, 8, "B=1 T=65536 H=HV=8 (an 8-way head shard)"),
     (2004, 2, 8192, 64, 64, "fixed MHA B=2 T=8192 H=64"),
     (2005, 1, 32768, 16, 16, "D=V=64: B=1 T=32768 H=HV=16"),
+    (2006, 1, 32768, 4, 4, "D=V=256: B=1 T=32768 H=HV=4"),
 )
 
 
@@ -700,18 +701,29 @@ def run_segment_sweep(args, device, stream, flush, hbm, hbm_kind, tflops, tf_kin
         return statistics.fmean(a.elapsed_time(b) for a, b in times)
 
     for seed, B, T, H, HV, name in SEGMENT_WORKLOADS:
-        p = W.custom(seed=seed, B=B, T=T, H=H, HV=HV, name=name, D=64 if name.startswith("D=V=64") else 128)
+        Dw = 64 if name.startswith("D=V=64") else 256 if name.startswith("D=V=256") else 128
+        p = W.custom(seed=seed, B=B, T=T, H=H, HV=HV, name=name, D=Dw)
         q, k, v = bf(p.q_bits), bf(p.k_bits), bf(p.v_bits)
         sl = torch.from_numpy(p.slopes).to(device)
         h0 = torch.from_numpy(p.h0).to(device)
         o = torch.empty((p.tokens, HV, p.V), dtype=torch.bfloat16, device=device)
         hf = torch.empty_like(h0)
-        nbytes_ws, seg = lap.la_prefill_segmented_workspace(B, T, B, HV, False, 0)
-        ws = torch.empty(max(nbytes_ws, 1), dtype=torch.uint8, device=device)
-        ms_plain = timed(lambda: lap.la_prefill_fwd(q, k, v, sl, p.scale, h0=h0, o=o, h_final=hf, seq_len=T,
-                                                    stream=stream))
-        ms_seg = timed(lambda: lap.la_prefill_fwd_segmented(q, k, v, sl, p.scale, h0=h0, o=o, h_final=hf,
-                                                            seq_len=T, segment_len=0, workspace=ws, stream=stream))
+        if Dw == 256:
+            nbytes_ws, seg = lap.la_prefill_d256_segmented_workspace(B, T, B, HV, False, 0, True)
+            ws = torch.empty(max(nbytes_ws, 1), dtype=torch.uint8, device=device)
+            ws_plain = torch.empty(lap.la_prefill_d256_workspace(B, T, B, HV, True), dtype=torch.uint8, device=device)
+            ms_plain = timed(lambda: lap.la_prefill_fwd_d256(q, k, v, sl, p.scale, h0=h0, o=o, h_final=hf, seq_len=T,
+                                                             workspace=ws_plain, stream=stream))
+            ms_seg = timed(lambda: lap.la_prefill_fwd_d256_segmented(q, k, v, sl, p.scale, h0=h0, o=o, h_final=hf,
+                                                                     seq_len=T, segment_len=0, workspace=ws,
+                                                                     stream=stream))
+        else:
+            nbytes_ws, seg = lap.la_prefill_segmented_workspace(B, T, B, HV, False, 0)
+            ws = torch.empty(max(nbytes_ws, 1), dtype=torch.uint8, device=device)
+            ms_plain = timed(lambda: lap.la_prefill_fwd(q, k, v, sl, p.scale, h0=h0, o=o, h_final=hf, seq_len=T,
+                                                        stream=stream))
+            ms_seg = timed(lambda: lap.la_prefill_fwd_segmented(q, k, v, sl, p.scale, h0=h0, o=o, h_final=hf,
+                                                                seq_len=T, segment_len=0, workspace=ws, stream=stream))
         toks, nbytes, flops = workload_roofline(p)
         t_roof = max(nbytes / (hbm * 1e9), flops / (tflops * 1e12))
         cpu = None if args.no_cpu_baseline else oracle_forward_baseline(p, ms_seg)

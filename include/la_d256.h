@@ -33,6 +33,7 @@
 #include <stdint.h>
 
 #include "la_prefill.h"
+#include "la_segment.h"
 
 #ifdef __cplusplus
 extern "C" {
@@ -65,6 +66,34 @@ la_status la_prefill_fwd_d256(const void* q, const void* k, const void* v, const
                               const float* h0, const int32_t* state_indices, const int32_t* cu_seqlens, void* o,
                               float* h_final, int B, int T, int N, int H, int HV, int D, int V, int pool_size,
                               void* workspace, size_t workspace_bytes, int* dev_error, void* stream);
+
+/*
+ * la_prefill_d256_segmented_workspace -- device workspace bytes la_prefill_fwd_d256_segmented
+ * needs: la_prefill_d256_workspace's, plus la_prefill_segmented_workspace's for the 4 HV block
+ * heads (B, T, N, packed and segment_len as there; 0 = automatic, resolved with the CURRENT
+ * device's SM count over the 4 N HV block chains).  Writes the resolved segment length to
+ * *resolved_segment_len (nullable; 0 when no segmentation is done).  Errors as the two queries.
+ */
+la_status la_prefill_d256_segmented_workspace(int B, int T, int N, int HV, int packed, int segment_len, int has_state,
+                                              size_t* bytes, int* resolved_segment_len);
+
+/*
+ * la_prefill_fwd_d256_segmented -- la_prefill_fwd_d256 with every sequence cut into segments of
+ * segment_len tokens that run in parallel from their exact initial states (include/la_segment.h),
+ * for batches with few (sequence, value head) chains.  The segmented prefill runs on the block
+ * heads (4 HV per sequence), so its local states, scan and chunkwise pass are those of D = 128;
+ * the sum of the key halves and the final blocks follow as in la_prefill_fwd_d256.  Every
+ * sequence, however short, takes this path (no tokenwise path).
+ *
+ * Arguments as la_prefill_fwd_d256, plus segment_len (as given to the workspace query); the
+ * workspace is at least la_prefill_d256_segmented_workspace(...) bytes.  Outputs equal
+ * la_prefill_fwd_d256's up to FP32 rounding order.  Returns as la_prefill_fwd_d256.
+ */
+la_status la_prefill_fwd_d256_segmented(const void* q, const void* k, const void* v, const float* slopes, float scale,
+                                        const float* h0, const int32_t* state_indices, const int32_t* cu_seqlens,
+                                        void* o, float* h_final, int B, int T, int N, int H, int HV, int D, int V,
+                                        int pool_size, int segment_len, void* workspace, size_t workspace_bytes,
+                                        int* dev_error, void* stream);
 
 #ifdef __cplusplus
 }

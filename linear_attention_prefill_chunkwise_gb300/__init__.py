@@ -20,6 +20,7 @@ from . import build as _build
 
 __all__ = ["la_prefill_fwd", "la_prefill_fwd_segmented", "la_prefill_fwd_segmented_static", "la_prefill_bwd",
            "la_prefill_bwd_workspace", "la_prefill_fwd_d256", "la_prefill_d256_workspace",
+           "la_prefill_fwd_d256_segmented", "la_prefill_d256_segmented_workspace",
            "la_prefill_segmented_workspace", "la_decode_mtp", "la_verify", "la_commit", "LaError", "load_library", "SCHEDULES", "DEV_ERR_BAD_SEQLENS",
            "DEV_ERR_BAD_INDEX", "DEV_ERR_TIMEOUT", "EXPORTED_SYMBOLS"]
 
@@ -31,7 +32,8 @@ EXPORTED_SYMBOLS = ("la_prefill_fwd", "la_status_string", "la_last_error", "la_p
                     "la_decode_mtp", "la_verify",
                     "la_commit", "la_prefill_segmented_workspace", "la_prefill_fwd_segmented",
                     "la_prefill_fwd_segmented_static", "la_prefill_bwd_workspace", "la_prefill_bwd",
-                    "la_prefill_d256_workspace", "la_prefill_fwd_d256")
+                    "la_prefill_d256_workspace", "la_prefill_fwd_d256", "la_prefill_d256_segmented_workspace",
+                    "la_prefill_fwd_d256_segmented")
 
 _lock = threading.Lock()
 _lib = None
@@ -92,6 +94,11 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
             lib.la_prefill_fwd_d256.argtypes = [vp, vp, vp, fp, ctypes.c_float, fp, i32p, i32p, vp, fp] + \
                 [ctypes.c_int] * 8 + [vp, ctypes.c_size_t, vp, vp]
             lib.la_prefill_fwd_d256.restype = ctypes.c_int
+            lib.la_prefill_d256_segmented_workspace.argtypes = [ctypes.c_int] * 7 + [vp, vp]
+            lib.la_prefill_d256_segmented_workspace.restype = ctypes.c_int
+            lib.la_prefill_fwd_d256_segmented.argtypes = [vp, vp, vp, fp, ctypes.c_float, fp, i32p, i32p, vp, fp] + \
+                [ctypes.c_int] * 9 + [vp, ctypes.c_size_t, vp, vp]
+            lib.la_prefill_fwd_d256_segmented.restype = ctypes.c_int
             _lib = lib
         return _lib
 
@@ -285,6 +292,42 @@ def la_prefill_fwd_d256(q, k, v, slopes, scale, h0=None, state_indices=None, cu_
                                  _ptr(state_indices), _ptr(cu_seqlens), _ptr(o), _ptr(h_final), int(B), int(T),
                                  int(N), int(H), int(HV), int(D), int(V), int(pool), _ptr(workspace),
                                  ctypes.c_size_t(workspace.numel()), _ptr(dev_error), ctypes.c_void_p(stream))
+    if st != 0:
+        _raise(lib, st)
+    return o
+
+
+def la_prefill_d256_segmented_workspace(B, T, N, HV, packed, segment_len, has_state):
+    """(bytes, resolved segment length) of device workspace la_prefill_fwd_d256_segmented needs."""
+    lib = load_library()
+    nbytes, res = ctypes.c_size_t(0), ctypes.c_int(0)
+    st = lib.la_prefill_d256_segmented_workspace(int(B), int(T), int(N), int(HV), int(bool(packed)), int(segment_len),
+                                                 int(bool(has_state)), ctypes.byref(nbytes), ctypes.byref(res))
+    if st != 0:
+        _raise(lib, st)
+    return nbytes.value, res.value
+
+
+def la_prefill_fwd_d256_segmented(q, k, v, slopes, scale, h0=None, state_indices=None, cu_seqlens=None, o=None,
+                                  h_final=None, seq_len=None, segment_len=0, workspace=None, dev_error=None,
+                                  stream=None):
+    """la_prefill_fwd_d256 with every sequence cut into segments of ``segment_len`` tokens (0 =
+    automatic) that run in parallel from their exact initial states; ``workspace`` as
+    la_prefill_d256_segmented_workspace(...)[0] bytes, allocated here when None.  Returns ``o``."""
+    import torch
+    lib = load_library()
+    o, B, T, N, H, HV, D, V, pool, stream = _prefill_args(q, k, v, slopes, h0, state_indices, cu_seqlens, o,
+                                                          h_final, seq_len, dev_error, stream)
+    if workspace is None:
+        nbytes, _ = la_prefill_d256_segmented_workspace(B, T, N, HV, cu_seqlens is not None, segment_len,
+                                                        h0 is not None or h_final is not None)
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+    _check(workspace, "workspace", torch.uint8, 1)
+    st = lib.la_prefill_fwd_d256_segmented(_ptr(q), _ptr(k), _ptr(v), _ptr(slopes), ctypes.c_float(scale), _ptr(h0),
+                                           _ptr(state_indices), _ptr(cu_seqlens), _ptr(o), _ptr(h_final), int(B),
+                                           int(T), int(N), int(H), int(HV), int(D), int(V), int(pool),
+                                           int(segment_len), _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+                                           _ptr(dev_error), ctypes.c_void_p(stream))
     if st != 0:
         _raise(lib, st)
     return o

@@ -18,6 +18,7 @@
 #include <cstdint>
 
 #include "../../include/la_d256.h"
+#include "../../include/la_segment.h"
 #include "la_decode_kernels.cuh"
 #include "la_host_common.h"
 #include "la_prefill_internal.h"
@@ -170,6 +171,95 @@ la_status launched(const char* what) {
   return LA_OK;
 }
 
+// The checks of la_prefill_fwd_d256 and its segmented form: D = V = 256, the head counts, and
+// la_prefill_fwd's checks on the same memory seen as 2 H q/k and 2 HV value heads of 128.
+la_status check_args(const void* q, const void* k, const void* v, const float* slopes, const float* h0,
+                     const int32_t* state_indices, const int32_t* cu_seqlens, const void* o, const float* h_final,
+                     int B, int T, int N, int H, int HV, int D, int V, int pool_size, const int* dev_error,
+                     bool* nothing) {
+  using la_host::fail;
+  if (D != 256 || V != 256) return fail(LA_ERR_UNSUPPORTED, "the D = 256 prefill needs D == V == 256 (got D=%d, V=%d)", D, V);
+  if (H <= 0 || HV <= 0) return fail(LA_ERR_INVALID_ARGUMENT, "H and HV must be positive (got %d, %d)", H, HV);
+  if (HV % H != 0) return fail(LA_ERR_UNSUPPORTED, "HV (%d) must be a multiple of H (%d)", HV, H);
+  const la_status st = la_host::check_prefill_args(q, k, v, slopes, h0, state_indices, cu_seqlens, o, h_final, B, T,
+                                                   N, 2 * H, 2 * HV, kHalf, kHalf, pool_size, dev_error, nothing);
+  if (st != LA_OK || *nothing) return st;
+  if (static_cast<int64_t>(N) * 4 * HV > INT32_MAX) return fail(LA_ERR_UNSUPPORTED, "4*N*HV too large");
+  return LA_OK;
+}
+
+// The block path of a call whose arguments are checked: the per-virtual-head tables, the h0
+// blocks, the D = 128 chunkwise kernel (segment_len < 0) or the segmented prefill
+// (segment_len >= 0, its seg_bytes of workspace after the block path's) over the 4 HV virtual
+// heads, the sum of the key halves and the final blocks.
+la_status blocks_path(const void* q, const void* k, const void* v, const float* slopes, float scale, const float* h0,
+                      const int32_t* state_indices, const int32_t* cu_seqlens, void* o, float* h_final, int B, int T,
+                      int N, int H, int HV, int pool_size, int segment_len, size_t seg_bytes, void* workspace,
+                      size_t workspace_bytes, int* dev_error, void* stream) {
+  using la_host::fail;
+  la_status st;
+  const int64_t tokens = static_cast<int64_t>(B) * T;
+  const int pool = la_host::effective_pool_size(h0, h_final, state_indices, pool_size, N);
+  const bool has_state = h0 || h_final;
+  const Layout l = layout(tokens, N, HV, has_state);
+  const size_t need = l.bytes + seg_bytes;
+  if (!workspace || workspace_bytes < need)
+    return fail(LA_ERR_INVALID_ARGUMENT, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
+  if (reinterpret_cast<uintptr_t>(workspace) % 256)
+    return fail(LA_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
+  if ((st = la_host::check_prefill_disjoint(q, k, v, slopes, h0, state_indices, cu_seqlens, o, h_final, dev_error, B,
+                                            T, N, H, HV, 256, 256, pool_size, workspace, need)) != LA_OK)
+    return st;
+  la_host::DeviceState* ds = nullptr;
+  if ((st = la_host::current_device(g_dev, &ds, setup_kernels)) != LA_OK) return st;
+
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* part = reinterpret_cast<float*>(ws + l.part);
+  float* blocks = has_state ? reinterpret_cast<float*>(ws + l.blocks) : nullptr;
+  float* slopes_q = reinterpret_cast<float*>(ws + l.slopes_q);
+  int32_t* slot_q = reinterpret_cast<int32_t*>(ws + l.slot_q);
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int G = HV / H;
+
+  // 1. per-virtual-head slopes, the sequences that run, and the h0 blocks
+  TableParams tp{slopes, state_indices, slopes_q, slot_q, dev_error, N, HV, G, pool};
+  const int tgrid = static_cast<int>(((N > 4 * HV ? N : 4 * HV) + kThreads - 1) / kThreads);
+  la_d256_tables_kernel<<<tgrid, kThreads, 0, s>>>(tp);
+  if ((st = launched("d256 tables")) != LA_OK) return st;
+  BlockParams bp{h0, h_final, blocks, state_indices, cu_seqlens, N, HV, G, pool, static_cast<int>(tokens)};
+  const dim3 bgrid(static_cast<unsigned>(N) * 4 * HV, kHalf / kRowsPerCta);
+  if (h0) {
+    la_d256_blocks_kernel<true><<<bgrid, kThreads, 0, s>>>(bp);
+    if ((st = launched("d256 gather")) != LA_OK) return st;
+  }
+
+  // 2. the D = 128 chunkwise kernel over the 4 HV virtual heads, FP32 parts of o, states in place;
+  //    or the segmented prefill of the same virtual problem, with its workspace after ours
+  if (segment_len < 0)
+    st = la_internal::chunkwise(q, k, v, slopes_q, scale, h0 ? blocks : nullptr, slot_q, cu_seqlens, nullptr, part,
+                                h_final ? blocks : nullptr, B, T, N, 2 * H, 4 * HV, 2 * HV, kHalf, N, false,
+                                dev_error, stream, 2 * G);
+  else
+    st = la_internal::segmented_f32(q, k, v, slopes_q, scale, h0 ? blocks : nullptr, slot_q, cu_seqlens, part,
+                                    h_final ? blocks : nullptr, B, T, N, 2 * H, 4 * HV, kHalf, N, segment_len,
+                                    seg_bytes ? ws + l.bytes : nullptr, seg_bytes, dev_error, stream, 2 * G);
+  if (st != LA_OK) return st;
+
+  // 3. o = the sum over the key halves, rounded once; the final blocks to h_final
+  if (tokens > 0) {
+    SumParams sp{part, static_cast<__nv_bfloat16*>(o), cu_seqlens, state_indices, N, cu_seqlens ? 0 : T,
+                        static_cast<int>(tokens), pool, HV, G};
+    const int rgrid = static_cast<int>(tokens < 16 * ds->sms ? tokens : 16 * ds->sms);
+    la_d256_sum_kernel<<<rgrid, kThreads, 0, s>>>(sp);
+    if ((st = launched("d256 sum")) != LA_OK) return st;
+  }
+  if (h_final) {
+    la_d256_blocks_kernel<false><<<bgrid, kThreads, 0, s>>>(bp);
+    if ((st = launched("d256 scatter")) != LA_OK) return st;
+  }
+  return LA_OK;
+}
+
 }  // namespace la256
 
 extern "C" {
@@ -192,18 +282,11 @@ la_status la_prefill_fwd_d256(const void* q, const void* k, const void* v, const
                               void* workspace, size_t workspace_bytes, int* dev_error, void* stream) {
   using la_host::fail;
   la_host::g_last_error[0] = '\0';
-  if (D != 256 || V != 256)
-    return fail(LA_ERR_UNSUPPORTED, "la_prefill_fwd_d256 needs D == V == 256 (got D=%d, V=%d)", D, V);
-  if (H <= 0 || HV <= 0) return fail(LA_ERR_INVALID_ARGUMENT, "H and HV must be positive (got %d, %d)", H, HV);
-  if (HV % H != 0) return fail(LA_ERR_UNSUPPORTED, "HV (%d) must be a multiple of H (%d)", HV, H);
-  // la_prefill_fwd's checks on the same memory seen as 2 H q/k and 2 HV value heads of 128
   bool nothing = false;
-  la_status st = la_host::check_prefill_args(q, k, v, slopes, h0, state_indices, cu_seqlens, o, h_final, B, T, N,
-                                             2 * H, 2 * HV, la256::kHalf, la256::kHalf, pool_size, dev_error,
-                                             &nothing);
+  la_status st = la256::check_args(q, k, v, slopes, h0, state_indices, cu_seqlens, o, h_final, B, T, N, H, HV, D, V,
+                                   pool_size, dev_error, &nothing);
   if (st != LA_OK || nothing) return st;
   const int64_t tokens = static_cast<int64_t>(B) * T;
-  if (static_cast<int64_t>(N) * 4 * HV > INT32_MAX) return fail(LA_ERR_UNSUPPORTED, "4*N*HV too large");
   la_host::DeviceState* ds = nullptr;
   const int pool = la_host::effective_pool_size(h0, h_final, state_indices, pool_size, N);
 
@@ -241,56 +324,47 @@ la_status la_prefill_fwd_d256(const void* q, const void* k, const void* v, const
     return LA_OK;
   }
 
-  const bool has_state = h0 || h_final;
-  const la256::Layout l = la256::layout(tokens, N, HV, has_state);
-  if (!workspace || workspace_bytes < l.bytes)
-    return fail(LA_ERR_INVALID_ARGUMENT, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, l.bytes);
-  if (reinterpret_cast<uintptr_t>(workspace) % 256)
-    return fail(LA_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
-  if ((st = la_host::check_prefill_disjoint(q, k, v, slopes, h0, state_indices, cu_seqlens, o, h_final, dev_error, B,
-                                            T, N, H, HV, D, V, pool_size, workspace, l.bytes)) != LA_OK)
-    return st;
-  if ((st = la_host::current_device(la256::g_dev, &ds, la256::setup_kernels)) != LA_OK) return st;
+  return la256::blocks_path(q, k, v, slopes, scale, h0, state_indices, cu_seqlens, o, h_final, B, T, N, H, HV,
+                            pool_size, -1, 0, workspace, workspace_bytes, dev_error, stream);
+}
 
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  float* part = reinterpret_cast<float*>(ws + l.part);
-  float* blocks = has_state ? reinterpret_cast<float*>(ws + l.blocks) : nullptr;
-  float* slopes_q = reinterpret_cast<float*>(ws + l.slopes_q);
-  int32_t* slot_q = reinterpret_cast<int32_t*>(ws + l.slot_q);
-  const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int G = HV / H;
-
-  // 1. per-virtual-head slopes, the sequences that run, and the h0 blocks
-  la256::TableParams tp{slopes, state_indices, slopes_q, slot_q, dev_error, N, HV, G, pool};
-  const int tgrid = static_cast<int>(((N > 4 * HV ? N : 4 * HV) + la256::kThreads - 1) / la256::kThreads);
-  la256::la_d256_tables_kernel<<<tgrid, la256::kThreads, 0, s>>>(tp);
-  if ((st = la256::launched("d256 tables")) != LA_OK) return st;
-  la256::BlockParams bp{h0, h_final, blocks, state_indices, cu_seqlens, N, HV, G, pool, static_cast<int>(tokens)};
-  const dim3 bgrid(static_cast<unsigned>(N) * 4 * HV, la256::kHalf / la256::kRowsPerCta);
-  if (h0) {
-    la256::la_d256_blocks_kernel<true><<<bgrid, la256::kThreads, 0, s>>>(bp);
-    if ((st = la256::launched("d256 gather")) != LA_OK) return st;
-  }
-
-  // 2. the D = 128 chunkwise kernel over the 4 HV virtual heads, FP32 parts of o, states in place
-  st = la_internal::chunkwise(q, k, v, slopes_q, scale, h0 ? blocks : nullptr, slot_q, cu_seqlens, nullptr, part,
-                              h_final ? blocks : nullptr, B, T, N, 2 * H, 4 * HV, 2 * HV, la256::kHalf, N, false,
-                              dev_error, stream, 2 * G);
+la_status la_prefill_d256_segmented_workspace(int B, int T, int N, int HV, int packed, int segment_len, int has_state,
+                                              size_t* bytes, int* resolved_segment_len) {
+  using la_host::fail;
+  la_host::g_last_error[0] = '\0';
+  if (!bytes) return fail(LA_ERR_INVALID_ARGUMENT, "bytes is null");
+  if (B < 0 || T < 0 || N < 0 || HV <= 0) return fail(LA_ERR_INVALID_ARGUMENT, "B, T, N >= 0 and HV > 0 required");
+  const int64_t tokens = static_cast<int64_t>(B) * T;
+  if (tokens + 64 > INT32_MAX || static_cast<int64_t>(N) * 4 * HV > INT32_MAX)
+    return fail(LA_ERR_UNSUPPORTED, "B*T or 4*N*HV too large");
+  size_t seg = 0;
+  int resolved = 0;
+  const la_status st = la_prefill_segmented_workspace(B, T, N, 4 * HV, packed, segment_len, &seg, &resolved);
   if (st != LA_OK) return st;
-
-  // 3. o = the sum over the key halves, rounded once; the final blocks to h_final
-  if (tokens > 0) {
-    la256::SumParams sp{part, static_cast<__nv_bfloat16*>(o), cu_seqlens, state_indices, N, cu_seqlens ? 0 : T,
-                        static_cast<int>(tokens), pool, HV, G};
-    const int rgrid = static_cast<int>(tokens < 16 * ds->sms ? tokens : 16 * ds->sms);
-    la256::la_d256_sum_kernel<<<rgrid, la256::kThreads, 0, s>>>(sp);
-    if ((st = la256::launched("d256 sum")) != LA_OK) return st;
-  }
-  if (h_final) {
-    la256::la_d256_blocks_kernel<false><<<bgrid, la256::kThreads, 0, s>>>(bp);
-    if ((st = la256::launched("d256 scatter")) != LA_OK) return st;
-  }
+  *bytes = la256::layout(tokens, N, HV, has_state != 0).bytes + seg;
+  if (resolved_segment_len) *resolved_segment_len = resolved;
   return LA_OK;
+}
+
+la_status la_prefill_fwd_d256_segmented(const void* q, const void* k, const void* v, const float* slopes, float scale,
+                                        const float* h0, const int32_t* state_indices, const int32_t* cu_seqlens,
+                                        void* o, float* h_final, int B, int T, int N, int H, int HV, int D, int V,
+                                        int pool_size, int segment_len, void* workspace, size_t workspace_bytes,
+                                        int* dev_error, void* stream) {
+  la_host::g_last_error[0] = '\0';
+  bool nothing = false;
+  la_status st = la256::check_args(q, k, v, slopes, h0, state_indices, cu_seqlens, o, h_final, B, T, N, H, HV, D, V,
+                                   pool_size, dev_error, &nothing);
+  if (st != LA_OK || nothing) return st;
+  // the segmented workspace of the virtual problem (4 HV heads of 128); 0 when the plan has no
+  // segments (every chain then runs whole, as in la_prefill_fwd_d256's block path)
+  size_t seg = 0;
+  int resolved = 0;
+  if ((st = la_prefill_segmented_workspace(B, T, N, 4 * HV, cu_seqlens != nullptr, segment_len, &seg, &resolved)) !=
+      LA_OK)
+    return st;
+  return la256::blocks_path(q, k, v, slopes, scale, h0, state_indices, cu_seqlens, o, h_final, B, T, N, H, HV,
+                            pool_size, segment_len, seg, workspace, workspace_bytes, dev_error, stream);
 }
 
 }  // extern "C"

@@ -28,6 +28,15 @@ la_status chunkwise(const void* q, const void* k, const void* v, const float* sl
                     int B, int T, int N, int H, int HV, int v_heads, int D, int pool_size, bool reverse,
                     int* dev_error, void* stream, int v_fold = 0);
 
+// The segmented prefill (include/la_segment.h) with FP32 output parts and the value-head fold
+// vfold (v with HV / 2 heads), on arguments the caller has checked: the D = 256 prefill's view
+// of its problem.  The workspace is la_prefill_segmented_workspace(B, T, N, HV, ...) bytes; a
+// plan without segments runs chunkwise() directly and needs none.
+la_status segmented_f32(const void* q, const void* k, const void* v, const float* slopes, float scale, const float* h0,
+                        const int32_t* state_indices, const int32_t* cu_seqlens, float* o_f32, float* h_final, int B,
+                        int T, int N, int H, int HV, int D, int pool_size, int segment_len, void* workspace,
+                        size_t workspace_bytes, int* dev_error, void* stream, int vfold);
+
 
 // The sequence of token row r (fixed length T, or the packed bounds cu_seqlens), or -1 when the
 // row belongs to no sequence that the chunkwise runs computed (bad bounds, a padded or invalid

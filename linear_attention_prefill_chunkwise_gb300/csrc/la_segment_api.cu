@@ -11,6 +11,7 @@
 
 #include "../../include/la_segment.h"
 #include "la_host_common.h"
+#include "la_prefill_internal.h"
 #include "la_segment_kernels.cuh"
 
 namespace {
@@ -118,6 +119,106 @@ la_status launched(const char* what, cudaError_t launch_result = cudaSuccess) {
   return LA_OK;
 }
 
+// Steps 1-5 of a segmented call on validated arguments and a workspace of at least pl.bytes.
+// With o_f32 (the D = 256 decomposition) the output is FP32 parts, and v is read through the
+// value-head fold vfold (v then has HV / 2 heads).
+la_status seg_launch(const SegPlan& pl, la_host::DeviceState* ds, const void* q, const void* k, const void* v,
+                     const float* slopes, float scale, const float* h0, const int32_t* state_indices,
+                     const int32_t* cu_seqlens, void* o, float* o_f32, float* h_final, int B, int T, int N, int H,
+                     int HV, int D, int V, int pool_size, void* workspace, int* dev_error, void* stream, int vfold) {
+  la_status st;
+  const int64_t tokens = static_cast<int64_t>(B) * T;
+  const int nseg = static_cast<int>(pl.nseg_max);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  float* states = reinterpret_cast<float*>(ws + pl.off_states);
+  int32_t* seg_cu = reinterpret_cast<int32_t*>(ws + pl.off_seg_cu);
+  int32_t* seg_slot = reinterpret_cast<int32_t*>(ws + pl.off_seg_slot);
+  int32_t* seg_flags = reinterpret_cast<int32_t*>(ws + pl.off_seg_flags);
+  int32_t* seq_seg0 = reinterpret_cast<int32_t*>(ws + pl.off_seq_seg0);
+  int32_t* seq_slot = reinterpret_cast<int32_t*>(ws + pl.off_seq_slot);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  CUtensorMap tm_k, tm_v;
+  memset(&tm_k, 0, sizeof(tm_k));
+  memset(&tm_v, 0, sizeof(tm_v));
+  if ((st = la_host::encode_bf16_rows_map(&tm_k, k, tokens, H, "k", D)) != LA_OK) return st;
+  if ((st = la_host::encode_bf16_rows_map(&tm_v, v, tokens, vfold ? HV / 2 : HV, "v", D)) != LA_OK) return st;
+
+  // 1. segment table
+  las::PlanParams pp;
+  pp.cu_seqlens = cu_seqlens;
+  pp.state_indices = state_indices;
+  pp.dev_error = dev_error;
+  pp.seg_cu = seg_cu;
+  pp.seg_slot = seg_slot;
+  pp.seg_flags = seg_flags;
+  pp.seq_seg0 = seq_seg0;
+  pp.seq_slot = seq_slot;
+  pp.N = N;
+  pp.T = cu_seqlens ? 0 : T;
+  pp.tokens = static_cast<int>(tokens);
+  pp.S = pl.S;
+  pp.S_last = pl.S_last;
+  pp.nseg_max = nseg;
+  pp.pool_size = la_host::effective_pool_size(h0, h_final, state_indices, pool_size, N);
+  if ((st = launched("segment plan", la_host::launch_pdl(las::la_segment_plan_kernel, 1, las::kPlanThreads, 0, s,
+                                                         pp))) != LA_OK)
+    return st;
+
+  // 2. local states of the segments that are not the last of their sequence
+  las::StateParams sp;
+  sp.slopes = slopes;
+  sp.seg_cu = seg_cu;
+  sp.seg_flags = seg_flags;
+  sp.states = states;
+  sp.dev_error = dev_error;
+  sp.HV = HV;
+  sp.G = HV / H;
+  sp.num_units = nseg * HV;
+  sp.vfold = vfold;
+  const int grid_a = sp.num_units < ds->sms ? sp.num_units : ds->sms;
+  if ((st = launched("segment state",
+                     la_host::launch_pdl(D == 128 ? las::la_segment_state_kernel<128> : las::la_segment_state_kernel<64>,
+                                         grid_a, las::kStThreads, state_smem_bytes(), s, tm_k, tm_v, sp))) != LA_OK)
+    return st;
+
+  // 3. initial state of every segment
+  las::CombineParams cp;
+  cp.slopes = slopes;
+  cp.h0 = h0;
+  cp.h_final = h_final;
+  cp.seg_cu = seg_cu;
+  cp.seq_seg0 = seq_seg0;
+  cp.seq_slot = seq_slot;
+  cp.states = states;
+  cp.HV = HV;
+  const dim3 grid_c(static_cast<unsigned>(N) * HV, D == 128 ? las::comb_split<128>() : las::comb_split<64>());
+  if ((st = launched("segment combine",
+                     la_host::launch_pdl(D == 128 ? las::la_segment_combine_kernel<128> : las::la_segment_combine_kernel<64>,
+                                         grid_c, las::kCombThreads, 0, s, cp))) != LA_OK)
+    return st;
+
+  // 4. the chunkwise prefill of every segment: a packed batch whose state pool is the
+  //    workspace (segment g reads its initial state from slot g and leaves its final one there)
+  if (o_f32)
+    st = la_internal::chunkwise(q, k, v, slopes, scale, states, seg_slot, seg_cu, nullptr, o_f32,
+                                h_final ? states : nullptr, 1, static_cast<int>(tokens), nseg, H, HV, HV / 2, D, nseg,
+                                false, dev_error, stream, vfold);
+  else
+    st = la_prefill_fwd(q, k, v, slopes, scale, states, seg_slot, seg_cu, o, h_final ? states : nullptr, 1,
+                        static_cast<int>(tokens), nseg, H, HV, D, V, nseg, LA_SCHED_AUTO, dev_error, stream);
+  if (st != LA_OK) return st;
+
+  // 5. final states
+  if (h_final) {
+    if ((st = launched("segment final",
+                       la_host::launch_pdl(D == 128 ? las::la_segment_final_kernel<128> : las::la_segment_final_kernel<64>,
+                                           grid_c, las::kCombThreads, 0, s, cp))) != LA_OK)
+      return st;
+  }
+  return LA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -174,90 +275,33 @@ la_status la_prefill_fwd_segmented(const void* q, const void* k, const void* v, 
   if (st != LA_OK) return st;
   if (!ds && (st = segment_device(&ds)) != LA_OK) return st;
 
-  const int64_t tokens = static_cast<int64_t>(B) * T;
-  const int nseg = static_cast<int>(pl.nseg_max);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  float* states = reinterpret_cast<float*>(ws + pl.off_states);
-  int32_t* seg_cu = reinterpret_cast<int32_t*>(ws + pl.off_seg_cu);
-  int32_t* seg_slot = reinterpret_cast<int32_t*>(ws + pl.off_seg_slot);
-  int32_t* seg_flags = reinterpret_cast<int32_t*>(ws + pl.off_seg_flags);
-  int32_t* seq_seg0 = reinterpret_cast<int32_t*>(ws + pl.off_seq_seg0);
-  int32_t* seq_slot = reinterpret_cast<int32_t*>(ws + pl.off_seq_slot);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-
-  CUtensorMap tm_k, tm_v;
-  memset(&tm_k, 0, sizeof(tm_k));
-  memset(&tm_v, 0, sizeof(tm_v));
-  if ((st = la_host::encode_bf16_rows_map(&tm_k, k, tokens, H, "k", D)) != LA_OK) return st;
-  if ((st = la_host::encode_bf16_rows_map(&tm_v, v, tokens, HV, "v", D)) != LA_OK) return st;
-
-  // 1. segment table
-  las::PlanParams pp;
-  pp.cu_seqlens = cu_seqlens;
-  pp.state_indices = state_indices;
-  pp.dev_error = dev_error;
-  pp.seg_cu = seg_cu;
-  pp.seg_slot = seg_slot;
-  pp.seg_flags = seg_flags;
-  pp.seq_seg0 = seq_seg0;
-  pp.seq_slot = seq_slot;
-  pp.N = N;
-  pp.T = cu_seqlens ? 0 : T;
-  pp.tokens = static_cast<int>(tokens);
-  pp.S = pl.S;
-  pp.S_last = pl.S_last;
-  pp.nseg_max = nseg;
-  pp.pool_size = la_host::effective_pool_size(h0, h_final, state_indices, pool_size, N);
-  if ((st = launched("segment plan", la_host::launch_pdl(las::la_segment_plan_kernel, 1, las::kPlanThreads, 0, s,
-                                                         pp))) != LA_OK)
-    return st;
-
-  // 2. local states of the segments that are not the last of their sequence
-  las::StateParams sp;
-  sp.slopes = slopes;
-  sp.seg_cu = seg_cu;
-  sp.seg_flags = seg_flags;
-  sp.states = states;
-  sp.dev_error = dev_error;
-  sp.HV = HV;
-  sp.G = HV / H;
-  sp.num_units = nseg * HV;
-  const int grid_a = sp.num_units < ds->sms ? sp.num_units : ds->sms;
-  if ((st = launched("segment state",
-                     la_host::launch_pdl(D == 128 ? las::la_segment_state_kernel<128> : las::la_segment_state_kernel<64>,
-                                         grid_a, las::kStThreads, state_smem_bytes(), s, tm_k, tm_v, sp))) != LA_OK)
-    return st;
-
-  // 3. initial state of every segment
-  las::CombineParams cp;
-  cp.slopes = slopes;
-  cp.h0 = h0;
-  cp.h_final = h_final;
-  cp.seg_cu = seg_cu;
-  cp.seq_seg0 = seq_seg0;
-  cp.seq_slot = seq_slot;
-  cp.states = states;
-  cp.HV = HV;
-  const dim3 grid_c(static_cast<unsigned>(N) * HV, D == 128 ? las::comb_split<128>() : las::comb_split<64>());
-  if ((st = launched("segment combine",
-                     la_host::launch_pdl(D == 128 ? las::la_segment_combine_kernel<128> : las::la_segment_combine_kernel<64>,
-                                         grid_c, las::kCombThreads, 0, s, cp))) != LA_OK)
-    return st;
-
-  // 4. the chunkwise prefill of every segment: a packed batch whose state pool is the
-  //    workspace (segment g reads its initial state from slot g and leaves its final one there)
-  st = la_prefill_fwd(q, k, v, slopes, scale, states, seg_slot, seg_cu, o, h_final ? states : nullptr, 1,
-                      static_cast<int>(tokens), nseg, H, HV, D, V, nseg, LA_SCHED_AUTO, dev_error, stream);
-  if (st != LA_OK) return st;
-
-  // 5. final states
-  if (h_final) {
-    if ((st = launched("segment final",
-                       la_host::launch_pdl(D == 128 ? las::la_segment_final_kernel<128> : las::la_segment_final_kernel<64>,
-                                           grid_c, las::kCombThreads, 0, s, cp))) != LA_OK)
-      return st;
-  }
-  return LA_OK;
+  return seg_launch(pl, ds, q, k, v, slopes, scale, h0, state_indices, cu_seqlens, o, nullptr, h_final, B, T, N, H,
+                    HV, D, V, pool_size, workspace, dev_error, stream, 0);
 }
 
 }  // extern "C"
+
+namespace la_internal {
+
+la_status segmented_f32(const void* q, const void* k, const void* v, const float* slopes, float scale, const float* h0,
+                        const int32_t* state_indices, const int32_t* cu_seqlens, float* o_f32, float* h_final, int B,
+                        int T, int N, int H, int HV, int D, int pool_size, int segment_len, void* workspace,
+                        size_t workspace_bytes, int* dev_error, void* stream, int vfold) {
+  la_host::DeviceState* ds = nullptr;
+  la_status st = segment_device(&ds);
+  if (st != LA_OK) return st;
+  SegPlan pl;
+  if ((st = make_plan(B, T, N, HV, cu_seqlens != nullptr, segment_len, ds->sms, &pl)) != LA_OK) return st;
+  if (pl.S == 0)
+    return chunkwise(q, k, v, slopes, scale, h0, state_indices, cu_seqlens, nullptr, o_f32, h_final, B, T, N, H, HV,
+                     HV / 2, D, pool_size, false, dev_error, stream, vfold);
+  if (!workspace || workspace_bytes < pl.bytes)
+    return fail(LA_ERR_INVALID_ARGUMENT, "segment workspace too small: %zu bytes given, %zu needed", workspace_bytes,
+                pl.bytes);
+  if (reinterpret_cast<uintptr_t>(workspace) % kWsAlign)
+    return fail(LA_ERR_INVALID_ARGUMENT, "workspace must be 256-byte aligned");
+  return seg_launch(pl, ds, q, k, v, slopes, scale, h0, state_indices, cu_seqlens, nullptr, o_f32, h_final, B, T, N, H,
+                    HV, D, D, pool_size, workspace, dev_error, stream, vfold);
+}
+
+}  // namespace la_internal

@@ -177,6 +177,9 @@ struct StateParams {
   float* states;  // [nseg_max, HV, D v, D k]
   int* dev_error;
   int HV, G, num_units;  // num_units = nseg_max * HV, unit u = g * HV + hv
+  // > 0: v's head of value head hv is hv with the digit of weight vfold dropped,
+  // (hv / (2 vfold)) vfold + hv % vfold (the D = 256 decomposition; as the prefill kernel's)
+  int vfold;
 };
 
 constexpr int kStStages = 4;          // K/V ring depth
@@ -236,6 +239,7 @@ __device__ __forceinline__ void st_producer(StateSmem& sm, const StateParams& p,
   SegUnit w;
   for (int u = blockIdx.x; next_seg_unit(p, u, w); u += gridDim.x) {
     const int hq = w.hv / p.G;
+    const int vh = p.vfold ? (w.hv / (2 * p.vfold)) * p.vfold + w.hv % p.vfold : w.hv;
     for (int c = 0; c < w.nchunks; ++c, ++it) {
       const uint32_t s = it % kStStages;
       if (!lap::mbar_wait(&sm.empty[s], ((it / kStStages) & 1u) ^ 1u, abort)) goto drain;
@@ -243,7 +247,7 @@ __device__ __forceinline__ void st_producer(StateSmem& sm, const StateParams& p,
 #pragma unroll
       for (int h = 0; h < kBoxes; ++h) {
         lap::tma_load_2d(sm.k[s][h], tm_k, &sm.full[s], hq * kD + 64 * h, w.bos + c * kChunk);
-        lap::tma_load_2d(sm.v[s][h], tm_v, &sm.full[s], w.hv * kD + 64 * h, w.bos + c * kChunk);
+        lap::tma_load_2d(sm.v[s][h], tm_v, &sm.full[s], vh * kD + 64 * h, w.bos + c * kChunk);
       }
     }
   }

@@ -396,3 +396,37 @@ def test_d256_workspace_size():
     with pytest.raises(lap.LaError) as e:
         lap.la_prefill_d256_workspace(-1, 8, 1, 1, False)
     assert e.value.status == LA_INVALID
+
+
+def call_d256_seg(**over):
+    a = dict(q=Q, k=K, v=VV, slopes=SL, scale=1.0, h0=None, idx=None, cu=None, o=O, hf=None,
+             B=1, T=4096, N=1, H=2, HV=2, D=256, V=256, P=0, seg=512, ws=WS, wsb=1 << 34, err=None, stream=None)
+    a.update(over)
+    lib = lap.load_library()
+    return lib.la_prefill_fwd_d256_segmented(a["q"], a["k"], a["v"], a["slopes"], ctypes.c_float(a["scale"]), a["h0"],
+                                             a["idx"], a["cu"], a["o"], a["hf"], a["B"], a["T"], a["N"], a["H"],
+                                             a["HV"], a["D"], a["V"], a["P"], a["seg"], a["ws"], a["wsb"], a["err"],
+                                             a["stream"])
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(D=128, V=128), LA_UNSUPPORTED),
+    (dict(H=3, HV=4), LA_UNSUPPORTED),
+    (dict(seg=100), LA_INVALID),             # not a multiple of 64
+    (dict(ws=None), LA_INVALID),
+    (dict(wsb=1024), LA_INVALID),
+    (dict(ws=WS + 16), LA_INVALID),
+    (dict(ws=Q), LA_INVALID),                # the workspace overlaps an input
+])
+def test_d256_segmented_host_validation(over, status):
+    assert call_d256_seg(**over) == status
+    assert lap.load_library().la_last_error() != b""
+
+
+def test_d256_segmented_workspace_adds_the_segment_states():
+    # an explicit segment length needs no device: 1 x 4096 tokens, 2 value heads, 512-token segments
+    n_seg, s_seg = lap.la_prefill_d256_segmented_workspace(1, 4096, 1, 2, False, 512, True)
+    n_plain = lap.la_prefill_d256_workspace(1, 4096, 1, 2, True)
+    seg_bytes, s2 = lap.la_prefill_segmented_workspace(1, 4096, 1, 8, False, 512)
+    assert s_seg == s2 == 512
+    assert n_seg == n_plain + seg_bytes

@@ -160,3 +160,47 @@ def test_d256_in_a_cuda_graph():
         torch.cuda.synchronize()
         assert torch.equal(d["o"].view(torch.int16), ref["o"].view(torch.int16))
         assert torch.equal(d["h0"].view(torch.int32), ref["h0"].view(torch.int32))
+
+
+def run_d256_seg(p, d, segment_len, dev_error=None):
+    import linear_attention_prefill_chunkwise_gb300 as lap
+    return lap.la_prefill_fwd_d256_segmented(d["q"], d["k"], d["v"], d["slopes"], p.scale, h0=d["h0"],
+                                             state_indices=d["idx"], cu_seqlens=d["cu"], o=d["o"],
+                                             h_final=d["h_final"], seq_len=None if p.cu_seqlens is not None else p.T,
+                                             segment_len=segment_len, dev_error=dev_error)
+
+
+@pytest.mark.parametrize("name", ["fixed_gva_ragged", "packed_pool_padded_in_place", "one_chunk_segments_no_h0",
+                                  "no_final_state", "pool_out_of_place", "lambda_one", "lambda_zero",
+                                  "segment_longer_than_some"])
+def test_d256_segmented_full(name):
+    """The segmented prefill's edge cases (tests/test_gpu_segment.py) at D = V = 256."""
+    from test_gpu_segment import CASES
+    kw, seg = CASES[name]
+    p = W.custom(seed=zlib.crc32(("d256seg" + name).encode()) % 10000, name=name, D=256, **kw)
+    d = upload(p)
+    run_d256_seg(p, d, seg)
+    compare_full(p, d, f"D=256 segmented {name} S={seg}")
+
+
+def test_d256_segmented_auto_length_full():
+    """B=1, T=8192, H=HV=2: 8 block chains, so the automatic length segments."""
+    import linear_attention_prefill_chunkwise_gb300 as lap
+    p = W.custom(seed=4010, B=1, T=8192, H=2, HV=2, D=256)
+    nbytes, seg = lap.la_prefill_d256_segmented_workspace(1, 8192, 1, 2, False, 0, True)
+    assert seg > 0 and seg % 64 == 0 and seg < 8192
+    d = upload(p)
+    run_d256_seg(p, d, 0)
+    compare_full(p, d, f"D=256 segmented auto S={seg}")
+
+
+def test_d256_segmented_close_to_plain_d256():
+    p = W.custom(seed=4011, lengths=[3000, 17, 2100], H=1, HV=2, D=256)
+    d1 = upload(p)
+    run_d256(p, d1)
+    d2 = upload(p)
+    run_d256_seg(p, d2, 256)
+    torch.cuda.synchronize()
+    from harness import rel_rms
+    assert rel_rms(d2["o"].float().cpu().numpy(), d1["o"].float().cpu().numpy()) < 2e-3
+    assert rel_rms(d2["h_final"].cpu().numpy(), d1["h_final"].cpu().numpy()) < 1e-4
