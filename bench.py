@@ -492,7 +492,8 @@ def run_sweep(args):
         ("d64_short", short_d64_problem()),
         ("d256", W.custom(seed=3010, B=2, T=8192, H=16, HV=16, D=256,
                           name="D=V=256 fixed B=2 T=8192 H=HV=16, h0 + final state")),
-        ("d256_short", d256_short_problem())]
+        ("d256_short", d256_short_problem()),
+        ("d256_short_packed", short_d64_problem(D=256, H=16, seed=1106))]
     for label, extra_p in (work if args.sweep_what in ("all", "prefill") else ()):
         p = W.config(label) if extra_p is None else extra_p
         q, k, v = bf(p.q_bits), bf(p.k_bits), bf(p.v_bits)

@@ -27,8 +27,9 @@ namespace la256 {
 
 constexpr int kThreads = 256;
 constexpr int kHalf = 128;       // the kernel's head dimension
-constexpr int kRowsPerCta = 8;   // rows of a 128 x 128 block per copy CTA (kThreads float4)
-constexpr int kShortMax = 32;    // longest fixed-length sequence taken by the tokenwise kernel
+constexpr int kRowsPerStep = 8;  // rows of a 128 x 128 block per copy step (kThreads float4)
+constexpr int kShortMax = 32;    // longest sequence taken by the tokenwise kernel
+constexpr int kSplitAvg = 64;    // packed batches of at most this many tokens per sequence on average are split
 
 // The value head hv, value half a and key half b of virtual head u (G value heads per q/k head).
 struct Virt {
@@ -77,9 +78,11 @@ struct BlockParams {
   const int32_t* state_indices;
   const int32_t* cu_seqlens;
   int N, HV, G, pool, tokens;
+  int short_max;  // packed: sequences of at most this many tokens are skipped (-1: none)
 };
 
-// grid (N * 4 HV, 128 / kRowsPerCta): one float4 per thread.  gather: blocks[n][u] <- the
+// grid (N * 4 HV, y): a block's 128 rows split over y CTAs (y divides 16), one float4 per thread
+// and step.  gather: blocks[n][u] <- the
 // (a, b) block of h0[slot(n)][hv]; scatter: the (a, b) block of h_final[slot(n)][hv] <-
 // blocks[n][u], for sequences that ran (valid slot and, packed, valid bounds).
 template <bool kGather>
@@ -91,18 +94,22 @@ __global__ void __launch_bounds__(kThreads) la_d256_blocks_kernel(const BlockPar
     slot = __ldg(p.state_indices + n);
     if (slot < 0 || slot >= p.pool) return;
   }
-  if (!kGather && p.cu_seqlens) {
+  if (p.cu_seqlens && (!kGather || p.short_max >= 0)) {
     const int b = __ldg(p.cu_seqlens + n), e = __ldg(p.cu_seqlens + n + 1);
-    if (b < 0 || e < b || e > p.tokens) return;  // the chunkwise kernel skipped this sequence
+    if (!kGather && (b < 0 || e < b || e > p.tokens)) return;  // the chunkwise kernel skipped this sequence
+    if (e - b <= p.short_max) return;  // a sequence of the tokenwise kernel, which reads and writes whole states
   }
   const Virt x = virt(u, p.G);
-  const int r = blockIdx.y * kRowsPerCta + (threadIdx.x >> 5), c = 4 * (threadIdx.x & 31);
-  const size_t big = ((static_cast<size_t>(slot) * p.HV + x.hv) * 256 + x.a * kHalf + r) * 256 + x.b * kHalf + c;
-  const size_t small = ((static_cast<size_t>(n) * HVq + u) * kHalf + r) * kHalf + c;
-  if (kGather)
-    *reinterpret_cast<float4*>(p.blocks + small) = __ldg(reinterpret_cast<const float4*>(p.big_in + big));
-  else
-    *reinterpret_cast<float4*>(p.big_out + big) = *reinterpret_cast<const float4*>(p.blocks + small);
+  const int c = 4 * (threadIdx.x & 31);
+  const int rows = kHalf / static_cast<int>(gridDim.y), r0 = static_cast<int>(blockIdx.y) * rows;
+  for (int r = r0 + static_cast<int>(threadIdx.x >> 5); r < r0 + rows; r += kRowsPerStep) {
+    const size_t big = ((static_cast<size_t>(slot) * p.HV + x.hv) * 256 + x.a * kHalf + r) * 256 + x.b * kHalf + c;
+    const size_t small = ((static_cast<size_t>(n) * HVq + u) * kHalf + r) * kHalf + c;
+    if (kGather)
+      *reinterpret_cast<float4*>(p.blocks + small) = __ldg(reinterpret_cast<const float4*>(p.big_in + big));
+    else
+      *reinterpret_cast<float4*>(p.big_out + big) = *reinterpret_cast<const float4*>(p.blocks + small);
+  }
 }
 
 struct SumParams {
@@ -111,6 +118,7 @@ struct SumParams {
   const int32_t* cu_seqlens;
   const int32_t* state_indices;
   int N, T, tokens, pool, HV, G;
+  int short_max;  // packed: rows of sequences of at most this many tokens are skipped (-1: none)
 };
 
 // o[r][hv][128 a + c] = bf16(part[r][u(b = 0)][c] + part[r][u(b = 1)][c]) for the rows of
@@ -118,7 +126,9 @@ struct SumParams {
 __global__ void __launch_bounds__(kThreads) la_d256_sum_kernel(const SumParams p) {
   const int per_row = p.HV * 256 / 8, G2 = 2 * p.G;
   for (int r = blockIdx.x; r < p.tokens; r += gridDim.x) {
-    if (la_internal::row_sequence(p.cu_seqlens, p.state_indices, p.N, p.T, p.tokens, p.pool, r) < 0) continue;
+    const int n = la_internal::row_sequence(p.cu_seqlens, p.state_indices, p.N, p.T, p.tokens, p.pool, r);
+    if (n < 0) continue;
+    if (p.short_max >= 0 && __ldg(p.cu_seqlens + n + 1) - __ldg(p.cu_seqlens + n) <= p.short_max) continue;
     for (int i = threadIdx.x; i < per_row; i += kThreads) {
       const int hv = i >> 5, d = 8 * (i & 31);
       const int a = d >> 7, c = d & (kHalf - 1);
@@ -171,6 +181,41 @@ la_status launched(const char* what) {
   return LA_OK;
 }
 
+// The tokenwise kernel's D = 256 instance in prefill mode on whole states: every sequence of a
+// fixed-length batch (T <= kShortMax), or the sequences of at most kShortMax tokens of a packed one.
+la_status launch_tokenwise(const void* q, const void* k, const void* v, const float* slopes, float scale,
+                           const float* h0, const int32_t* state_indices, const int32_t* cu_seqlens, void* o,
+                           float* h_final, int T, int N, int H, int HV, int pool, int64_t tokens,
+                           la_host::DeviceState* ds, int* dev_error, void* stream) {
+  lad::Params tp{};
+  tp.q = static_cast<const __nv_bfloat16*>(q);
+  tp.k = static_cast<const __nv_bfloat16*>(k);
+  tp.v = static_cast<const __nv_bfloat16*>(v);
+  tp.slopes = slopes;
+  tp.state_indices = state_indices;
+  tp.o = static_cast<__nv_bfloat16*>(o);
+  tp.h0 = h0;
+  tp.h_final = h_final;
+  tp.cu_seqlens = cu_seqlens;
+  tp.dev_error = dev_error;
+  tp.scale = scale;
+  tp.B = N;
+  tp.T = cu_seqlens ? 0 : T;
+  tp.H = H;
+  tp.HV = HV;
+  tp.G = HV / H;
+  tp.pool_size = pool;
+  tp.num_tokens = static_cast<int>(tokens);
+  tp.short_max = kShortMax;
+  const int parts = N * HV * lad::split_of<256>();  // <= 4 N HV, checked by check_args
+  cudaError_t ce = la_host::launch_pdl(lad::la_tokenwise_kernel<lad::kPrefill, 256>,
+                                       lad::tokenwise_grid<256>(parts, ds->sms), lad::threads_of<256>(),
+                                       lad::tokenwise_smem_bytes<256>(), static_cast<cudaStream_t>(stream), tp);
+  if (ce == cudaSuccess) ce = cudaGetLastError();
+  if (ce != cudaSuccess) return la_host::fail(LA_ERR_CUDA, "tokenwise kernel launch failed: %s", cudaGetErrorString(ce));
+  return LA_OK;
+}
+
 // The checks of la_prefill_fwd_d256 and its segmented form: D = V = 256, the head counts, and
 // la_prefill_fwd's checks on the same memory seen as 2 H q/k and 2 HV value heads of 128.
 la_status check_args(const void* q, const void* k, const void* v, const float* slopes, const float* h0,
@@ -212,6 +257,13 @@ la_status blocks_path(const void* q, const void* k, const void* v, const float* 
     return st;
   la_host::DeviceState* ds = nullptr;
   if ((st = la_host::current_device(g_dev, &ds, setup_kernels)) != LA_OK) return st;
+  // a packed batch of mostly short sequences (not segmented): those of at most kShortMax tokens
+  // run the tokenwise kernel on whole states, the block path skips them
+  const bool split = segment_len < 0 && cu_seqlens && tokens <= static_cast<int64_t>(kSplitAvg) * N;
+  const int short_max = split ? kShortMax : -1;
+  if (split && (st = launch_tokenwise(q, k, v, slopes, scale, h0, state_indices, cu_seqlens, o, h_final, T, N, H, HV,
+                                      pool, tokens, ds, dev_error, stream)) != LA_OK)
+    return st;
 
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   float* part = reinterpret_cast<float*>(ws + l.part);
@@ -226,8 +278,11 @@ la_status blocks_path(const void* q, const void* k, const void* v, const float* 
   const int tgrid = static_cast<int>(((N > 4 * HV ? N : 4 * HV) + kThreads - 1) / kThreads);
   la_d256_tables_kernel<<<tgrid, kThreads, 0, s>>>(tp);
   if ((st = launched("d256 tables")) != LA_OK) return st;
-  BlockParams bp{h0, h_final, blocks, state_indices, cu_seqlens, N, HV, G, pool, static_cast<int>(tokens)};
-  const dim3 bgrid(static_cast<unsigned>(N) * 4 * HV, kHalf / kRowsPerCta);
+  BlockParams bp{h0, h_final, blocks, state_indices, cu_seqlens, N, HV, G, pool, static_cast<int>(tokens), short_max};
+  // few blocks: split each over 16 CTAs (8 rows each); many: one CTA per block, so that the
+  // blocks of short sequences cost one CTA each
+  const unsigned nblocks = static_cast<unsigned>(N) * 4 * HV;
+  const dim3 bgrid(nblocks, nblocks < 1024 ? kHalf / kRowsPerStep : 1);
   if (h0) {
     la_d256_blocks_kernel<true><<<bgrid, kThreads, 0, s>>>(bp);
     if ((st = launched("d256 gather")) != LA_OK) return st;
@@ -238,7 +293,7 @@ la_status blocks_path(const void* q, const void* k, const void* v, const float* 
   if (segment_len < 0)
     st = la_internal::chunkwise(q, k, v, slopes_q, scale, h0 ? blocks : nullptr, slot_q, cu_seqlens, nullptr, part,
                                 h_final ? blocks : nullptr, B, T, N, 2 * H, 4 * HV, 2 * HV, kHalf, N, false,
-                                dev_error, stream, 2 * G);
+                                dev_error, stream, 2 * G, short_max);
   else
     st = la_internal::segmented_f32(q, k, v, slopes_q, scale, h0 ? blocks : nullptr, slot_q, cu_seqlens, part,
                                     h_final ? blocks : nullptr, B, T, N, 2 * H, 4 * HV, kHalf, N, segment_len,
@@ -248,7 +303,7 @@ la_status blocks_path(const void* q, const void* k, const void* v, const float* 
   // 3. o = the sum over the key halves, rounded once; the final blocks to h_final
   if (tokens > 0) {
     SumParams sp{part, static_cast<__nv_bfloat16*>(o), cu_seqlens, state_indices, N, cu_seqlens ? 0 : T,
-                        static_cast<int>(tokens), pool, HV, G};
+                 static_cast<int>(tokens), pool, HV, G, short_max};
     const int rgrid = static_cast<int>(tokens < 16 * ds->sms ? tokens : 16 * ds->sms);
     la_d256_sum_kernel<<<rgrid, kThreads, 0, s>>>(sp);
     if ((st = launched("d256 sum")) != LA_OK) return st;
@@ -296,32 +351,8 @@ la_status la_prefill_fwd_d256(const void* q, const void* k, const void* v, const
                                               B, T, N, H, HV, D, V, pool_size)) != LA_OK)
       return st;
     if ((st = la_host::current_device(la256::g_dev, &ds, la256::setup_kernels)) != LA_OK) return st;
-    lad::Params tp{};
-    tp.q = static_cast<const __nv_bfloat16*>(q);
-    tp.k = static_cast<const __nv_bfloat16*>(k);
-    tp.v = static_cast<const __nv_bfloat16*>(v);
-    tp.slopes = slopes;
-    tp.state_indices = state_indices;
-    tp.o = static_cast<__nv_bfloat16*>(o);
-    tp.h0 = h0;
-    tp.h_final = h_final;
-    tp.dev_error = dev_error;
-    tp.scale = scale;
-    tp.B = N;
-    tp.T = T;
-    tp.H = H;
-    tp.HV = HV;
-    tp.G = HV / H;
-    tp.pool_size = pool;
-    tp.num_tokens = static_cast<int>(tokens);
-    tp.short_max = la256::kShortMax;
-    const int parts = N * HV * lad::split_of<256>();  // <= 4 N HV, checked above
-    cudaError_t ce = la_host::launch_pdl(lad::la_tokenwise_kernel<lad::kPrefill, 256>,
-                                         lad::tokenwise_grid<256>(parts, ds->sms), lad::threads_of<256>(),
-                                         lad::tokenwise_smem_bytes<256>(), static_cast<cudaStream_t>(stream), tp);
-    if (ce == cudaSuccess) ce = cudaGetLastError();
-    if (ce != cudaSuccess) return fail(LA_ERR_CUDA, "tokenwise kernel launch failed: %s", cudaGetErrorString(ce));
-    return LA_OK;
+    return la256::launch_tokenwise(q, k, v, slopes, scale, h0, state_indices, nullptr, o, h_final, T, N, H, HV, pool,
+                                   tokens, ds, dev_error, stream);
   }
 
   return la256::blocks_path(q, k, v, slopes, scale, h0, state_indices, cu_seqlens, o, h_final, B, T, N, H, HV,

@@ -192,7 +192,7 @@ namespace la_internal {
 la_status chunkwise(const void* q, const void* k, const void* v, const float* slopes, float scale, const float* h0,
                     const int32_t* state_indices, const int32_t* cu_seqlens, void* o, float* o_f32, float* h_final,
                     int B, int T, int N, int H, int HV, int v_heads, int D, int pool_size, bool reverse,
-                    int* dev_error, void* stream, int v_fold) {
+                    int* dev_error, void* stream, int v_fold, int short_max) {
   if (v_heads <= 0 || HV % v_heads != 0)
     return fail(LA_ERR_UNSUPPORTED, "HV (%d) must be a multiple of v's heads (%d)", HV, v_heads);
   if (v_fold < 0 || (v_fold > 0 && (!o_f32 || v_heads * 2 != HV || HV % (2 * v_fold) != 0)))
@@ -238,7 +238,7 @@ la_status chunkwise(const void* q, const void* k, const void* v, const float* sl
   p.vfold = v_fold;
   p.pool_size = la_host::effective_pool_size(h0, h_final, state_indices, pool_size, N);
   p.num_units = static_cast<int>(units);
-  p.short_max = -1;  // every sequence, however short, runs here
+  p.short_max = cu_seqlens ? short_max : -1;  // -1: every sequence, however short, runs here
   const int grid = static_cast<int>(units < dsp->sms ? units : dsp->sms);
   const cudaStream_t cs = static_cast<cudaStream_t>(stream);
   const int variant = (D == 128 ? 0 : 4) + (reverse ? 2 : 0) + (o_f32 ? 1 : 0);

@@ -21,12 +21,13 @@ namespace la_internal {
 // into `o_f32` when that is not null (same [tokens, HV, D] layout).  With v_fold > 0 (FP32 output
 // only, v_heads = HV / 2) head h reads v's head (h / (2 v_fold)) v_fold + h % v_fold instead: the
 // digit of weight v_fold of h is dropped (the D = 256 decomposition, where it selects a half of
-// the key dimension).  Arguments, layouts and checks otherwise as la_prefill_fwd (D == V).  Used
-// by the backward pass and by the D = 256 prefill.
+// the key dimension).  short_max >= 0 (packed batches) leaves the sequences of at most that many
+// tokens to another kernel.  Arguments, layouts and checks otherwise as la_prefill_fwd (D == V).
+// Used by the backward pass and by the D = 256 prefill.
 la_status chunkwise(const void* q, const void* k, const void* v, const float* slopes, float scale, const float* h0,
                     const int32_t* state_indices, const int32_t* cu_seqlens, void* o, float* o_f32, float* h_final,
                     int B, int T, int N, int H, int HV, int v_heads, int D, int pool_size, bool reverse,
-                    int* dev_error, void* stream, int v_fold = 0);
+                    int* dev_error, void* stream, int v_fold = 0, int short_max = -1);
 
 // The segmented prefill (include/la_segment.h) with FP32 output parts and the value-head fold
 // vfold (v with HV / 2 heads), on arguments the caller has checked: the D = 256 prefill's view

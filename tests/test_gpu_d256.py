@@ -48,6 +48,10 @@ D256_CASES = {
     "short_fixed_T17_pool_in_place_tokenwise": dict(B=3, T=17, H=1, HV=2, pool=5, indices=[4, -1, 1],
                                                     in_place=True),
     "short_fixed_T8_no_h0_tokenwise": dict(B=2, T=8, H=2, HV=2, with_h0=False),
+    # packed, at most 64 tokens per sequence on average: the short ones on the tokenwise kernel
+    "split_pool_in_place_padded": dict(lengths=[9, 32, 0, 17, 33, 2, 100], H=1, HV=2, pool=9,
+                                       indices=[4, 0, 8, -1, 2, 6, 1], in_place=True),
+    "split_gva_no_h0": dict(lengths=[8, 8, 70, 8, 8, 8], H=2, HV=4, with_h0=False),
 }
 
 
