@@ -5,7 +5,8 @@ D = 128 chunkwise kernel and adds the two key halves of every output in FP32 bef
 The oracle runs the D = 256 recurrence itself, so these cases check the decomposition as well as
 the kernels: ragged and packed batches, a pool in place with padding, GVA, no h0, no final state,
 lambda = 1 and lambda -> 0, a bad state index, isolation from a non-finite neighbour, and two
-calls bitwise equal.
+calls bitwise equal; the short fixed-length and packed split paths (tokenwise kernel); the
+segmented form; and the decoding ops at D = 256 in a CUDA graph.
 """
 import zlib
 
@@ -208,3 +209,60 @@ def test_d256_segmented_close_to_plain_d256():
     from harness import rel_rms
     assert rel_rms(d2["o"].float().cpu().numpy(), d1["o"].float().cpu().numpy()) < 2e-3
     assert rel_rms(d2["h_final"].cpu().numpy(), d1["h_final"].cpu().numpy()) < 1e-4
+
+
+def test_d256_segmented_two_calls_share_a_garbage_workspace():
+    import linear_attention_prefill_chunkwise_gb300 as lap
+    p = W.custom(seed=4012, lengths=[700, 0, 333], H=1, HV=2, D=256, pool=5, indices=[4, -1, 0])
+    nbytes, seg = lap.la_prefill_d256_segmented_workspace(p.B, p.T, p.N, p.HV, True, 128, True)
+    assert seg == 128
+    ws = torch.full((nbytes,), 0x7F, dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(2):
+        d = upload(p)
+        lap.la_prefill_fwd_d256_segmented(d["q"], d["k"], d["v"], d["slopes"], p.scale, h0=d["h0"],
+                                          state_indices=d["idx"], cu_seqlens=d["cu"], o=d["o"], h_final=d["h_final"],
+                                          segment_len=128, workspace=ws)
+        torch.cuda.synchronize()
+        outs.append((d["o"].view(torch.int16).clone(), d["h_final"].view(torch.int32).clone()))
+        compare_full(p, d, "D=256 segmented, garbage workspace")
+    assert torch.equal(outs[0][0], outs[1][0])
+    assert torch.equal(outs[0][1], outs[1][1])
+
+
+def test_d256_decode_and_commit_in_a_cuda_graph():
+    """MTP decode and commit at D = 256 (the tokenwise kernel's 256-thread instance) captured in
+    one CUDA graph replay bitwise like the eager calls."""
+    import linear_attention_prefill_chunkwise_gb300 as lap
+    from test_gpu_decode import make_case
+    from test_gpu_decode import upload as dec_upload
+    c = make_case(seed=4013, B=6, T=5, H=1, HV=2, P=8, n_pad=1, D=256)
+    d = dec_upload(c)
+    pool0 = d["pool"].clone()
+    B, T, H, HV, P = c["B"], c["T"], c["H"], c["HV"], c["P"]
+    kbuf = torch.zeros((P, T, H, 256), dtype=torch.bfloat16, device="cuda")
+    vbuf = torch.zeros((P, T, HV, 256), dtype=torch.bfloat16, device="cuda")
+    acc = torch.tensor([5, 0, 3, 5, 1, 2], dtype=torch.int32, device="cuda")
+
+    def calls(o, pool):
+        lap.la_verify(d["q"], d["k"], d["v"], d["slopes"], c["scale"], pool, T, state_indices=d["idx"], o=o,
+                      kbuf=kbuf, vbuf=vbuf)
+        lap.la_commit(pool, kbuf, vbuf, acc, d["slopes"], state_indices=d["idx"])
+
+    o_ref = torch.full((B * T, HV, 256), float("nan"), dtype=torch.bfloat16, device="cuda")
+    pool_ref = pool0.clone()
+    calls(o_ref, pool_ref)
+    torch.cuda.synchronize()
+    o = torch.full_like(o_ref, float("nan"))
+    pool = pool0.clone()
+    s = torch.cuda.Stream()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        calls(o, pool)
+    for _ in range(2):
+        pool.copy_(pool0)
+        o.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16))
+        assert torch.equal(pool.view(torch.int32), pool_ref.view(torch.int32))
