@@ -266,3 +266,47 @@ def test_d256_decode_and_commit_in_a_cuda_graph():
         torch.cuda.synchronize()
         assert torch.equal(o.view(torch.int16), o_ref.view(torch.int16))
         assert torch.equal(pool.view(torch.int32), pool_ref.view(torch.int32))
+
+
+def test_d256_parts_past_two_to_the_31_elements():
+    """A packed batch of 266,240 tokens with 16 value heads at D = 256: the FP32 parts of o
+    (tokens x 64 block heads x 128) hold 2.18e9 elements.  The first sequence is padded (never
+    read or written); the second, the last 100 tokens, lies past element 2^31 of the parts, so
+    their stores, the sum's loads and the output rows exercise 64-bit offsets: outputs and final
+    state against the oracle, the padded rows and slot untouched."""
+    import oracle
+    from harness import check_output, check_state, to_torch_bf16
+    tokens, H, HV, L = (1 << 18) + (1 << 12), 16, 16, 100
+    assert (tokens - L) * 4 * HV * 128 > 2 ** 31
+    dev = "cuda"
+    rng = np.random.default_rng(41)
+    qb, kb, vb = W.make_qkv(rng, L, H, HV, d=256, v_dim=256)
+    h0_np = W.make_states(rng, 2, HV, d=256, v_dim=256)
+    slopes = W.slopes_for(HV)
+    scale = 1.0 / 16.0
+    q = torch.empty((tokens, H, 256), dtype=torch.bfloat16, device=dev)
+    k = torch.empty_like(q)
+    v = torch.empty((tokens, HV, 256), dtype=torch.bfloat16, device=dev)
+    q[-L:] = to_torch_bf16(qb, dev)
+    k[-L:] = to_torch_bf16(kb, dev)
+    v[-L:] = to_torch_bf16(vb, dev)
+    o = torch.full((tokens, HV, 256), float("nan"), dtype=torch.bfloat16, device=dev)
+    h0 = torch.from_numpy(h0_np).to(dev)
+    hf = torch.full_like(h0, float("nan"))
+    idx = torch.tensor([-1, 1], dtype=torch.int32, device=dev)
+    cu = torch.tensor([0, tokens - L, tokens], dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    import linear_attention_prefill_chunkwise_gb300 as lap
+    lap.la_prefill_fwd_d256(q, k, v, torch.from_numpy(slopes).to(dev), scale, h0=h0, state_indices=idx,
+                            cu_seqlens=cu, o=o, h_final=hf, dev_error=err)
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    o_ref, h_ref = oracle.tokenwise(W.bf16_to_f32(qb), W.bf16_to_f32(kb), W.bf16_to_f32(vb), slopes, scale,
+                                    h0=h0_np[1:2].astype(np.float64), cu_seqlens=np.array([0, L], dtype=np.int32))
+    check_output(o[-L:].float().cpu().numpy(), o_ref, "D=256 rows past 2^31 part elements")
+    check_state(hf[1].cpu().numpy(), h_ref[0], "D=256 state of the sequence past 2^31 part elements")
+    assert bool(torch.isnan(hf[0]).all())
+    for r in (0, tokens // 2, tokens - L - 1):
+        assert bool(torch.isnan(o[r].float()).all())
+    del q, k, v, o
+    torch.cuda.empty_cache()
